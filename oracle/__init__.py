@@ -1,0 +1,167 @@
+"""CPU oracle for the product-VQ encode step (``quantize_vq``).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library under ``product_vq_kv_gb300/`` and never imports it.
+
+The arithmetic lives in ``vq_oracle.c`` (plain C, fp32, no FMA contraction);
+this module compiles it with the host ``gcc`` on first use and wraps it with
+``ctypes``.  See that file's header for what is computed and which passage of
+"I Wrote a Metal Kernel to Stop My Mac From OOMing" each step follows.
+
+Parity pins: every exported function is pinned in ``tests/test_oracle.py``
+against float64 brute force, closed forms, invariants and golden fixtures.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "vq_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libvqoracle.so")
+
+# Flags: no FMA contraction and no fast-math, so every fp32 multiply and add
+# rounds separately, as the encode formula requires.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+          "-fno-fast-math", "-fno-unsafe-math-optimizations"]
+
+DTYPE_F16, DTYPE_BF16, DTYPE_F32 = 0, 1, 2
+
+_lock = threading.Lock()
+_default = None
+
+
+def compile_source(src_path: str, out_path: str) -> str:
+    """Compile one C source of the oracle into a shared library."""
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(out_path))
+    os.close(fd)
+    try:
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, src_path, "-lm"], check=True,
+                       capture_output=True, text=True)
+        os.replace(tmp, out_path)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return out_path
+
+
+def build(force: bool = False) -> str:
+    """Compile ``vq_oracle.c`` into ``oracle/_build/libvqoracle.so``."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    fresh = (os.path.exists(_LIB_PATH)
+             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC))
+    if fresh and not force:
+        return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
+
+
+def _dtype_code(arr: np.ndarray, bf16: bool) -> int:
+    if arr.dtype == np.float16:
+        return DTYPE_F16
+    if arr.dtype == np.float32:
+        return DTYPE_F32
+    if arr.dtype == np.uint16 and bf16:
+        return DTYPE_BF16
+    raise TypeError(f"unsupported dtype {arr.dtype} (bf16={bf16})")
+
+
+class OracleLib:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        lib.vqo_f16_to_f32.restype = ctypes.c_float
+        lib.vqo_f16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.vqo_bf16_to_f32.restype = ctypes.c_float
+        lib.vqo_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.vqo_distance.restype = ctypes.c_float
+        lib.vqo_distance.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int32, ctypes.c_int32]
+        lib.vqo_encode_grouped.restype = ctypes.c_int32
+        lib.vqo_encode_grouped.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+            ctypes.c_int32]
+        self.path = path
+        self._lib = lib
+
+    def f16_to_f32(self, bits: int) -> float:
+        return float(self._lib.vqo_f16_to_f32(bits))
+
+    def bf16_to_f32(self, bits: int) -> float:
+        return float(self._lib.vqo_bf16_to_f32(bits))
+
+    def distance(self, x: np.ndarray, c: np.ndarray, bf16: bool = False) -> np.float32:
+        """fp32 squared distance of one sub-vector to one centroid."""
+        x = np.ascontiguousarray(x)
+        c = np.ascontiguousarray(c)
+        if x.shape != c.shape or x.ndim != 1 or x.dtype != c.dtype:
+            raise ValueError("x and c must be 1-D arrays of the same shape and dtype")
+        code = _dtype_code(x, bf16)
+        return np.float32(self._lib.vqo_distance(x.ctypes.data, c.ctypes.data,
+                                                 x.shape[0], code))
+
+    def encode(self, x: np.ndarray, codebook: np.ndarray, *, bf16: bool = False,
+               n_threads: int = 1) -> np.ndarray:
+        """Nearest-centroid indices (uint32), by the fp32 encode formula.
+
+        ``x`` is ``[N, sub_dim]`` with ``codebook`` ``[n_centroids, sub_dim]``,
+        or grouped: ``x`` ``[G, M, sub_dim]`` with ``codebook`` ``[G,
+        n_centroids, sub_dim]``.  fp16 and fp32 arrays are taken as they are;
+        bf16 data is passed as its raw ``uint16`` bits with ``bf16=True``.
+        Returns ``[N]`` or ``[G, M]`` uint32.
+        """
+        x = np.ascontiguousarray(x)
+        codebook = np.ascontiguousarray(codebook)
+        if x.dtype != codebook.dtype:
+            raise TypeError("x and codebook must share a dtype")
+        code = _dtype_code(x, bf16)
+        if x.ndim == 2 and codebook.ndim == 2:
+            groups, per_group, sub_dim = 1, x.shape[0], x.shape[1]
+            out_shape = (x.shape[0],)
+        elif x.ndim == 3 and codebook.ndim == 3 and x.shape[0] == codebook.shape[0]:
+            groups, per_group, sub_dim = x.shape
+            out_shape = (groups, per_group)
+        else:
+            raise ValueError(f"bad shapes x{x.shape} codebook{codebook.shape}")
+        if codebook.shape[-1] != sub_dim:
+            raise ValueError("sub_dim mismatch between x and codebook")
+        n_centroids = codebook.shape[-2]
+        out = np.zeros(out_shape, dtype=np.uint32)
+        rc = self._lib.vqo_encode_grouped(x.ctypes.data, codebook.ctypes.data, groups,
+                                          per_group, n_centroids, sub_dim, code,
+                                          out.ctypes.data, int(n_threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle encode failed with status {rc}")
+        return out
+
+
+def default() -> OracleLib:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = OracleLib(build())
+    return _default
+
+
+def f16_to_f32(bits: int) -> float:
+    return default().f16_to_f32(bits)
+
+
+def bf16_to_f32(bits: int) -> float:
+    return default().bf16_to_f32(bits)
+
+
+def distance(x, c, bf16: bool = False):
+    return default().distance(x, c, bf16=bf16)
+
+
+def encode(x, codebook, *, bf16: bool = False, n_threads: int = 1):
+    return default().encode(x, codebook, bf16=bf16, n_threads=n_threads)

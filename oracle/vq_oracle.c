@@ -1,0 +1,211 @@
+/*
+ * vq_oracle.c -- plain, slow, obviously correct CPU oracle for the
+ * product-vector-quantisation encode step ("quantize_vq").
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The product path
+ * (the CUDA library and its Python binding) never calls it, and the two
+ * share no code, headers, tables or helpers.
+ *
+ * What it computes (source: "I Wrote a Metal Kernel to Stop My Mac From
+ * OOMing", sections "What Even Is a KV Cache" steps 1-3, "What quantize_vq
+ * Was Doing Wrong" and "The Kernel: 18 Lines of MSL"):
+ *
+ *   for every sub-vector x[n] (length sub_dim) and its codebook cb
+ *   [n_centroids][sub_dim]:
+ *     best = +inf (fp32), idx = 0
+ *     for c = 0 .. n_centroids-1 (ascending):
+ *       dist = 0 (fp32)
+ *       for i = 0 .. sub_dim-1 (ascending):
+ *         d    = float(x[n][i]) - float(cb[c][i])     fp32, round to nearest
+ *         dist = dist + d * d                           separate fp32 multiply
+ *                                                      and add, never fused
+ *       if dist < best: best = dist; idx = c           strict "<"
+ *     out[n] = idx   (uint32)
+ *
+ * Readings where the page is silent (each is also listed with the design
+ * notes): the multiply and add are not contracted into an FMA (this file
+ * must be compiled with -ffp-contract=off and without fast-math); fp16 and
+ * bf16 inputs are widened to fp32 before the subtraction (the shader's
+ * float(...) casts); a NaN distance never wins and a row whose distances
+ * are all NaN or +inf encodes to 0 (consequence of the (+inf, 0) start and
+ * the strict compare); denormals are kept (IEEE, no flush to zero).
+ *
+ * Grouped layout (one codebook per (layer, head) group): x is
+ * [n_groups][n_per_group][sub_dim], codebooks [n_groups][n_centroids]
+ * [sub_dim], out [n_groups][n_per_group]; row n of the flattened x uses
+ * codebook n / n_per_group.  The ungrouped call is n_groups = 1.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { VQO_F16 = 0, VQO_BF16 = 1, VQO_F32 = 2 };
+
+enum {
+    VQO_OK = 0,
+    VQO_ERR_INVALID_ARG = 1,
+    VQO_ERR_THREAD = 2
+};
+
+/* IEEE 754 binary16 -> binary32, from the format's definition:
+ * value = (-1)^s * 2^(e-15) * (1 + m/1024) for 0 < e < 31,
+ *         (-1)^s * 2^-14 * (m/1024)          for e == 0,
+ *         inf / NaN                          for e == 31.        */
+float vqo_f16_to_f32(uint16_t h)
+{
+    uint32_t s = (h >> 15) & 1u;
+    uint32_t e = (h >> 10) & 0x1fu;
+    uint32_t m = h & 0x3ffu;
+    float v;
+    if (e == 0)
+        v = ldexpf((float)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexpf((float)(m | 0x400u), (int)e - 25);
+    return s ? -v : v;
+}
+
+/* bfloat16 is the upper half of a binary32. */
+float vqo_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static float load_elem(const void *base, int dtype, int64_t k)
+{
+    switch (dtype) {
+    case VQO_F16:
+        return vqo_f16_to_f32(((const uint16_t *)base)[k]);
+    case VQO_BF16:
+        return vqo_bf16_to_f32(((const uint16_t *)base)[k]);
+    default:
+        return ((const float *)base)[k];
+    }
+}
+
+/* Squared distance of one sub-vector to one centroid, the fp32 formula
+ * above.  Exported so the tests can pin the arithmetic on its own. */
+float vqo_distance(const void *x, const void *c, int32_t sub_dim, int32_t dtype)
+{
+    float dist = 0.0f;
+    for (int32_t i = 0; i < sub_dim; ++i) {
+        float d = load_elem(x, dtype, i) - load_elem(c, dtype, i);
+        float sq = d * d;
+        dist = dist + sq;
+    }
+    return dist;
+}
+
+static size_t elem_size(int dtype)
+{
+    return dtype == VQO_F32 ? 4u : 2u;
+}
+
+/* Encode flattened rows [row_begin, row_end). */
+static void encode_rows(const void *x, const void *codebooks, int64_t n_per_group,
+                        int32_t n_centroids, int32_t sub_dim, int32_t dtype,
+                        uint32_t *out, int64_t row_begin, int64_t row_end)
+{
+    const size_t es = elem_size(dtype);
+    const char *xb = (const char *)x;
+    const char *cbb = (const char *)codebooks;
+    for (int64_t n = row_begin; n < row_end; ++n) {
+        const int64_t g = n / n_per_group;
+        const char *xn = xb + (size_t)n * (size_t)sub_dim * es;
+        const char *cb = cbb + (size_t)g * (size_t)n_centroids * (size_t)sub_dim * es;
+        float best = INFINITY;
+        uint32_t idx = 0;
+        for (int32_t c = 0; c < n_centroids; ++c) {
+            float dist = vqo_distance(xn, cb + (size_t)c * (size_t)sub_dim * es, sub_dim, dtype);
+            if (dist < best) {
+                best = dist;
+                idx = (uint32_t)c;
+            }
+        }
+        out[n] = idx;
+    }
+}
+
+struct job {
+    const void *x;
+    const void *codebooks;
+    int64_t n_per_group;
+    int32_t n_centroids, sub_dim, dtype;
+    uint32_t *out;
+    int64_t begin, end;
+};
+
+static void *job_main(void *arg)
+{
+    struct job *j = (struct job *)arg;
+    encode_rows(j->x, j->codebooks, j->n_per_group, j->n_centroids, j->sub_dim, j->dtype,
+                j->out, j->begin, j->end);
+    return NULL;
+}
+
+/* Encode all n_groups * n_per_group rows with n_threads host threads
+ * (rows split into equal contiguous ranges; the result does not depend on
+ * the thread count).  Returns VQO_OK or an error code. */
+int32_t vqo_encode_grouped(const void *x, const void *codebooks, int64_t n_groups,
+                           int64_t n_per_group, int32_t n_centroids, int32_t sub_dim,
+                           int32_t dtype, uint32_t *out, int32_t n_threads)
+{
+    if (n_groups < 0 || n_per_group < 0 || n_centroids < 1 || sub_dim < 1)
+        return VQO_ERR_INVALID_ARG;
+    if (dtype != VQO_F16 && dtype != VQO_BF16 && dtype != VQO_F32)
+        return VQO_ERR_INVALID_ARG;
+    const int64_t rows = n_groups * n_per_group;
+    if (rows == 0)
+        return VQO_OK;
+    if (!x || !codebooks || !out)
+        return VQO_ERR_INVALID_ARG;
+    if (n_threads < 1)
+        n_threads = 1;
+    if ((int64_t)n_threads > rows)
+        n_threads = (int32_t)rows;
+    if (n_threads == 1) {
+        encode_rows(x, codebooks, n_per_group, n_centroids, sub_dim, dtype, out, 0, rows);
+        return VQO_OK;
+    }
+    pthread_t *tid = (pthread_t *)calloc((size_t)n_threads, sizeof *tid);
+    struct job *jobs = (struct job *)calloc((size_t)n_threads, sizeof *jobs);
+    if (!tid || !jobs) {
+        free(tid);
+        free(jobs);
+        return VQO_ERR_THREAD;
+    }
+    int32_t started = 0;
+    int32_t rc = VQO_OK;
+    for (int32_t t = 0; t < n_threads; ++t) {
+        jobs[t] = (struct job){x, codebooks, n_per_group, n_centroids, sub_dim, dtype, out,
+                               rows * t / n_threads, rows * (t + 1) / n_threads};
+        if (pthread_create(&tid[t], NULL, job_main, &jobs[t]) != 0) {
+            rc = VQO_ERR_THREAD;
+            break;
+        }
+        ++started;
+    }
+    for (int32_t t = 0; t < started; ++t)
+        pthread_join(tid[t], NULL);
+    if (rc != VQO_OK) /* finish the rows of threads that never started */
+        for (int32_t t = started; t < n_threads; ++t)
+            job_main(&jobs[t]);
+    free(tid);
+    free(jobs);
+    return VQO_OK;
+}
+
+int32_t vqo_encode(const void *x, const void *codebook, int64_t n, int32_t n_centroids,
+                   int32_t sub_dim, int32_t dtype, uint32_t *out, int32_t n_threads)
+{
+    if (n < 0)
+        return VQO_ERR_INVALID_ARG;
+    return vqo_encode_grouped(x, codebook, 1, n, n_centroids, sub_dim, dtype, out, n_threads);
+}

@@ -1,0 +1,90 @@
+"""The oracle's pins must catch plausible mistakes (CPU only).
+
+Each case plants one mistake in a copy of the oracle's C source, compiles the
+copy, and runs the pins of ``test_oracle.py`` against it: at least one pin
+must fail.  Nothing here touches a GPU.
+"""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+import test_oracle as pins
+from conftest import read_golden
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "vq_oracle.c")
+
+MUTATIONS = {
+    # fused multiply-add instead of a separate multiply and add
+    "fma": ("float sq = d * d;\n        dist = dist + sq;",
+            "dist = fmaf(d, d, dist);"),
+    # sum the squares in descending i
+    "descending_sum": ("for (int32_t i = 0; i < sub_dim; ++i) {\n        float d",
+                       "for (int32_t i = sub_dim - 1; i >= 0; --i) {\n        float d"),
+    # ties go to the highest index
+    "tie_rule": ("if (dist < best) {", "if (dist <= best) {"),
+    # one coordinate dropped from the distance
+    "dropped_term": ("for (int32_t i = 0; i < sub_dim; ++i) {\n        float d",
+                     "for (int32_t i = 1; i < sub_dim; ++i) {\n        float d"),
+    # codebook read with a transposed stride
+    "transposed_codebook": ("cb + (size_t)c * (size_t)sub_dim * es",
+                            "cb + (size_t)c * es"),
+    # wrong group for grouped rows
+    "wrong_group": ("const int64_t g = n / n_per_group;",
+                    "const int64_t g = n % (n_per_group ? n_per_group : 1) % 2;"),
+    # fp16 exponent bias off by one
+    "f16_bias": ("(int)e - 25", "(int)e - 24"),
+    # bf16 read from the wrong half
+    "bf16_half": ("(uint32_t)b << 16", "(uint32_t)b << 15"),
+    # the running best starts at a finite value
+    "finite_init": ("float best = INFINITY;", "float best = 1e30f;"),
+    # squared difference replaced by absolute difference
+    "abs_distance": ("float sq = d * d;", "float sq = fabsf(d);"),
+}
+
+
+def _pins(lib):
+    """Every pin of test_oracle.py, bound to one oracle library."""
+    yield lambda: pins.test_f16_decode_matches_numpy_for_every_bit_pattern(lib)
+    yield lambda: pins.test_bf16_decode_matches_torch_for_every_bit_pattern(lib)
+    for row in read_golden("distance_rounding.txt"):
+        yield lambda row=row: pins.test_distance_golden_rounding(lib, row)
+    yield lambda: pins.test_distance_exact_on_small_integers(lib)
+    yield lambda: pins.test_distance_within_fp32_error_bound_of_exact(lib)
+    yield lambda: pins.test_encode_exact_integers_with_ties(lib)
+    for dt in ("f16", "bf16", "f32"):
+        yield lambda dt=dt: pins.test_encode_brute_force_float64(lib, dt, 4)
+    yield lambda: pins.test_exact_copies_map_to_first_equal_row(lib)
+    yield lambda: pins.test_duplicated_rows_resolve_to_lower_index(lib)
+    yield lambda: pins.test_single_centroid_encodes_everything_to_zero(lib)
+    yield lambda: pins.test_sub_dim_one_reduces_to_boundary_count(lib)
+    yield lambda: pins.test_permuting_codebook_rows_permutes_indices(lib)
+    yield lambda: pins.test_chunking_grouping_and_threads_do_not_change_results(lib)
+    yield lambda: pins.test_special_values(lib)
+
+
+def test_unmutated_source_passes_every_pin():
+    lib = oracle.default()
+    for pin in _pins(lib):
+        pin()
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name):
+    before, after = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, f"mutation anchor for {name} not found exactly once"
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "mutant.c")
+        with open(path, "w") as f:
+            f.write(src.replace(before, after))
+        lib = oracle.OracleLib(oracle.compile_source(path, os.path.join(tmp, "mutant.so")))
+        caught = 0
+        for pin in _pins(lib):
+            try:
+                pin()
+            except (AssertionError, RuntimeError, ValueError):
+                caught += 1
+                break
+        assert caught, f"no pin caught the '{name}' mutation"
