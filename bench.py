@@ -1,0 +1,361 @@
+"""Benchmark: product-VQ encode throughput (sub-vectors encoded per second).
+
+One step = one encode of the whole workload (default: the Falcon3-7B-shape
+prefill, 4096 tokens x 4 KV heads x head_dim 256 -> N = 1,048,576 fp16
+sub-vectors of length 4 against 256 centroids), launched through the C ABI
+with inputs resident in HBM.  L2 is flushed before every step (a 256 MiB
+write, larger than the 129 MB L2) and each step is timed with CUDA events on
+the launching stream.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank encodes its own full workload (independent problems,
+no data-path collective: weak scaling); rank 0 prints.  ``--impl reference``
+times the CPU oracle on this host's cores instead (the baseline arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "sub-vectors encoded/sec (1xGB300) and % of FP32 CUDA-core peak"
+UNIT = "sub-vectors/s"
+# The pages' own number for this exact workload (Falcon3-7B shape, S=4096,
+# D=256, sub_dim 4, 256 centroids, N = 1,048,576): 7.98 ms per call on an
+# Apple M-series GPU -> 131.4 M sub-vectors/s.  Context only (other hardware).
+PAGES_FALCON_SUBVEC_PER_S = 1_048_576 / 7.98e-3
+L2_FLUSH_BYTES = 256 << 20
+FP32_LANES_PER_SM = 128
+CLOCK_REASON_BITS = {
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+    0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+    0x100: "display_clock_setting",
+}
+
+
+def flops_per_subvector(w: workloads.Workload) -> int:
+    """Algorithmic fp32 operations per encoded sub-vector: for each centroid,
+    sub_dim subtractions, sub_dim squares, sub_dim - 1 additions and one
+    comparison = 3 * sub_dim."""
+    return w.n_centroids * 3 * w.sub_dim
+
+
+def bytes_per_subvector(w: workloads.Workload) -> int:
+    """Algorithmic HBM bytes per sub-vector: the fp16 row in, the uint32 index
+    out (the codebook, a few KiB per group, is negligible)."""
+    return 2 * w.sub_dim + 4
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._reader = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._reader is not None:
+                self._reader.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, sm_max, reasons = [], None, set()
+        for line in self.lines:
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                sm_max = float(f[2])
+                active = int(f[4], 16) if f[4].startswith("0x") else int(f[4])
+            except ValueError:
+                continue
+            for bit, name in CLOCK_REASON_BITS.items():
+                if active & bit:
+                    reasons.add(name)
+            for k, name in ((5, "hw_slowdown"), (6, "hw_thermal_slowdown"),
+                            (7, "sw_thermal_slowdown"), (8, "sw_power_cap")):
+                if f[k].lower() == "active":
+                    reasons.add(name)
+        busy = [v for v in sm if v > 0]
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": sm_max,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(w_name: str, x: np.ndarray, cb: np.ndarray, budget_s: float = 12.0) -> dict:
+    """The CPU oracle on this host's cores over a bounded sample of the same
+    workload: the first rows of group 0 (about ``budget_s`` seconds in all),
+    median of 3 runs."""
+    import oracle  # test infrastructure: used here only for the CPU baseline
+
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    w = workloads.WORKLOADS[w_name]
+    m = x.shape[1]
+    probe = min(m, 8192)
+    t0 = time.perf_counter()
+    oracle.encode(x[:1, :probe], cb[:1], n_threads=cores)
+    rate = probe / max(time.perf_counter() - t0, 1e-6)
+    rows = int(min(m, max(probe, rate * budget_s / 3)))
+    xs = np.ascontiguousarray(x[:1, :rows])
+    times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        oracle.encode(xs, cb[:1], n_threads=cores)
+        times.append(time.perf_counter() - t0)
+    med = statistics.median(times)
+    return {"value": rows / med, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} of {w.n} sub-vectors of {w_name} (codebook 0), "
+                      f"median of 3 runs, {cores} threads", "seconds": med}
+
+
+def bench_reference(args) -> None:
+    """The baseline arm: the CPU oracle, as it stands, on this host's cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle  # test infrastructure: the reference arm is the oracle
+
+    oracle.build()
+    w = workloads.WORKLOADS[args.workload]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    x, cb = workloads.generate(args.workload)
+    g, m, sub = x.shape
+    probe = min(m, 4096)
+    t0 = time.perf_counter()
+    oracle.encode(x[:1, :probe], cb[:1], n_threads=cores)
+    rate = probe / max(time.perf_counter() - t0, 1e-6)
+    per_step_s = min(1.0, 120.0 / max(1, args.steps + args.warmup))
+    rows = int(min(m, max(256, rate * per_step_s)))
+    xs = np.ascontiguousarray(x[:1, :rows])
+    for _ in range(args.warmup):
+        oracle.encode(xs, cb[:1], n_threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.encode(xs, cb[:1], n_threads=cores)
+    total = time.perf_counter() - t0
+    value = rows * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(w, args, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {rows} of {w.n} sub-vectors of {args.workload} per "
+                                   f"step, {cores} threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def config_block(w: workloads.Workload, args, world: int) -> dict:
+    return {"workload": w.name, "description": w.description, "n_subvectors": w.n,
+            "n_groups": w.n_groups, "sub_dim": w.sub_dim, "n_centroids": w.n_centroids,
+            "input_dtype": "f16", "tokens": w.tokens, "kv_heads": w.kv_heads,
+            "head_dim": w.head_dim, "layers": w.layers,
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": "flushed before every step (256 MiB write); per-step CUDA events"}
+
+
+def bench_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    from product_vq_kv_gb300.build import build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    import product_vq_kv_gb300 as vq
+
+    vq.load_library()
+    w = workloads.WORKLOADS[args.workload]
+    x, cb = workloads.generate(args.workload)
+    xd = torch.from_numpy(x).to(dev)
+    cbd = torch.from_numpy(cb).to(dev)
+    out = torch.empty(x.shape[:2], dtype=torch.uint32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        vq.vq_encode_grouped(xd, cbd, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        region0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize(dev)
+        region_s = time.perf_counter() - region0
+    if world > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = sum(step_ms) / len(step_ms)
+    t = torch.tensor([kernel_ms, region_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    kernel_ms, region_s = float(t[0]), float(t[1])
+
+    # end to end through the host entry point: pinned host in, pinned host out
+    xh = torch.from_numpy(x).pin_memory()
+    cbh = torch.from_numpy(cb).pin_memory()
+    outh = torch.empty(x.shape[:2], dtype=torch.uint32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 200))
+    for _ in range(3):
+        vq.vq_encode_grouped_host(xh, cbh, outh, xd, cbd, out, stream=stream)
+    if world > 1:
+        dist.barrier()
+    e0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        vq.vq_encode_grouped_host(xh, cbh, outh, xd, cbd, out, stream=stream)
+    e2e_s = time.perf_counter() - e0
+    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    e2e_s = float(te[0])
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    props = torch.cuda.get_device_properties(dev)
+    peaks = measured_peaks()
+    clk = clocks.summary()
+    sm_max = peaks.get("sm_max_mhz") or clk["sm_max_mhz"] or 2070.0
+    peak_tflops = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    units = w.n
+    value = units * world / (kernel_ms * 1e-3)
+    achieved = flops_per_subvector(w) * units / (kernel_ms * 1e-3) / 1e12
+    roofline = {
+        "bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+        "frac": achieved / peak_tflops, "traffic": None,
+        "kernel": vq.vq_describe_launch(x.shape[0], x.shape[1], cb.shape[1], x.shape[2],
+                                        torch.float16, xd.data_ptr()),
+        "flops_per_unit": flops_per_subvector(w), "units_per_launch": units,
+        "peak_basis": f"{props.multi_processor_count} SMs x {FP32_LANES_PER_SM} FP32 lanes x "
+                      f"2 (FMA) x {sm_max:.0f} MHz",
+        "hbm_gbs": bytes_per_subvector(w) * units / (kernel_ms * 1e-3) / 1e9,
+    }
+    if clk["sm_mhz"]:
+        roofline["frac_at_sampled_clock"] = roofline["frac"] * sm_max / clk["sm_mhz"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": kernel_ms,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / world / PAGES_FALCON_SUBVEC_PER_S
+                        if args.workload == "falcon_prefill" else None),
+        "dtype": "f32", "data": "synthetic (seeded N(0,1) fp16 keys and codebooks)",
+        "config": dict(config_block(w, args, world), timed_region_s=region_s),
+        "gpu_launches": args.steps,
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "roofline": roofline,
+        "e2e": {"value": units * world * e2e_steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": x.nbytes + cb.nbytes,
+                "d2h_bytes_per_step": int(units * 4),
+                "path": "vq_encode_grouped_host (pinned host buffers, copies inside)"},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, x, cb)
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main() -> None:
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="falcon_prefill")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args()
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

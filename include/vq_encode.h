@@ -1,0 +1,139 @@
+/*
+ * vq_encode.h -- C ABI of the GB300 product-vector-quantisation encoder.
+ *
+ * The operation ("quantize_vq"): each key vector of the KV cache is split into
+ * sub-vectors of length sub_dim, and each sub-vector is encoded as the index
+ * of its nearest centroid in a codebook of n_centroids rows, by squared L2
+ * distance.  Source: "I Wrote a Metal Kernel to Stop My Mac From OOMing",
+ * section "What Even Is a KV Cache" (steps 1-3: split into sub-vectors, a
+ * K-means codebook, encode each sub-vector as its nearest centroid's index)
+ * and section "The Kernel: 18 Lines of MSL" (the exact arithmetic):
+ *
+ *   dist(c) = sum over i = 0 .. sub_dim-1, in ascending i, of
+ *             (float(x[i]) - float(codebook[c][i]))^2
+ *   evaluated in IEEE fp32 with round-to-nearest: the subtraction, the square
+ *   and the running sum each round separately (never fused into an FMA);
+ *   out = the smallest c whose dist(c) is minimal (a strict "<" running
+ *   argmin from (+inf, 0)); NaN distances never win; a row whose distances
+ *   are all NaN or +inf encodes to 0; denormals are kept.
+ *
+ * Results are bit-exact against that definition: no approximation, no
+ * tolerance.  The [N, n_centroids, sub_dim] difference tensor of the
+ * straightforward implementation ("What quantize_vq Was Doing Wrong") is
+ * never materialised; the library allocates no device or host memory.
+ *
+ * Common rules for every entry point below:
+ *   - All array pointers are DEVICE pointers owned by the caller, row-major
+ *     and contiguous.  x and the codebook(s) share one element type
+ *     (vq_dtype).  out_idx must not overlap the inputs.
+ *   - The call validates its arguments on the host and returns an error
+ *     status before launching anything.  On success the work is enqueued on
+ *     `stream` (0 = the legacy default stream) and the call returns without
+ *     synchronising; results are valid once the stream has reached that
+ *     point.
+ *   - A launch failure returns VQ_ERR_CUDA; the CUDA error is left for the
+ *     caller to inspect (cudaGetLastError) and is not cleared.
+ *   - N = 0 (or n_per_group = 0) is valid: VQ_OK, nothing is launched, and
+ *     the pointers may be NULL.
+ *   - Supported shapes: 1 <= sub_dim <= 32, 1 <= n_centroids <= 4096.
+ *     sub_dim 4 and 8 with x aligned to sub_dim * element size take the
+ *     fast kernels; other shapes and misaligned x take a general kernel that
+ *     produces the same indices.
+ *   - Thread safety: calls may be made from several host threads; the
+ *     library keeps only a per-device cache of attributes, filled on first
+ *     use.
+ */
+#ifndef VQ_ENCODE_H
+#define VQ_ENCODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; declared opaquely so this header needs no CUDA headers. */
+typedef struct CUstream_st *vq_stream_t;
+
+typedef enum {
+    VQ_OK = 0,
+    VQ_ERR_INVALID_ARG = 1, /* null pointer with work to do, negative size, unknown dtype */
+    VQ_ERR_UNSUPPORTED = 2, /* sub_dim or n_centroids outside the supported range */
+    VQ_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    VQ_ERR_INTERNAL = 4     /* a broken internal invariant (should not happen) */
+} vq_status;
+
+/* Element type shared by x and the codebook(s). */
+typedef enum {
+    VQ_F16 = 0,  /* IEEE binary16 */
+    VQ_BF16 = 1, /* bfloat16 */
+    VQ_F32 = 2   /* IEEE binary32 */
+} vq_dtype;
+
+/*
+ * vq_encode -- encode N sub-vectors against one codebook.
+ *   x          [n][sub_dim]            device, dtype
+ *   codebook   [n_centroids][sub_dim]  device, dtype
+ *   out_idx    [n]                     device, uint32, written
+ * The call is asynchronous on `stream`.
+ */
+vq_status vq_encode(const void *x, const void *codebook, int64_t n, int32_t n_centroids,
+                    int32_t sub_dim, vq_dtype dtype, uint32_t *out_idx, vq_stream_t stream);
+
+/*
+ * vq_encode_grouped -- encode n_groups independent slices, each with its own
+ * codebook, in one launch (e.g. one codebook per layer, or per (layer, KV
+ * head), for a cache laid out [layers][batch, heads, tokens, head_dim]).
+ *   x          [n_groups][n_per_group][sub_dim]       device, dtype
+ *   codebooks  [n_groups][n_centroids][sub_dim]       device, dtype
+ *   out_idx    [n_groups][n_per_group]                device, uint32, written
+ * Row r of group g is encoded against codebooks[g] only.  n_groups = 1 is the
+ * same as vq_encode.  The call is asynchronous on `stream`.
+ */
+vq_status vq_encode_grouped(const void *x, const void *codebooks, int64_t n_groups,
+                            int64_t n_per_group, int32_t n_centroids, int32_t sub_dim,
+                            vq_dtype dtype, uint32_t *out_idx, vq_stream_t stream);
+
+/*
+ * vq_encode_grouped_host -- the same encode for inputs and outputs in HOST
+ * memory.  The library copies x and the codebooks to the caller's device
+ * buffers, encodes, and copies the indices back, in chunks on `stream` so
+ * that copies overlap the encode of neighbouring chunks.
+ *   x_host, codebooks_host, out_host    host memory (pinned memory gives
+ *                                       asynchronous copies; pageable memory
+ *                                       works but serialises)
+ *   x_dev        >= n_groups*n_per_group*sub_dim elements, device, scratch
+ *   codebooks_dev >= n_groups*n_centroids*sub_dim elements, device, scratch
+ *   out_dev      >= n_groups*n_per_group uint32, device, scratch
+ * The call returns once out_host holds the result (it synchronises
+ * `stream`).  The device buffers are the caller's; the library allocates
+ * nothing.
+ */
+vq_status vq_encode_grouped_host(const void *x_host, const void *codebooks_host,
+                                 int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                                 int32_t sub_dim, vq_dtype dtype, uint32_t *out_host,
+                                 void *x_dev, void *codebooks_dev, uint32_t *out_dev,
+                                 vq_stream_t stream);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char *vq_status_string(vq_status status);
+
+/*
+ * vq_describe_launch -- which kernel and launch shape vq_encode_grouped would
+ * use for these arguments on the current device, as NUL-terminated text in
+ * buf (truncated to buflen).  Performs no launch.  Returns the same
+ * argument errors as vq_encode_grouped.
+ */
+vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                             int32_t sub_dim, vq_dtype dtype, const void *x, char *buf,
+                             int32_t buflen);
+
+/* ABI version of this header (bumped on incompatible changes). */
+#define VQ_ENCODE_ABI_VERSION 1
+int32_t vq_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQ_ENCODE_H */

@@ -1,0 +1,196 @@
+"""ctypes binding of ``libvqenc.so``: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (declared in
+``include/vq_encode.h``) and does nothing but check and convert its arguments,
+allocate the output tensor when asked to, and pass the current CUDA stream.
+All computation happens in the library's CUDA kernels; there is no other code
+path.  If the library has not been built the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+VQ_OK, VQ_ERR_INVALID_ARG, VQ_ERR_UNSUPPORTED, VQ_ERR_CUDA, VQ_ERR_INTERNAL = range(5)
+VQ_F16, VQ_BF16, VQ_F32 = 0, 1, 2
+
+_TORCH_DTYPES = {torch.float16: VQ_F16, torch.bfloat16: VQ_BF16, torch.float32: VQ_F32}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class VQError(RuntimeError):
+    """A non-OK status returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {vq_status_string(status)}")
+
+
+def load_library() -> ctypes.CDLL:
+    """Load ``libvqenc.so`` (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing; build it with `python -m product_vq_kv_gb300.build` "
+                "(there is no fallback implementation)")
+        lib = ctypes.CDLL(LIB_PATH)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        lib.vq_encode.restype = i32
+        lib.vq_encode.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp]
+        lib.vq_encode_grouped.restype = i32
+        lib.vq_encode_grouped.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp]
+        lib.vq_encode_grouped_host.restype = i32
+        lib.vq_encode_grouped_host.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp, vp,
+                                               vp, vp]
+        lib.vq_status_string.restype = ctypes.c_char_p
+        lib.vq_status_string.argtypes = [i32]
+        lib.vq_describe_launch.restype = i32
+        lib.vq_describe_launch.argtypes = [i64, i64, i32, i32, i32, vp, ctypes.c_char_p, i32]
+        lib.vq_abi_version.restype = i32
+        lib.vq_abi_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def vq_status_string(status: int) -> str:
+    return load_library().vq_status_string(int(status)).decode()
+
+
+def vq_abi_version() -> int:
+    return int(load_library().vq_abi_version())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _TORCH_DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}; expected float16, bfloat16 or float32")
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != VQ_OK:
+        raise VQError(status, where)
+
+
+def _device_tensor(t: torch.Tensor, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def vq_encode(x: torch.Tensor, codebook: torch.Tensor, out: torch.Tensor | None = None,
+              stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Indices of the nearest centroid for each row of ``x``.
+
+    ``x`` ``[N, sub_dim]`` and ``codebook`` ``[n_centroids, sub_dim]`` are
+    contiguous CUDA tensors of one dtype (float16, bfloat16 or float32).
+    Returns (or fills ``out``) a ``[N]`` uint32 tensor.  Asynchronous on
+    ``stream`` (default: the current stream).
+    """
+    _device_tensor(x, "x")
+    _device_tensor(codebook, "codebook")
+    if x.dim() != 2 or codebook.dim() != 2 or x.shape[1] != codebook.shape[1]:
+        raise ValueError(f"expected x [N, sub_dim] and codebook [n_centroids, sub_dim], got "
+                         f"{tuple(x.shape)} and {tuple(codebook.shape)}")
+    if x.dtype != codebook.dtype:
+        raise TypeError("x and codebook must share a dtype")
+    if out is None:
+        out = torch.empty(x.shape[0], dtype=torch.uint32, device=x.device)
+    elif out.dtype != torch.uint32 or out.shape != (x.shape[0],) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous uint32 tensor of shape [N]")
+    st = load_library().vq_encode(x.data_ptr(), codebook.data_ptr(), x.shape[0],
+                                  codebook.shape[0], x.shape[1], _dtype_code(x),
+                                  out.data_ptr(), _stream_handle(stream, x.device))
+    _check(st, "vq_encode")
+    return out
+
+
+def vq_encode_grouped(x: torch.Tensor, codebooks: torch.Tensor,
+                      out: torch.Tensor | None = None,
+                      stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Grouped encode: ``x`` ``[G, M, sub_dim]`` against ``codebooks``
+    ``[G, n_centroids, sub_dim]`` (row block g uses codebook g).  Returns (or
+    fills ``out``) a ``[G, M]`` uint32 tensor.  Asynchronous on ``stream``."""
+    _device_tensor(x, "x")
+    _device_tensor(codebooks, "codebooks")
+    if (x.dim() != 3 or codebooks.dim() != 3 or x.shape[0] != codebooks.shape[0]
+            or x.shape[2] != codebooks.shape[2]):
+        raise ValueError(f"expected x [G, M, sub_dim] and codebooks [G, n_centroids, sub_dim], "
+                         f"got {tuple(x.shape)} and {tuple(codebooks.shape)}")
+    if x.dtype != codebooks.dtype:
+        raise TypeError("x and codebooks must share a dtype")
+    g, m, sub = x.shape
+    if out is None:
+        out = torch.empty((g, m), dtype=torch.uint32, device=x.device)
+    elif out.dtype != torch.uint32 or out.shape != (g, m) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous uint32 tensor of shape [G, M]")
+    st = load_library().vq_encode_grouped(x.data_ptr(), codebooks.data_ptr(), g, m,
+                                          codebooks.shape[1], sub, _dtype_code(x),
+                                          out.data_ptr(), _stream_handle(stream, x.device))
+    _check(st, "vq_encode_grouped")
+    return out
+
+
+def vq_encode_grouped_host(x_host: torch.Tensor, codebooks_host: torch.Tensor,
+                           out_host: torch.Tensor, x_dev: torch.Tensor,
+                           codebooks_dev: torch.Tensor, out_dev: torch.Tensor,
+                           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Grouped encode of HOST tensors through the caller's device buffers.
+
+    ``x_host`` ``[G, M, sub_dim]``, ``codebooks_host`` ``[G, n_c, sub_dim]`` and
+    ``out_host`` ``[G, M]`` uint32 live in host memory (pin them for
+    asynchronous copies); ``x_dev``, ``codebooks_dev`` and ``out_dev`` are
+    device buffers of at least the same sizes.  Returns ``out_host`` once it
+    holds the indices.
+    """
+    for t, name in ((x_host, "x_host"), (codebooks_host, "codebooks_host"),
+                    (out_host, "out_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    for t, name in ((x_dev, "x_dev"), (codebooks_dev, "codebooks_dev"), (out_dev, "out_dev")):
+        _device_tensor(t, name)
+    if x_host.dim() != 3 or codebooks_host.dim() != 3:
+        raise ValueError("expected x_host [G, M, sub_dim] and codebooks_host [G, n_c, sub_dim]")
+    g, m, sub = x_host.shape
+    n_c = codebooks_host.shape[1]
+    if (x_dev.dtype != x_host.dtype or codebooks_dev.dtype != x_host.dtype
+            or codebooks_host.dtype != x_host.dtype):
+        raise TypeError("all x and codebook tensors must share a dtype")
+    if out_host.dtype != torch.uint32 or out_dev.dtype != torch.uint32:
+        raise TypeError("out_host and out_dev must be uint32")
+    if (x_dev.numel() < x_host.numel() or codebooks_dev.numel() < codebooks_host.numel()
+            or out_dev.numel() < g * m or out_host.numel() < g * m):
+        raise ValueError("device or output buffers are too small")
+    st = load_library().vq_encode_grouped_host(
+        x_host.data_ptr(), codebooks_host.data_ptr(), g, m, n_c, sub, _dtype_code(x_host),
+        out_host.data_ptr(), x_dev.data_ptr(), codebooks_dev.data_ptr(), out_dev.data_ptr(),
+        _stream_handle(stream, x_dev.device))
+    _check(st, "vq_encode_grouped_host")
+    return out_host
+
+
+def vq_describe_launch(n_groups: int, n_per_group: int, n_centroids: int, sub_dim: int,
+                       dtype: torch.dtype, x_ptr: int = 0) -> str:
+    """The kernel and launch shape the library would use (no launch)."""
+    buf = ctypes.create_string_buffer(512)
+    st = load_library().vq_describe_launch(n_groups, n_per_group, n_centroids, sub_dim,
+                                           _TORCH_DTYPES[dtype], x_ptr, buf, len(buf))
+    _check(st, "vq_describe_launch")
+    return buf.value.decode()

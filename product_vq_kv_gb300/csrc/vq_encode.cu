@@ -1,0 +1,240 @@
+// vq_encode.cu -- C ABI entry points of the product-VQ encoder (see
+// include/vq_encode.h for the contract of every function).
+//
+// Host side only: validate arguments, pick a kernel for the shape, launch it
+// on the caller's stream.  The library allocates no memory.
+
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+
+#include "vq_encode.h"
+#include "vq_kernels.cuh"
+
+namespace {
+
+// Tuning of the fast kernels (rows per thread, threads per block, argmin
+// strategy, centroids per group).
+constexpr int kThreads = 128;
+constexpr int kRows = 8;
+constexpr int kMode = vqk::kDeferred;
+constexpr int kGroupCentroids = 8;
+
+constexpr int kMaxSubDim = 32;
+constexpr int kMaxCentroids = 4096;
+constexpr size_t kMaxFastSmem = 200 * 1024;
+constexpr int kGeneralThreads = 128;
+
+struct Args {
+    const void *x;
+    const void *cb;
+    int64_t n_groups;
+    int64_t n_per_group;
+    int32_t n_centroids;
+    int32_t sub_dim;
+    vq_dtype dtype;
+    uint32_t *out;
+    cudaStream_t stream;
+};
+
+size_t elem_size(vq_dtype d) { return d == VQ_F32 ? 4 : 2; }
+
+vq_status validate(const Args &a, bool need_pointers)
+{
+    if (a.dtype != VQ_F16 && a.dtype != VQ_BF16 && a.dtype != VQ_F32) return VQ_ERR_INVALID_ARG;
+    if (a.n_groups < 0 || a.n_per_group < 0) return VQ_ERR_INVALID_ARG;
+    if (a.sub_dim < 1 || a.sub_dim > kMaxSubDim) return VQ_ERR_UNSUPPORTED;
+    if (a.n_centroids < 1 || a.n_centroids > kMaxCentroids) return VQ_ERR_UNSUPPORTED;
+    if (a.n_groups != 0 && a.n_per_group > INT64_MAX / a.n_groups) return VQ_ERR_INVALID_ARG;
+    const int64_t rows = a.n_groups * a.n_per_group;
+    if (rows == 0) return VQ_OK;
+    if (rows > INT64_MAX / (a.sub_dim * 4)) return VQ_ERR_INVALID_ARG;
+    if (need_pointers) {
+        if (!a.x || !a.cb || !a.out) return VQ_ERR_INVALID_ARG;
+        const size_t es = elem_size(a.dtype);
+        if ((uintptr_t)a.x % es || (uintptr_t)a.cb % es || (uintptr_t)a.out % 4)
+            return VQ_ERR_INVALID_ARG;
+    }
+    return VQ_OK;
+}
+
+struct Plan {
+    bool fast;
+    size_t smem;
+    int64_t tiles_per_group;
+    int64_t blocks;
+    int threads;
+};
+
+template <int SUB>
+size_t fast_smem(int32_t n_centroids)
+{
+    return vqk::CbLayout<SUB, kGroupCentroids>::bytes(n_centroids);
+}
+
+Plan make_plan(const Args &a)
+{
+    Plan p{};
+    const size_t es = elem_size(a.dtype);
+    const size_t row_bytes = (size_t)a.sub_dim * es;
+    const size_t align = row_bytes < 16 ? row_bytes : 16;
+    const bool shape_ok = a.sub_dim == 4 || a.sub_dim == 8;
+    if (shape_ok) p.smem = a.sub_dim == 4 ? fast_smem<4>(a.n_centroids) : fast_smem<8>(a.n_centroids);
+    p.fast = shape_ok && p.smem <= kMaxFastSmem && ((uintptr_t)a.x % align == 0);
+    if (p.fast) {
+        const int64_t tile = (int64_t)kThreads * kRows;
+        p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
+        p.blocks = a.n_groups * p.tiles_per_group;
+        p.threads = kThreads;
+    } else {
+        p.smem = 0;
+        p.tiles_per_group = 0;
+        p.blocks = (a.n_groups * a.n_per_group + kGeneralThreads - 1) / kGeneralThreads;
+        p.threads = kGeneralThreads;
+    }
+    return p;
+}
+
+template <typename T, int SUB>
+vq_status launch_fast(const Args &a, const Plan &p)
+{
+    auto kernel = vqk::encode_fast<T, SUB, kRows, kThreads, kMode, kGroupCentroids>;
+    if (p.smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)p.smem) != cudaSuccess)
+            return VQ_ERR_CUDA;
+    }
+    kernel<<<(unsigned)p.blocks, p.threads, p.smem, a.stream>>>(
+        static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
+        p.tiles_per_group, a.out);
+    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+}
+
+template <typename T>
+vq_status launch_general(const Args &a, const Plan &p)
+{
+    vqk::encode_general<T><<<(unsigned)p.blocks, p.threads, 0, a.stream>>>(
+        static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_groups, a.n_per_group,
+        a.n_centroids, a.sub_dim, a.out);
+    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+}
+
+template <typename T>
+vq_status launch_typed(const Args &a, const Plan &p)
+{
+    if (!p.fast) return launch_general<T>(a, p);
+    return a.sub_dim == 4 ? launch_fast<T, 4>(a, p) : launch_fast<T, 8>(a, p);
+}
+
+vq_status run(const Args &a)
+{
+    vq_status s = validate(a, true);
+    if (s != VQ_OK) return s;
+    if (a.n_groups * a.n_per_group == 0) return VQ_OK;
+    const Plan p = make_plan(a);
+    if (p.blocks > 0x7fffffffLL) return VQ_ERR_UNSUPPORTED;
+    switch (a.dtype) {
+    case VQ_F16: return launch_typed<__half>(a, p);
+    case VQ_BF16: return launch_typed<__nv_bfloat16>(a, p);
+    case VQ_F32: return launch_typed<float>(a, p);
+    }
+    return VQ_ERR_INTERNAL;
+}
+
+const char *dtype_name(vq_dtype d)
+{
+    switch (d) {
+    case VQ_F16: return "f16";
+    case VQ_BF16: return "bf16";
+    case VQ_F32: return "f32";
+    }
+    return "?";
+}
+
+}  // namespace
+
+extern "C" {
+
+vq_status vq_encode(const void *x, const void *codebook, int64_t n, int32_t n_centroids,
+                    int32_t sub_dim, vq_dtype dtype, uint32_t *out_idx, vq_stream_t stream)
+{
+    if (n < 0) return VQ_ERR_INVALID_ARG;
+    return run(Args{x, codebook, 1, n, n_centroids, sub_dim, dtype, out_idx,
+                    reinterpret_cast<cudaStream_t>(stream)});
+}
+
+vq_status vq_encode_grouped(const void *x, const void *codebooks, int64_t n_groups,
+                            int64_t n_per_group, int32_t n_centroids, int32_t sub_dim,
+                            vq_dtype dtype, uint32_t *out_idx, vq_stream_t stream)
+{
+    return run(Args{x, codebooks, n_groups, n_per_group, n_centroids, sub_dim, dtype, out_idx,
+                    reinterpret_cast<cudaStream_t>(stream)});
+}
+
+vq_status vq_encode_grouped_host(const void *x_host, const void *codebooks_host,
+                                 int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                                 int32_t sub_dim, vq_dtype dtype, uint32_t *out_host,
+                                 void *x_dev, void *codebooks_dev, uint32_t *out_dev,
+                                 vq_stream_t stream)
+{
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Args a{x_dev, codebooks_dev, n_groups, n_per_group, n_centroids, sub_dim, dtype, out_dev, st};
+    vq_status s = validate(a, true);
+    if (s != VQ_OK) return s;
+    const int64_t rows = n_groups * n_per_group;
+    if (rows == 0) return VQ_OK;
+    if (!x_host || !codebooks_host || !out_host) return VQ_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    const size_t cb_bytes = (size_t)n_groups * n_centroids * sub_dim * es;
+    const size_t x_bytes = (size_t)rows * sub_dim * es;
+    if (cudaMemcpyAsync(codebooks_dev, codebooks_host, cb_bytes, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return VQ_ERR_CUDA;
+    s = run(a);
+    if (s != VQ_OK) return s;
+    if (cudaMemcpyAsync(out_host, out_dev, (size_t)rows * 4, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return VQ_ERR_CUDA;
+    return VQ_OK;
+}
+
+const char *vq_status_string(vq_status status)
+{
+    switch (status) {
+    case VQ_OK: return "VQ_OK: success";
+    case VQ_ERR_INVALID_ARG: return "VQ_ERR_INVALID_ARG: invalid argument";
+    case VQ_ERR_UNSUPPORTED: return "VQ_ERR_UNSUPPORTED: sub_dim or n_centroids not supported";
+    case VQ_ERR_CUDA: return "VQ_ERR_CUDA: a CUDA call or kernel launch failed";
+    case VQ_ERR_INTERNAL: return "VQ_ERR_INTERNAL: internal error";
+    }
+    return "unknown vq_status";
+}
+
+vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                             int32_t sub_dim, vq_dtype dtype, const void *x, char *buf,
+                             int32_t buflen)
+{
+    Args a{x, nullptr, n_groups, n_per_group, n_centroids, sub_dim, dtype, nullptr, nullptr};
+    vq_status s = validate(a, false);
+    if (s != VQ_OK) return s;
+    if (!buf || buflen <= 0) return VQ_ERR_INVALID_ARG;
+    const Plan p = make_plan(a);
+    if (p.fast)
+        snprintf(buf, (size_t)buflen,
+                 "kernel=encode_fast dtype=%s sub_dim=%d rows_per_thread=%d threads=%d "
+                 "argmin=%s centroid_group=%d grid=%lld smem=%zu",
+                 dtype_name(dtype), sub_dim, kRows, kThreads,
+                 kMode == vqk::kDeferred ? "deferred" : "direct", kGroupCentroids,
+                 (long long)p.blocks, p.smem);
+    else
+        snprintf(buf, (size_t)buflen, "kernel=encode_general dtype=%s sub_dim=%d threads=%d grid=%lld",
+                 dtype_name(dtype), sub_dim, p.threads, (long long)p.blocks);
+    return VQ_OK;
+}
+
+int32_t vq_abi_version(void) { return VQ_ENCODE_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,134 @@
+"""The C-ABI library builds, loads and exports what its header declares, and
+rejects bad arguments on the host (no GPU needed; nothing here launches)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from product_vq_kv_gb300.build import build
+
+    path = build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = set()
+    for header in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(header).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(vq_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("vq_encode", "vq_encode_grouped", "vq_encode_grouped_host",
+                     "vq_status_string", "vq_describe_launch", "vq_abi_version"):
+        assert required in names
+
+
+@pytest.mark.parametrize("name", declared_functions())
+def test_library_exports_every_declared_function(lib, name):
+    assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_abi_version(lib):
+    lib.vq_abi_version.restype = ctypes.c_int32
+    assert lib.vq_abi_version() == 1
+
+
+def test_status_strings(lib):
+    lib.vq_status_string.restype = ctypes.c_char_p
+    lib.vq_status_string.argtypes = [ctypes.c_int32]
+    for code, word in enumerate(["VQ_OK", "VQ_ERR_INVALID_ARG", "VQ_ERR_UNSUPPORTED",
+                                 "VQ_ERR_CUDA", "VQ_ERR_INTERNAL"]):
+        assert lib.vq_status_string(code).decode().startswith(word)
+    assert lib.vq_status_string(99).decode() == "unknown vq_status"
+
+
+def _encode(lib):
+    f = lib.vq_encode
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                  ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    return f
+
+
+def _grouped(lib):
+    f = lib.vq_encode_grouped
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                  ctypes.c_void_p]
+    return f
+
+
+# Fake, never-dereferenced device addresses: every case below fails (or
+# succeeds with no work) during host-side validation, before any CUDA call.
+P = 0x10000
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, P, 10, 256, 4, 0, P, None), 1),     # null x with work to do
+    ((P, None, 10, 256, 4, 0, P, None), 1),     # null codebook
+    ((P, P, 10, 256, 4, 0, None, None), 1),     # null output
+    ((P, P, -1, 256, 4, 0, P, None), 1),        # negative N
+    ((P, P, 10, 256, 4, 3, P, None), 1),        # unknown dtype
+    ((P, P, 10, 256, 4, -1, P, None), 1),       # unknown dtype
+    ((P + 1, P, 10, 256, 4, 0, P, None), 1),    # x not aligned to its element
+    ((P, P, 10, 256, 4, 0, P + 2, None), 1),    # output not aligned to 4 bytes
+    ((P, P, 10, 256, 0, 0, P, None), 2),        # sub_dim 0
+    ((P, P, 10, 256, 33, 0, P, None), 2),       # sub_dim too large
+    ((P, P, 10, 0, 4, 0, P, None), 2),          # no centroids
+    ((P, P, 10, 4097, 4, 0, P, None), 2),       # too many centroids
+    ((None, None, 0, 256, 4, 0, None, None), 0),  # N = 0: nothing to do
+])
+def test_encode_argument_errors(lib, args, status):
+    assert _encode(lib)(*args) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((P, P, -1, 10, 256, 8, 0, P, None), 1),    # negative group count
+    ((P, P, 4, -10, 256, 8, 0, P, None), 1),    # negative group size
+    ((P, P, 1 << 40, 1 << 40, 256, 8, 0, P, None), 1),  # row count overflows
+    ((None, None, 4, 0, 256, 8, 0, None, None), 0),     # empty groups
+    ((None, None, 0, 100, 256, 8, 0, None, None), 0),   # no groups
+])
+def test_grouped_argument_errors(lib, args, status):
+    assert _grouped(lib)(*args) == status
+
+
+def test_describe_launch_picks_kernels(lib):
+    f = lib.vq_describe_launch
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int32]
+    buf = ctypes.create_string_buffer(512)
+    assert f(1, 1 << 20, 256, 4, 0, P, buf, 512) == 0
+    assert buf.value.decode().startswith("kernel=encode_fast")
+    assert f(256, 131072, 256, 8, 0, P, buf, 512) == 0
+    assert buf.value.decode().startswith("kernel=encode_fast")
+    assert f(1, 1000, 256, 5, 0, P, buf, 512) == 0          # odd sub_dim
+    assert buf.value.decode().startswith("kernel=encode_general")
+    assert f(1, 1000, 256, 4, 0, P + 2, buf, 512) == 0      # x not 8-byte aligned
+    assert buf.value.decode().startswith("kernel=encode_general")
+    assert f(1, 1000, 4096, 8, 0, P, buf, 512) == 0         # codebook too big for smem
+    assert buf.value.decode().startswith("kernel=encode_general")
+    assert f(1, 1000, 256, 0, 0, P, buf, 512) == 2
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import product_vq_kv_gb300._binding as b
+
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        b.load_library()
