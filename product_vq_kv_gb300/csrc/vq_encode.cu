@@ -107,7 +107,7 @@ vq_status launch_fast(const Args &a, const Plan &p)
     }
     kernel<<<(unsigned)p.blocks, p.threads, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
-        p.tiles_per_group, a.out);
+        p.tiles_per_group, 1.0f, a.out);
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
@@ -116,7 +116,7 @@ vq_status launch_general(const Args &a, const Plan &p)
 {
     vqk::encode_general<T><<<(unsigned)p.blocks, p.threads, 0, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_groups, a.n_per_group,
-        a.n_centroids, a.sub_dim, a.out);
+        a.n_centroids, a.sub_dim, 1.0f, a.out);
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 

@@ -16,7 +16,10 @@
 //  * Each thread owns R sub-vectors, held in registers as R/2 packed pairs.
 //    One packed f32x2 add / multiply evaluates the same centroid against two
 //    sub-vectors at once; each lane rounds exactly like the scalar fp32 op
-//    (add.rn / mul.rn, no contraction), so the result is bit-identical.
+//    (see "Exact fp32 arithmetic" below for how contraction into an FMA is
+//    ruled out), so the result is bit-identical.  Packed ops issue at half the rate of scalar
+//    ones (same FP32 lane throughput) but halve the issue slots taken, which
+//    leaves room for the argmin's compare/select work on the ALU pipe.
 //  * x is read with 8/16-byte vector loads in a coalesced pattern (thread t
 //    of a block owns rows t, t+THREADS, ...); indices leave with coalesced
 //    32-bit streaming stores.  Nothing but x, the codebooks and the indices
@@ -104,33 +107,112 @@ __device__ __forceinline__ float min3(float a, float b, float c)
     return r;
 }
 
-// Squared distances of one centroid (negated, duplicated: nc[i] = (-c_i, -c_i))
-// to the two sub-vectors packed in xp[i] = (x_i, x'_i).  Ascending i; every
-// add and multiply rounds to nearest on its own.
-template <int SUB>
-__device__ __forceinline__ float2 pair_dist(const float2 (&xp)[SUB], const float2 (&nc)[SUB])
+// Exact fp32 arithmetic.
+//
+// The distance needs the square and the running sum rounded separately.
+// ptxas contracts a packed mul.rn.f32x2 whose only use is an add.rn.f32x2
+// into one fused multiply-add, whatever the rounding modifiers and the -fmad
+// setting say, which changes the last bit of about one distance in ten.  So
+// the running sum is never written as an add of a product: it is
+//     acc = fma.rn(one, sq, acc)
+// where `one` is 1.0 passed in as a kernel argument.  1 * sq is exact, so
+// this is exactly one rounding of acc + sq (the add), and because `one` is
+// unknown when the kernel is compiled the optimiser can neither turn it back
+// into an add nor fold the multiply that produced sq into it.  The subtract
+// and the square are plain round-to-nearest packed operations; packed forms
+// round each lane exactly like the scalar instruction, so one lane of a
+// packed distance is bit-identical to the scalar distance below.
+
+__device__ __forceinline__ float add_rn(float a, float b)
 {
-    float2 d = __fadd2_rn(xp[0], nc[0]);
-    float2 acc = __fmul2_rn(d, d);
+    float r;
+    asm("add.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float mul_rn(float a, float b)
+{
+    float r;
+    asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float fma_rn(float a, float b, float c)
+{
+    float r;
+    asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "add.rn.f32x2 pd, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "mov.b64 pc, {%6, %7};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pc;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// Squared distances of one centroid (negated, duplicated: nc[i] = (-c_i, -c_i))
+// to the two sub-vectors packed in xp[i] = (x_i, x'_i).  Ascending i; the
+// subtract, the square and the sum each round to nearest on their own.
+// `one` must hold (1.0f, 1.0f) (see above).
+template <int SUB>
+__device__ __forceinline__ float2 pair_dist(const float2 (&xp)[SUB], const float2 (&nc)[SUB],
+                                            float2 one)
+{
+    float2 d = add2_rn(xp[0], nc[0]);
+    float2 acc = mul2_rn(d, d);
 #pragma unroll
     for (int i = 1; i < SUB; ++i) {
-        d = __fadd2_rn(xp[i], nc[i]);
-        acc = __fadd2_rn(acc, __fmul2_rn(d, d));
+        d = add2_rn(xp[i], nc[i]);
+        acc = fma2_rn(one, mul2_rn(d, d), acc);
     }
     return acc;
 }
 
 // The same distance for one sub-vector, scalar.  Bit-identical to one lane
-// of pair_dist.
+// of pair_dist.  `one` must be 1.0f.
 template <int SUB>
-__device__ __forceinline__ float one_dist(const float (&x)[SUB], const float (&nc)[SUB])
+__device__ __forceinline__ float one_dist(const float (&x)[SUB], const float (&nc)[SUB], float one)
 {
-    float d = __fadd_rn(x[0], nc[0]);
-    float acc = __fmul_rn(d, d);
+    float d = add_rn(x[0], nc[0]);
+    float acc = mul_rn(d, d);
 #pragma unroll
     for (int i = 1; i < SUB; ++i) {
-        d = __fadd_rn(x[i], nc[i]);
-        acc = __fadd_rn(acc, __fmul_rn(d, d));
+        d = add_rn(x[i], nc[i]);
+        acc = fma_rn(one, mul_rn(d, d), acc);
     }
     return acc;
 }
@@ -200,14 +282,15 @@ __device__ __forceinline__ void read_centroid_scalar(const float4 *__restrict__ 
 // ------------------------------------------------------------------ fast kernel
 
 // Launch: grid.x = n_groups * tiles_per_group, block = THREADS; dynamic shared
-// memory = CbLayout<SUB, GC>::bytes(n_centroids).  Block b encodes tile
+// memory = CbLayout<SUB, GC>::bytes(n_centroids); `one` = 1.0f.  Block b encodes tile
 // (b % tiles_per_group) of group (b / tiles_per_group); a tile is THREADS * R
 // consecutive rows of that group.  Requires x aligned to SUB * sizeof(T)
 // bytes (16 bytes at most), 1 <= n_centroids and the shared memory to fit.
 template <typename T, int SUB, int R, int THREADS, int MODE, int GC>
 __global__ void __launch_bounds__(THREADS)
     encode_fast(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
-                int32_t n_centroids, int64_t tiles_per_group, uint32_t *__restrict__ out)
+                int32_t n_centroids, int64_t tiles_per_group, float one,
+                uint32_t *__restrict__ out)
 {
     static_assert(R % 2 == 0, "rows per thread come in packed pairs");
     static_assert(SUB % 2 == 0, "sub_dim must be even for the packed layout");
@@ -250,6 +333,7 @@ __global__ void __launch_bounds__(THREADS)
     __syncthreads();
 
     const int n_cgroups = L::groups(n_centroids);
+    const float2 one2 = make_float2(one, one);
     uint32_t result[R];
 
     if constexpr (MODE == kDirect) {
@@ -268,7 +352,7 @@ __global__ void __launch_bounds__(THREADS)
                 const uint32_t cid = (uint32_t)(cg * GC + cc);
 #pragma unroll
                 for (int rp = 0; rp < R / 2; ++rp) {
-                    const float2 dd = pair_dist<SUB>(xp[rp], nc);
+                    const float2 dd = pair_dist<SUB>(xp[rp], nc, one2);
                     if (dd.x < best[2 * rp]) {
                         best[2 * rp] = dd.x;
                         result[2 * rp] = cid;
@@ -298,8 +382,8 @@ __global__ void __launch_bounds__(THREADS)
                 read_centroid<SUB>(gp + (cc + 1) * L::kF4PerCentroid, nb);
 #pragma unroll
                 for (int rp = 0; rp < R / 2; ++rp) {
-                    const float2 da = pair_dist<SUB>(xp[rp], na);
-                    const float2 db = pair_dist<SUB>(xp[rp], nb);
+                    const float2 da = pair_dist<SUB>(xp[rp], na, one2);
+                    const float2 db = pair_dist<SUB>(xp[rp], nb, one2);
                     run[2 * rp] = min3(run[2 * rp], da.x, db.x);
                     run[2 * rp + 1] = min3(run[2 * rp + 1], da.y, db.y);
                 }
@@ -324,7 +408,7 @@ __global__ void __launch_bounds__(THREADS)
                 for (int cc = GC - 1; cc >= 0; --cc) {
                     float nc[SUB];
                     read_centroid_scalar<SUB>(gp + cc * L::kF4PerCentroid, nc);
-                    if (one_dist<SUB>(xr, nc) == run[r]) id = (uint32_t)(win[r] * GC + cc);
+                    if (one_dist<SUB>(xr, nc, one) == run[r]) id = (uint32_t)(win[r] * GC + cc);
                 }
             }
             result[r] = id;
@@ -343,11 +427,11 @@ __global__ void __launch_bounds__(THREADS)
 // Any sub_dim, any n_centroids, x and codebooks aligned to their element
 // size only: one thread per row, scalar fp32 arithmetic, x and the codebook
 // read through the read-only cache.
-// Launch: grid.x = ceil(n_groups * n_per_group / blockDim.x).
+// Launch: grid.x = ceil(n_groups * n_per_group / blockDim.x); `one` = 1.0f.
 template <typename T>
 __global__ void encode_general(const T *__restrict__ x, const T *__restrict__ codebooks,
                                int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
-                               int32_t sub_dim, uint32_t *__restrict__ out)
+                               int32_t sub_dim, float one, uint32_t *__restrict__ out)
 {
     const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (row >= n_groups * n_per_group) return;
@@ -358,11 +442,11 @@ __global__ void encode_general(const T *__restrict__ x, const T *__restrict__ co
     uint32_t idx = 0;
     for (int32_t c = 0; c < n_centroids; ++c) {
         const T *__restrict__ cr = cb + (size_t)c * sub_dim;
-        float d = __fsub_rn(widen(__ldg(xr)), widen(__ldg(cr)));
-        float acc = __fmul_rn(d, d);
+        float d = add_rn(widen(__ldg(xr)), -widen(__ldg(cr)));
+        float acc = mul_rn(d, d);
         for (int32_t i = 1; i < sub_dim; ++i) {
-            d = __fsub_rn(widen(__ldg(xr + i)), widen(__ldg(cr + i)));
-            acc = __fadd_rn(acc, __fmul_rn(d, d));
+            d = add_rn(widen(__ldg(xr + i)), -widen(__ldg(cr + i)));
+            acc = fma_rn(one, mul_rn(d, d), acc);
         }
         if (acc < best) {
             best = acc;
