@@ -10,16 +10,24 @@
 #include <cstring>
 
 #include "vq_encode.h"
+#include "vq_filter.cuh"
 #include "vq_kernels.cuh"
 
 namespace {
 
-// Tuning of the fast kernels (rows per thread, threads per block, argmin
-// strategy, centroids per group).
+// Tuning of the exact brute-force kernel (rows per thread, threads per block,
+// argmin strategy, centroids per group).
 constexpr int kThreads = 128;
 constexpr int kRows = 8;
 constexpr int kMode = vqk::kDeferred;
 constexpr int kGroupCentroids = 8;
+// Tuning of the filter-and-refine kernel.
+constexpr int kFThreads = 128;
+constexpr int kFRows = 8;
+constexpr int kFGroup = 16;
+// Codebooks smaller than this many centroids are brute-forced: screening pays
+// off only with several centroid groups to rule out.
+constexpr int kFilterMinCentroids = 4 * kFGroup;
 
 constexpr int kMaxSubDim = 32;
 constexpr int kMaxCentroids = 4096;
@@ -59,8 +67,10 @@ vq_status validate(const Args &a, bool need_pointers)
     return VQ_OK;
 }
 
+enum KernelKind { kGeneral = 0, kBrute = 1, kFilter = 2 };
+
 struct Plan {
-    bool fast;
+    KernelKind kind;
     size_t smem;
     int64_t tiles_per_group;
     int64_t blocks;
@@ -73,20 +83,33 @@ size_t fast_smem(int32_t n_centroids)
     return vqk::CbLayout<SUB, kGroupCentroids>::bytes(n_centroids);
 }
 
+template <int SUB>
+size_t filter_smem(int32_t n_centroids)
+{
+    return vqk::FilterLayout<SUB, kFGroup>::bytes(n_centroids, kFThreads * kFRows);
+}
+
 Plan make_plan(const Args &a)
 {
     Plan p{};
     const size_t es = elem_size(a.dtype);
     const size_t row_bytes = (size_t)a.sub_dim * es;
     const size_t align = row_bytes < 16 ? row_bytes : 16;
-    const bool shape_ok = a.sub_dim == 4 || a.sub_dim == 8;
-    if (shape_ok) p.smem = a.sub_dim == 4 ? fast_smem<4>(a.n_centroids) : fast_smem<8>(a.n_centroids);
-    p.fast = shape_ok && p.smem <= kMaxFastSmem && ((uintptr_t)a.x % align == 0);
-    if (p.fast) {
-        const int64_t tile = (int64_t)kThreads * kRows;
+    const bool shape_ok = (a.sub_dim == 4 || a.sub_dim == 8) && ((uintptr_t)a.x % align == 0);
+    p.kind = kGeneral;
+    if (shape_ok && a.n_centroids >= kFilterMinCentroids) {
+        p.smem = a.sub_dim == 4 ? filter_smem<4>(a.n_centroids) : filter_smem<8>(a.n_centroids);
+        if (p.smem <= kMaxFastSmem) p.kind = kFilter;
+    }
+    if (shape_ok && p.kind == kGeneral) {
+        p.smem = a.sub_dim == 4 ? fast_smem<4>(a.n_centroids) : fast_smem<8>(a.n_centroids);
+        if (p.smem <= kMaxFastSmem) p.kind = kBrute;
+    }
+    if (p.kind != kGeneral) {
+        const int64_t tile = p.kind == kFilter ? (int64_t)kFThreads * kFRows : (int64_t)kThreads * kRows;
         p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
         p.blocks = a.n_groups * p.tiles_per_group;
-        p.threads = kThreads;
+        p.threads = p.kind == kFilter ? kFThreads : kThreads;
     } else {
         p.smem = 0;
         p.tiles_per_group = 0;
@@ -94,6 +117,21 @@ Plan make_plan(const Args &a)
         p.threads = kGeneralThreads;
     }
     return p;
+}
+
+template <typename T, int SUB>
+vq_status launch_filter(const Args &a, const Plan &p)
+{
+    auto kernel = vqk::encode_filter<T, SUB, kFRows, kFThreads, kFGroup>;
+    if (p.smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)p.smem) != cudaSuccess)
+            return VQ_ERR_CUDA;
+    }
+    kernel<<<(unsigned)p.blocks, p.threads, p.smem, a.stream>>>(
+        static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
+        p.tiles_per_group, 1.0f, a.out);
+    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
 template <typename T, int SUB>
@@ -123,8 +161,12 @@ vq_status launch_general(const Args &a, const Plan &p)
 template <typename T>
 vq_status launch_typed(const Args &a, const Plan &p)
 {
-    if (!p.fast) return launch_general<T>(a, p);
-    return a.sub_dim == 4 ? launch_fast<T, 4>(a, p) : launch_fast<T, 8>(a, p);
+    switch (p.kind) {
+    case kFilter: return a.sub_dim == 4 ? launch_filter<T, 4>(a, p) : launch_filter<T, 8>(a, p);
+    case kBrute: return a.sub_dim == 4 ? launch_fast<T, 4>(a, p) : launch_fast<T, 8>(a, p);
+    case kGeneral: return launch_general<T>(a, p);
+    }
+    return VQ_ERR_INTERNAL;
 }
 
 vq_status run(const Args &a)
@@ -222,7 +264,13 @@ vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_ce
     if (s != VQ_OK) return s;
     if (!buf || buflen <= 0) return VQ_ERR_INVALID_ARG;
     const Plan p = make_plan(a);
-    if (p.fast)
+    if (p.kind == kFilter)
+        snprintf(buf, (size_t)buflen,
+                 "kernel=encode_filter dtype=%s sub_dim=%d rows_per_thread=%d threads=%d "
+                 "centroid_group=%d grid=%lld smem=%zu",
+                 dtype_name(dtype), sub_dim, kFRows, kFThreads, kFGroup, (long long)p.blocks,
+                 p.smem);
+    else if (p.kind == kBrute)
         snprintf(buf, (size_t)buflen,
                  "kernel=encode_fast dtype=%s sub_dim=%d rows_per_thread=%d threads=%d "
                  "argmin=%s centroid_group=%d grid=%lld smem=%zu",

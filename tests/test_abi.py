@@ -113,8 +113,12 @@ def test_describe_launch_picks_kernels(lib):
                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int32]
     buf = ctypes.create_string_buffer(512)
     assert f(1, 1 << 20, 256, 4, 0, P, buf, 512) == 0
-    assert buf.value.decode().startswith("kernel=encode_fast")
+    assert buf.value.decode().startswith("kernel=encode_filter")
     assert f(256, 131072, 256, 8, 0, P, buf, 512) == 0
+    assert buf.value.decode().startswith("kernel=encode_filter")
+    assert f(1, 1000, 32, 8, 0, P, buf, 512) == 0           # small codebook: brute force
+    assert buf.value.decode().startswith("kernel=encode_fast")
+    assert f(1, 1000, 4096, 4, 0, P, buf, 512) == 0         # filter layout too big: brute force
     assert buf.value.decode().startswith("kernel=encode_fast")
     assert f(1, 1000, 256, 5, 0, P, buf, 512) == 0          # odd sub_dim
     assert buf.value.decode().startswith("kernel=encode_general")

@@ -1,0 +1,134 @@
+"""GPU parity of the filter-and-refine encoder on inputs built to stress it.
+
+The filter screens centroids with a fused multiply-add score and re-evaluates
+the exact formula only inside the centroid groups its error bound cannot rule
+out; rows with three or more such groups, or with non-finite or huge values,
+go to an exact per-block queue.  These cases put the deciding difference at
+the last bit of the fp32 distance, spread tied centroids over several groups,
+and push rows into the queue, and every index must still equal the oracle's.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+THREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def vq():
+    from product_vq_kv_gb300.build import build
+
+    build()
+    import product_vq_kv_gb300 as m
+
+    m.load_library()
+    return m
+
+
+def run(vq, x, cb):
+    xd, cbd = torch.from_numpy(np.ascontiguousarray(x)).cuda(), torch.from_numpy(cb).cuda()
+    desc = vq.vq_describe_launch(x.shape[0], x.shape[1], cb.shape[1], x.shape[2],
+                                 xd.dtype, xd.data_ptr())
+    out = vq.vq_encode_grouped(xd, cbd)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), desc
+
+
+def check(vq, oracle_mod, x, cb, kernel="encode_filter"):
+    got, desc = run(vq, x, cb)
+    assert desc.startswith("kernel=" + kernel), desc
+    want = oracle_mod.encode(x, cb, n_threads=THREADS)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
+
+
+@pytest.mark.parametrize("sub_dim", [4, 8])
+def test_permuted_coordinate_ties(vq, oracle_mod, sub_dim):
+    """Rows x = (a, a, b, b, ...) are exactly equidistant (in real arithmetic)
+    from a centroid and its copy with coordinates swapped pairwise; the fp32
+    sums differ only by rounding order, so the winner is decided at the last
+    bit.  The swapped copies sit in other centroid groups."""
+    rng = np.random.default_rng(11 + sub_dim)
+    n_c, m = 256, 20000
+    half = n_c // 2
+    base = rng.standard_normal((half, sub_dim)).astype(np.float16)
+    swapped = base.reshape(half, sub_dim // 2, 2)[:, :, ::-1].reshape(half, sub_dim)
+    cb = np.empty((n_c, sub_dim), np.float16)
+    cb[0::2] = base          # centroid 2k
+    cb[1::2] = swapped       # centroid 2k+1, same group
+    perm = rng.permutation(n_c)
+    cb = cb[perm]            # scatter the partners over all groups
+    pairs = rng.standard_normal((m, sub_dim // 2)).astype(np.float16)
+    x = np.repeat(pairs, 2, axis=1)  # (a, a, b, b, ...)
+    check(vq, oracle_mod, x[None], cb[None])
+
+
+@pytest.mark.parametrize("copies", [2, 3, 5])
+def test_duplicated_centroids_across_groups(vq, oracle_mod, copies):
+    """Exact duplicate centroids in `copies` different groups: with three or
+    more, rows near them take the exact queue."""
+    rng = np.random.default_rng(20 + copies)
+    n_c, sub = 256, 8
+    cb = rng.standard_normal((n_c, sub)).astype(np.float16)
+    for src in range(0, 40, 4):
+        for k in range(1, copies):
+            cb[(src + 37 * k) % n_c] = cb[src]
+    src = rng.integers(0, n_c, 30000)
+    x = cb[src].astype(np.float32)
+    x += rng.standard_normal(x.shape).astype(np.float32) * 0.05
+    check(vq, oracle_mod, x.astype(np.float16)[None], cb[None])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_extreme_magnitudes(vq, oracle_mod, dtype):
+    """Huge rows (queued: the bound would be near overflow) and tiny rows
+    (gradual underflow; the bound's absolute term) next to ordinary ones."""
+    rng = np.random.default_rng(5)
+    sub, n_c = 4, 256
+    cb = rng.standard_normal((n_c, sub)).astype(np.float32)
+    x = rng.standard_normal((6000, sub)).astype(np.float32)
+    x[:1000] *= 1e25
+    x[1000:2000] *= 1e-30
+    cb[:8] *= 1e-30
+    if dtype == "bf16":
+        xt = torch.from_numpy(x).to(torch.bfloat16)
+        ct = torch.from_numpy(cb).to(torch.bfloat16)
+        got = None
+        desc = vq.vq_describe_launch(1, x.shape[0], n_c, sub, torch.bfloat16, xt.cuda().data_ptr())
+        assert desc.startswith("kernel=encode_filter")
+        got = vq.vq_encode(xt.cuda(), ct.cuda()).cpu().numpy()
+        want = oracle_mod.encode(xt.view(torch.int16).numpy().view(np.uint16),
+                                 ct.view(torch.int16).numpy().view(np.uint16), bf16=True,
+                                 n_threads=THREADS)
+        assert np.array_equal(got, want)
+    else:
+        check(vq, oracle_mod, x[None], cb[None])
+
+
+def test_codebook_with_nan_queues_every_row(vq, oracle_mod):
+    rng = np.random.default_rng(6)
+    cb = rng.standard_normal((300, 4)).astype(np.float16)
+    cb[123, 2] = np.nan
+    x = rng.standard_normal((5000, 4)).astype(np.float16)
+    check(vq, oracle_mod, x[None], cb[None])
+
+
+@pytest.mark.parametrize("n_c", [63, 64, 65, 100, 512, 2000])
+def test_codebook_sizes_around_the_groups(vq, oracle_mod, n_c):
+    rng = np.random.default_rng(n_c)
+    x = rng.standard_normal((2, 3000, 4)).astype(np.float16)
+    cb = rng.standard_normal((2, n_c, 4)).astype(np.float16)
+    check(vq, oracle_mod, x, cb, kernel="encode_filter" if n_c >= 64 else "encode_fast")
+
+
+def test_clustered_keys_near_many_centroids(vq, oracle_mod):
+    """Keys concentrated near the origin, where many centroids are at similar
+    distances: more candidate groups per row."""
+    rng = np.random.default_rng(8)
+    cb = (rng.standard_normal((256, 8)) * 0.01).astype(np.float16)
+    x = (rng.standard_normal((20000, 8)) * 0.01).astype(np.float16)
+    check(vq, oracle_mod, x[None], cb[None])
