@@ -38,6 +38,13 @@ UNIT = "sub-vectors/s"
 # D=256, sub_dim 4, 256 centroids, N = 1,048,576): 7.98 ms per call on an
 # Apple M-series GPU -> 131.4 M sub-vectors/s.  Context only (other hardware).
 PAGES_FALCON_SUBVEC_PER_S = 1_048_576 / 7.98e-3
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture, keyed by the exact launch description it was taken on; a
+# kernel that has changed since reports null (see profiles/).
+MEASURED_TRAFFIC = {
+    "kernel=encode_filter dtype=f16 sub_dim=4 rows_per_thread=8 threads=128 "
+    "centroid_group=16 grid=1024 smem=18712": 8_446_720,
+}
 L2_FLUSH_BYTES = 256 << 20
 FP32_LANES_PER_SM = 128
 CLOCK_REASON_BITS = {
@@ -299,6 +306,8 @@ def bench_ours(args) -> None:
 
     props = torch.cuda.get_device_properties(dev)
     peaks = measured_peaks()
+    desc = vq.vq_describe_launch(x.shape[0], x.shape[1], cb.shape[1], x.shape[2], torch.float16,
+                                 xd.data_ptr())
     clk = clocks.summary()
     sm_max = peaks.get("sm_max_mhz") or clk["sm_max_mhz"] or 2070.0
     peak_tflops = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
@@ -307,9 +316,8 @@ def bench_ours(args) -> None:
     achieved = flops_per_subvector(w) * units / (kernel_ms * 1e-3) / 1e12
     roofline = {
         "bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
-        "frac": achieved / peak_tflops, "traffic": None,
-        "kernel": vq.vq_describe_launch(x.shape[0], x.shape[1], cb.shape[1], x.shape[2],
-                                        torch.float16, xd.data_ptr()),
+        "frac": achieved / peak_tflops, "traffic": MEASURED_TRAFFIC.get(desc),
+        "kernel": desc,
         "flops_per_unit": flops_per_subvector(w), "units_per_launch": units,
         "peak_basis": f"{props.multi_processor_count} SMs x {FP32_LANES_PER_SM} FP32 lanes x "
                       f"2 (FMA) x {sm_max:.0f} MHz",
