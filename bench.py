@@ -339,7 +339,8 @@ def bench_ours(args) -> None:
         "e2e": {"value": units * world * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": x.nbytes + cb.nbytes,
                 "d2h_bytes_per_step": int(units * 4),
-                "path": "vq_encode_grouped_host (pinned host buffers, copies inside)"},
+                "path": "vq_encode_grouped_host with pinned host buffers: the kernel reads x and "
+                        "writes the indices across the CPU-GPU link; codebooks copied"},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, x, cb)

@@ -96,18 +96,21 @@ vq_status vq_encode_grouped(const void *x, const void *codebooks, int64_t n_grou
 
 /*
  * vq_encode_grouped_host -- the same encode for inputs and outputs in HOST
- * memory.  The library copies x and the codebooks to the caller's device
- * buffers, encodes, and copies the indices back, in chunks on `stream` so
- * that copies overlap the encode of neighbouring chunks.
- *   x_host, codebooks_host, out_host    host memory (pinned memory gives
- *                                       asynchronous copies; pageable memory
- *                                       works but serialises)
+ * memory; returns once out_host holds the indices (it synchronises `stream`).
+ *   x_host, codebooks_host, out_host    host memory, same layouts as above
  *   x_dev        >= n_groups*n_per_group*sub_dim elements, device, scratch
  *   codebooks_dev >= n_groups*n_centroids*sub_dim elements, device, scratch
  *   out_dev      >= n_groups*n_per_group uint32, device, scratch
- * The call returns once out_host holds the result (it synchronises
- * `stream`).  The device buffers are the caller's; the library allocates
- * nothing.
+ * If x_host and out_host are page-locked (pinned) memory the GPU can address,
+ * the kernel reads x and writes the indices directly across the CPU-GPU link
+ * (on GB300 the coherent NVLink-C2C) while it computes: only the codebooks
+ * are copied (to codebooks_dev), and x_dev / out_dev are not touched.
+ * Otherwise x is copied to x_dev and the indices back from out_dev, in chunks
+ * on two internal copy streams that overlap the encode of neighbouring chunks
+ * when the input is large.  The internal streams and events are created on
+ * the first such call on a device and kept until exit; host calls on one
+ * device are serialised by a lock.  The device buffers are the caller's; the
+ * library allocates no memory.
  */
 vq_status vq_encode_grouped_host(const void *x_host, const void *codebooks_host,
                                  int64_t n_groups, int64_t n_per_group, int32_t n_centroids,

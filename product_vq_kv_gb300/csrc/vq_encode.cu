@@ -6,8 +6,10 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "vq_encode.h"
 #include "vq_filter.cuh"
@@ -194,6 +196,54 @@ const char *dtype_name(vq_dtype d)
     return "?";
 }
 
+// Per-device copy streams and events of the host entry point's copy path,
+// created on the first such call on a device and kept until exit.  The mutex
+// serialises host calls on one device, which share them.
+constexpr int kMaxDevices = 64;
+constexpr int kHostChunks = 4;
+constexpr int kHostEvents = 8;
+// A chunk must fill the GPU several times over, or its encode runs below
+// full occupancy and the overlap gains nothing.
+constexpr int64_t kHostChunkMinRows = int64_t(1) << 22;
+
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t loaded[kHostEvents] = {}, encoded[kHostEvents] = {}, copied[kHostEvents] = {};
+
+    vq_status init()
+    {
+        const unsigned ev_flags = cudaEventDisableTiming;
+        bool ok = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&start, ev_flags) == cudaSuccess;
+        for (int i = 0; ok && i < kHostEvents; ++i)
+            ok = cudaEventCreateWithFlags(&loaded[i], ev_flags) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&encoded[i], ev_flags) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&copied[i], ev_flags) == cudaSuccess;
+        ready = ok;
+        return ok ? VQ_OK : VQ_ERR_CUDA;
+    }
+};
+
+HostPipe host_pipes[kMaxDevices];
+
+// The device-side address of a host pointer, if the GPU can access it
+// (page-locked host memory on a unified-address system).
+bool device_view(const void *p, void **dptr)
+{
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // not a CUDA-known pointer: clear the non-sticky error
+        return false;
+    }
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return false;
+    *dptr = at.devicePointer;
+    return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,18 +279,84 @@ vq_status vq_encode_grouped_host(const void *x_host, const void *codebooks_host,
     if (!x_host || !codebooks_host || !out_host) return VQ_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     const size_t cb_bytes = (size_t)n_groups * n_centroids * sub_dim * es;
-    const size_t x_bytes = (size_t)rows * sub_dim * es;
-    if (cudaMemcpyAsync(codebooks_dev, codebooks_host, cb_bytes, cudaMemcpyHostToDevice, st) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return VQ_ERR_CUDA;
-    s = run(a);
-    if (s != VQ_OK) return s;
-    if (cudaMemcpyAsync(out_host, out_dev, (size_t)rows * 4, cudaMemcpyDeviceToHost, st) !=
-            cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return VQ_ERR_CUDA;
-    return VQ_OK;
+
+    // Pinned (page-locked, mapped) host buffers are addressable by the GPU: on
+    // GB300 the kernel then reads x and writes the indices across the
+    // coherent CPU-GPU link while it computes, with no staging copies.  Only
+    // the codebooks (a few KiB per group) are copied to the device.
+    void *x_view = nullptr, *out_view = nullptr;
+    if (device_view(x_host, &x_view) && device_view(out_host, &out_view)) {
+        if (cudaMemcpyAsync(codebooks_dev, codebooks_host, cb_bytes, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess)
+            return VQ_ERR_CUDA;
+        Args z{x_view, codebooks_dev, n_groups, n_per_group, n_centroids, sub_dim, dtype,
+               static_cast<uint32_t *>(out_view), st};
+        s = run(z);
+        if (s != VQ_OK) return s;
+        return cudaStreamSynchronize(st) == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+    }
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VQ_ERR_CUDA;
+    HostPipe &hp = host_pipes[dev];
+    std::lock_guard<std::mutex> guard(hp.mu);
+    if (!hp.ready && (s = hp.init()) != VQ_OK) return s;
+
+    const size_t row_bytes = (size_t)sub_dim * es;
+    const size_t cb_group_bytes = (size_t)n_centroids * sub_dim * es;
+    const char *xh = static_cast<const char *>(x_host);
+    char *xd = static_cast<char *>(x_dev);
+    const char *cbd = static_cast<const char *>(codebooks_dev);
+
+    // Chunks: whole groups when there are many, else equal row ranges of each
+    // group; never smaller than kHostChunkMinRows rows.
+    const int64_t want = std::max<int64_t>(1, std::min<int64_t>(kHostChunks, rows / kHostChunkMinRows));
+    const int64_t groups_per_chunk = n_groups >= want ? (n_groups + want - 1) / want : 1;
+    const int64_t splits = n_groups >= want ? 1 : (want + n_groups - 1) / n_groups;
+    const int64_t rows_per_split = (n_per_group + splits - 1) / splits;
+
+    // The copy streams must not overwrite device buffers still in use by work
+    // already queued on the caller's stream.
+    bool ok = cudaEventRecord(hp.start, st) == cudaSuccess &&
+              cudaStreamWaitEvent(hp.h2d, hp.start, 0) == cudaSuccess &&
+              cudaMemcpyAsync(codebooks_dev, codebooks_host, cb_bytes, cudaMemcpyHostToDevice,
+                              hp.h2d) == cudaSuccess;
+    int ci = 0;
+    for (int64_t g0 = 0; ok && g0 < n_groups; g0 += groups_per_chunk) {
+        const int64_t ng = std::min(groups_per_chunk, n_groups - g0);
+        for (int64_t r0 = 0; ok && r0 < n_per_group; r0 += rows_per_split) {
+            const int64_t nr = std::min(rows_per_split, n_per_group - r0);
+            const int slot = ci % kHostEvents;
+            // rows [g0*M + r0, ...): with splits == 1 the chunk is ng whole groups
+            const int64_t first = g0 * n_per_group + r0;
+            const int64_t count = splits == 1 ? ng * n_per_group : nr;
+            if (ci >= kHostEvents)  // slot reuse: its previous copy back must be done
+                ok = cudaEventSynchronize(hp.copied[slot]) == cudaSuccess;
+            ok = ok &&
+                 cudaMemcpyAsync(xd + first * row_bytes, xh + first * row_bytes,
+                                 (size_t)count * row_bytes, cudaMemcpyHostToDevice,
+                                 hp.h2d) == cudaSuccess &&
+                 cudaEventRecord(hp.loaded[slot], hp.h2d) == cudaSuccess &&
+                 cudaStreamWaitEvent(st, hp.loaded[slot], 0) == cudaSuccess;
+            if (!ok) break;
+            Args c{xd + first * row_bytes, cbd + g0 * cb_group_bytes, splits == 1 ? ng : 1,
+                   splits == 1 ? n_per_group : nr, n_centroids, sub_dim, dtype, out_dev + first, st};
+            s = run(c);
+            if (s != VQ_OK) return s;
+            ok = cudaEventRecord(hp.encoded[slot], st) == cudaSuccess &&
+                 cudaStreamWaitEvent(hp.d2h, hp.encoded[slot], 0) == cudaSuccess &&
+                 cudaMemcpyAsync(out_host + first, out_dev + first, (size_t)count * 4,
+                                 cudaMemcpyDeviceToHost, hp.d2h) == cudaSuccess &&
+                 cudaEventRecord(hp.copied[slot], hp.d2h) == cudaSuccess;
+            ++ci;
+            if (splits == 1) break;
+        }
+    }
+    // The caller's stream ends after the last copy back; return once it is done.
+    ok = ok && cudaEventRecord(hp.start, hp.d2h) == cudaSuccess &&
+         cudaStreamWaitEvent(st, hp.start, 0) == cudaSuccess &&
+         cudaStreamSynchronize(hp.d2h) == cudaSuccess;
+    return ok ? VQ_OK : VQ_ERR_CUDA;
 }
 
 const char *vq_status_string(vq_status status)

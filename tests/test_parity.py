@@ -278,16 +278,34 @@ def test_no_device_allocation(vq):
     assert free1 == free0
 
 
-def test_host_entry_point(vq, oracle_mod):
-    x, cb = workloads.generate("long_context", tokens=512)
-    xh = torch.from_numpy(x).pin_memory()
-    cbh = torch.from_numpy(cb).pin_memory()
-    outh = torch.empty(x.shape[:2], dtype=torch.uint32).pin_memory()
-    xd = torch.empty_like(xh, device="cuda")
-    cbd = torch.empty_like(cbh, device="cuda")
-    outd = torch.empty(x.shape[:2], dtype=torch.uint32, device="cuda")
-    vq.vq_encode_grouped_host(xh, cbh, outh, xd, cbd, outd)
-    assert_same(outh.numpy(), oracle_mod.encode(x, cb, n_threads=THREADS))
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("g,m,sub", [(1, 9_000_000, 4), (3, 3_000_000, 8), (40, 9000, 8),
+                                     (2, 7, 4)])
+def test_host_entry_point(vq, oracle_mod, g, m, sub, pinned):
+    """Host buffers in, host buffers out.  Pinned buffers are read and written
+    by the kernel directly (the device scratch stays untouched); pageable ones
+    go through the device buffers, in overlapped chunks when large.  Both must
+    give the device entry point's indices, twice in a row."""
+    rng = np.random.default_rng(g * 1000 + sub)
+    x = rng.standard_normal((g, m, sub)).astype(np.float16)
+    cb = rng.standard_normal((g, 256, sub)).astype(np.float16)
+    xh, cbh = torch.from_numpy(x), torch.from_numpy(cb)
+    outh = torch.full((g, m), 0xFFFF, dtype=torch.int32).view(torch.uint32)
+    if pinned:
+        xh, cbh, outh = xh.pin_memory(), cbh.pin_memory(), outh.pin_memory()
+    xd = torch.full(x.shape, 7.0, dtype=torch.float16, device="cuda")
+    cbd = torch.empty(cb.shape, dtype=torch.float16, device="cuda")
+    outd = torch.full((g, m), 12345, dtype=torch.int32, device="cuda").view(torch.uint32)
+    want = vq.vq_encode_grouped(torch.from_numpy(x).cuda(), torch.from_numpy(cb).cuda())
+    want = want.cpu().numpy()
+    for _ in range(2):
+        vq.vq_encode_grouped_host(xh, cbh, outh, xd, cbd, outd)
+        assert_same(outh.numpy(), want)
+    if pinned:
+        torch.cuda.synchronize()
+        assert bool((xd == 7.0).all()) and bool((outd.view(torch.int32) == 12345).all())
+    rows = np.unique(rng.integers(0, m, 2000))
+    assert_same(want[:, rows], oracle_mod.encode(x[:, rows], cb, n_threads=THREADS))
 
 
 def test_argument_errors_raise(vq):
