@@ -13,6 +13,7 @@
 
 #include "vq_encode.h"
 #include "vq_filter.cuh"
+#include "vq_tc.cuh"
 #include "vq_kernels.cuh"
 
 namespace {
@@ -27,6 +28,10 @@ constexpr int kGroupCentroids = 8;
 constexpr int kFThreads = 128;
 constexpr int kFRows = 8;
 constexpr int kFGroup = 16;
+// Tuning of the tensor-core screening kernel (tensor-memory columns per CTA,
+// 128-row tiles per CTA).
+constexpr int kTcCols = 128;
+constexpr int kTcTiles = 4;
 // Codebooks smaller than this many centroids are brute-forced: screening pays
 // off only with several centroid groups to rule out.
 constexpr int kFilterMinCentroids = 4 * kFGroup;
@@ -69,7 +74,7 @@ vq_status validate(const Args &a, bool need_pointers)
     return VQ_OK;
 }
 
-enum KernelKind { kGeneral = 0, kBrute = 1, kFilter = 2 };
+enum KernelKind { kGeneral = 0, kBrute = 1, kFilter = 2, kTc = 3 };
 
 struct Plan {
     KernelKind kind;
@@ -99,7 +104,14 @@ Plan make_plan(const Args &a)
     const size_t align = row_bytes < 16 ? row_bytes : 16;
     const bool shape_ok = (a.sub_dim == 4 || a.sub_dim == 8) && ((uintptr_t)a.x % align == 0);
     p.kind = kGeneral;
-    if (shape_ok && a.n_centroids >= kFilterMinCentroids) {
+    // tf32 holds fp16 and bf16 values exactly, not fp32 ones
+    if (shape_ok && a.dtype != VQ_F32 && a.n_centroids >= kFilterMinCentroids &&
+        a.n_centroids <= 256) {
+        p.kind = kTc;
+        p.smem = a.sub_dim == 4 ? vqk::TcLayout<4, kTcCols>::bytes(a.n_centroids)
+                                : vqk::TcLayout<8, kTcCols>::bytes(a.n_centroids);
+    }
+    if (shape_ok && p.kind == kGeneral && a.n_centroids >= kFilterMinCentroids) {
         p.smem = a.sub_dim == 4 ? filter_smem<4>(a.n_centroids) : filter_smem<8>(a.n_centroids);
         if (p.smem <= kMaxFastSmem) p.kind = kFilter;
     }
@@ -108,10 +120,12 @@ Plan make_plan(const Args &a)
         if (p.smem <= kMaxFastSmem) p.kind = kBrute;
     }
     if (p.kind != kGeneral) {
-        const int64_t tile = p.kind == kFilter ? (int64_t)kFThreads * kFRows : (int64_t)kThreads * kRows;
+        const int64_t tile = p.kind == kTc       ? (int64_t)128 * kTcTiles
+                             : p.kind == kFilter ? (int64_t)kFThreads * kFRows
+                                                 : (int64_t)kThreads * kRows;
         p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
         p.blocks = a.n_groups * p.tiles_per_group;
-        p.threads = p.kind == kFilter ? kFThreads : kThreads;
+        p.threads = p.kind == kTc ? 128 : p.kind == kFilter ? kFThreads : kThreads;
     } else {
         p.smem = 0;
         p.tiles_per_group = 0;
@@ -119,6 +133,19 @@ Plan make_plan(const Args &a)
         p.threads = kGeneralThreads;
     }
     return p;
+}
+
+template <typename T, int SUB>
+vq_status launch_tc(const Args &a, const Plan &p)
+{
+    auto kernel = vqk::encode_tc<T, SUB, kTcCols, kTcTiles>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
+        cudaSuccess)
+        return VQ_ERR_CUDA;
+    kernel<<<(unsigned)p.blocks, 128, p.smem, a.stream>>>(
+        static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
+        p.tiles_per_group, 1.0f, a.out);
+    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
 template <typename T, int SUB>
@@ -164,6 +191,10 @@ template <typename T>
 vq_status launch_typed(const Args &a, const Plan &p)
 {
     switch (p.kind) {
+    case kTc:
+        if constexpr (sizeof(T) == 2)
+            return a.sub_dim == 4 ? launch_tc<T, 4>(a, p) : launch_tc<T, 8>(a, p);
+        return VQ_ERR_INTERNAL;
     case kFilter: return a.sub_dim == 4 ? launch_filter<T, 4>(a, p) : launch_filter<T, 8>(a, p);
     case kBrute: return a.sub_dim == 4 ? launch_fast<T, 4>(a, p) : launch_fast<T, 8>(a, p);
     case kGeneral: return launch_general<T>(a, p);
@@ -380,7 +411,12 @@ vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_ce
     if (s != VQ_OK) return s;
     if (!buf || buflen <= 0) return VQ_ERR_INVALID_ARG;
     const Plan p = make_plan(a);
-    if (p.kind == kFilter)
+    if (p.kind == kTc)
+        snprintf(buf, (size_t)buflen,
+                 "kernel=encode_tc dtype=%s sub_dim=%d tmem_cols=%d tiles_per_block=%d "
+                 "grid=%lld smem=%zu",
+                 dtype_name(dtype), sub_dim, kTcCols, kTcTiles, (long long)p.blocks, p.smem);
+    else if (p.kind == kFilter)
         snprintf(buf, (size_t)buflen,
                  "kernel=encode_filter dtype=%s sub_dim=%d rows_per_thread=%d threads=%d "
                  "centroid_group=%d grid=%lld smem=%zu",

@@ -1,0 +1,449 @@
+// vq_tc.cuh -- exact product-VQ encode with the screening contraction on the
+// 5th-generation tensor cores (tcgen05, accumulator in tensor memory).
+//
+// Same scheme and the same proof as vq_filter.cuh, with one change: the
+// screening values s~(c) = |c|^2 - 2 x.c of a tile of 128 rows against all
+// centroids come from one tcgen05.mma of kind::tf32 per 256 centroids,
+//     A (128 x K, rows)      = [x_0 .. x_SUB-1, 1, 1, 1, 0 ...]
+//     B (n_pad x K, centroids) = [-2c_0 .. -2c_SUB-1, n_hi, n_mid, n_lo, 0 ...]
+// where n_hi + n_mid + n_lo is the fp32 |c|^2 split into three tf32 pieces.
+// fp16 and bf16 values, -2c and 1 are exact in tf32, so every product is
+// exact; only the accumulation inside the tensor core rounds.  Its error is
+// bounded by eps_tc times the sum of the magnitudes of the terms, which is at
+// most 2 (C2 + sum_i |x_i| A_i); eps_tc = 2^-13 is taken, some 250 times the
+// error of an fp32 accumulator that truncates every partial sum.  Adding the
+// rounding of the fp32 |c|^2 (gamma_SUB) gives the screening bound
+//     B(x) = (2 eps_tc + 2 gamma_SUB) (C2 + sum_i |x_i| A_i),
+// and the threshold, candidate groups, exact re-evaluation and exact queue
+// follow as in vq_filter.cuh.  fp32 inputs are not exact in tf32 and use
+// encode_filter instead.
+//
+// The accumulator of a tile is a 128-lane x n_pad-column fp32 block of tensor
+// memory, so thread t of the block owns row t of the tile: it reads its own
+// row's scores (tcgen05.ld) and reduces them without any exchange.
+//
+// Launch: block = 128 threads; dynamic shared memory = TcLayout::bytes(...)
+// (at least 512/NCOL CTAs' worth of a 228 KiB SM, which caps the CTAs per SM
+// at the tensor-memory budget: NCOL columns each); grid.x = n_groups *
+// tiles_per_group, each block encoding TILES consecutive 128-row tiles of one
+// group.  Requirements: T is __half or __nv_bfloat16, 64 <= n_centroids <=
+// 256, x aligned to SUB * sizeof(T) bytes.
+#pragma once
+
+#include "vq_filter.cuh"
+#include "vq_kernels.cuh"
+
+namespace vqk {
+
+// ------------------------------------------------------------------ tcgen05 / mbarrier helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Shared-memory matrix descriptor: no swizzle, K-major core matrices of
+// 8 rows x 16 bytes; lbo = byte distance between core matrices adjacent in K,
+// sbo = between core matrices adjacent in M/N.
+__device__ __forceinline__ uint64_t umma_smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((addr >> 4) & 0x3fff) | ((uint64_t)((lbo >> 4) & 0x3fff) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3fff) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor: kind::tf32, fp32 accumulator, A and B K-major,
+// M = 128, N = n.
+__host__ __device__ constexpr uint32_t umma_idesc_tf32(uint32_t n)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+// Wait for the barrier's phase `parity` to complete, giving up after a bounded
+// number of polls; returns whether it completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done = 0;
+    for (int it = 0; it < (1 << 22) && !done; ++it) {
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(smem_addr(bar)), "r"(parity)
+                     : "memory");
+    }
+    return done != 0;
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Keep the top 10 bits of an fp32 significand (the tf32 value, exactly).
+__device__ __forceinline__ float tf32_trunc(float v) { return __uint_as_float(__float_as_uint(v) & 0xffffe000u); }
+
+// ------------------------------------------------------------------ layout
+
+template <int SUB, int NCOL>
+struct TcLayout {
+    static constexpr int kK = SUB == 4 ? 8 : 16;       // MMA K (tf32 elements), 8 per instruction
+    static constexpr int kRowBytes = kK * 4;
+    static constexpr int kGC = 16;                       // centroids per screening group
+    static constexpr int kX4 = SUB / 4;                  // float4 per centroid, exact layout
+    static constexpr int kGroupStride = kGC * kX4 + 1;   // float4, one pad per group
+    static constexpr int kCtasPerSm = 512 / NCOL;
+    __host__ __device__ static int padded(int nc) { return (nc + 31) / 32 * 32; }
+    __host__ __device__ static int groups(int nc) { return padded(nc) / kGC; }
+    // byte offsets
+    __host__ __device__ static size_t a_off() { return 0; }
+    __host__ __device__ static size_t b_off() { return (size_t)128 * kRowBytes; }
+    __host__ __device__ static size_t x_off(int nc) { return b_off() + (size_t)256 * kRowBytes; }
+    __host__ __device__ static size_t misc_off(int nc)
+    {
+        return x_off(nc) + (size_t)groups(nc) * kGroupStride * 16;
+    }
+    // misc: SUB + 1 maxima, queue counter, tensor-memory address, pad, mbarrier (8-aligned), queue
+    __host__ __device__ static size_t used(int nc) { return misc_off(nc) + 64 + 128 * 4; }
+    __host__ __device__ static size_t bytes(int nc)
+    {
+        const size_t cap = (size_t)228 * 1024 / (kCtasPerSm + 1) + 1024;
+        const size_t u = used(nc) + 1024;  // room to align the base to 1 KiB
+        return u > cap ? u : cap;
+    }
+};
+
+// ------------------------------------------------------------------ kernel
+
+template <typename T, int SUB, int NCOL, int TILES>
+__global__ void __launch_bounds__(128)
+    encode_tc(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
+              int32_t n_centroids, int64_t tiles_per_group, float one, uint32_t *__restrict__ out)
+{
+    static_assert(SUB == 4 || SUB == 8, "sub_dim 4 or 8");
+    static_assert(NCOL == 128 || NCOL == 256, "tensor-memory columns");
+    using L = TcLayout<SUB, NCOL>;
+    constexpr int kK = L::kK;
+    constexpr int kKB = kK / 4;  // 16-byte core-matrix columns per row
+    constexpr int kGC = L::kGC;
+    constexpr uint32_t kQueued = 0xffffffffu;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *sa = reinterpret_cast<float *>(sm + L::a_off());
+    float *sb = reinterpret_cast<float *>(sm + L::b_off());
+    float4 *sx = reinterpret_cast<float4 *>(sm + L::x_off(n_centroids));
+    uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::misc_off(n_centroids));
+    uint32_t *smax = misc;              // [0] = C2, [1 + i] = A_i
+    uint32_t *qcount = misc + SUB + 1;
+    uint32_t *tslot = misc + SUB + 2;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(misc + 12);  // 48 bytes in: 8-aligned
+    uint32_t *queue = misc + 16;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int n_pad = L::padded(n_centroids);
+    const int n_groups_c = L::groups(n_centroids);
+    const int64_t g = blockIdx.x / tiles_per_group;
+    const int64_t blk = blockIdx.x - g * tiles_per_group;
+    const T *__restrict__ cb = codebooks + (size_t)g * (size_t)n_centroids * SUB;
+    const T *__restrict__ xg = x + (size_t)g * (size_t)n_per_group * SUB;
+    uint32_t *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
+    const int64_t row_base = blk * (int64_t)(128 * TILES);
+
+    // ---- set-up: maxima, barrier, tensor memory, constant part of A
+    if (tid < SUB + 2) misc[tid] = 0u;
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tslot)),
+                     "r"(NCOL));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    {
+        // A row `tid`: columns SUB.. of the row are the constant [1, 1, 1, 0 ...]
+        float *arow = sa;
+#pragma unroll
+        for (int kb = SUB / 4; kb < kKB; ++kb) {
+            const float4 v = kb == SUB / 4 ? make_float4(1.f, 1.f, 1.f, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4 *>(arow + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) = v;
+        }
+    }
+    __syncthreads();
+
+    // ---- stage the codebook: B operand, exact layout, maxima
+    for (int c = tid; c < 256; c += 128) {
+        const bool real = c < n_centroids;
+        float v[SUB];
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) v[i] = real ? widen(cb[(size_t)c * SUB + i]) : 0.f;
+        float nrm = mul_rn(v[0], v[0]);
+#pragma unroll
+        for (int i = 1; i < SUB; ++i) nrm = fma_rn(v[i], v[i], nrm);
+        float bk[kK];
+#pragma unroll
+        for (int k = 0; k < kK; ++k) bk[k] = 0.f;
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) bk[i] = -2.0f * v[i];
+        if (real) {
+            const float hi = tf32_trunc(nrm);
+            const float mid = tf32_trunc(nrm - hi);
+            bk[SUB] = hi;
+            bk[SUB + 1] = mid;
+            bk[SUB + 2] = tf32_trunc(nrm - hi - mid);
+        } else {
+            bk[SUB] = __int_as_float(0x7f800000);  // padding never screens in
+        }
+#pragma unroll
+        for (int kb = 0; kb < kKB; ++kb)
+            *reinterpret_cast<float4 *>(sb + ((c >> 3) * (kKB * 128) + kb * 128 + (c & 7) * 16) / 4) =
+                make_float4(bk[4 * kb], bk[4 * kb + 1], bk[4 * kb + 2], bk[4 * kb + 3]);
+        if (c < n_pad) {
+            float4 *ex = sx + (c / kGC) * L::kGroupStride + (c % kGC) * L::kX4;
+#pragma unroll
+            for (int k = 0; k < SUB / 4; ++k)
+                ex[k] = real ? make_float4(-v[4 * k], -v[4 * k + 1], -v[4 * k + 2], -v[4 * k + 3])
+                             : make_float4(__int_as_float(0x7fc00000), 0.f, 0.f, 0.f);
+        }
+        if (real) {
+            atomicMax(&smax[0], __float_as_uint(nrm));
+#pragma unroll
+            for (int i = 0; i < SUB; ++i) atomicMax(&smax[1 + i], __float_as_uint(fabsf(v[i])));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const float c2 = __uint_as_float(smax[0]);
+    float amax[SUB];
+#pragma unroll
+    for (int i = 0; i < SUB; ++i) amax[i] = __uint_as_float(smax[1 + i]);
+    const float kBtc = 2.0f * 1.2207031e-4f + 2.0f * gamma_u(SUB);  // 2 eps_tc + 2 gamma_SUB
+    const float kD = 4.0f * gamma_u(SUB + 2);
+    const float kTiny = 7.8886091e-31f;  // 2^-100
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint32_t sa_addr = smem_addr(sa), sb_addr = smem_addr(sb);
+    constexpr uint32_t kSbo = kKB * 128;
+
+    // this thread's row of the first tile
+    float xr[SUB];
+    auto load_x = [&](int64_t row, float (&v)[SUB]) {
+        if (row < n_per_group) {
+            load_row<T, SUB>(xg + (size_t)row * SUB, v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < SUB; ++i) v[i] = 0.f;
+        }
+    };
+    load_x(row_base + tid, xr);
+
+    uint32_t phase = 0;
+    bool alive = true;
+    for (int tile = 0; tile < TILES; ++tile) {
+        const int64_t row = row_base + (int64_t)tile * 128 + tid;
+        if (row_base + (int64_t)tile * 128 >= n_per_group) break;  // block-uniform
+
+        // A rows of this tile (the MMA of the previous tile has completed)
+#pragma unroll
+        for (int kb = 0; kb < SUB / 4; ++kb)
+            *reinterpret_cast<float4 *>(sa + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) =
+                make_float4(xr[4 * kb], xr[4 * kb + 1], xr[4 * kb + 2], xr[4 * kb + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        float gmin[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) gmin[k] = __int_as_float(0x7f800000);
+#pragma unroll
+        for (int pass = 0; pass < 256 / NCOL; ++pass) {
+            const int c0 = pass * NCOL;
+            if (c0 >= n_pad) break;  // block-uniform
+            const int ncols = n_pad - c0 < NCOL ? n_pad - c0 : NCOL;
+            if (tid == 0) {
+                const uint32_t idesc = umma_idesc_tf32((uint32_t)ncols);
+#pragma unroll
+                for (int kstep = 0; kstep < kK / 8; ++kstep) {
+                    const uint64_t ad = umma_smem_desc(sa_addr + kstep * 256, 128, kSbo);
+                    const uint64_t bd = umma_smem_desc(sb_addr + (c0 >> 3) * kSbo + kstep * 256, 128, kSbo);
+                    umma_tf32(tmem, ad, bd, idesc, kstep > 0);
+                }
+                umma_commit(bar);
+            }
+            const bool done = mbar_wait(bar, phase);
+            phase ^= 1u;
+            tc_fence_after();
+            if (!__syncthreads_and(done)) {
+                alive = false;
+                break;
+            }
+#pragma unroll
+            for (int j = 0; j < NCOL; j += 32) {
+                if (j < ncols) {  // block-uniform
+                    float v[32];
+                    tmem_load32(tmem + lane_base + (uint32_t)j, v);
+                    float a = min3(v[0], v[1], v[2]), b = min3(v[16], v[17], v[18]);
+#pragma unroll
+                    for (int k = 3; k < 15; k += 2) {
+                        a = min3(a, v[k], v[k + 1]);
+                        b = min3(b, v[16 + k], v[17 + k]);
+                    }
+                    gmin[(c0 + j) / kGC] = fminf(a, v[15]);
+                    gmin[(c0 + j) / kGC + 1] = fminf(b, v[31]);
+                }
+            }
+            tc_fence_before();
+            __syncthreads();  // tensor memory is read before the next MMA writes it
+            tc_fence_after();
+        }
+        if (!alive) {
+            if (row < n_per_group) __stcs(og + row, kQueued);
+            break;
+        }
+
+        // next tile's row, in flight during the bookkeeping below
+        float xn[SUB];
+        load_x(row + 128, xn);
+
+        // ---- bound, candidate groups, exact re-evaluation
+        float m1 = gmin[0];
+#pragma unroll
+        for (int k = 1; k < 16; ++k) m1 = fminf(m1, gmin[k]);
+        float sabs = 0.f, xx = 0.f;
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) {
+            sabs = fmaf(fabsf(xr[i]), amax[i], sabs);
+            xx = fmaf(xr[i], xr[i], xx);
+        }
+        const float base = c2 + sabs;
+        const float bnd = kBtc * base + kTiny;
+        const float dmax = fmaxf(0.f, xx + m1 + bnd);
+        const float thr = m1 + (2.0f * bnd + kD * dmax + kTiny);
+        const bool ok = base < 1e30f && dmax < 1e37f;
+        int cnt = 0, ga = -1, gb = -1;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const bool q = k < n_groups_c && gmin[k] <= thr;
+            gb = (q && cnt == 1) ? k : gb;
+            ga = (q && cnt == 0) ? k : ga;
+            cnt += q ? 1 : 0;
+        }
+        if (tid == 0) *qcount = 0u;
+        __syncthreads();
+        uint32_t id = 0;
+        if (!ok || cnt > 2 || cnt == 0) {
+            id = kQueued;
+            if (row < n_per_group) queue[atomicAdd(qcount, 1u)] = (uint32_t)tid;
+        } else {
+            float best = __int_as_float(0x7f800000);
+            for (int pass = 0; pass < 2; ++pass) {
+                const int gsel = pass == 0 ? ga : gb;
+                if (gsel < 0) break;
+                const float4 *gp = sx + gsel * L::kGroupStride;
+#pragma unroll 4
+                for (int cc = 0; cc < kGC; ++cc) {
+                    float nc[SUB];
+#pragma unroll
+                    for (int k = 0; k < SUB / 4; ++k) {
+                        const float4 q = gp[cc * L::kX4 + k];
+                        nc[4 * k] = q.x;
+                        nc[4 * k + 1] = q.y;
+                        nc[4 * k + 2] = q.z;
+                        nc[4 * k + 3] = q.w;
+                    }
+                    const float d = one_dist<SUB>(xr, nc, one);
+                    if (d < best) {
+                        best = d;
+                        id = (uint32_t)(gsel * kGC + cc);
+                    }
+                }
+            }
+        }
+        if (row < n_per_group && id != kQueued) __stcs(og + row, id);
+        __syncthreads();
+
+        // ---- queued rows of this tile: one warp per row, exact scan
+        const uint32_t nq = *qcount;
+        for (uint32_t q = (uint32_t)warp; q < nq; q += 4) {
+            const int64_t qrow = row_base + (int64_t)tile * 128 + queue[q];
+            float xq[SUB];
+#pragma unroll
+            for (int i = 0; i < SUB; ++i) xq[i] = widen(xg[(size_t)qrow * SUB + i]);
+            float best = __int_as_float(0x7f800000);
+            uint32_t bi = kQueued;
+            for (int c = lane; c < n_centroids; c += 32) {
+                const float4 *cp = sx + (c / kGC) * L::kGroupStride + (c % kGC) * L::kX4;
+                float nc[SUB];
+#pragma unroll
+                for (int k = 0; k < SUB / 4; ++k) {
+                    const float4 qv = cp[k];
+                    nc[4 * k] = qv.x;
+                    nc[4 * k + 1] = qv.y;
+                    nc[4 * k + 2] = qv.z;
+                    nc[4 * k + 3] = qv.w;
+                }
+                const float d = one_dist<SUB>(xq, nc, one);
+                if (d < best) {
+                    best = d;
+                    bi = (uint32_t)c;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+                const uint32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (ob < best || (ob == best && oi < bi)) {
+                    best = ob;
+                    bi = oi;
+                }
+            }
+            if (lane == 0) __stcs(og + qrow, bi == kQueued ? 0u : bi);
+        }
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) xr[i] = xn[i];
+        // the __syncthreads at the top of the next tile orders queue reuse
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && alive)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOL));
+}
+
+}  // namespace vqk

@@ -112,9 +112,13 @@ def test_describe_launch_picks_kernels(lib):
     f.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int32]
     buf = ctypes.create_string_buffer(512)
-    assert f(1, 1 << 20, 256, 4, 0, P, buf, 512) == 0
+    assert f(1, 1 << 20, 256, 4, 0, P, buf, 512) == 0        # fp16: tensor-core screening
+    assert buf.value.decode().startswith("kernel=encode_tc")
+    assert f(256, 131072, 256, 8, 1, P, buf, 512) == 0       # bf16
+    assert buf.value.decode().startswith("kernel=encode_tc")
+    assert f(1, 1 << 20, 256, 4, 2, P, buf, 512) == 0        # fp32: CUDA-core screening
     assert buf.value.decode().startswith("kernel=encode_filter")
-    assert f(256, 131072, 256, 8, 0, P, buf, 512) == 0
+    assert f(1, 1 << 20, 1000, 8, 0, P, buf, 512) == 0       # more than 256 centroids
     assert buf.value.decode().startswith("kernel=encode_filter")
     assert f(1, 1000, 32, 8, 0, P, buf, 512) == 0           # small codebook: brute force
     assert buf.value.decode().startswith("kernel=encode_fast")

@@ -1,6 +1,9 @@
-"""GPU parity of the filter-and-refine encoder on inputs built to stress it.
+"""GPU parity of the screening encoders on inputs built to stress them.
 
-The filter screens centroids with a fused multiply-add score and re-evaluates
+Both screening kernels -- tensor-core scores (fp16 / bf16 inputs with at most
+256 centroids) and fused multiply-add scores on the CUDA cores (fp32 inputs,
+larger codebooks) -- screen centroids with a bounded-error score and
+re-evaluate
 the exact formula only inside the centroid groups its error bound cannot rule
 out; rows with three or more such groups, or with non-finite or huge values,
 go to an exact per-block queue.  These cases put the deciding difference at
@@ -38,16 +41,28 @@ def run(vq, x, cb):
     return out.cpu().numpy(), desc
 
 
-def check(vq, oracle_mod, x, cb, kernel="encode_filter"):
+def expected_kernel(dtype, n_c):
+    if n_c > 1024:
+        return ""  # large codebooks: whichever exact kernel fits in shared memory
+    if n_c < 64:
+        return "encode_fast"
+    if dtype in (np.float16, "bf16") and n_c <= 256:
+        return "encode_tc"
+    return "encode_filter"
+
+
+def check(vq, oracle_mod, x, cb, kernel=None):
     got, desc = run(vq, x, cb)
+    kernel = kernel or expected_kernel(x.dtype.type, cb.shape[1])
     assert desc.startswith("kernel=" + kernel), desc
     want = oracle_mod.encode(x, cb, n_threads=THREADS)
     bad = np.argwhere(got != want)
     assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
 
 
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
 @pytest.mark.parametrize("sub_dim", [4, 8])
-def test_permuted_coordinate_ties(vq, oracle_mod, sub_dim):
+def test_permuted_coordinate_ties(vq, oracle_mod, sub_dim, dtype):
     """Rows x = (a, a, b, b, ...) are exactly equidistant (in real arithmetic)
     from a centroid and its copy with coordinates swapped pairwise; the fp32
     sums differ only by rounding order, so the winner is decided at the last
@@ -55,32 +70,33 @@ def test_permuted_coordinate_ties(vq, oracle_mod, sub_dim):
     rng = np.random.default_rng(11 + sub_dim)
     n_c, m = 256, 20000
     half = n_c // 2
-    base = rng.standard_normal((half, sub_dim)).astype(np.float16)
+    base = rng.standard_normal((half, sub_dim)).astype(dtype)
     swapped = base.reshape(half, sub_dim // 2, 2)[:, :, ::-1].reshape(half, sub_dim)
-    cb = np.empty((n_c, sub_dim), np.float16)
+    cb = np.empty((n_c, sub_dim), dtype)
     cb[0::2] = base          # centroid 2k
     cb[1::2] = swapped       # centroid 2k+1, same group
     perm = rng.permutation(n_c)
     cb = cb[perm]            # scatter the partners over all groups
-    pairs = rng.standard_normal((m, sub_dim // 2)).astype(np.float16)
+    pairs = rng.standard_normal((m, sub_dim // 2)).astype(dtype)
     x = np.repeat(pairs, 2, axis=1)  # (a, a, b, b, ...)
     check(vq, oracle_mod, x[None], cb[None])
 
 
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
 @pytest.mark.parametrize("copies", [2, 3, 5])
-def test_duplicated_centroids_across_groups(vq, oracle_mod, copies):
+def test_duplicated_centroids_across_groups(vq, oracle_mod, copies, dtype):
     """Exact duplicate centroids in `copies` different groups: with three or
     more, rows near them take the exact queue."""
     rng = np.random.default_rng(20 + copies)
     n_c, sub = 256, 8
-    cb = rng.standard_normal((n_c, sub)).astype(np.float16)
+    cb = rng.standard_normal((n_c, sub)).astype(dtype)
     for src in range(0, 40, 4):
         for k in range(1, copies):
             cb[(src + 37 * k) % n_c] = cb[src]
     src = rng.integers(0, n_c, 30000)
     x = cb[src].astype(np.float32)
     x += rng.standard_normal(x.shape).astype(np.float32) * 0.05
-    check(vq, oracle_mod, x.astype(np.float16)[None], cb[None])
+    check(vq, oracle_mod, x.astype(dtype)[None], cb[None])
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -99,7 +115,7 @@ def test_extreme_magnitudes(vq, oracle_mod, dtype):
         ct = torch.from_numpy(cb).to(torch.bfloat16)
         got = None
         desc = vq.vq_describe_launch(1, x.shape[0], n_c, sub, torch.bfloat16, xt.cuda().data_ptr())
-        assert desc.startswith("kernel=encode_filter")
+        assert desc.startswith("kernel=encode_tc")
         got = vq.vq_encode(xt.cuda(), ct.cuda()).cpu().numpy()
         want = oracle_mod.encode(xt.view(torch.int16).numpy().view(np.uint16),
                                  ct.view(torch.int16).numpy().view(np.uint16), bf16=True,
@@ -109,26 +125,39 @@ def test_extreme_magnitudes(vq, oracle_mod, dtype):
         check(vq, oracle_mod, x[None], cb[None])
 
 
-def test_codebook_with_nan_queues_every_row(vq, oracle_mod):
+@pytest.mark.parametrize("n_c", [200, 300])
+def test_codebook_with_nan_queues_every_row(vq, oracle_mod, n_c):
     rng = np.random.default_rng(6)
-    cb = rng.standard_normal((300, 4)).astype(np.float16)
+    cb = rng.standard_normal((n_c, 4)).astype(np.float16)
     cb[123, 2] = np.nan
     x = rng.standard_normal((5000, 4)).astype(np.float16)
     check(vq, oracle_mod, x[None], cb[None])
 
 
-@pytest.mark.parametrize("n_c", [63, 64, 65, 100, 512, 2000])
-def test_codebook_sizes_around_the_groups(vq, oracle_mod, n_c):
-    rng = np.random.default_rng(n_c)
-    x = rng.standard_normal((2, 3000, 4)).astype(np.float16)
-    cb = rng.standard_normal((2, n_c, 4)).astype(np.float16)
-    check(vq, oracle_mod, x, cb, kernel="encode_filter" if n_c >= 64 else "encode_fast")
+@pytest.mark.parametrize("sub_dim", [4, 8])
+@pytest.mark.parametrize("n_c", [63, 64, 65, 100, 224, 255, 256, 257, 512, 2000])
+def test_codebook_sizes_around_the_groups(vq, oracle_mod, n_c, sub_dim):
+    rng = np.random.default_rng(n_c + sub_dim)
+    x = rng.standard_normal((2, 3000, sub_dim)).astype(np.float16)
+    cb = rng.standard_normal((2, n_c, sub_dim)).astype(np.float16)
+    check(vq, oracle_mod, x, cb)
 
 
-def test_clustered_keys_near_many_centroids(vq, oracle_mod):
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+@pytest.mark.parametrize("scale", [0.01, 1000.0])
+def test_clustered_keys_near_many_centroids(vq, oracle_mod, dtype, scale):
     """Keys concentrated near the origin, where many centroids are at similar
-    distances: more candidate groups per row."""
+    distances (more candidate groups per row), at small and large scale."""
     rng = np.random.default_rng(8)
-    cb = (rng.standard_normal((256, 8)) * 0.01).astype(np.float16)
-    x = (rng.standard_normal((20000, 8)) * 0.01).astype(np.float16)
+    cb = (rng.standard_normal((256, 8)) * scale).astype(dtype)
+    x = (rng.standard_normal((20000, 8)) * scale).astype(dtype)
     check(vq, oracle_mod, x[None], cb[None])
+
+
+@pytest.mark.parametrize("m", [1, 127, 128, 129, 1023, 1024, 1025, 3000])
+def test_tensor_core_tile_boundaries(vq, oracle_mod, m):
+    """Row counts around the 128-row tensor-core tile and the 1024-row block."""
+    rng = np.random.default_rng(m)
+    x = rng.standard_normal((3, m, 4)).astype(np.float16)
+    cb = rng.standard_normal((3, 256, 4)).astype(np.float16)
+    check(vq, oracle_mod, x, cb)
