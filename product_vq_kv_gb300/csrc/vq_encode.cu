@@ -30,8 +30,19 @@ constexpr int kFRows = 8;
 constexpr int kFGroup = 16;
 // Tuning of the tensor-core screening kernel (tensor-memory columns per CTA,
 // 128-row tiles per CTA).
-constexpr int kTcCols = 128;
-constexpr int kTcTiles = 4;
+// Per sub_dim: tensor-memory columns per CTA, 128-row tiles per CTA, centroids
+// per screening group, minimum CTAs per SM (register budget).  Measured best
+// on GB300 for 256-centroid codebooks.
+template <int SUB>
+struct TcConfig;
+template <>
+struct TcConfig<4> {
+    static constexpr int kCols = 64, kTiles = 4, kGroup = 16, kMinBlocks = 8;
+};
+template <>
+struct TcConfig<8> {
+    static constexpr int kCols = 64, kTiles = 4, kGroup = 8, kMinBlocks = 6;
+};
 // Codebooks smaller than this many centroids are brute-forced: screening pays
 // off only with several centroid groups to rule out.
 constexpr int kFilterMinCentroids = 4 * kFGroup;
@@ -91,6 +102,13 @@ size_t fast_smem(int32_t n_centroids)
 }
 
 template <int SUB>
+size_t tc_smem(int32_t n_centroids)
+{
+    using C = TcConfig<SUB>;
+    return vqk::TcLayout<SUB, C::kCols, C::kGroup>::bytes(n_centroids);
+}
+
+template <int SUB>
 size_t filter_smem(int32_t n_centroids)
 {
     return vqk::FilterLayout<SUB, kFGroup>::bytes(n_centroids, kFThreads * kFRows);
@@ -108,8 +126,7 @@ Plan make_plan(const Args &a)
     if (shape_ok && a.dtype != VQ_F32 && a.n_centroids >= kFilterMinCentroids &&
         a.n_centroids <= 256) {
         p.kind = kTc;
-        p.smem = a.sub_dim == 4 ? vqk::TcLayout<4, kTcCols>::bytes(a.n_centroids)
-                                : vqk::TcLayout<8, kTcCols>::bytes(a.n_centroids);
+        p.smem = a.sub_dim == 4 ? tc_smem<4>(a.n_centroids) : tc_smem<8>(a.n_centroids);
     }
     if (shape_ok && p.kind == kGeneral && a.n_centroids >= kFilterMinCentroids) {
         p.smem = a.sub_dim == 4 ? filter_smem<4>(a.n_centroids) : filter_smem<8>(a.n_centroids);
@@ -120,7 +137,8 @@ Plan make_plan(const Args &a)
         if (p.smem <= kMaxFastSmem) p.kind = kBrute;
     }
     if (p.kind != kGeneral) {
-        const int64_t tile = p.kind == kTc       ? (int64_t)128 * kTcTiles
+        const int tc_tiles = a.sub_dim == 4 ? TcConfig<4>::kTiles : TcConfig<8>::kTiles;
+        const int64_t tile = p.kind == kTc       ? (int64_t)128 * tc_tiles
                              : p.kind == kFilter ? (int64_t)kFThreads * kFRows
                                                  : (int64_t)kThreads * kRows;
         p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
@@ -138,7 +156,8 @@ Plan make_plan(const Args &a)
 template <typename T, int SUB>
 vq_status launch_tc(const Args &a, const Plan &p)
 {
-    auto kernel = vqk::encode_tc<T, SUB, kTcCols, kTcTiles>;
+    using C = TcConfig<SUB>;
+    auto kernel = vqk::encode_tc<T, SUB, C::kCols, C::kTiles, C::kGroup, C::kMinBlocks>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
         return VQ_ERR_CUDA;
@@ -414,8 +433,10 @@ vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_ce
     if (p.kind == kTc)
         snprintf(buf, (size_t)buflen,
                  "kernel=encode_tc dtype=%s sub_dim=%d tmem_cols=%d tiles_per_block=%d "
-                 "grid=%lld smem=%zu",
-                 dtype_name(dtype), sub_dim, kTcCols, kTcTiles, (long long)p.blocks, p.smem);
+                 "centroid_group=%d grid=%lld smem=%zu",
+                 dtype_name(dtype), sub_dim, sub_dim == 4 ? TcConfig<4>::kCols : TcConfig<8>::kCols,
+                 sub_dim == 4 ? TcConfig<4>::kTiles : TcConfig<8>::kTiles,
+                 sub_dim == 4 ? TcConfig<4>::kGroup : TcConfig<8>::kGroup, (long long)p.blocks, p.smem);
     else if (p.kind == kFilter)
         snprintf(buf, (size_t)buflen,
                  "kernel=encode_filter dtype=%s sub_dim=%d rows_per_thread=%d threads=%d "
