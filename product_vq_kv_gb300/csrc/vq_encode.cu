@@ -37,12 +37,65 @@ template <int SUB>
 struct TcConfig;
 template <>
 struct TcConfig<4> {
-    static constexpr int kCols = 64, kTiles = 4, kGroup = 16, kMinBlocks = 8;
+    static constexpr int kCols = 64, kGroup = 16, kMinBlocks = 8;
 };
 template <>
 struct TcConfig<8> {
-    static constexpr int kCols = 64, kTiles = 4, kGroup = 8, kMinBlocks = 6;
+    static constexpr int kCols = 64, kGroup = 8, kMinBlocks = 6;
 };
+
+// Streaming multiprocessors of the current device, cached per device; 0 if
+// there is no usable device.
+int device_sms()
+{
+    constexpr int kMax = 64;
+    static int cache[kMax] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMax) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (cache[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        cache[dev] = sms;
+    }
+    return cache[dev];
+}
+
+// Blocks per group and 128-row tiles per block.  A block's time is taken as
+// its tiles plus half a tile of set-up (codebook staging); the launch's time
+// as waves of `slots` resident blocks times that.  The best of 1..64 tiles per
+// block and the one-wave shape is used.
+void tc_shape(int64_t n_groups, int64_t n_per_group, int slots, int64_t *blocks_per_group,
+              int32_t *tiles_per_block)
+{
+    const int64_t tiles = (n_per_group + 127) / 128;
+    int64_t per_group = slots / n_groups;
+    if (per_group < 1) per_group = 1;
+    const int64_t one_wave = (tiles + per_group - 1) / per_group;
+    int64_t best_t = 1;
+    double best_cost = 1e300;
+    auto consider = [&](int64_t t) {
+        if (t < 1 || t > tiles) return;
+        const int64_t blocks = n_groups * ((tiles + t - 1) / t);
+        const int64_t waves = (blocks + slots - 1) / slots;
+        const double cost = (double)waves * ((double)t + 0.5);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best_t = t;
+        }
+    };
+    consider(one_wave);
+    for (int64_t t = 1; t <= 64; ++t) consider(t);
+    if (best_t > (1 << 30)) best_t = 1 << 30;
+    *tiles_per_block = (int32_t)best_t;
+    *blocks_per_group = (tiles + best_t - 1) / best_t;
+}
+
 // Codebooks smaller than this many centroids are brute-forced: screening pays
 // off only with several centroid groups to rule out.
 constexpr int kFilterMinCentroids = 4 * kFGroup;
@@ -90,9 +143,10 @@ enum KernelKind { kGeneral = 0, kBrute = 1, kFilter = 2, kTc = 3 };
 struct Plan {
     KernelKind kind;
     size_t smem;
-    int64_t tiles_per_group;
+    int64_t tiles_per_group;  // blocks per group
     int64_t blocks;
     int threads;
+    int32_t tc_tiles;         // 128-row tiles per block (tensor-core kernel)
 };
 
 template <int SUB>
@@ -106,6 +160,23 @@ size_t tc_smem(int32_t n_centroids)
 {
     using C = TcConfig<SUB>;
     return vqk::TcLayout<SUB, C::kCols, C::kGroup>::bytes(n_centroids);
+}
+
+template <typename T, int SUB>
+auto tc_kernel()
+{
+    using C = TcConfig<SUB>;
+    return vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks>;
+}
+
+// Resident tensor-core CTAs on the device: the register budget of the launch
+// bounds admits kMinBlocks per SM, and the shared-memory request caps them at
+// the tensor-memory budget (512 / kCols), which is not smaller.
+int tc_slots(int sub_dim)
+{
+    const int sms = device_sms();
+    const int per_sm = sub_dim == 4 ? TcConfig<4>::kMinBlocks : TcConfig<8>::kMinBlocks;
+    return (sms > 0 ? sms : 152) * per_sm;
 }
 
 template <int SUB>
@@ -136,11 +207,12 @@ Plan make_plan(const Args &a)
         p.smem = a.sub_dim == 4 ? fast_smem<4>(a.n_centroids) : fast_smem<8>(a.n_centroids);
         if (p.smem <= kMaxFastSmem) p.kind = kBrute;
     }
-    if (p.kind != kGeneral) {
-        const int tc_tiles = a.sub_dim == 4 ? TcConfig<4>::kTiles : TcConfig<8>::kTiles;
-        const int64_t tile = p.kind == kTc       ? (int64_t)128 * tc_tiles
-                             : p.kind == kFilter ? (int64_t)kFThreads * kFRows
-                                                 : (int64_t)kThreads * kRows;
+    if (p.kind == kTc) {
+        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim), &p.tiles_per_group, &p.tc_tiles);
+        p.blocks = a.n_groups * p.tiles_per_group;
+        p.threads = 128;
+    } else if (p.kind != kGeneral) {
+        const int64_t tile = p.kind == kFilter ? (int64_t)kFThreads * kFRows : (int64_t)kThreads * kRows;
         p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
         p.blocks = a.n_groups * p.tiles_per_group;
         p.threads = p.kind == kTc ? 128 : p.kind == kFilter ? kFThreads : kThreads;
@@ -156,14 +228,13 @@ Plan make_plan(const Args &a)
 template <typename T, int SUB>
 vq_status launch_tc(const Args &a, const Plan &p)
 {
-    using C = TcConfig<SUB>;
-    auto kernel = vqk::encode_tc<T, SUB, C::kCols, C::kTiles, C::kGroup, C::kMinBlocks>;
+    auto kernel = tc_kernel<T, SUB>();
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
         return VQ_ERR_CUDA;
     kernel<<<(unsigned)p.blocks, 128, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
-        p.tiles_per_group, 1.0f, a.out);
+        p.tiles_per_group, p.tc_tiles, 1.0f, a.out);
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
@@ -429,14 +500,15 @@ vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_ce
     vq_status s = validate(a, false);
     if (s != VQ_OK) return s;
     if (!buf || buflen <= 0) return VQ_ERR_INVALID_ARG;
+    // without a usable GPU the tensor-core kernel's shape assumes 152 SMs
     const Plan p = make_plan(a);
     if (p.kind == kTc)
         snprintf(buf, (size_t)buflen,
                  "kernel=encode_tc dtype=%s sub_dim=%d tmem_cols=%d tiles_per_block=%d "
                  "centroid_group=%d grid=%lld smem=%zu",
                  dtype_name(dtype), sub_dim, sub_dim == 4 ? TcConfig<4>::kCols : TcConfig<8>::kCols,
-                 sub_dim == 4 ? TcConfig<4>::kTiles : TcConfig<8>::kTiles,
-                 sub_dim == 4 ? TcConfig<4>::kGroup : TcConfig<8>::kGroup, (long long)p.blocks, p.smem);
+                 (int)p.tc_tiles, sub_dim == 4 ? TcConfig<4>::kGroup : TcConfig<8>::kGroup,
+                 (long long)p.blocks, p.smem);
     else if (p.kind == kFilter)
         snprintf(buf, (size_t)buflen,
                  "kernel=encode_filter dtype=%s sub_dim=%d rows_per_thread=%d threads=%d "

@@ -27,8 +27,8 @@
 // Launch: block = 128 threads; dynamic shared memory = TcLayout::bytes(...)
 // (at least 512/NCOL CTAs' worth of a 228 KiB SM, which caps the CTAs per SM
 // at the tensor-memory budget: NCOL columns each); grid.x = n_groups *
-// tiles_per_group, each block encoding TILES consecutive 128-row tiles of one
-// group.  Requirements: T is __half or __nv_bfloat16, 64 <= n_centroids <=
+// blocks_per_group, each block encoding tiles_per_block consecutive 128-row
+// tiles of one group.  Requirements: T is __half or __nv_bfloat16, 64 <= n_centroids <=
 // 256, x aligned to SUB * sizeof(T) bytes.
 #pragma once
 
@@ -147,10 +147,11 @@ struct TcLayout {
 
 // ------------------------------------------------------------------ kernel
 
-template <typename T, int SUB, int NCOL, int TILES, int GC, int MINB>
+template <typename T, int SUB, int NCOL, int GC, int MINB>
 __global__ void __launch_bounds__(128, MINB)
     encode_tc(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
-              int32_t n_centroids, int64_t tiles_per_group, float one, uint32_t *__restrict__ out)
+              int32_t n_centroids, int64_t blocks_per_group, int32_t tiles_per_block, float one,
+              uint32_t *__restrict__ out)
 {
     static_assert(SUB == 4 || SUB == 8, "sub_dim 4 or 8");
     static_assert(NCOL == 32 || NCOL == 64 || NCOL == 128 || NCOL == 256, "tensor-memory columns");
@@ -179,12 +180,12 @@ __global__ void __launch_bounds__(128, MINB)
     const int warp = tid >> 5, lane = tid & 31;
     const int n_pad = L::padded(n_centroids);
     const int n_groups_c = L::groups(n_centroids);
-    const int64_t g = blockIdx.x / tiles_per_group;
-    const int64_t blk = blockIdx.x - g * tiles_per_group;
+    const int64_t g = blockIdx.x / blocks_per_group;
+    const int64_t blk = blockIdx.x - g * blocks_per_group;
     const T *__restrict__ cb = codebooks + (size_t)g * (size_t)n_centroids * SUB;
     const T *__restrict__ xg = x + (size_t)g * (size_t)n_per_group * SUB;
     uint32_t *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
-    const int64_t row_base = blk * (int64_t)(128 * TILES);
+    const int64_t row_base = blk * (int64_t)tiles_per_block * 128;
 
     // ---- set-up: maxima, barrier, tensor memory, constant part of A
     if (tid < SUB + 2) misc[tid] = 0u;
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(128, MINB)
 
     uint32_t phase = 0;
     bool alive = true;
-    for (int tile = 0; tile < TILES; ++tile) {
+    for (int tile = 0; tile < tiles_per_block; ++tile) {
         const int64_t row = row_base + (int64_t)tile * 128 + tid;
         if (row_base + (int64_t)tile * 128 >= n_per_group) break;  // block-uniform
 
