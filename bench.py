@@ -140,6 +140,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max(values, device) -> list:
+    """Element-wise maximum of ``values`` over all ranks of the default process
+    group (the values themselves when running as a single process)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_throughput(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job rate: every rank encodes its own workload of ``units_per_rank``
+    sub-vectors; the job takes as long as the slowest rank."""
+    return units_per_rank * world / seconds_max
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -275,10 +293,7 @@ def bench_ours(args) -> None:
         dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kernel_ms = sum(step_ms) / len(step_ms)
-    t = torch.tensor([kernel_ms, region_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    kernel_ms, region_s = float(t[0]), float(t[1])
+    kernel_ms, region_s = reduce_max([kernel_ms, region_s], dev)
 
     # end to end through the host entry point: pinned host in, pinned host out
     xh = torch.from_numpy(x).pin_memory()
@@ -293,11 +308,9 @@ def bench_ours(args) -> None:
     for _ in range(e2e_steps):
         vq.vq_encode_grouped_host(xh, cbh, outh, xd, cbd, out, stream=stream)
     e2e_s = time.perf_counter() - e0
-    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    (e2e_s,) = reduce_max([e2e_s], dev)
     if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
         dist.barrier()
-    e2e_s = float(te[0])
 
     if rank != 0:
         if world > 1:
@@ -312,7 +325,7 @@ def bench_ours(args) -> None:
     sm_max = peaks.get("sm_max_mhz") or clk["sm_max_mhz"] or 2070.0
     peak_tflops = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
     units = w.n
-    value = units * world / (kernel_ms * 1e-3)
+    value = job_throughput(units, world, kernel_ms * 1e-3)
     achieved = flops_per_subvector(w) * units / (kernel_ms * 1e-3) / 1e12
     roofline = {
         "bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
@@ -336,7 +349,7 @@ def bench_ours(args) -> None:
         "gpu_launches": args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": roofline,
-        "e2e": {"value": units * world * e2e_steps / e2e_s, "unit": UNIT,
+        "e2e": {"value": job_throughput(units * e2e_steps, world, e2e_s), "unit": UNIT,
                 "h2d_bytes_per_step": x.nbytes + cb.nbytes,
                 "d2h_bytes_per_step": int(units * 4),
                 "path": "vq_encode_grouped_host with pinned host buffers: the kernel reads x and "
