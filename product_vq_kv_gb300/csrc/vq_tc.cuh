@@ -122,8 +122,10 @@ struct TcLayout {
     static constexpr int kK = SUB == 4 ? 8 : 16;       // MMA K (tf32 elements), 8 per instruction
     static constexpr int kRowBytes = kK * 4;
     static constexpr int kGC = GC;                       // centroids per screening group
-    static constexpr int kX4 = SUB / 4;                  // float4 per centroid, exact layout
-    static constexpr int kGroupStride = kGC * kX4 + 1;   // float4, one pad per group
+    // exact layout: per group, centroid pairs interleaved -- component i of
+    // centroids (2p, 2p+1) is the float2 (-c_2p_i, -c_2p+1_i) -- so one packed
+    // f32x2 evaluation covers two centroids; one 16-byte pad per group
+    static constexpr int kGroupFloats = kGC * SUB + 4;
     static constexpr int kCtasPerSm = 512 / NCOL;
     __host__ __device__ static int padded(int nc) { return (nc + 31) / 32 * 32; }
     __host__ __device__ static int groups(int nc) { return padded(nc) / kGC; }
@@ -133,7 +135,7 @@ struct TcLayout {
     __host__ __device__ static size_t x_off(int nc) { return b_off() + (size_t)256 * kRowBytes; }
     __host__ __device__ static size_t misc_off(int nc)
     {
-        return x_off(nc) + (size_t)groups(nc) * kGroupStride * 16;
+        return x_off(nc) + (size_t)groups(nc) * kGroupFloats * 4;
     }
     // misc: SUB + 1 maxima, queue counter, tensor-memory address, pad, mbarrier (8-aligned), queue
     __host__ __device__ static size_t used(int nc) { return misc_off(nc) + 64 + 128 * 4; }
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(128, MINB)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *sa = reinterpret_cast<float *>(sm + L::a_off());
     float *sb = reinterpret_cast<float *>(sm + L::b_off());
-    float4 *sx = reinterpret_cast<float4 *>(sm + L::x_off(n_centroids));
+    float *sx = reinterpret_cast<float *>(sm + L::x_off(n_centroids));
     uint32_t *misc = reinterpret_cast<uint32_t *>(sm + L::misc_off(n_centroids));
     uint32_t *smax = misc;              // [0] = C2, [1 + i] = A_i
     uint32_t *qcount = misc + SUB + 1;
@@ -238,11 +240,9 @@ __global__ void __launch_bounds__(128, MINB)
             *reinterpret_cast<float4 *>(sb + ((c >> 3) * (kKB * 128) + kb * 128 + (c & 7) * 16) / 4) =
                 make_float4(bk[4 * kb], bk[4 * kb + 1], bk[4 * kb + 2], bk[4 * kb + 3]);
         if (c < n_pad) {
-            float4 *ex = sx + (c / kGC) * L::kGroupStride + (c % kGC) * L::kX4;
+            float *ex = sx + (c / kGC) * L::kGroupFloats + ((c % kGC) >> 1) * (2 * SUB) + (c & 1);
 #pragma unroll
-            for (int k = 0; k < SUB / 4; ++k)
-                ex[k] = real ? make_float4(-v[4 * k], -v[4 * k + 1], -v[4 * k + 2], -v[4 * k + 3])
-                             : make_float4(__int_as_float(0x7fc00000), 0.f, 0.f, 0.f);
+            for (int i = 0; i < SUB; ++i) ex[2 * i] = real ? -v[i] : __int_as_float(0x7fc00000);
         }
         // maxima over the block's centroids: warp reduction, then one atomic per
         // warp (nonnegative floats, and NaN above +inf, order as their bits)
@@ -378,26 +378,35 @@ __global__ void __launch_bounds__(128, MINB)
             id = kQueued;
             if (row < n_per_group) queue[atomicAdd(qcount, 1u)] = (uint32_t)tid;
         } else {
+            // exact distances, two centroids per packed evaluation, ascending
+            // index with a strict "<" (lowest index wins ties)
+            float2 xx[SUB];
+#pragma unroll
+            for (int i = 0; i < SUB; ++i) xx[i] = make_float2(xr[i], xr[i]);
+            const float2 one2 = make_float2(one, one);
             float best = __int_as_float(0x7f800000);
             for (int pass = 0; pass < 2; ++pass) {
                 const int gsel = pass == 0 ? ga : gb;
                 if (gsel < 0) break;
-                const float4 *gp = sx + gsel * L::kGroupStride;
+                const float *gp = sx + gsel * L::kGroupFloats;  // per-lane group: divergent reads
 #pragma unroll 4
-                for (int cc = 0; cc < kGC; ++cc) {
-                    float nc[SUB];
+                for (int pr = 0; pr < kGC / 2; ++pr) {
+                    float2 nc[SUB];
 #pragma unroll
-                    for (int k = 0; k < SUB / 4; ++k) {
-                        const float4 q = gp[cc * L::kX4 + k];
-                        nc[4 * k] = q.x;
-                        nc[4 * k + 1] = q.y;
-                        nc[4 * k + 2] = q.z;
-                        nc[4 * k + 3] = q.w;
+                    for (int k = 0; k < SUB / 2; ++k) {
+                        const float4 q = *reinterpret_cast<const float4 *>(gp + pr * 2 * SUB + 4 * k);
+                        nc[2 * k] = make_float2(q.x, q.y);
+                        nc[2 * k + 1] = make_float2(q.z, q.w);
                     }
-                    const float d = one_dist<SUB>(xr, nc, one);
-                    if (d < best) {
-                        best = d;
-                        id = (uint32_t)(gsel * kGC + cc);
+                    const float2 dd = pair_dist<SUB>(xx, nc, one2);
+                    const uint32_t c0 = (uint32_t)(gsel * kGC + 2 * pr);
+                    if (dd.x < best) {
+                        best = dd.x;
+                        id = c0;
+                    }
+                    if (dd.y < best) {
+                        best = dd.y;
+                        id = c0 + 1;
                     }
                 }
             }
@@ -415,16 +424,10 @@ __global__ void __launch_bounds__(128, MINB)
             float best = __int_as_float(0x7f800000);
             uint32_t bi = kQueued;
             for (int c = lane; c < n_centroids; c += 32) {
-                const float4 *cp = sx + (c / kGC) * L::kGroupStride + (c % kGC) * L::kX4;
+                const float *cp = sx + (c / kGC) * L::kGroupFloats + ((c % kGC) >> 1) * (2 * SUB) + (c & 1);
                 float nc[SUB];
 #pragma unroll
-                for (int k = 0; k < SUB / 4; ++k) {
-                    const float4 qv = cp[k];
-                    nc[4 * k] = qv.x;
-                    nc[4 * k + 1] = qv.y;
-                    nc[4 * k + 2] = qv.z;
-                    nc[4 * k + 3] = qv.w;
-                }
+                for (int i = 0; i < SUB; ++i) nc[i] = cp[2 * i];
                 const float d = one_dist<SUB>(xq, nc, one);
                 if (d < best) {
                     best = d;
