@@ -362,6 +362,57 @@ def bench_ours(args) -> None:
         dist.destroy_process_group()
 
 
+def bench_dequantize(args) -> None:
+    """Decode throughput: 8-bit codes of the workload back to fp16 sub-vectors
+    (one ``vq_dequantize_grouped`` per step), against the HBM roofline."""
+    import torch
+
+    from product_vq_kv_gb300.build import build
+
+    build()
+    import product_vq_kv_gb300 as vq
+
+    dev = torch.device("cuda", 0)
+    w = workloads.WORKLOADS[args.workload]
+    x, cb = workloads.generate(args.workload)
+    xd, cbd = torch.from_numpy(x).to(dev), torch.from_numpy(cb).to(dev)
+    codes = vq.vq_encode_grouped_u8(xd, cbd)
+    out = torch.empty_like(xd)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        vq.vq_dequantize_grouped(codes, cbd, out=out, stream=stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(0) as clocks:
+        for k in range(args.steps):
+            flush.zero_()
+            starts[k].record(stream)
+            vq.vq_dequantize_grouped(codes, cbd, out=out, stream=stream)
+            ends[k].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    bytes_per_unit = 1 + 2 * w.sub_dim  # uint8 code in, fp16 row out
+    achieved = bytes_per_unit * w.n / (ms * 1e-3) / 1e9
+    peak = measured_peaks().get("hbm_gbs") or 6800.0
+    clk = clocks.summary()
+    line = {
+        "metric": "sub-vectors decoded/sec (1xGB300)", "value": w.n / (ms * 1e-3),
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8->f16", "data": "synthetic", "op": "dequantize",
+        "config": config_block(w, args, 1), "gpu_launches": args.steps,
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "bytes_per_unit": bytes_per_unit, "units_per_launch": w.n},
+        "e2e": None,
+    }
+    print(json.dumps(line))
+
+
 def main() -> None:
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -370,11 +421,14 @@ def main() -> None:
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="falcon_prefill")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--op", choices=["encode", "dequantize"], default="encode")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
         bench_reference(args)
+    elif args.op == "dequantize":
+        bench_dequantize(args)
     else:
         bench_ours(args)
 

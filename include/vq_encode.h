@@ -118,6 +118,36 @@ vq_status vq_encode_grouped_host(const void *x_host, const void *codebooks_host,
                                  void *x_dev, void *codebooks_dev, uint32_t *out_dev,
                                  vq_stream_t stream);
 
+/*
+ * vq_encode_grouped_u8 -- vq_encode_grouped writing 8-bit codes: the same
+ * indices, one byte each ("What Even Is a KV Cache": 16 indices at 8 bits
+ * each for a 128-dim key, the 16x compression).  Requires n_centroids <= 256
+ * (VQ_ERR_UNSUPPORTED otherwise).
+ *   out_idx    [n_groups][n_per_group]   device, uint8, written
+ * Same arguments, rules and asynchrony as vq_encode_grouped.
+ */
+vq_status vq_encode_grouped_u8(const void *x, const void *codebooks, int64_t n_groups,
+                               int64_t n_per_group, int32_t n_centroids, int32_t sub_dim,
+                               vq_dtype dtype, uint8_t *out_idx, vq_stream_t stream);
+
+/*
+ * vq_dequantize_grouped -- decode ("dequantize_vq"): rebuild each sub-vector
+ * as a copy of its codebook row ("I Wrote a Metal Kernel to Stop My Mac From
+ * OOMing", section "Mistake 1: I Wrote the Dequant Kernel First": indices in,
+ * reconstructed vectors out, a gather).
+ *   idx        [n_groups][n_per_group]              device, uint32 (index_bytes
+ *                                                   = 4) or uint8 (index_bytes = 1)
+ *   codebooks  [n_groups][n_centroids][sub_dim]     device, dtype
+ *   out        [n_groups][n_per_group][sub_dim]     device, dtype, written
+ * out[g][m][:] = codebooks[g][idx[g][m]][:] bit for bit; an index outside
+ * [0, n_centroids) writes a row of zeros.  Same pointer, size and error rules
+ * as vq_encode_grouped (index_bytes other than 1 or 4: VQ_ERR_INVALID_ARG);
+ * asynchronous on `stream`.
+ */
+vq_status vq_dequantize_grouped(const void *idx, int32_t index_bytes, const void *codebooks,
+                                int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                                int32_t sub_dim, vq_dtype dtype, void *out, vq_stream_t stream);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char *vq_status_string(vq_status status);
 

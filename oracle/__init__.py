@@ -143,6 +143,28 @@ class OracleLib:
         return out
 
 
+def dequantize(idx: np.ndarray, codebooks: np.ndarray) -> np.ndarray:
+    """Decode ("dequantize_vq"): each index becomes a copy of its codebook row.
+
+    Source: "I Wrote a Metal Kernel to Stop My Mac From OOMing", section
+    "Mistake 1: I Wrote the Dequant Kernel First" -- the operation takes
+    codebook indices and reconstructs the vectors, a gather (``mx.take``).
+    ``idx`` is ``[G, M]`` (any integer dtype), ``codebooks`` ``[G, n_c, sub]``
+    (any dtype, including raw bf16 bits as uint16); returns ``[G, M, sub]`` in
+    the codebooks' dtype.  Reading where the page is silent: an index outside
+    ``[0, n_c)`` decodes to a row of zeros.
+    """
+    idx = np.asarray(idx)
+    codebooks = np.asarray(codebooks)
+    g, m = idx.shape
+    n_c, sub = codebooks.shape[1], codebooks.shape[2]
+    out = np.zeros((g, m, sub), dtype=codebooks.dtype)
+    for k in range(g):
+        valid = idx[k].astype(np.int64) < n_c
+        out[k, valid] = codebooks[k, idx[k][valid].astype(np.int64)]
+    return out
+
+
 def default() -> OracleLib:
     global _default
     with _lock:

@@ -18,9 +18,11 @@ from ._binding import (  # noqa: F401
     load_library,
     vq_abi_version,
     vq_describe_launch,
+    vq_dequantize_grouped,
     vq_encode,
     vq_encode_grouped,
     vq_encode_grouped_host,
+    vq_encode_grouped_u8,
     vq_status_string,
 )
 from .build import LIB_PATH  # noqa: F401

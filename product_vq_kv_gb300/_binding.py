@@ -52,6 +52,10 @@ def load_library() -> ctypes.CDLL:
         lib.vq_encode_grouped_host.restype = i32
         lib.vq_encode_grouped_host.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp, vp,
                                                vp, vp]
+        lib.vq_encode_grouped_u8.restype = i32
+        lib.vq_encode_grouped_u8.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp]
+        lib.vq_dequantize_grouped.restype = i32
+        lib.vq_dequantize_grouped.argtypes = [vp, i32, vp, i64, i64, i32, i32, i32, vp, vp]
         lib.vq_status_string.restype = ctypes.c_char_p
         lib.vq_status_string.argtypes = [i32]
         lib.vq_describe_launch.restype = i32
@@ -145,6 +149,59 @@ def vq_encode_grouped(x: torch.Tensor, codebooks: torch.Tensor,
                                           codebooks.shape[1], sub, _dtype_code(x),
                                           out.data_ptr(), _stream_handle(stream, x.device))
     _check(st, "vq_encode_grouped")
+    return out
+
+
+def vq_encode_grouped_u8(x: torch.Tensor, codebooks: torch.Tensor,
+                         out: torch.Tensor | None = None,
+                         stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Grouped encode to 8-bit codes (at most 256 centroids): the indices of
+    :func:`vq_encode_grouped` as a ``[G, M]`` uint8 tensor."""
+    _device_tensor(x, "x")
+    _device_tensor(codebooks, "codebooks")
+    if (x.dim() != 3 or codebooks.dim() != 3 or x.shape[0] != codebooks.shape[0]
+            or x.shape[2] != codebooks.shape[2]):
+        raise ValueError(f"expected x [G, M, sub_dim] and codebooks [G, n_centroids, sub_dim], "
+                         f"got {tuple(x.shape)} and {tuple(codebooks.shape)}")
+    if x.dtype != codebooks.dtype:
+        raise TypeError("x and codebooks must share a dtype")
+    g, m, sub = x.shape
+    if out is None:
+        out = torch.empty((g, m), dtype=torch.uint8, device=x.device)
+    elif out.dtype != torch.uint8 or out.shape != (g, m) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous uint8 tensor of shape [G, M]")
+    st = load_library().vq_encode_grouped_u8(x.data_ptr(), codebooks.data_ptr(), g, m,
+                                             codebooks.shape[1], sub, _dtype_code(x),
+                                             out.data_ptr(), _stream_handle(stream, x.device))
+    _check(st, "vq_encode_grouped_u8")
+    return out
+
+
+def vq_dequantize_grouped(idx: torch.Tensor, codebooks: torch.Tensor,
+                          out: torch.Tensor | None = None,
+                          stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Decode ``idx`` ``[G, M]`` (uint32 or uint8) against ``codebooks``
+    ``[G, n_centroids, sub_dim]``: returns (or fills ``out``) the ``[G, M,
+    sub_dim]`` tensor of codebook rows, in the codebooks' dtype; out-of-range
+    indices give zero rows.  Asynchronous on ``stream``."""
+    _device_tensor(idx, "idx")
+    _device_tensor(codebooks, "codebooks")
+    if idx.dtype not in (torch.uint32, torch.uint8):
+        raise TypeError("idx must be uint32 or uint8")
+    if idx.dim() != 2 or codebooks.dim() != 3 or idx.shape[0] != codebooks.shape[0]:
+        raise ValueError(f"expected idx [G, M] and codebooks [G, n_centroids, sub_dim], got "
+                         f"{tuple(idx.shape)} and {tuple(codebooks.shape)}")
+    g, m = idx.shape
+    n_c, sub = codebooks.shape[1], codebooks.shape[2]
+    if out is None:
+        out = torch.empty((g, m, sub), dtype=codebooks.dtype, device=idx.device)
+    elif out.dtype != codebooks.dtype or out.shape != (g, m, sub) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of shape [G, M, sub_dim] in the "
+                         "codebooks' dtype")
+    st = load_library().vq_dequantize_grouped(
+        idx.data_ptr(), 4 if idx.dtype == torch.uint32 else 1, codebooks.data_ptr(), g, m, n_c,
+        sub, _dtype_code(codebooks), out.data_ptr(), _stream_handle(stream, idx.device))
+    _check(st, "vq_dequantize_grouped")
     return out
 
 

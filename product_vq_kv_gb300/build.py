@@ -19,7 +19,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libvqenc.so")
 PTXAS_LOG = os.path.join(LIB_DIR, "ptxas.txt")
 SOURCES = [os.path.join(CSRC, "vq_encode.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, "vq_kernels.cuh"), os.path.join(CSRC, "vq_filter.cuh"), os.path.join(CSRC, "vq_tc.cuh"),
+DEPENDS = SOURCES + [os.path.join(CSRC, "vq_kernels.cuh"), os.path.join(CSRC, "vq_filter.cuh"), os.path.join(CSRC, "vq_tc.cuh"), os.path.join(CSRC, "vq_decode.cuh"),
                      os.path.join(ROOT, "include", "vq_encode.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

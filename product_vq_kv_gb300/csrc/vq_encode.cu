@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "vq_encode.h"
+#include "vq_decode.cuh"
 #include "vq_filter.cuh"
 #include "vq_tc.cuh"
 #include "vq_kernels.cuh"
@@ -113,8 +114,9 @@ struct Args {
     int32_t n_centroids;
     int32_t sub_dim;
     vq_dtype dtype;
-    uint32_t *out;
+    void *out;
     cudaStream_t stream;
+    int out_bytes = 4;  // index width: 4 (uint32) or 1 (uint8 codes)
 };
 
 size_t elem_size(vq_dtype d) { return d == VQ_F32 ? 4 : 2; }
@@ -125,6 +127,7 @@ vq_status validate(const Args &a, bool need_pointers)
     if (a.n_groups < 0 || a.n_per_group < 0) return VQ_ERR_INVALID_ARG;
     if (a.sub_dim < 1 || a.sub_dim > kMaxSubDim) return VQ_ERR_UNSUPPORTED;
     if (a.n_centroids < 1 || a.n_centroids > kMaxCentroids) return VQ_ERR_UNSUPPORTED;
+    if (a.out_bytes == 1 && a.n_centroids > 256) return VQ_ERR_UNSUPPORTED;  // 8-bit codes
     if (a.n_groups != 0 && a.n_per_group > INT64_MAX / a.n_groups) return VQ_ERR_INVALID_ARG;
     const int64_t rows = a.n_groups * a.n_per_group;
     if (rows == 0) return VQ_OK;
@@ -132,7 +135,7 @@ vq_status validate(const Args &a, bool need_pointers)
     if (need_pointers) {
         if (!a.x || !a.cb || !a.out) return VQ_ERR_INVALID_ARG;
         const size_t es = elem_size(a.dtype);
-        if ((uintptr_t)a.x % es || (uintptr_t)a.cb % es || (uintptr_t)a.out % 4)
+        if ((uintptr_t)a.x % es || (uintptr_t)a.cb % es || (uintptr_t)a.out % a.out_bytes)
             return VQ_ERR_INVALID_ARG;
     }
     return VQ_OK;
@@ -162,11 +165,11 @@ size_t tc_smem(int32_t n_centroids)
     return vqk::TcLayout<SUB, C::kCols, C::kGroup>::bytes(n_centroids);
 }
 
-template <typename T, int SUB>
+template <typename T, int SUB, typename OutT = uint32_t>
 auto tc_kernel()
 {
     using C = TcConfig<SUB>;
-    return vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks>;
+    return vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks, OutT>;
 }
 
 // Resident tensor-core CTAs on the device: the register budget of the launch
@@ -225,23 +228,23 @@ Plan make_plan(const Args &a)
     return p;
 }
 
-template <typename T, int SUB>
+template <typename T, int SUB, typename OutT>
 vq_status launch_tc(const Args &a, const Plan &p)
 {
-    auto kernel = tc_kernel<T, SUB>();
+    auto kernel = tc_kernel<T, SUB, OutT>();
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
         return VQ_ERR_CUDA;
     kernel<<<(unsigned)p.blocks, 128, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
-        p.tiles_per_group, p.tc_tiles, 1.0f, a.out);
+        p.tiles_per_group, p.tc_tiles, 1.0f, static_cast<OutT *>(a.out));
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
-template <typename T, int SUB>
+template <typename T, int SUB, typename OutT>
 vq_status launch_filter(const Args &a, const Plan &p)
 {
-    auto kernel = vqk::encode_filter<T, SUB, kFRows, kFThreads, kFGroup>;
+    auto kernel = vqk::encode_filter<T, SUB, kFRows, kFThreads, kFGroup, OutT>;
     if (p.smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)p.smem) != cudaSuccess)
@@ -249,14 +252,14 @@ vq_status launch_filter(const Args &a, const Plan &p)
     }
     kernel<<<(unsigned)p.blocks, p.threads, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
-        p.tiles_per_group, 1.0f, a.out);
+        p.tiles_per_group, 1.0f, static_cast<OutT *>(a.out));
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
-template <typename T, int SUB>
+template <typename T, int SUB, typename OutT>
 vq_status launch_fast(const Args &a, const Plan &p)
 {
-    auto kernel = vqk::encode_fast<T, SUB, kRows, kThreads, kMode, kGroupCentroids>;
+    auto kernel = vqk::encode_fast<T, SUB, kRows, kThreads, kMode, kGroupCentroids, OutT>;
     if (p.smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)p.smem) != cudaSuccess)
@@ -264,30 +267,43 @@ vq_status launch_fast(const Args &a, const Plan &p)
     }
     kernel<<<(unsigned)p.blocks, p.threads, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
-        p.tiles_per_group, 1.0f, a.out);
+        p.tiles_per_group, 1.0f, static_cast<OutT *>(a.out));
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
-template <typename T>
+template <typename T, typename OutT>
 vq_status launch_general(const Args &a, const Plan &p)
 {
-    vqk::encode_general<T><<<(unsigned)p.blocks, p.threads, 0, a.stream>>>(
+    vqk::encode_general<T, OutT><<<(unsigned)p.blocks, p.threads, 0, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_groups, a.n_per_group,
-        a.n_centroids, a.sub_dim, 1.0f, a.out);
+        a.n_centroids, a.sub_dim, 1.0f, static_cast<OutT *>(a.out));
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
-template <typename T>
+template <typename T, typename OutT>
 vq_status launch_typed(const Args &a, const Plan &p)
 {
     switch (p.kind) {
     case kTc:
         if constexpr (sizeof(T) == 2)
-            return a.sub_dim == 4 ? launch_tc<T, 4>(a, p) : launch_tc<T, 8>(a, p);
+            return a.sub_dim == 4 ? launch_tc<T, 4, OutT>(a, p) : launch_tc<T, 8, OutT>(a, p);
         return VQ_ERR_INTERNAL;
-    case kFilter: return a.sub_dim == 4 ? launch_filter<T, 4>(a, p) : launch_filter<T, 8>(a, p);
-    case kBrute: return a.sub_dim == 4 ? launch_fast<T, 4>(a, p) : launch_fast<T, 8>(a, p);
-    case kGeneral: return launch_general<T>(a, p);
+    case kFilter:
+        return a.sub_dim == 4 ? launch_filter<T, 4, OutT>(a, p) : launch_filter<T, 8, OutT>(a, p);
+    case kBrute:
+        return a.sub_dim == 4 ? launch_fast<T, 4, OutT>(a, p) : launch_fast<T, 8, OutT>(a, p);
+    case kGeneral: return launch_general<T, OutT>(a, p);
+    }
+    return VQ_ERR_INTERNAL;
+}
+
+template <typename OutT>
+vq_status launch_dtype(const Args &a, const Plan &p)
+{
+    switch (a.dtype) {
+    case VQ_F16: return launch_typed<__half, OutT>(a, p);
+    case VQ_BF16: return launch_typed<__nv_bfloat16, OutT>(a, p);
+    case VQ_F32: return launch_typed<float, OutT>(a, p);
     }
     return VQ_ERR_INTERNAL;
 }
@@ -299,12 +315,7 @@ vq_status run(const Args &a)
     if (a.n_groups * a.n_per_group == 0) return VQ_OK;
     const Plan p = make_plan(a);
     if (p.blocks > 0x7fffffffLL) return VQ_ERR_UNSUPPORTED;
-    switch (a.dtype) {
-    case VQ_F16: return launch_typed<__half>(a, p);
-    case VQ_BF16: return launch_typed<__nv_bfloat16>(a, p);
-    case VQ_F32: return launch_typed<float>(a, p);
-    }
-    return VQ_ERR_INTERNAL;
+    return a.out_bytes == 1 ? launch_dtype<uint8_t>(a, p) : launch_dtype<uint32_t>(a, p);
 }
 
 const char *dtype_name(vq_dtype d)
@@ -411,7 +422,7 @@ vq_status vq_encode_grouped_host(const void *x_host, const void *codebooks_host,
             cudaSuccess)
             return VQ_ERR_CUDA;
         Args z{x_view, codebooks_dev, n_groups, n_per_group, n_centroids, sub_dim, dtype,
-               static_cast<uint32_t *>(out_view), st};
+               out_view, st};
         s = run(z);
         if (s != VQ_OK) return s;
         return cudaStreamSynchronize(st) == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
@@ -478,6 +489,88 @@ vq_status vq_encode_grouped_host(const void *x_host, const void *codebooks_host,
          cudaStreamWaitEvent(st, hp.start, 0) == cudaSuccess &&
          cudaStreamSynchronize(hp.d2h) == cudaSuccess;
     return ok ? VQ_OK : VQ_ERR_CUDA;
+}
+
+vq_status vq_encode_grouped_u8(const void *x, const void *codebooks, int64_t n_groups,
+                               int64_t n_per_group, int32_t n_centroids, int32_t sub_dim,
+                               vq_dtype dtype, uint8_t *out_idx, vq_stream_t stream)
+{
+    Args a{x, codebooks, n_groups, n_per_group, n_centroids, sub_dim, dtype, out_idx,
+           reinterpret_cast<cudaStream_t>(stream)};
+    a.out_bytes = 1;
+    return run(a);
+}
+
+vq_status vq_dequantize_grouped(const void *idx, int32_t index_bytes, const void *codebooks,
+                                int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                                int32_t sub_dim, vq_dtype dtype, void *out, vq_stream_t stream)
+{
+    if (dtype != VQ_F16 && dtype != VQ_BF16 && dtype != VQ_F32) return VQ_ERR_INVALID_ARG;
+    if (index_bytes != 1 && index_bytes != 4) return VQ_ERR_INVALID_ARG;
+    if (n_groups < 0 || n_per_group < 0) return VQ_ERR_INVALID_ARG;
+    if (sub_dim < 1 || sub_dim > kMaxSubDim) return VQ_ERR_UNSUPPORTED;
+    if (n_centroids < 1 || n_centroids > kMaxCentroids) return VQ_ERR_UNSUPPORTED;
+    if (n_groups != 0 && n_per_group > INT64_MAX / n_groups) return VQ_ERR_INVALID_ARG;
+    const int64_t rows = n_groups * n_per_group;
+    if (rows == 0) return VQ_OK;
+    if (rows > INT64_MAX / (sub_dim * 4)) return VQ_ERR_INVALID_ARG;
+    if (!idx || !codebooks || !out) return VQ_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if ((uintptr_t)idx % index_bytes || (uintptr_t)codebooks % es || (uintptr_t)out % es)
+        return VQ_ERR_INVALID_ARG;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t row_bytes = (size_t)sub_dim * es;
+    const size_t align = row_bytes < 16 ? row_bytes : 16;
+    const bool fast = (row_bytes == 8 || row_bytes == 16 || row_bytes == 32) &&
+                      (uintptr_t)codebooks % align == 0 && (uintptr_t)out % align == 0;
+    if (fast) {
+        constexpr int kT = 256, kR = 8;
+        const int64_t per_group = (n_per_group + kT * kR - 1) / (kT * kR);
+        const int64_t blocks = n_groups * per_group;
+        if (blocks > 0x7fffffffLL) return VQ_ERR_UNSUPPORTED;
+        const auto *cb = static_cast<const unsigned char *>(codebooks);
+        auto *o = static_cast<unsigned char *>(out);
+        const unsigned nb = (unsigned)blocks;
+#define VQ_DECODE(IDXT, BYTES)                                                                     \
+    vqk::decode_rows<IDXT, BYTES, kT, kR><<<nb, kT, 0, st>>>(static_cast<const IDXT *>(idx), cb,     \
+                                                            n_per_group, n_centroids, per_group, o)
+        if (index_bytes == 4) {
+            if (row_bytes == 8) VQ_DECODE(uint32_t, 8);
+            else if (row_bytes == 16) VQ_DECODE(uint32_t, 16);
+            else VQ_DECODE(uint32_t, 32);
+        } else {
+            if (row_bytes == 8) VQ_DECODE(uint8_t, 8);
+            else if (row_bytes == 16) VQ_DECODE(uint8_t, 16);
+            else VQ_DECODE(uint8_t, 32);
+        }
+#undef VQ_DECODE
+    } else {
+        constexpr int kT = 256;
+        const int64_t total = rows * sub_dim;
+        const int64_t blocks = (total + kT - 1) / kT;
+        if (blocks > 0x7fffffffLL) return VQ_ERR_UNSUPPORTED;
+        const unsigned nb = (unsigned)blocks;
+        if (es == 2) {
+            if (index_bytes == 4)
+                vqk::decode_elems<uint32_t, uint16_t><<<nb, kT, 0, st>>>(
+                    static_cast<const uint32_t *>(idx), static_cast<const uint16_t *>(codebooks),
+                    n_groups, n_per_group, n_centroids, sub_dim, static_cast<uint16_t *>(out));
+            else
+                vqk::decode_elems<uint8_t, uint16_t><<<nb, kT, 0, st>>>(
+                    static_cast<const uint8_t *>(idx), static_cast<const uint16_t *>(codebooks),
+                    n_groups, n_per_group, n_centroids, sub_dim, static_cast<uint16_t *>(out));
+        } else {
+            if (index_bytes == 4)
+                vqk::decode_elems<uint32_t, uint32_t><<<nb, kT, 0, st>>>(
+                    static_cast<const uint32_t *>(idx), static_cast<const uint32_t *>(codebooks),
+                    n_groups, n_per_group, n_centroids, sub_dim, static_cast<uint32_t *>(out));
+            else
+                vqk::decode_elems<uint8_t, uint32_t><<<nb, kT, 0, st>>>(
+                    static_cast<const uint8_t *>(idx), static_cast<const uint32_t *>(codebooks),
+                    n_groups, n_per_group, n_centroids, sub_dim, static_cast<uint32_t *>(out));
+        }
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
 const char *vq_status_string(vq_status status)

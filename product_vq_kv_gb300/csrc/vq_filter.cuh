@@ -74,11 +74,11 @@ __device__ __forceinline__ float gamma_u(int k)
 // Launch: grid.x = n_groups * tiles_per_group, block = THREADS, dynamic shared
 // memory = FilterLayout<SUB, GC>::bytes(n_centroids, THREADS * R); `one` =
 // 1.0f.  Same tiling and alignment requirements as encode_fast.
-template <typename T, int SUB, int R, int THREADS, int GC>
+template <typename T, int SUB, int R, int THREADS, int GC, typename OutT = uint32_t>
 __global__ void __launch_bounds__(THREADS)
     encode_filter(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
                   int32_t n_centroids, int64_t tiles_per_group, float one,
-                  uint32_t *__restrict__ out)
+                  OutT *__restrict__ out)
 {
     static_assert(R % 2 == 0 && SUB % 4 == 0 && GC % 2 == 0, "layout constraints");
     using L = FilterLayout<SUB, GC>;
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(THREADS)
     const int64_t tile = blockIdx.x - g * tiles_per_group;
     const T *__restrict__ cb = codebooks + (size_t)g * (size_t)n_centroids * SUB;
     const T *__restrict__ xg = x + (size_t)g * (size_t)n_per_group * SUB;
-    uint32_t *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
+    OutT *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
     const int64_t row0 = tile * (int64_t)kTile + threadIdx.x;
 
     // Rows of this thread: row0 + r * THREADS, rows 2rp and 2rp+1 packed in
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(THREADS)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int64_t row = row0 + (int64_t)r * THREADS;
-        if (row < n_per_group && result[r] != kQueued) __stcs(og + row, result[r]);
+        if (row < n_per_group && result[r] != kQueued) store_index(og + row, result[r]);
     }
 
     // ---- queued rows: one warp per row, exact scan over all centroids
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(THREADS)
             }
         }
         // no finite, non-NaN distance anywhere: index 0, as the definition gives
-        if (lane == 0) __stcs(og + row, id == kQueued ? 0u : id);
+        if (lane == 0) store_index(og + row, id == kQueued ? 0u : id);
     }
 }
 

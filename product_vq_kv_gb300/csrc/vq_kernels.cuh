@@ -96,6 +96,10 @@ __device__ __forceinline__ void load_row(const T *__restrict__ p, float (&v)[SUB
     }
 }
 
+// Store one index: uint32 (streaming store) or uint8 codes.
+__device__ __forceinline__ void store_index(uint32_t *p, uint32_t v) { __stcs(p, v); }
+__device__ __forceinline__ void store_index(uint8_t *p, uint32_t v) { *p = (uint8_t)v; }
+
 // ------------------------------------------------------------------ arithmetic
 
 // Three-input fp32 minimum (sm_100+).  NaN inputs are ignored unless all are
@@ -286,11 +290,11 @@ __device__ __forceinline__ void read_centroid_scalar(const float4 *__restrict__ 
 // (b % tiles_per_group) of group (b / tiles_per_group); a tile is THREADS * R
 // consecutive rows of that group.  Requires x aligned to SUB * sizeof(T)
 // bytes (16 bytes at most), 1 <= n_centroids and the shared memory to fit.
-template <typename T, int SUB, int R, int THREADS, int MODE, int GC>
+template <typename T, int SUB, int R, int THREADS, int MODE, int GC, typename OutT = uint32_t>
 __global__ void __launch_bounds__(THREADS)
     encode_fast(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
                 int32_t n_centroids, int64_t tiles_per_group, float one,
-                uint32_t *__restrict__ out)
+                OutT *__restrict__ out)
 {
     static_assert(R % 2 == 0, "rows per thread come in packed pairs");
     static_assert(SUB % 2 == 0, "sub_dim must be even for the packed layout");
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(THREADS)
     const int64_t tile = blockIdx.x - g * tiles_per_group;
     const T *__restrict__ cb = codebooks + (size_t)g * (size_t)n_centroids * SUB;
     const T *__restrict__ xg = x + (size_t)g * (size_t)n_per_group * SUB;
-    uint32_t *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
+    OutT *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
     const int64_t row0 = tile * (int64_t)(THREADS * R) + threadIdx.x;
 
     // Rows of this thread: row0 + r * THREADS.  Rows past the end compute on
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(THREADS)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int64_t row = row0 + (int64_t)r * THREADS;
-        if (row < n_per_group) __stcs(og + row, result[r]);
+        if (row < n_per_group) store_index(og + row, result[r]);
     }
 }
 
@@ -428,10 +432,10 @@ __global__ void __launch_bounds__(THREADS)
 // size only: one thread per row, scalar fp32 arithmetic, x and the codebook
 // read through the read-only cache.
 // Launch: grid.x = ceil(n_groups * n_per_group / blockDim.x); `one` = 1.0f.
-template <typename T>
+template <typename T, typename OutT = uint32_t>
 __global__ void encode_general(const T *__restrict__ x, const T *__restrict__ codebooks,
                                int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
-                               int32_t sub_dim, float one, uint32_t *__restrict__ out)
+                               int32_t sub_dim, float one, OutT *__restrict__ out)
 {
     const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (row >= n_groups * n_per_group) return;
@@ -453,7 +457,7 @@ __global__ void encode_general(const T *__restrict__ x, const T *__restrict__ co
             idx = (uint32_t)c;
         }
     }
-    out[row] = idx;
+    store_index(out + row, idx);
 }
 
 }  // namespace vqk

@@ -149,11 +149,11 @@ struct TcLayout {
 
 // ------------------------------------------------------------------ kernel
 
-template <typename T, int SUB, int NCOL, int GC, int MINB>
+template <typename T, int SUB, int NCOL, int GC, int MINB, typename OutT = uint32_t>
 __global__ void __launch_bounds__(128, MINB)
     encode_tc(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
               int32_t n_centroids, int64_t blocks_per_group, int32_t tiles_per_block, float one,
-              uint32_t *__restrict__ out)
+              OutT *__restrict__ out)
 {
     static_assert(SUB == 4 || SUB == 8, "sub_dim 4 or 8");
     static_assert(NCOL == 32 || NCOL == 64 || NCOL == 128 || NCOL == 256, "tensor-memory columns");
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(128, MINB)
     const int64_t blk = blockIdx.x - g * blocks_per_group;
     const T *__restrict__ cb = codebooks + (size_t)g * (size_t)n_centroids * SUB;
     const T *__restrict__ xg = x + (size_t)g * (size_t)n_per_group * SUB;
-    uint32_t *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
+    OutT *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
     const int64_t row_base = blk * (int64_t)tiles_per_block * 128;
 
     // ---- set-up: maxima, barrier, tensor memory, constant part of A
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(128, MINB)
             tc_fence_after();
         }
         if (!alive) {
-            if (row < n_per_group) __stcs(og + row, kQueued);
+            if (row < n_per_group) store_index(og + row, kQueued);
             break;
         }
 
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(128, MINB)
                 }
             }
         }
-        if (row < n_per_group && id != kQueued) __stcs(og + row, id);
+        if (row < n_per_group && id != kQueued) store_index(og + row, id);
         __syncthreads();
 
         // ---- queued rows of this tile: one warp per row, exact scan
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(128, MINB)
                     bi = oi;
                 }
             }
-            if (lane == 0) __stcs(og + qrow, bi == kQueued ? 0u : bi);
+            if (lane == 0) store_index(og + qrow, bi == kQueued ? 0u : bi);
         }
 #pragma unroll
         for (int i = 0; i < SUB; ++i) xr[i] = xn[i];

@@ -31,6 +31,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("vq_encode", "vq_encode_grouped", "vq_encode_grouped_host",
+                     "vq_encode_grouped_u8", "vq_dequantize_grouped",
                      "vq_status_string", "vq_describe_launch", "vq_abi_version"):
         assert required in names
 

@@ -225,3 +225,33 @@ def test_empty_input(oracle_mod):
     assert oracle_mod.encode(x, cb).shape == (0,)
     assert oracle_mod.encode(np.zeros((3, 0, 8), np.float16),
                              np.zeros((3, 256, 8), np.float16)).shape == (3, 0)
+
+
+# ---------------------------------------------------------------- decode
+
+def test_dequantize_identity_permutation_and_range(oracle_mod):
+    rng = np.random.default_rng(110)
+    cb = rng.standard_normal((3, 256, 8)).astype(np.float16)
+    ar = np.tile(np.arange(256, dtype=np.uint32), (3, 1))
+    assert np.array_equal(oracle_mod.dequantize(ar, cb), cb)
+    perm = rng.permutation(256).astype(np.uint32)
+    got = oracle_mod.dequantize(np.tile(perm, (3, 1)), cb)
+    assert np.array_equal(got, cb[:, perm])
+    bad = np.array([[0, 255, 256, 1000, 0xFFFFFFFF]], dtype=np.uint32)
+    got = oracle_mod.dequantize(bad, cb[:1])
+    assert np.array_equal(got[0, :2], cb[0, [0, 255]])
+    assert not got[0, 2:].any()
+
+
+def test_encode_then_dequantize_round_trips_exact_copies(oracle_mod):
+    """Rows that are exact codebook copies come back unchanged; every other
+    row comes back as its nearest centroid (no centroid is strictly closer)."""
+    rng = np.random.default_rng(111)
+    cb = rng.standard_normal((2, 256, 4)).astype(np.float16)
+    x = rng.standard_normal((2, 3000, 4)).astype(np.float16)
+    x[:, :500] = cb[:, rng.integers(0, 256, 500)]
+    rec = oracle_mod.dequantize(oracle_mod.encode(x, cb), cb)
+    assert np.array_equal(rec[:, :500], x[:, :500])
+    d_rec = ((rec.astype(np.float64) - x) ** 2).sum(-1)
+    d_all = ((x.astype(np.float64)[:, :, None, :] - cb[:, None, :, :]) ** 2).sum(-1)
+    assert np.all(d_rec <= d_all.min(-1) * (1 + 1e-6) + 1e-12)
