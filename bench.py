@@ -413,6 +413,107 @@ def bench_dequantize(args) -> None:
     print(json.dumps(line))
 
 
+def bench_attention(args) -> None:
+    """Decode attention over the 8-bit product-VQ KV cache of the Llama-shape
+    workload (one ``vq_attention_decode`` per step: table build, scores,
+    softmax and value sum per token slice, then the merge of the slices),
+    reported as query-head x cached-token scores per second against the HBM
+    roofline of the code bytes it must read."""
+    import torch
+
+    from product_vq_kv_gb300.build import build
+
+    build()
+    import product_vq_kv_gb300 as vq
+
+    dev = torch.device("cuda", 0)
+    aw = workloads.ATTENTION_WORKLOADS["llama_attention"]
+    arrays = workloads.generate_attention(aw.name)
+    q, kc, kcb, vc, vcb = (torch.from_numpy(a).to(dev) for a in arrays)
+    out = torch.empty_like(q)
+    nbytes = vq.vq_attention_workspace_bytes(aw.batch, aw.heads_q, aw.heads_kv, aw.tokens,
+                                             aw.head_dim, aw.sub_dim, aw.n_centroids)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        vq.vq_attention_decode(q, kc, kcb, vc, vcb, out=out, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(0) as clocks:
+        for k in range(args.steps):
+            flush.zero_()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    scores = aw.batch * aw.heads_q * aw.tokens
+    # algorithmic bytes: key and value codes, queries and outputs, codebooks
+    small = 2 * aw.batch * aw.heads_q * aw.head_dim * 2 + 2 * aw.heads_kv * aw.n_centroids * aw.sub_dim * 2
+    algo_bytes = aw.code_bytes + small
+    achieved = algo_bytes / (ms * 1e-3) / 1e9
+    peak = measured_peaks().get("hbm_gbs") or 6800.0
+
+    # end to end: queries and codes copied from pinned host memory, the
+    # output read back, every step (a decode step that starts from a host cache)
+    hosts = [torch.from_numpy(a).pin_memory() for a in arrays]
+    dev_in = [torch.empty_like(h, device=dev) for h in hosts]
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for h in hosts)
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for d_, h_ in zip(dev_in, hosts):
+            d_.copy_(h_, non_blocking=True)
+        vq.vq_attention_decode(*dev_in, out=out, workspace=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        qh, kch, kcbh, vch, vcbh = arrays
+        t0 = time.perf_counter()
+        oracle.attention_decode(qh[:1], kch[:1], kcbh, vch[:1], vcbh)
+        dt = time.perf_counter() - t0
+        cpu = {"value": aw.heads_q * aw.tokens / dt, "unit": "scores/s", "cores": 1,
+               "kind": "oracle", "sample": f"batch row 0 of {aw.batch} ({aw.heads_q} query heads "
+               f"x {aw.tokens} tokens), numpy float64"}
+    clk = clocks.summary()
+    line = {
+        "metric": "decode-attention scores/sec over 8-bit VQ codes (1xGB300)",
+        "value": scores / (ms * 1e-3), "unit": "scores/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8 codes, f16 q/codebooks, f32 accumulate",
+        "data": "synthetic", "op": "attention",
+        "config": {"workload": aw.name, "batch": aw.batch, "heads_q": aw.heads_q,
+                   "heads_kv": aw.heads_kv, "tokens": aw.tokens, "head_dim": aw.head_dim,
+                   "sub_dim": aw.sub_dim, "n_centroids": aw.n_centroids,
+                   "l2": "flushed before every step (256 MiB write)"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "bytes_per_launch": algo_bytes,
+                     "timed": "whole step (partial + combine kernels)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": scores / e2e_s, "unit": "scores/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+    }
+    print(json.dumps(line))
+
+
 def main() -> None:
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -421,7 +522,7 @@ def main() -> None:
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="falcon_prefill")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--op", choices=["encode", "dequantize"], default="encode")
+    p.add_argument("--op", choices=["encode", "dequantize", "attention"], default="encode")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -429,6 +530,8 @@ def main() -> None:
         bench_reference(args)
     elif args.op == "dequantize":
         bench_dequantize(args)
+    elif args.op == "attention":
+        bench_attention(args)
     else:
         bench_ours(args)
 

@@ -46,6 +46,7 @@
 #ifndef VQ_ENCODE_H
 #define VQ_ENCODE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -147,6 +148,43 @@ vq_status vq_encode_grouped_u8(const void *x, const void *codebooks, int64_t n_g
 vq_status vq_dequantize_grouped(const void *idx, int32_t index_bytes, const void *codebooks,
                                 int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
                                 int32_t sub_dim, vq_dtype dtype, void *out, vq_stream_t stream);
+
+/*
+ * vq_attention_decode -- attention of one decode query per (batch, query
+ * head) over a KV cache held as 8-bit product-VQ codes, without rebuilding the
+ * keys or values ("I Wrote a Metal Kernel to Stop My Mac From OOMing",
+ * section "What's Next: Phase 2": the per-query LUT q @ codebook^T, scores by
+ * LUT lookup, softmax-weighted value sum in one fused pass).
+ *   q            [batch][heads_q][head_dim]                 device, dtype
+ *   k_codes      [batch][heads_kv][tokens][head_dim/sub_dim] device, uint8
+ *   k_codebooks  [heads_kv][n_centroids][sub_dim]           device, dtype
+ *   v_codes, v_codebooks                                    same, for values
+ *   out          [batch][heads_q][head_dim]                 device, dtype, written
+ *   workspace    >= vq_attention_workspace_bytes(...) bytes, device, 16-byte
+ *                aligned, scratch owned by the caller (smaller: fewer token
+ *                slices are used, down to one; too small for one: error)
+ * Query head h uses KV head h / (heads_q / heads_kv) (grouped-query
+ * attention).  With K^[t] and V^[t] the codebook rows the codes select:
+ *   out = softmax_t(scale * q . K^[t]) @ V^[t]
+ * over the last `window` tokens (0: all tokens); scale <= 0 means
+ * 1/sqrt(head_dim).  Accumulation is fp32; no tokens gives zeros.
+ * Requirements: heads_q % heads_kv == 0, head_dim % sub_dim == 0,
+ * head_dim <= 512, head_dim/sub_dim <= 64, n_centroids <= 256
+ * (VQ_ERR_INVALID_ARG / VQ_ERR_UNSUPPORTED otherwise).  Asynchronous on
+ * `stream`; the library allocates nothing.
+ */
+vq_status vq_attention_decode(const void *q, const uint8_t *k_codes, const void *k_codebooks,
+                              const uint8_t *v_codes, const void *v_codebooks, int64_t batch,
+                              int32_t heads_q, int32_t heads_kv, int64_t tokens, int32_t head_dim,
+                              int32_t sub_dim, int32_t n_centroids, int64_t window, float scale,
+                              vq_dtype dtype, void *out, void *workspace, size_t workspace_bytes,
+                              vq_stream_t stream);
+
+/* Workspace vq_attention_decode uses for these sizes on the current device
+ * (0 for invalid sizes). */
+size_t vq_attention_workspace_bytes(int64_t batch, int32_t heads_q, int32_t heads_kv,
+                                    int64_t tokens, int32_t head_dim, int32_t sub_dim,
+                                    int32_t n_centroids, int64_t window);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char *vq_status_string(vq_status status);

@@ -165,6 +165,47 @@ def dequantize(idx: np.ndarray, codebooks: np.ndarray) -> np.ndarray:
     return out
 
 
+def attention_decode(q, k_codes, k_codebooks, v_codes, v_codebooks, window: int = 0,
+                     scale: float = 0.0) -> np.ndarray:
+    """Decode attention over product-VQ codes, in float64.
+
+    Source: "I Wrote a Metal Kernel to Stop My Mac From OOMing", section
+    "What's Next: Phase 2" -- scores from a per-query table of q against the
+    codebook, looked up by the key codes, then softmax and the weighted sum of
+    the values.  Written here as what that computes: keys and values rebuilt
+    from their codes by :func:`dequantize` (so a code outside ``[0, n_c)`` is
+    a zero row), then ``softmax(scale * K^ q) @ V^`` for every (batch, query
+    head), query head ``h`` reading KV head ``h // (Hq / Hkv)``, over the last
+    ``window`` tokens (0: all).  Readings where the pages are silent: no
+    tokens gives zeros; ``scale <= 0`` means ``1 / sqrt(D)``.  ``q`` is
+    ``[B, Hq, D]`` (float16 or float32; bf16 decoded by the caller); codes
+    ``[B, Hkv, T, D / sub]``; codebooks ``[Hkv, n_c, sub]``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k_codes = np.asarray(k_codes)
+    v_codes = np.asarray(v_codes)
+    b, hq, d = q.shape
+    _, hkv, t, ns = k_codes.shape
+    qpk = hq // hkv
+    scale = scale if scale > 0 else 1.0 / np.sqrt(d)
+    first = t - window if 0 < window < t else 0
+    n = t - first
+    out = np.zeros((b, hq, d))
+    if n == 0:
+        return out
+    for bi in range(b):
+        for h in range(hkv):
+            keys = dequantize(k_codes[bi, h, first:].reshape(1, n * ns),
+                              np.asarray(k_codebooks)[h:h + 1]).astype(np.float64).reshape(n, d)
+            vals = dequantize(v_codes[bi, h, first:].reshape(1, n * ns),
+                              np.asarray(v_codebooks)[h:h + 1]).astype(np.float64).reshape(n, d)
+            for g in range(qpk):
+                logits = scale * (keys @ q[bi, h * qpk + g])
+                p = np.exp(logits - logits.max())
+                out[bi, h * qpk + g] = (p / p.sum()) @ vals
+    return out
+
+
 def default() -> OracleLib:
     global _default
     with _lock:

@@ -17,6 +17,8 @@ from ._binding import (  # noqa: F401
     VQError,
     load_library,
     vq_abi_version,
+    vq_attention_decode,
+    vq_attention_workspace_bytes,
     vq_describe_launch,
     vq_dequantize_grouped,
     vq_encode,

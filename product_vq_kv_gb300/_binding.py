@@ -56,6 +56,11 @@ def load_library() -> ctypes.CDLL:
         lib.vq_encode_grouped_u8.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp]
         lib.vq_dequantize_grouped.restype = i32
         lib.vq_dequantize_grouped.argtypes = [vp, i32, vp, i64, i64, i32, i32, i32, vp, vp]
+        lib.vq_attention_decode.restype = i32
+        lib.vq_attention_decode.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i64, i32, i32, i32,
+                                            i64, ctypes.c_float, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.vq_attention_workspace_bytes.restype = ctypes.c_size_t
+        lib.vq_attention_workspace_bytes.argtypes = [i64, i32, i32, i64, i32, i32, i32, i64]
         lib.vq_status_string.restype = ctypes.c_char_p
         lib.vq_status_string.argtypes = [i32]
         lib.vq_describe_launch.restype = i32
@@ -202,6 +207,54 @@ def vq_dequantize_grouped(idx: torch.Tensor, codebooks: torch.Tensor,
         idx.data_ptr(), 4 if idx.dtype == torch.uint32 else 1, codebooks.data_ptr(), g, m, n_c,
         sub, _dtype_code(codebooks), out.data_ptr(), _stream_handle(stream, idx.device))
     _check(st, "vq_dequantize_grouped")
+    return out
+
+
+def vq_attention_workspace_bytes(batch: int, heads_q: int, heads_kv: int, tokens: int,
+                                 head_dim: int, sub_dim: int, n_centroids: int,
+                                 window: int = 0) -> int:
+    return int(load_library().vq_attention_workspace_bytes(batch, heads_q, heads_kv, tokens,
+                                                           head_dim, sub_dim, n_centroids,
+                                                           window))
+
+
+def vq_attention_decode(q: torch.Tensor, k_codes: torch.Tensor, k_codebooks: torch.Tensor,
+                        v_codes: torch.Tensor, v_codebooks: torch.Tensor, window: int = 0,
+                        scale: float = 0.0, out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None,
+                        stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Decode attention over 8-bit product-VQ codes.
+
+    ``q`` ``[B, Hq, D]``; ``k_codes`` / ``v_codes`` ``[B, Hkv, T, D/sub_dim]``
+    uint8; ``k_codebooks`` / ``v_codebooks`` ``[Hkv, n_c, sub_dim]`` in q's
+    dtype.  Returns (or fills ``out``) ``[B, Hq, D]``.  ``workspace`` is a
+    device byte tensor for the per-slice partials; if omitted one of
+    :func:`vq_attention_workspace_bytes` bytes is allocated here (by torch).
+    """
+    for t, name in ((q, "q"), (k_codes, "k_codes"), (k_codebooks, "k_codebooks"),
+                    (v_codes, "v_codes"), (v_codebooks, "v_codebooks")):
+        _device_tensor(t, name)
+    if k_codes.dtype != torch.uint8 or v_codes.dtype != torch.uint8:
+        raise TypeError("codes must be uint8")
+    if k_codebooks.dtype != q.dtype or v_codebooks.dtype != q.dtype:
+        raise TypeError("codebooks must share q's dtype")
+    b, hq, d = q.shape
+    _, hkv, tokens, ns = k_codes.shape
+    n_c, sub = k_codebooks.shape[1], k_codebooks.shape[2]
+    if (k_codes.shape != v_codes.shape or k_codes.shape[0] != b or ns * sub != d
+            or k_codebooks.shape != (hkv, n_c, sub) or v_codebooks.shape != (hkv, n_c, sub)):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = vq_attention_workspace_bytes(b, hq, hkv, tokens, d, sub, n_c, window)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = load_library().vq_attention_decode(
+        q.data_ptr(), k_codes.data_ptr(), k_codebooks.data_ptr(), v_codes.data_ptr(),
+        v_codebooks.data_ptr(), b, hq, hkv, tokens, d, sub, n_c, window, scale, _dtype_code(q),
+        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream, q.device))
+    _check(st, "vq_attention_decode")
     return out
 
 

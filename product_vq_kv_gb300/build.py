@@ -18,16 +18,17 @@ CSRC = os.path.join(PKG, "csrc")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libvqenc.so")
 PTXAS_LOG = os.path.join(LIB_DIR, "ptxas.txt")
-SOURCES = [os.path.join(CSRC, "vq_encode.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, "vq_kernels.cuh"), os.path.join(CSRC, "vq_filter.cuh"), os.path.join(CSRC, "vq_tc.cuh"), os.path.join(CSRC, "vq_decode.cuh"),
-                     os.path.join(ROOT, "include", "vq_encode.h")]
+SOURCES = [os.path.join(CSRC, "vq_encode.cu"), os.path.join(CSRC, "vq_attn.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, name) for name in (
+    "vq_kernels.cuh", "vq_filter.cuh", "vq_tc.cuh", "vq_decode.cuh", "vq_attn.cuh", "vq_host.h")] + [
+    os.path.join(ROOT, "include", "vq_encode.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # --fmad=false: no plain multiply-add in these sources may be contracted into an
 # FMA (the encode formula rounds the square and the sum separately); the hot
 # loops use explicit round-to-nearest intrinsics as well.
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xptxas", "-v",
-              "-Xcompiler", "-fPIC", "-shared"]
+              "-Xcompiler", "-fPIC"]
 
 
 def nvcc() -> str:
@@ -45,25 +46,37 @@ def is_fresh() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library unless it is newer than all of its sources."""
+    """Compile the library unless it is newer than all of its sources.
+
+    The translation units compile in parallel, then link into one shared
+    library."""
     if not force and is_fresh():
         return LIB_PATH
     os.makedirs(LIB_DIR, exist_ok=True)
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=LIB_DIR)
-    os.close(fd)
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-o", tmp, *SOURCES]
-    try:
-        res = subprocess.run(cmd, capture_output=True, text=True)
+    with tempfile.TemporaryDirectory(dir=LIB_DIR) as tmpdir:
+        jobs = []
+        for src in SOURCES:
+            obj = os.path.join(tmpdir, os.path.basename(src) + ".o")
+            cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", "-o",
+                   obj, src]
+            jobs.append((cmd, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                                    stderr=subprocess.PIPE, text=True)))
+        log = []
+        for cmd, _, proc in jobs:
+            out, err = proc.communicate()
+            if proc.returncode != 0:
+                raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + out + err)
+            log.append(" ".join(cmd) + "\n" + err)
+        tmp = os.path.join(tmpdir, "lib.so")
+        link = [nvcc(), *ARCH, "-shared", "-o", tmp, *(obj for _, obj, _ in jobs)]
+        res = subprocess.run(link, capture_output=True, text=True)
         if res.returncode != 0:
-            raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
+            raise RuntimeError("nvcc link failed:\n" + " ".join(link) + "\n" + res.stdout + res.stderr)
         with open(PTXAS_LOG, "w") as f:
-            f.write(" ".join(cmd) + "\n" + res.stderr)
+            f.write("\n".join(log))
         if verbose:
-            sys.stderr.write(res.stderr)
+            sys.stderr.write("\n".join(log))
         os.replace(tmp, LIB_PATH)
-    finally:
-        if os.path.exists(tmp):
-            os.unlink(tmp)
     return LIB_PATH
 
 

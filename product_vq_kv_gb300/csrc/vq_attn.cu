@@ -1,0 +1,194 @@
+// vq_attn.cu -- C ABI entry points of decode attention over product-VQ codes
+// (see include/vq_encode.h for the contract of each function).
+//
+// Host side only: validate arguments, plan the launch (query heads per
+// block, token runs per block), launch the partial and combine kernels of
+// vq_attn.cuh on the caller's stream.  The library allocates no memory: the
+// partials go to the caller's workspace.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "vq_encode.h"
+#include "vq_attn.cuh"
+#include "vq_host.h"
+
+namespace {
+
+size_t elem_size(vq_dtype d) { return d == VQ_F32 ? 4 : 2; }
+
+int device_sms() { return vqh_device_sms(); }
+
+struct AttnPlan {
+    vqk::AttnShape sh;
+    size_t smem;
+    size_t part_bytes_per_split;
+    int64_t base;  // blocks per split: batch * heads_kv * head groups
+};
+
+constexpr int kAttnThreads = 256;
+constexpr int kAttnChunk = kAttnThreads * vqk::kAttnTokPerThread;
+constexpr size_t kAttnMaxSmem = 200 * 1024;
+constexpr size_t kSmemPerSm = 228 * 1024;  // shared memory per SM, 1 KiB of it per block reserved
+
+bool attn_ns_supported(int ns) { return ns == 4 || ns == 8 || ns == 16 || ns == 32 || ns == 64; }
+
+vq_status attn_validate(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_t tokens,
+                        int32_t head_dim, int32_t sub_dim, int32_t n_centroids, int64_t window)
+{
+    if (batch < 0 || tokens < 0 || window < 0) return VQ_ERR_INVALID_ARG;
+    if (heads_q < 1 || heads_kv < 1 || heads_q % heads_kv) return VQ_ERR_INVALID_ARG;
+    if (sub_dim < 1 || head_dim < 1 || head_dim % sub_dim) return VQ_ERR_INVALID_ARG;
+    if (head_dim > 512 || !attn_ns_supported(head_dim / sub_dim)) return VQ_ERR_UNSUPPORTED;
+    if (n_centroids < 1 || n_centroids > 256) return VQ_ERR_UNSUPPORTED;
+    return VQ_OK;
+}
+
+// Query heads per block: the largest divisor of the GQA ratio, at most 8,
+// whose tables fit in shared memory.  Chunk runs (splits): the count that
+// minimises waves * (chunks per run + the ~0.7 chunk a block spends on its
+// tables and final product).
+vq_status attn_plan(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_t tokens,
+                    int32_t head_dim, int32_t sub_dim, int32_t n_centroids, int64_t window,
+                    float scale, AttnPlan *p)
+{
+    const int qpk = heads_q / heads_kv;
+    const int ns = head_dim / sub_dim;
+    int gpb = 0;
+    for (int g = qpk < vqk::kAttnMaxHeads ? qpk : vqk::kAttnMaxHeads; g >= 1; --g)
+        if (qpk % g == 0 && vqk::attn_smem_bytes(g, ns) <= kAttnMaxSmem) {
+            gpb = g;
+            break;
+        }
+    if (gpb == 0) return VQ_ERR_UNSUPPORTED;
+    const size_t smem = vqk::attn_smem_bytes(gpb, ns);
+    const int64_t first = window > 0 && window < tokens ? tokens - window : 0;
+    const int64_t chunks = (tokens - first + kAttnChunk - 1) / kAttnChunk;
+    const int64_t base = batch * heads_kv * (qpk / gpb);
+    const int sms = device_sms() > 0 ? device_sms() : 152;
+    int64_t per_sm = (int64_t)(kSmemPerSm / (smem + 1024));
+    if (per_sm > 2048 / kAttnThreads) per_sm = 2048 / kAttnThreads;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t slots = sms * per_sm;
+    int64_t best = 1;
+    double best_cost = 1e300;
+    const int64_t max_splits = chunks < 4096 ? chunks : 4096;
+    for (int64_t k = 1; k <= max_splits && base > 0; ++k) {
+        const int64_t waves = (base * k + slots - 1) / slots;
+        const double cost = (double)waves * ((double)((chunks + k - 1) / k) + 0.7);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = k;
+        }
+    }
+    p->sh = vqk::AttnShape{batch, heads_q, heads_kv, head_dim, sub_dim, n_centroids, tokens, first,
+                           chunks, gpb, (int32_t)best,
+                           (scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim)) *
+                               1.4426950408889634f};
+    p->smem = smem;
+    p->part_bytes_per_split = (size_t)batch * heads_q * (head_dim + 2) * sizeof(float);
+    p->base = base;
+    return VQ_OK;
+}
+
+template <typename T, int NS>
+vq_status attn_launch_ns(const AttnPlan &p, const void *q, const uint8_t *kcodes, const void *kcb,
+                         const uint8_t *vcodes, const void *vcb, float *part, cudaStream_t st)
+{
+    auto kp = vqk::attn_partial<T, kAttnThreads, NS>;
+    if (p.smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
+            cudaSuccess)
+        return VQ_ERR_CUDA;
+    kp<<<(unsigned)(p.base * p.sh.splits), kAttnThreads, p.smem, st>>>(
+        static_cast<const T *>(q), kcodes, static_cast<const T *>(kcb), vcodes,
+        static_cast<const T *>(vcb), p.sh, part);
+    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+}
+
+template <typename T>
+vq_status attn_launch(const AttnPlan &p, const void *q, const uint8_t *kcodes, const void *kcb,
+                      const uint8_t *vcodes, const void *vcb, void *out, float *part,
+                      cudaStream_t st)
+{
+    vq_status s = VQ_ERR_INTERNAL;
+    switch (p.sh.head_dim / p.sh.sub_dim) {
+    case 4: s = attn_launch_ns<T, 4>(p, q, kcodes, kcb, vcodes, vcb, part, st); break;
+    case 8: s = attn_launch_ns<T, 8>(p, q, kcodes, kcb, vcodes, vcb, part, st); break;
+    case 16: s = attn_launch_ns<T, 16>(p, q, kcodes, kcb, vcodes, vcb, part, st); break;
+    case 32: s = attn_launch_ns<T, 32>(p, q, kcodes, kcb, vcodes, vcb, part, st); break;
+    case 64: s = attn_launch_ns<T, 64>(p, q, kcodes, kcb, vcodes, vcb, part, st); break;
+    }
+    if (s != VQ_OK) return s;
+    const int64_t rows = p.sh.batch * p.sh.heads_q;
+    const int threads = (p.sh.head_dim + 31) / 32 * 32;
+    vqk::attn_combine<T><<<(unsigned)rows, threads, 0, st>>>(part, rows, p.sh.head_dim,
+                                                             p.sh.splits, static_cast<T *>(out));
+    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t vq_attention_workspace_bytes(int64_t batch, int32_t heads_q, int32_t heads_kv,
+                                    int64_t tokens, int32_t head_dim, int32_t sub_dim,
+                                    int32_t n_centroids, int64_t window)
+{
+    if (attn_validate(batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids, window) !=
+        VQ_OK)
+        return 0;
+    AttnPlan p;
+    if (attn_plan(batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids, window, 0.f,
+                  &p) != VQ_OK)
+        return 0;
+    return p.part_bytes_per_split * (size_t)p.sh.splits;
+}
+
+vq_status vq_attention_decode(const void *q, const uint8_t *k_codes, const void *k_codebooks,
+                              const uint8_t *v_codes, const void *v_codebooks, int64_t batch,
+                              int32_t heads_q, int32_t heads_kv, int64_t tokens, int32_t head_dim,
+                              int32_t sub_dim, int32_t n_centroids, int64_t window, float scale,
+                              vq_dtype dtype, void *out, void *workspace, size_t workspace_bytes,
+                              vq_stream_t stream)
+{
+    if (dtype != VQ_F16 && dtype != VQ_BF16 && dtype != VQ_F32) return VQ_ERR_INVALID_ARG;
+    vq_status s = attn_validate(batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids,
+                                window);
+    if (s != VQ_OK) return s;
+    if (batch == 0) return VQ_OK;
+    const size_t es = elem_size(dtype);
+    if (!q || !k_codebooks || !v_codebooks || !out || !workspace) return VQ_ERR_INVALID_ARG;
+    if (tokens > 0 && (!k_codes || !v_codes)) return VQ_ERR_INVALID_ARG;
+    const uintptr_t code_align = head_dim / sub_dim < 16 ? head_dim / sub_dim : 16;
+    if ((uintptr_t)q % es || (uintptr_t)k_codebooks % es || (uintptr_t)v_codebooks % es ||
+        (uintptr_t)out % es || (uintptr_t)workspace % 16 || (uintptr_t)k_codes % code_align ||
+        (uintptr_t)v_codes % code_align)
+        return VQ_ERR_INVALID_ARG;
+    AttnPlan p;
+    if ((s = attn_plan(batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids, window,
+                       scale, &p)) != VQ_OK)
+        return s;
+    // fewer token slices if the workspace holds fewer partials
+    const int64_t fit = (int64_t)(workspace_bytes / p.part_bytes_per_split);
+    if (fit < 1) return VQ_ERR_INVALID_ARG;
+    if (fit < p.sh.splits) p.sh.splits = (int32_t)fit;
+    if (p.base * p.sh.splits > 0x7fffffffLL || p.sh.batch * p.sh.heads_q > 0x7fffffffLL)
+        return VQ_ERR_UNSUPPORTED;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float *part = static_cast<float *>(workspace);
+    switch (dtype) {
+    case VQ_F16: return attn_launch<__half>(p, q, k_codes, k_codebooks, v_codes, v_codebooks, out, part, st);
+    case VQ_BF16:
+        return attn_launch<__nv_bfloat16>(p, q, k_codes, k_codebooks, v_codes, v_codebooks, out,
+                                          part, st);
+    case VQ_F32: return attn_launch<float>(p, q, k_codes, k_codebooks, v_codes, v_codebooks, out, part, st);
+    }
+    return VQ_ERR_INTERNAL;
+}
+
+}  // extern "C"

@@ -7,15 +7,38 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
 
 #include "vq_encode.h"
+#include "vq_host.h"
 #include "vq_decode.cuh"
 #include "vq_filter.cuh"
 #include "vq_tc.cuh"
 #include "vq_kernels.cuh"
+
+// Declared in vq_host.h.
+int vqh_device_sms()
+{
+    constexpr int kMax = 64;
+    static int cache[kMax] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMax) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (cache[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        cache[dev] = sms;
+    }
+    return cache[dev];
+}
 
 namespace {
 
@@ -45,27 +68,7 @@ struct TcConfig<8> {
     static constexpr int kCols = 64, kGroup = 8, kMinBlocks = 6;
 };
 
-// Streaming multiprocessors of the current device, cached per device; 0 if
-// there is no usable device.
-int device_sms()
-{
-    constexpr int kMax = 64;
-    static int cache[kMax] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMax) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    if (cache[dev] == 0) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return 0;
-        }
-        cache[dev] = sms;
-    }
-    return cache[dev];
-}
+int device_sms() { return vqh_device_sms(); }
 
 // Blocks per group and 128-row tiles per block.  A block's time is taken as
 // its tiles plus half a tile of set-up (codebook staging); the launch's time

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("vq_encode", "vq_encode_grouped", "vq_encode_grouped_host",
                      "vq_encode_grouped_u8", "vq_dequantize_grouped",
-                     "vq_status_string", "vq_describe_launch", "vq_abi_version"):
+                     "vq_status_string", "vq_describe_launch", "vq_abi_version",
+                     "vq_attention_decode", "vq_attention_workspace_bytes"):
         assert required in names
 
 
@@ -105,6 +106,52 @@ def test_encode_argument_errors(lib, args, status):
 ])
 def test_grouped_argument_errors(lib, args, status):
     assert _grouped(lib)(*args) == status
+
+
+def _attention(lib):
+    f = lib.vq_attention_decode
+    f.restype = ctypes.c_int32
+    i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    f.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i64, i32, i32, i32, i64, ctypes.c_float, i32,
+                  vp, vp, ctypes.c_size_t, vp]
+    return f
+
+
+# (batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids, window, dtype,
+#  pointer offset, workspace bytes) -> status; pointers are fake and never used
+@pytest.mark.parametrize("shape,status", [
+    ((2, 8, 3, 100, 128, 8, 256, 0, 0, 0, 1 << 20), 1),    # heads_q not a multiple of heads_kv
+    ((2, 8, 2, 100, 128, 7, 256, 0, 0, 0, 1 << 20), 1),    # head_dim not a multiple of sub_dim
+    ((2, 8, 2, 100, 128, 8, 257, 0, 0, 0, 1 << 20), 2),    # codes wider than 8 bits
+    ((2, 8, 2, 100, 1024, 8, 256, 0, 0, 0, 1 << 20), 2),   # head_dim above 512
+    ((2, 8, 2, 100, 128, 1, 256, 0, 0, 0, 1 << 20), 2),    # 128 sub-spaces
+    ((2, 8, 2, 100, 96, 8, 256, 0, 0, 0, 1 << 20), 2),     # 12 sub-spaces
+    ((2, 8, 2, -1, 128, 8, 256, 0, 0, 0, 1 << 20), 1),     # negative tokens
+    ((2, 8, 2, 100, 128, 8, 256, -5, 0, 0, 1 << 20), 1),   # negative window
+    ((2, 8, 2, 100, 128, 8, 256, 0, 7, 0, 1 << 20), 1),    # unknown dtype
+    ((2, 8, 2, 100, 128, 8, 256, 0, 0, 1, 1 << 20), 1),    # misaligned pointers
+    ((2, 8, 2, 100, 128, 8, 256, 0, 0, 0, 64), 1),         # workspace too small for one slice
+    ((0, 8, 2, 100, 128, 8, 256, 0, 0, 0, 0), 0),          # no batch: nothing to do
+])
+def test_attention_argument_errors(lib, shape, status):
+    b, hq, hkv, t, d, sub, nc, window, dtype, off, ws = shape
+    p = P + off
+    assert _attention(lib)(p, P, p, P, p, b, hq, hkv, t, d, sub, nc, window, 0.0, dtype, p, P, ws,
+                           None) == status
+
+
+def test_attention_workspace_bytes(lib):
+    f = lib.vq_attention_workspace_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]
+    per_slice = 8 * 32 * (128 + 2) * 4
+    n = f(8, 32, 8, 32768, 128, 8, 256, 0)
+    assert n > 0 and n % per_slice == 0 and n // per_slice <= 32
+    assert f(8, 32, 8, 0, 128, 8, 256, 0) == per_slice      # empty cache: one slice
+    assert f(8, 32, 8, 500, 128, 8, 256, 0) == per_slice    # one chunk: one slice
+    assert f(8, 32, 7, 32768, 128, 8, 256, 0) == 0          # invalid sizes
+    assert f(8, 32, 8, 32768, 128, 8, 256, 100) == per_slice  # a short window
 
 
 def test_describe_launch_picks_kernels(lib):

@@ -88,3 +88,57 @@ def test_mutation_is_caught(name):
                 caught += 1
                 break
         assert caught, f"no pin caught the '{name}' mutation"
+
+
+# ---- decode attention (Python oracle): mutate the function's source, run the
+# pins of test_oracle_attention.py against the mutant
+
+ATTENTION_MUTATIONS = {
+    # query head h reads KV head h % Hkv instead of h // (Hq / Hkv)
+    "gqa_interleave": ("out[bi, h * qpk + g] =", "out[bi, g * hkv + h] ="),
+    # the first `window` tokens instead of the last
+    "window_first": ("first = t - window if", "first = window if"),
+    # default scale 1/D instead of 1/sqrt(D)
+    "scale_default": ("1.0 / np.sqrt(d)", "1.0 / d"),
+    # softmax without the maximum subtracted
+    "no_max_shift": ("np.exp(logits - logits.max())", "np.exp(logits)"),
+    # weights not normalised
+    "no_normalise": ("(p / p.sum()) @ vals", "p @ vals"),
+    # scores against the values
+    "keys_values_swapped": ("logits = scale * (keys @ q", "logits = scale * (vals @ q"),
+    # keys decoded with the value codebook
+    "key_codebook": ("np.asarray(k_codebooks)[h:h + 1]", "np.asarray(v_codebooks)[h:h + 1]"),
+}
+
+
+def _mutant_attention(before, after):
+    import inspect
+    import textwrap
+
+    src = textwrap.dedent(inspect.getsource(oracle.attention_decode))
+    assert src.count(before) == 1, f"mutation anchor {before!r} not found exactly once"
+    namespace = dict(vars(oracle))
+    exec(compile(src.replace(before, after), "<mutant>", "exec"), namespace)
+    return namespace["attention_decode"]
+
+
+def test_unmutated_attention_passes_every_pin():
+    import test_oracle_attention as apins
+
+    for pin in apins.PINS:
+        pin(oracle.attention_decode)
+
+
+@pytest.mark.parametrize("name", sorted(ATTENTION_MUTATIONS))
+def test_attention_mutation_is_caught(name):
+    import test_oracle_attention as apins
+
+    fn = _mutant_attention(*ATTENTION_MUTATIONS[name])
+    caught = 0
+    for pin in apins.PINS:
+        try:
+            pin(fn)
+        except (AssertionError, FloatingPointError, ValueError, IndexError):
+            caught += 1
+            break
+    assert caught, f"no pin caught the '{name}' mutation"

@@ -177,6 +177,57 @@ def _make_adversarial(x, cb, dup_seed, copy_seed):
             x[k, rows] = cb[k, src]
 
 
+@dataclasses.dataclass(frozen=True)
+class AttentionWorkload:
+    """One decode step of attention over an 8-bit product-VQ KV cache."""
+
+    name: str
+    description: str
+    batch: int
+    heads_q: int
+    heads_kv: int
+    tokens: int
+    head_dim: int
+    sub_dim: int
+    n_centroids: int
+    window: int = 0
+
+    @property
+    def code_bytes(self) -> int:
+        """Bytes of key + value codes read per step."""
+        return 2 * self.batch * self.heads_kv * self.tokens * (self.head_dim // self.sub_dim)
+
+
+ATTENTION_WORKLOADS = {
+    # Llama-3.1-8B decode step: 32 query heads, 8 KV heads, head_dim 128,
+    # sub_dim 8 (16 codes per token and head), batch 8, 32k cached tokens.
+    "llama_attention": AttentionWorkload("llama_attention", "Llama-3.1-8B-shape decode "
+                                         "attention, batch 8, 32768 cached tokens",
+                                         batch=8, heads_q=32, heads_kv=8, tokens=32768,
+                                         head_dim=128, sub_dim=8, n_centroids=256),
+}
+
+ATTENTION_SEEDS = {"llama_attention": (13, 14, 15, 16, 17)}
+
+
+def generate_attention(name: str, tokens: int | None = None, batch: int | None = None):
+    """``(q, k_codes, k_codebooks, v_codes, v_codebooks)`` for an attention
+    workload: fp16 queries and codebooks ~ N(0, 1), codes uniform in
+    [0, n_centroids) (keys and values of a cache encoded elsewhere)."""
+    w = ATTENTION_WORKLOADS[name]
+    tokens = w.tokens if tokens is None else int(tokens)
+    batch = w.batch if batch is None else int(batch)
+    s = ATTENTION_SEEDS[name]
+    ns = w.head_dim // w.sub_dim
+    q = _normal(s[0], (batch, w.heads_q, w.head_dim)).astype(np.float16)
+    kcb = _normal(s[1], (w.heads_kv, w.n_centroids, w.sub_dim)).astype(np.float16)
+    vcb = _normal(s[2], (w.heads_kv, w.n_centroids, w.sub_dim)).astype(np.float16)
+    shape = (batch, w.heads_kv, tokens, ns)
+    kc = np.random.Generator(np.random.PCG64(s[3])).integers(0, w.n_centroids, shape, dtype=np.uint8)
+    vc = np.random.Generator(np.random.PCG64(s[4])).integers(0, w.n_centroids, shape, dtype=np.uint8)
+    return q, kc, kcb, vc, vcb
+
+
 def flat(x: np.ndarray) -> np.ndarray:
     """View ``[G, M, sub]`` as ``[G*M, sub]``."""
     return x.reshape(-1, x.shape[-1])
