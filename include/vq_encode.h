@@ -186,6 +186,35 @@ size_t vq_attention_workspace_bytes(int64_t batch, int32_t heads_q, int32_t head
                                     int64_t tokens, int32_t head_dim, int32_t sub_dim,
                                     int32_t n_centroids, int64_t window);
 
+/* Bytes of device scratch built into the library for
+ * vq_attention_decode_static. */
+#define VQ_ATTN_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * vq_attention_decode_static -- vq_attention_decode without a workspace
+ * argument: the partials go to an array of VQ_ATTN_STATIC_SCRATCH_BYTES
+ * (8 MiB) that the library holds in device memory for each device.  The pages
+ * have no counterpart; this is an interface for callers that cannot allocate
+ * device memory per call: a decode loop whose HBM is fully planned up front
+ * (the quantised KV cache takes what the weights leave), or plain C host code
+ * with no caching allocator, for which a cudaMalloc / cudaFree per decode step
+ * would synchronise the device.  The call allocates nothing.
+ * Arguments, layouts and results are those of vq_attention_decode.  When the
+ * partials of the shape's default plan need more than the array holds, fewer
+ * token slices are used; a shape whose single slice,
+ * batch * heads_q * (head_dim + 2) * 4 bytes, exceeds the array returns
+ * VQ_ERR_INVALID_ARG.  Every call on a device shares the one array: calls whose
+ * kernels overlap on the GPU (on different streams, or from several host
+ * threads without ordering between them) race on it and give wrong results,
+ * so issue them in one stream order.  Nothing in the array needs clearing.
+ */
+vq_status vq_attention_decode_static(const void *q, const uint8_t *k_codes,
+                                     const void *k_codebooks, const uint8_t *v_codes,
+                                     const void *v_codebooks, int64_t batch, int32_t heads_q,
+                                     int32_t heads_kv, int64_t tokens, int32_t head_dim,
+                                     int32_t sub_dim, int32_t n_centroids, int64_t window,
+                                     float scale, vq_dtype dtype, void *out, vq_stream_t stream);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char *vq_status_string(vq_status status);
 

@@ -17,7 +17,9 @@ from ._binding import (  # noqa: F401
     VQError,
     load_library,
     vq_abi_version,
+    ATTN_STATIC_SCRATCH_BYTES,
     vq_attention_decode,
+    vq_attention_decode_static,
     vq_attention_workspace_bytes,
     vq_describe_launch,
     vq_dequantize_grouped,

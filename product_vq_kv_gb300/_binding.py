@@ -59,6 +59,9 @@ def load_library() -> ctypes.CDLL:
         lib.vq_attention_decode.restype = i32
         lib.vq_attention_decode.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i64, i32, i32, i32,
                                             i64, ctypes.c_float, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.vq_attention_decode_static.restype = i32
+        lib.vq_attention_decode_static.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i64, i32,
+                                                   i32, i32, i64, ctypes.c_float, i32, vp, vp]
         lib.vq_attention_workspace_bytes.restype = ctypes.c_size_t
         lib.vq_attention_workspace_bytes.argtypes = [i64, i32, i32, i64, i32, i32, i32, i64]
         lib.vq_status_string.restype = ctypes.c_char_p
@@ -255,6 +258,37 @@ def vq_attention_decode(q: torch.Tensor, k_codes: torch.Tensor, k_codebooks: tor
         out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _stream_handle(stream, q.device))
     _check(st, "vq_attention_decode")
+    return out
+
+
+# Bytes of the library's built-in scratch array (VQ_ATTN_STATIC_SCRATCH_BYTES).
+ATTN_STATIC_SCRATCH_BYTES = 8 << 20
+
+
+def vq_attention_decode_static(q: torch.Tensor, k_codes: torch.Tensor, k_codebooks: torch.Tensor,
+                               v_codes: torch.Tensor, v_codebooks: torch.Tensor, window: int = 0,
+                               scale: float = 0.0, out: torch.Tensor | None = None,
+                               stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """:func:`vq_attention_decode` with its partials in the library's one
+    built-in device array instead of a workspace, for callers that cannot
+    allocate device memory per call (a decode loop whose HBM is planned up
+    front, host code without a caching allocator).  The library allocates
+    nothing; pass ``out`` to allocate nothing here either.  Calls that overlap
+    on the GPU share that array and race: keep them in one stream order."""
+    b, hq, d = q.shape
+    if b * hq * (d + 2) * 4 > ATTN_STATIC_SCRATCH_BYTES:
+        raise VQError(VQ_ERR_INVALID_ARG,
+                      f"vq_attention_decode_static (one token slice needs {b * hq * (d + 2) * 4} "
+                      f"bytes of scratch; the built-in array holds {ATTN_STATIC_SCRATCH_BYTES})")
+    if out is None:
+        out = torch.empty_like(q)
+    _, hkv, tokens, _ = k_codes.shape
+    n_c, sub = k_codebooks.shape[1], k_codebooks.shape[2]
+    st = load_library().vq_attention_decode_static(
+        q.data_ptr(), k_codes.data_ptr(), k_codebooks.data_ptr(), v_codes.data_ptr(),
+        v_codebooks.data_ptr(), b, hq, hkv, tokens, d, sub, n_c, window, scale, _dtype_code(q),
+        out.data_ptr(), _stream_handle(stream, q.device))
+    _check(st, "vq_attention_decode_static")
     return out
 
 

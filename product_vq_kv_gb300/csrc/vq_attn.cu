@@ -12,6 +12,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "vq_encode.h"
 #include "vq_attn.cuh"
@@ -131,6 +132,36 @@ vq_status attn_launch(const AttnPlan &p, const void *q, const uint8_t *kcodes, c
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
+// Scratch of vq_attention_decode_static: the per-slice partials live in this
+// one array instead of a caller workspace.  Nothing in it has to start at
+// zero (every partial the merge reads is written earlier in the same call).
+// All calls on a device share it.
+static __device__ __align__(256) unsigned char g_attn_scratch[VQ_ATTN_STATIC_SCRATCH_BYTES];
+
+// Device address of g_attn_scratch on the current device, looked up once per
+// device; nullptr if the lookup fails.
+void *static_scratch()
+{
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -189,6 +220,28 @@ vq_status vq_attention_decode(const void *q, const uint8_t *k_codes, const void 
     case VQ_F32: return attn_launch<float>(p, q, k_codes, k_codebooks, v_codes, v_codebooks, out, part, st);
     }
     return VQ_ERR_INTERNAL;
+}
+
+vq_status vq_attention_decode_static(const void *q, const uint8_t *k_codes,
+                                     const void *k_codebooks, const uint8_t *v_codes,
+                                     const void *v_codebooks, int64_t batch, int32_t heads_q,
+                                     int32_t heads_kv, int64_t tokens, int32_t head_dim,
+                                     int32_t sub_dim, int32_t n_centroids, int64_t window,
+                                     float scale, vq_dtype dtype, void *out, vq_stream_t stream)
+{
+    vq_status s = attn_validate(batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids,
+                                window);
+    if (s != VQ_OK) return s;
+    if (batch == 0) return VQ_OK;
+    // one token slice of partials must fit in the array
+    if ((uint64_t)batch * (uint64_t)heads_q * (uint64_t)(head_dim + 2) * sizeof(float) >
+        VQ_ATTN_STATIC_SCRATCH_BYTES)
+        return VQ_ERR_INVALID_ARG;
+    void *scratch = static_scratch();
+    if (scratch == nullptr) return VQ_ERR_CUDA;
+    return vq_attention_decode(q, k_codes, k_codebooks, v_codes, v_codebooks, batch, heads_q,
+                               heads_kv, tokens, head_dim, sub_dim, n_centroids, window, scale,
+                               dtype, out, scratch, VQ_ATTN_STATIC_SCRATCH_BYTES, stream);
 }
 
 }  // extern "C"
