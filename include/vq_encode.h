@@ -169,7 +169,8 @@ vq_status vq_dequantize_grouped(const void *idx, int32_t index_bytes, const void
  * over the last `window` tokens (0: all tokens); scale <= 0 means
  * 1/sqrt(head_dim).  Accumulation is fp32; no tokens gives zeros.
  * Requirements: heads_q % heads_kv == 0, head_dim % sub_dim == 0,
- * head_dim <= 512, head_dim/sub_dim <= 64, n_centroids <= 256
+ * sub_dim % 4 == 0, head_dim <= 512, head_dim/sub_dim in {4, 8, 16, 32, 64},
+ * n_centroids <= 256, code arrays aligned to min(head_dim/sub_dim, 16) bytes
  * (VQ_ERR_INVALID_ARG / VQ_ERR_UNSUPPORTED otherwise).  Asynchronous on
  * `stream`; the library allocates nothing.
  */

@@ -26,13 +26,13 @@ int device_sms() { return vqh_device_sms(); }
 
 struct AttnPlan {
     vqk::AttnShape sh;
+    int gpb;  // query heads per block
     size_t smem;
     size_t part_bytes_per_split;
     int64_t base;  // blocks per split: batch * heads_kv * head groups
 };
 
-constexpr int kAttnThreads = 256;
-constexpr int kAttnChunk = kAttnThreads * vqk::kAttnTokPerThread;
+constexpr int kAttnThreads = vqk::kAttnThreads;
 constexpr size_t kAttnMaxSmem = 200 * 1024;
 constexpr size_t kSmemPerSm = 228 * 1024;  // shared memory per SM, 1 KiB of it per block reserved
 
@@ -44,15 +44,16 @@ vq_status attn_validate(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_
     if (batch < 0 || tokens < 0 || window < 0) return VQ_ERR_INVALID_ARG;
     if (heads_q < 1 || heads_kv < 1 || heads_q % heads_kv) return VQ_ERR_INVALID_ARG;
     if (sub_dim < 1 || head_dim < 1 || head_dim % sub_dim) return VQ_ERR_INVALID_ARG;
-    if (head_dim > 512 || !attn_ns_supported(head_dim / sub_dim)) return VQ_ERR_UNSUPPORTED;
+    if (head_dim > 512 || sub_dim % vqk::kAttnVw || !attn_ns_supported(head_dim / sub_dim))
+        return VQ_ERR_UNSUPPORTED;
     if (n_centroids < 1 || n_centroids > 256) return VQ_ERR_UNSUPPORTED;
     return VQ_OK;
 }
 
-// Query heads per block: the largest divisor of the GQA ratio, at most 8,
-// whose tables fit in shared memory.  Chunk runs (splits): the count that
+// Query heads per block: the largest of 8, 4, 2, 1 that divides the GQA ratio
+// and whose shared memory fits.  Chunk runs (splits): the count that
 // minimises waves * (chunks per run + the ~0.7 chunk a block spends on its
-// tables and final product).
+// tables and the final merge).
 vq_status attn_plan(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_t tokens,
                     int32_t head_dim, int32_t sub_dim, int32_t n_centroids, int64_t window,
                     float scale, AttnPlan *p)
@@ -60,15 +61,16 @@ vq_status attn_plan(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_t to
     const int qpk = heads_q / heads_kv;
     const int ns = head_dim / sub_dim;
     int gpb = 0;
-    for (int g = qpk < vqk::kAttnMaxHeads ? qpk : vqk::kAttnMaxHeads; g >= 1; --g)
-        if (qpk % g == 0 && vqk::attn_smem_bytes(g, ns) <= kAttnMaxSmem) {
+    for (int g = 8; g >= 1; g /= 2)
+        if (qpk % g == 0 && vqk::attn_smem(g, ns, sub_dim).total <= kAttnMaxSmem) {
             gpb = g;
             break;
         }
     if (gpb == 0) return VQ_ERR_UNSUPPORTED;
-    const size_t smem = vqk::attn_smem_bytes(gpb, ns);
+    const size_t smem = vqk::attn_smem(gpb, ns, sub_dim).total;
+    const int chunk = vqk::attn_chunk(ns);
     const int64_t first = window > 0 && window < tokens ? tokens - window : 0;
-    const int64_t chunks = (tokens - first + kAttnChunk - 1) / kAttnChunk;
+    const int64_t chunks = (tokens - first + chunk - 1) / chunk;
     const int64_t base = batch * heads_kv * (qpk / gpb);
     const int sms = device_sms() > 0 ? device_sms() : 152;
     int64_t per_sm = (int64_t)(kSmemPerSm / (smem + 1024));
@@ -87,20 +89,21 @@ vq_status attn_plan(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_t to
         }
     }
     p->sh = vqk::AttnShape{batch, heads_q, heads_kv, head_dim, sub_dim, n_centroids, tokens, first,
-                           chunks, gpb, (int32_t)best,
+                           chunks, (int32_t)best,
                            (scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim)) *
                                1.4426950408889634f};
+    p->gpb = gpb;
     p->smem = smem;
     p->part_bytes_per_split = (size_t)batch * heads_q * (head_dim + 2) * sizeof(float);
     p->base = base;
     return VQ_OK;
 }
 
-template <typename T, int NS>
-vq_status attn_launch_ns(const AttnPlan &p, const void *q, const uint8_t *kcodes, const void *kcb,
-                         const uint8_t *vcodes, const void *vcb, float *part, cudaStream_t st)
+template <typename T, int NS, int GPB>
+vq_status attn_launch_k(const AttnPlan &p, const void *q, const uint8_t *kcodes, const void *kcb,
+                        const uint8_t *vcodes, const void *vcb, float *part, cudaStream_t st)
 {
-    auto kp = vqk::attn_partial<T, kAttnThreads, NS>;
+    auto kp = vqk::attn_partial<T, NS, GPB>;
     if (p.smem > 48 * 1024 &&
         cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
             cudaSuccess)
@@ -109,6 +112,19 @@ vq_status attn_launch_ns(const AttnPlan &p, const void *q, const uint8_t *kcodes
         static_cast<const T *>(q), kcodes, static_cast<const T *>(kcb), vcodes,
         static_cast<const T *>(vcb), p.sh, part);
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+}
+
+template <typename T, int NS>
+vq_status attn_launch_ns(const AttnPlan &p, const void *q, const uint8_t *kcodes, const void *kcb,
+                         const uint8_t *vcodes, const void *vcb, float *part, cudaStream_t st)
+{
+    switch (p.gpb) {
+    case 1: return attn_launch_k<T, NS, 1>(p, q, kcodes, kcb, vcodes, vcb, part, st);
+    case 2: return attn_launch_k<T, NS, 2>(p, q, kcodes, kcb, vcodes, vcb, part, st);
+    case 4: return attn_launch_k<T, NS, 4>(p, q, kcodes, kcb, vcodes, vcb, part, st);
+    case 8: return attn_launch_k<T, NS, 8>(p, q, kcodes, kcb, vcodes, vcb, part, st);
+    }
+    return VQ_ERR_INTERNAL;
 }
 
 template <typename T>

@@ -11,22 +11,27 @@
 //   score[t]     = sum_s LUT[s][kcode[t][s]]          = kappa * q . K^[t]
 //   p[t]         = 2^(score[t] - max) / sum_t' 2^(score[t'] - max)
 //   out[s*SUB+i] = sum_t p[t] * Vcb[vcode[t][s]][i]    = sum_t p[t] V^[t]
-// (2^(kappa x) = e^(scale x), so this is the usual softmax.)  The value sum is
-// regrouped by code: W[s][c] = sum of 2^(score - max) over the tokens whose
-// value code in sub-space s is c, so a token costs NS shared-memory adds
-// instead of D multiply-adds, and out = (W @ Vcb) / l at the end.
+// (2^(kappa x) = e^(scale x), so this is the usual softmax.)
 //
-// GB300 shape: a block owns GPB query heads of one KV head (grouped-query
-// attention: they share that head's codes and codebooks) and one run of
-// CHUNK-token chunks, so each code row is read from HBM once for all of them.
-// Tables and W sit in shared memory with a row stride of kLutStride floats:
-// entries past n_centroids stay zero, so a code >= n_centroids reads a zero
-// key row and adds to a value row that is never read (the decode of such a
-// code is a zero row).  Scores of a chunk stay in registers between the max
-// and the accumulation; W is rescaled when a later chunk raises the running
-// maximum (online softmax at chunk granularity).  Each block writes a partial
-// (max, sum, out[D]) per query head to the caller's workspace; attn_combine
-// merges the partials (flash-decoding).
+// GB300 shape.  A block owns GPB query heads of one KV head (grouped-query
+// attention: they share that head's codes and codebooks) and a run of
+// CHUNK-token chunks of the cache, so each code row is read from HBM once for
+// all GPB heads.  Per chunk:
+//   phase A, one thread per token: the key code row is read with vector
+//     loads and its score looked up for every head; the tables of up to four
+//     heads are interleaved so one 16-byte shared load serves four heads.
+//     The chunk maximum raises the running maximum (online softmax: the
+//     register accumulators are rescaled), and the weights 2^(score - max)
+//     and the value code rows go to shared memory;
+//   phase B, one thread per (4-column slice of the head, token stream): the
+//     value rows are gathered from the fp32 codebook in shared memory and
+//     accumulated with the weights of every head in registers (no atomics).
+// Shared-memory random gathers bound this kernel (about 8 random 4-byte or 3
+// random 16-byte lane accesses per clock per SM, with bank conflicts), not
+// HBM.  Each block writes a partial (max, sum, out[D]) per query head to the
+// caller's workspace; attn_combine merges the partials (flash-decoding).
+// A code >= n_centroids reads a zero table entry and a zero value row (the
+// decode of such a code is a zero row).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -35,19 +40,18 @@
 
 namespace vqk {
 
-constexpr int kLutStride = 260;  // >= 256 codes; 4 * s spreads sub-spaces over banks
-constexpr int kAttnMaxHeads = 8;
-constexpr int kAttnTokPerThread = 4;
+constexpr int kLutStride = 260;  // table row stride (>= 256 codes), in vectors
+constexpr int kAttnThreads = 256;
+constexpr int kAttnVw = 4;       // value columns per phase-B thread
 
 struct AttnShape {
     int64_t batch;
     int32_t heads_q, heads_kv, head_dim, sub_dim, n_centroids;
-    int64_t tokens;           // cached tokens T
-    int64_t first_token;      // first attended token (sliding window), else 0
-    int64_t chunks;           // ceil((T - first_token) / CHUNK)
-    int32_t heads_per_block;  // GPB
-    int32_t splits;           // chunk runs per (batch, KV head, head group)
-    float kappa;              // scale * log2(e)
+    int64_t tokens;       // cached tokens T
+    int64_t first_token;  // first attended token (sliding window), else 0
+    int64_t chunks;       // ceil((T - first_token) / CHUNK)
+    int32_t splits;       // chunk runs per (batch, KV head, head group)
+    float kappa;          // scale * log2(e)
 };
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -57,11 +61,32 @@ __device__ __forceinline__ void from_f32(float &d, float v) { d = v; }
 __device__ __forceinline__ void from_f32(__half &d, float v) { d = __float2half_rn(v); }
 __device__ __forceinline__ void from_f32(__nv_bfloat16 &d, float v) { d = __float2bfloat16_rn(v); }
 
-// Shared memory: LUT [GPB][NS][kLutStride], W [GPB][NS][kLutStride], block
-// reduction scratch [3][GPB][32] (two alternating max buffers, one sum).
-__host__ __device__ inline size_t attn_smem_bytes(int gpb, int ns)
+// Tokens per phase-A thread and per chunk, by sub-space count.
+__host__ __device__ constexpr int attn_tok_per_thread(int ns) { return ns <= 16 ? 4 : ns == 32 ? 2 : 1; }
+__host__ __device__ constexpr int attn_chunk(int ns) { return kAttnThreads * attn_tok_per_thread(ns); }
+
+// Shared-memory layout (floats unless noted), in order:
+//   lut  [GPB / GP][NS][kLutStride][GP]   GP = min(GPB, 4) heads per vector
+//   vcb  [256][SUB]                       value codebook, fp32, zero past n_c
+//   pw   [CHUNK][GPB]                     weights of the chunk
+//   red  [3][GPB][32]                     block maxima (two buffers), sums
+//   vtile[CHUNK][NS] bytes                value codes of the chunk
+// After the last chunk, the lut region holds the per-stream accumulators
+// [streams][GPB][D] (it is at least that large).
+struct AttnSmem {
+    size_t lut, vcb, pw, red, vtile, total;
+};
+__host__ __device__ inline AttnSmem attn_smem(int gpb, int ns, int sub)
 {
-    return ((size_t)2 * gpb * ns * kLutStride + 3 * (size_t)gpb * 32) * sizeof(float);
+    AttnSmem m;
+    const int chunk = attn_chunk(ns);
+    m.lut = 0;
+    m.vcb = m.lut + (size_t)gpb * ns * kLutStride * 4;
+    m.pw = m.vcb + (size_t)256 * sub * 4;
+    m.red = m.pw + (size_t)chunk * gpb * 4;
+    m.vtile = m.red + (size_t)3 * gpb * 32 * 4;
+    m.total = m.vtile + (size_t)chunk * ns;
+    return m;
 }
 
 // Code row of one token as 32-bit words (NS bytes, NS % 4 == 0, row address
@@ -87,36 +112,88 @@ __device__ __forceinline__ void load_code_row(const uint8_t *p, uint32_t (&w)[NS
     }
 }
 
+template <int NS>
+__device__ __forceinline__ void store_code_row(uint8_t *p, const uint32_t (&w)[NS / 4])
+{
+    if constexpr (NS % 16 == 0) {
+#pragma unroll
+        for (int k = 0; k < NS / 16; ++k)
+            reinterpret_cast<uint4 *>(p)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    } else if constexpr (NS % 8 == 0) {
+#pragma unroll
+        for (int k = 0; k < NS / 8; ++k) reinterpret_cast<uint2 *>(p)[k] = make_uint2(w[2 * k], w[2 * k + 1]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < NS / 4; ++k) reinterpret_cast<uint32_t *>(p)[k] = w[k];
+    }
+}
+
 __device__ __forceinline__ uint32_t code_at(uint32_t w, int k) { return (w >> (8 * k)) & 0xffu; }
 
+// (a.x * b + c.x, a.y * b + c.y) as one packed f32x2 FMA, each lane rounded
+// once as fmaf would.
+__device__ __forceinline__ float2 fma2_bcast(float2 a, float b, float2 c)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %4};\n\t"
+        "mov.b64 pc, {%5, %6};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pc;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// GP consecutive floats from shared memory (GP = 1, 2 or 4, aligned).
+template <int GP>
+__device__ __forceinline__ void load_vec(const float *p, float (&v)[GP])
+{
+    if constexpr (GP == 4) {
+        const float4 a = *reinterpret_cast<const float4 *>(p);
+        v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w;
+    } else if constexpr (GP == 2) {
+        const float2 a = *reinterpret_cast<const float2 *>(p);
+        v[0] = a.x, v[1] = a.y;
+    } else {
+        v[0] = *p;
+    }
+}
+
 // Launch: grid.x = batch * heads_kv * (heads_q / heads_kv / GPB) * splits,
-// block = THREADS, dynamic shared memory attn_smem_bytes(GPB, NS).  NS (the
-// number of sub-spaces, head_dim / sub_dim) is a compile-time multiple of 4;
-// code rows are NS bytes apart and the code arrays are 16-byte aligned.
+// block = kAttnThreads, dynamic shared memory attn_smem(GPB, NS, SUB).total.
+// NS = head_dim / sub_dim in {4, 8, 16, 32, 64}; sub_dim % 4 == 0; code rows
+// are NS bytes apart and the code arrays aligned to min(NS, 16) bytes.
 // Partial of (b, hq, split) at part[((b * heads_q + hq) * splits + split) *
 // (D + 2)]: {0: max (log2 domain), 1: sum, 2..: unnormalised out}.
-template <typename T, int THREADS, int NS>
-__global__ void __launch_bounds__(THREADS)
+template <typename T, int NS, int GPB>
+__global__ void __launch_bounds__(kAttnThreads)
     attn_partial(const T *__restrict__ q, const uint8_t *__restrict__ kcodes,
                  const T *__restrict__ kcb, const uint8_t *__restrict__ vcodes,
                  const T *__restrict__ vcb, AttnShape sh, float *__restrict__ part)
 {
-    constexpr int TPT = kAttnTokPerThread;
-    constexpr int CHUNK = THREADS * TPT;
-    constexpr int G = kAttnMaxHeads;
+    constexpr int THREADS = kAttnThreads;
+    constexpr int TPT = attn_tok_per_thread(NS);
+    constexpr int CHUNK = attn_chunk(NS);
+    constexpr int GP = GPB < 4 ? GPB : 4;
+    constexpr int NPACK = GPB / GP;
     constexpr int NW = THREADS / 32;
+    constexpr int VW = kAttnVw;
     constexpr float kNegInf = -__builtin_huge_valf();
-    extern __shared__ float smem_attn[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     const int sub = sh.sub_dim;
+    const int d = sh.head_dim;
     const int nc = sh.n_centroids;
-    const int gpb = sh.heads_per_block;
-    const int qpk = sh.heads_q / sh.heads_kv;  // query heads per KV head
-    const int hgroups = qpk / gpb;
-    const int tab = NS * kLutStride;           // floats per head
-    float *lut = smem_attn;                    // [gpb][NS][kLutStride]
-    float *wsum = lut + (size_t)gpb * tab;     // [gpb][NS][kLutStride]
-    float *red = wsum + (size_t)gpb * tab;     // [3][gpb][32]
+    const AttnSmem lay = attn_smem(GPB, NS, sub);
+    float *lut = reinterpret_cast<float *>(smem_raw + lay.lut);
+    float *vcs = reinterpret_cast<float *>(smem_raw + lay.vcb);
+    float *pw = reinterpret_cast<float *>(smem_raw + lay.pw);
+    float *red = reinterpret_cast<float *>(smem_raw + lay.red);
+    uint8_t *vtile = smem_raw + lay.vtile;
 
+    const int qpk = sh.heads_q / sh.heads_kv;  // query heads per KV head
+    const int hgroups = qpk / GPB;
     int64_t bid = blockIdx.x;
     const int split = (int)(bid % sh.splits);
     bid /= sh.splits;
@@ -124,7 +201,7 @@ __global__ void __launch_bounds__(THREADS)
     bid /= hgroups;
     const int hkv = (int)(bid % sh.heads_kv);
     const int64_t b = bid / sh.heads_kv;
-    const int hq0 = hkv * qpk + hg * gpb;
+    const int hq0 = hkv * qpk + hg * GPB;
 
     const T *kc = kcb + (size_t)hkv * nc * sub;
     const T *vc = vcb + (size_t)hkv * nc * sub;
@@ -132,141 +209,231 @@ __global__ void __launch_bounds__(THREADS)
     const uint8_t *kb = kcodes + cache_off;
     const uint8_t *vb = vcodes + cache_off;
 
-    // chunks [c0, c1) of the attended span belong to this block
-    const int64_t c0 = sh.chunks * split / sh.splits;
-    const int64_t c1 = sh.chunks * (split + 1) / sh.splits;
-
-    // ---- tables (kappa folded in; zero past n_centroids) and zeroed W
-    for (int e = threadIdx.x; e < gpb * tab; e += THREADS) {
-        const int c = e % kLutStride;
-        const int s = (e / kLutStride) % NS;
-        const int g = e / tab;
-        float acc = 0.f;
-        if (c < nc) {
-            const T *qv = q + ((size_t)b * sh.heads_q + hq0 + g) * sh.head_dim + (size_t)s * sub;
-            const T *cv = kc + (size_t)c * sub;
-            for (int i = 0; i < sub; ++i) acc = fmaf(to_f32(qv[i]), to_f32(cv[i]), acc);
+    // ---- tables (kappa folded in, zero past n_centroids), value codebook
+    {
+        const int entries = GPB * NS * kLutStride;
+        for (int e = threadIdx.x; e < entries; e += THREADS) {
+            const int gi = e % GP;                    // head within the pack
+            const int c = (e / GP) % kLutStride;
+            const int s = (e / (GP * kLutStride)) % NS;
+            const int pk = e / (GP * kLutStride * NS);
+            const int g = pk * GP + gi;
+            float acc = 0.f;
+            if (c < nc) {
+                const T *qv = q + ((size_t)b * sh.heads_q + hq0 + g) * d + (size_t)s * sub;
+                const T *cv = kc + (size_t)c * sub;
+                for (int i = 0; i < sub; ++i) acc = fmaf(to_f32(qv[i]), to_f32(cv[i]), acc);
+            }
+            lut[e] = acc * sh.kappa;
         }
-        lut[e] = acc * sh.kappa;
-        wsum[e] = 0.f;
+        for (int e = threadIdx.x; e < 256 * sub; e += THREADS)
+            vcs[e] = e < nc * sub ? to_f32(vc[e]) : 0.f;
     }
     __syncthreads();
+
+    // phase-B role: 4-column slice `col` (columns col*4 .. col*4+3 of the
+    // head), token stream `stream` of `streams`
+    const int ncols = d / VW;
+    const int streams = THREADS / ncols;
+    const int col = threadIdx.x % ncols;
+    const int stream = threadIdx.x / ncols;
+    const bool b_active = stream < streams;
+    const int bs = (col * VW) / sub;            // sub-space of the slice
+    const int bi = (col * VW) - bs * sub;       // first element in the row
+    float2 acc[GPB][VW / 2];  // columns (0, 1) and (2, 3) of the slice
+#pragma unroll
+    for (int g = 0; g < GPB; ++g)
+#pragma unroll
+        for (int i = 0; i < VW / 2; ++i) acc[g][i] = make_float2(0.f, 0.f);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float m_run[G], l_run[G];
+    float m_run[GPB], l_run[GPB];
 #pragma unroll
-    for (int g = 0; g < G; ++g) m_run[g] = kNegInf, l_run[g] = 0.f;
+    for (int g = 0; g < GPB; ++g) m_run[g] = kNegInf, l_run[g] = 0.f;
 
-    for (int64_t ch = c0; ch < c1; ++ch) {
-        const int64_t tbase = sh.first_token + ch * CHUNK + threadIdx.x;
-        float sc[TPT][G];
-        float cm[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) cm[g] = kNegInf;
+    const int64_t c0 = sh.chunks * split / sh.splits;
+    const int64_t c1 = sh.chunks * (split + 1) / sh.splits;
+    // code rows of this thread's phase-A tokens, loaded one chunk ahead
+    uint32_t wk[TPT][NS / 4], wv[TPT][NS / 4];
+    auto load_rows = [&](int64_t ch) {
+        const int64_t tb = sh.first_token + ch * CHUNK + threadIdx.x;
 #pragma unroll
         for (int r = 0; r < TPT; ++r) {
-            const int64_t t = tbase + (int64_t)r * THREADS;
-#pragma unroll
-            for (int g = 0; g < G; ++g) sc[r][g] = kNegInf;
+            const int64_t t = tb + (int64_t)r * THREADS;
             if (t < sh.tokens) {
-                uint32_t w[NS / 4];
-                load_code_row<NS>(kb + (size_t)t * NS, w);
+                load_code_row<NS>(kb + (size_t)t * NS, wk[r]);
+                load_code_row<NS>(vb + (size_t)t * NS, wv[r]);
+            }
+        }
+    };
+    if (c0 < c1) load_rows(c0);
+    for (int64_t ch = c0; ch < c1; ++ch) {
+        const int64_t tbase = sh.first_token + ch * CHUNK;
+        // ---- phase A: scores of TPT tokens per thread
+        float sc[TPT][GPB];
+        float cm[GPB];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    if (g < gpb) {
-                        const float *lg = lut + g * tab;
-                        float a = 0.f;
+        for (int g = 0; g < GPB; ++g) cm[g] = kNegInf;
 #pragma unroll
-                        for (int s = 0; s < NS; ++s) a += lg[s * kLutStride + code_at(w[s / 4], s % 4)];
-                        sc[r][g] = a;
-                        cm[g] = fmaxf(cm[g], a);
+        for (int r = 0; r < TPT; ++r) {
+            const int64_t t = tbase + r * THREADS + threadIdx.x;
+#pragma unroll
+            for (int g = 0; g < GPB; ++g) sc[r][g] = kNegInf;
+            if (t < sh.tokens) {
+                float a[GPB];
+#pragma unroll
+                for (int g = 0; g < GPB; ++g) a[g] = 0.f;
+#pragma unroll
+                for (int s = 0; s < NS; ++s) {
+                    const int code = (int)code_at(wk[r][s / 4], s % 4);
+#pragma unroll
+                    for (int pk = 0; pk < NPACK; ++pk) {
+                        float v[GP];
+                        load_vec<GP>(lut + ((size_t)(pk * NS + s) * kLutStride + code) * GP, v);
+#pragma unroll
+                        for (int gi = 0; gi < GP; ++gi) a[pk * GP + gi] += v[gi];
                     }
+                }
+#pragma unroll
+                for (int g = 0; g < GPB; ++g) {
+                    sc[r][g] = a[g];
+                    cm[g] = fmaxf(cm[g], a[g]);
                 }
             }
         }
-        // block maximum of the chunk, per head (alternating buffers, so one
-        // barrier per chunk suffices)
-        float *rmax = red + (size_t)(ch & 1) * gpb * 32;
+        // block maximum of the chunk (alternating buffers).  This barrier
+        // also ends the previous chunk's phase B, so the weights and value
+        // codes below may be overwritten after it.
+        float *rmax = red + (size_t)(ch & 1) * GPB * 32;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            if (g < gpb) {
-                float m = cm[g];
+        for (int g = 0; g < GPB; ++g) {
+            float m = cm[g];
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                if (lane == 0) rmax[g * 32 + warp] = m;
-            }
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0) rmax[g * 32 + warp] = m;
         }
         __syncthreads();
-        bool rescale = false;
-        float f[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            f[g] = 1.f;
-            if (g < gpb) {
-                float m = m_run[g];
+        for (int g = 0; g < GPB; ++g) {
+            float m = m_run[g];
 #pragma unroll
-                for (int k = 0; k < NW; ++k) m = fmaxf(m, rmax[g * 32 + k]);
-                if (m > m_run[g] && m_run[g] > kNegInf) {
-                    f[g] = exp2f(m_run[g] - m);
-                    rescale = true;
-                }
-                l_run[g] *= f[g];
-                m_run[g] = m;
+            for (int k = 0; k < NW; ++k) m = fmaxf(m, rmax[g * 32 + k]);
+            if (m > m_run[g] && m_run[g] > kNegInf) {  // rescale what is accumulated
+                const float f = exp2f(m_run[g] - m);
+                l_run[g] *= f;
+#pragma unroll
+                for (int i = 0; i < VW / 2; ++i) acc[g][i] = make_float2(acc[g][i].x * f, acc[g][i].y * f);
             }
-        }
-        if (rescale) {  // same value in every thread of the block
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-                if (g < gpb && f[g] != 1.f)
-                    for (int e = threadIdx.x; e < tab; e += THREADS) wsum[g * tab + e] *= f[g];
-            __syncthreads();
+            m_run[g] = m;
         }
 #pragma unroll
         for (int r = 0; r < TPT; ++r) {
-            const int64_t t = tbase + (int64_t)r * THREADS;
-            if (t < sh.tokens) {
-                uint32_t w[NS / 4];
-                load_code_row<NS>(vb + (size_t)t * NS, w);
+            const int tl = r * THREADS + threadIdx.x;
+            float p[GPB];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    if (g < gpb) {
-                        const float p = exp2f(sc[r][g] - m_run[g]);
-                        l_run[g] += p;
-                        float *wg = wsum + g * tab;
+            for (int g = 0; g < GPB; ++g) {
+                // tokens past the end: sc = -inf, weight 0
+                p[g] = sc[r][g] == kNegInf ? 0.f : exp2f(sc[r][g] - m_run[g]);
+                l_run[g] += p[g];
+            }
 #pragma unroll
-                        for (int s = 0; s < NS; ++s) atomicAdd(&wg[s * kLutStride + code_at(w[s / 4], s % 4)], p);
+            for (int pk = 0; pk < NPACK; ++pk) {
+                float *dst = pw + (size_t)tl * GPB + pk * GP;
+                if constexpr (GP == 4) {
+                    *reinterpret_cast<float4 *>(dst) = make_float4(p[pk * 4], p[pk * 4 + 1], p[pk * 4 + 2], p[pk * 4 + 3]);
+                } else if constexpr (GP == 2) {
+                    *reinterpret_cast<float2 *>(dst) = make_float2(p[pk * 2], p[pk * 2 + 1]);
+                } else {
+                    dst[0] = p[pk];
+                }
+            }
+            if (tbase + tl < sh.tokens) store_code_row<NS>(vtile + (size_t)tl * NS, wv[r]);
+        }
+        if (ch + 1 < c1) load_rows(ch + 1);  // in flight during phase B
+        __syncthreads();
+        // ---- phase B: weighted value rows, accumulated in registers
+        const int64_t n_in = sh.tokens - tbase;
+        const int n_chunk = n_in < CHUNK ? (int)n_in : CHUNK;
+        if (b_active) {
+            constexpr int U = 4;
+            int tl = stream;
+            for (; tl + (U - 1) * streams < n_chunk; tl += U * streams) {
+                int code[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) code[u] = vtile[(size_t)(tl + u * streams) * NS + bs];
+                float4 row[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    row[u] = *reinterpret_cast<const float4 *>(vcs + (size_t)code[u] * sub + bi);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float p[GPB];
+#pragma unroll
+                    for (int pk = 0; pk < NPACK; ++pk) {
+                        float v[GP];
+                        load_vec<GP>(pw + (size_t)(tl + u * streams) * GPB + pk * GP, v);
+#pragma unroll
+                        for (int gi = 0; gi < GP; ++gi) p[pk * GP + gi] = v[gi];
                     }
+#pragma unroll
+                    for (int g = 0; g < GPB; ++g) {
+                        acc[g][0] = fma2_bcast(make_float2(row[u].x, row[u].y), p[g], acc[g][0]);
+                        acc[g][1] = fma2_bcast(make_float2(row[u].z, row[u].w), p[g], acc[g][1]);
+                    }
+                }
+            }
+            for (; tl < n_chunk; tl += streams) {
+                const int code = vtile[(size_t)tl * NS + bs];
+                const float4 row = *reinterpret_cast<const float4 *>(vcs + (size_t)code * sub + bi);
+                float p[GPB];
+#pragma unroll
+                for (int pk = 0; pk < NPACK; ++pk) {
+                    float v[GP];
+                    load_vec<GP>(pw + (size_t)tl * GPB + pk * GP, v);
+#pragma unroll
+                    for (int gi = 0; gi < GP; ++gi) p[pk * GP + gi] = v[gi];
+                }
+#pragma unroll
+                for (int g = 0; g < GPB; ++g) {
+                    acc[g][0] = fma2_bcast(make_float2(row.x, row.y), p[g], acc[g][0]);
+                    acc[g][1] = fma2_bcast(make_float2(row.z, row.w), p[g], acc[g][1]);
                 }
             }
         }
     }
+    __syncthreads();  // the tables are reused below
 
-    // ---- block sums, then out[g][s*SUB + i] = sum_c W[g][s][c] * Vcb[c][i]
-    float *rsum = red + (size_t)2 * gpb * 32;
+    // ---- block sums and the merge of the token streams
+    float *rsum = red + (size_t)2 * GPB * 32;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        if (g < gpb) {
-            float l = l_run[g];
+    for (int g = 0; g < GPB; ++g) {
+        float l = l_run[g];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-            if (lane == 0) rsum[g * 32 + warp] = l;
-        }
+        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        if (lane == 0) rsum[g * 32 + warp] = l;
+    }
+    float *accs = lut;  // [streams][GPB][D]; the tables are no longer read
+    if (b_active) {
+#pragma unroll
+        for (int g = 0; g < GPB; ++g)
+            *reinterpret_cast<float4 *>(accs + ((size_t)stream * GPB + g) * d + col * VW) =
+                make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
     }
     __syncthreads();
-    const int d = sh.head_dim;
-    for (int e = threadIdx.x; e < gpb * d; e += THREADS) {
+    for (int e = threadIdx.x; e < GPB * d; e += THREADS) {
         const int g = e / d;
         const int j = e - g * d;
-        const int s = j / sub, i = j - s * sub;
-        const float *wg = wsum + g * tab + s * kLutStride;
-        float acc = 0.f;
-        for (int c = 0; c < nc; ++c) acc = fmaf(wg[c], to_f32(vc[(size_t)c * sub + i]), acc);
+        float o = 0.f;
+        for (int k = 0; k < streams; ++k) o += accs[((size_t)k * GPB + g) * d + j];
         float *pp = part + (((size_t)b * sh.heads_q + hq0 + g) * sh.splits + split) * (size_t)(d + 2);
-        pp[2 + j] = acc;
+        pp[2 + j] = o;
         if (j == 0) {
-            float l = 0.f;
+            float l = 0.f, m = m_run[0];
             for (int k = 0; k < NW; ++k) l += rsum[g * 32 + k];
-            pp[0] = m_run[g];
+#pragma unroll
+            for (int gg = 1; gg < GPB; ++gg)
+                if (gg == g) m = m_run[gg];  // static register index
+            pp[0] = m;
             pp[1] = l;
         }
     }

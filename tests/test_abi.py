@@ -126,6 +126,7 @@ def _attention(lib):
     ((2, 8, 2, 100, 1024, 8, 256, 0, 0, 0, 1 << 20), 2),   # head_dim above 512
     ((2, 8, 2, 100, 128, 1, 256, 0, 0, 0, 1 << 20), 2),    # 128 sub-spaces
     ((2, 8, 2, 100, 96, 8, 256, 0, 0, 0, 1 << 20), 2),     # 12 sub-spaces
+    ((2, 8, 2, 100, 128, 2, 256, 0, 0, 0, 1 << 20), 2),    # sub_dim not a multiple of 4
     ((2, 8, 2, -1, 128, 8, 256, 0, 0, 0, 1 << 20), 1),     # negative tokens
     ((2, 8, 2, 100, 128, 8, 256, -5, 0, 0, 1 << 20), 1),   # negative window
     ((2, 8, 2, 100, 128, 8, 256, 0, 7, 0, 1 << 20), 1),    # unknown dtype
