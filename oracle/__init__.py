@@ -89,6 +89,11 @@ class OracleLib:
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
             ctypes.c_int32]
+        lib.vqo_encode_grouped_smooth.restype = ctypes.c_int32
+        lib.vqo_encode_grouped_smooth.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+            ctypes.c_int32]
         self.path = path
         self._lib = lib
 
@@ -140,6 +145,33 @@ class OracleLib:
                                           out.ctypes.data, int(n_threads))
         if rc != 0:
             raise RuntimeError(f"oracle encode failed with status {rc}")
+        return out
+
+    def encode_smooth(self, x: np.ndarray, smooth: np.ndarray, codebooks: np.ndarray,
+                      head_dim: int, *, bf16: bool = False, n_threads: int = 1) -> np.ndarray:
+        """Encode with per-channel smoothing: each element divided (fp32,
+        round to nearest) by its channel's factor before the encode formula.
+
+        ``x`` ``[G, M, sub_dim]``, ``smooth`` ``[G, head_dim]`` float32,
+        ``codebooks`` ``[G, n_centroids, sub_dim]``; row ``m`` of a group holds
+        channels ``(m % (head_dim // sub_dim)) * sub_dim + i``.  Returns
+        ``[G, M]`` uint32.
+        """
+        x = np.ascontiguousarray(x)
+        codebooks = np.ascontiguousarray(codebooks)
+        smooth = np.ascontiguousarray(smooth, dtype=np.float32)
+        if x.dtype != codebooks.dtype or x.ndim != 3 or codebooks.ndim != 3:
+            raise ValueError("x [G, M, sub_dim] and codebooks [G, n_c, sub_dim] of one dtype")
+        groups, per_group, sub_dim = x.shape
+        if smooth.shape != (groups, head_dim) or codebooks.shape[0] != groups:
+            raise ValueError(f"bad shapes smooth{smooth.shape} for x{x.shape}")
+        out = np.zeros((groups, per_group), dtype=np.uint32)
+        rc = self._lib.vqo_encode_grouped_smooth(
+            x.ctypes.data, smooth.ctypes.data, codebooks.ctypes.data, groups, per_group,
+            codebooks.shape[1], sub_dim, int(head_dim), _dtype_code(x, bf16), out.ctypes.data,
+            int(n_threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle smoothed encode failed with status {rc}")
         return out
 
 
@@ -224,6 +256,11 @@ def bf16_to_f32(bits: int) -> float:
 
 def distance(x, c, bf16: bool = False):
     return default().distance(x, c, bf16=bf16)
+
+
+def encode_smooth(x, smooth, codebooks, head_dim, *, bf16: bool = False, n_threads: int = 1):
+    return default().encode_smooth(x, smooth, codebooks, head_dim, bf16=bf16,
+                                   n_threads=n_threads)
 
 
 def encode(x, codebook, *, bf16: bool = False, n_threads: int = 1):

@@ -90,17 +90,24 @@ static float load_elem(const void *base, int dtype, int64_t k)
     }
 }
 
-/* Squared distance of one sub-vector to one centroid, the fp32 formula
- * above.  Exported so the tests can pin the arithmetic on its own. */
-float vqo_distance(const void *x, const void *c, int32_t sub_dim, int32_t dtype)
+/* The fp32 formula above for a row x (elements of x_dtype) and a centroid
+ * c (elements of c_dtype). */
+static float distance_of(const void *x, int x_dtype, const void *c, int c_dtype, int32_t sub_dim)
 {
     float dist = 0.0f;
     for (int32_t i = 0; i < sub_dim; ++i) {
-        float d = load_elem(x, dtype, i) - load_elem(c, dtype, i);
+        float d = load_elem(x, x_dtype, i) - load_elem(c, c_dtype, i);
         float sq = d * d;
         dist = dist + sq;
     }
     return dist;
+}
+
+/* Squared distance of one sub-vector to one centroid, the fp32 formula
+ * above.  Exported so the tests can pin the arithmetic on its own. */
+float vqo_distance(const void *x, const void *c, int32_t sub_dim, int32_t dtype)
+{
+    return distance_of(x, dtype, c, dtype, sub_dim);
 }
 
 static size_t elem_size(int dtype)
@@ -108,22 +115,38 @@ static size_t elem_size(int dtype)
     return dtype == VQO_F32 ? 4u : 2u;
 }
 
-/* Encode flattened rows [row_begin, row_end). */
+/* Encode flattened rows [row_begin, row_end).  With smooth != NULL each
+ * element is first divided by its channel's smooth factor (fp32, round to
+ * nearest): row m of group g holds channels (m % (head_dim / sub_dim)) *
+ * sub_dim + i of a key vector, factors smooth[g][head_dim]. */
 static void encode_rows(const void *x, const void *codebooks, int64_t n_per_group,
                         int32_t n_centroids, int32_t sub_dim, int32_t dtype,
+                        const float *smooth, int32_t head_dim,
                         uint32_t *out, int64_t row_begin, int64_t row_end)
 {
     const size_t es = elem_size(dtype);
     const char *xb = (const char *)x;
     const char *cbb = (const char *)codebooks;
+    float *xs = smooth ? (float *)malloc((size_t)sub_dim * sizeof(float)) : NULL;
     for (int64_t n = row_begin; n < row_end; ++n) {
         const int64_t g = n / n_per_group;
         const char *xn = xb + (size_t)n * (size_t)sub_dim * es;
         const char *cb = cbb + (size_t)g * (size_t)n_centroids * (size_t)sub_dim * es;
+        const void *row = xn;
+        int row_dtype = dtype;
+        if (xs) {
+            const int64_t block = (n - g * n_per_group) % (head_dim / sub_dim);
+            const float *f = smooth + (size_t)g * (size_t)head_dim + (size_t)block * (size_t)sub_dim;
+            for (int32_t i = 0; i < sub_dim; ++i)
+                xs[i] = load_elem(xn, dtype, i) / f[i];
+            row = xs;
+            row_dtype = VQO_F32;
+        }
         float best = INFINITY;
         uint32_t idx = 0;
         for (int32_t c = 0; c < n_centroids; ++c) {
-            float dist = vqo_distance(xn, cb + (size_t)c * (size_t)sub_dim * es, sub_dim, dtype);
+            float dist = distance_of(row, row_dtype, cb + (size_t)c * (size_t)sub_dim * es, dtype,
+                                     sub_dim);
             if (dist < best) {
                 best = dist;
                 idx = (uint32_t)c;
@@ -131,6 +154,7 @@ static void encode_rows(const void *x, const void *codebooks, int64_t n_per_grou
         }
         out[n] = idx;
     }
+    free(xs);
 }
 
 struct job {
@@ -138,6 +162,8 @@ struct job {
     const void *codebooks;
     int64_t n_per_group;
     int32_t n_centroids, sub_dim, dtype;
+    const float *smooth;
+    int32_t head_dim;
     uint32_t *out;
     int64_t begin, end;
 };
@@ -146,16 +172,17 @@ static void *job_main(void *arg)
 {
     struct job *j = (struct job *)arg;
     encode_rows(j->x, j->codebooks, j->n_per_group, j->n_centroids, j->sub_dim, j->dtype,
-                j->out, j->begin, j->end);
+                j->smooth, j->head_dim, j->out, j->begin, j->end);
     return NULL;
 }
 
 /* Encode all n_groups * n_per_group rows with n_threads host threads
  * (rows split into equal contiguous ranges; the result does not depend on
  * the thread count).  Returns VQO_OK or an error code. */
-int32_t vqo_encode_grouped(const void *x, const void *codebooks, int64_t n_groups,
-                           int64_t n_per_group, int32_t n_centroids, int32_t sub_dim,
-                           int32_t dtype, uint32_t *out, int32_t n_threads)
+static int32_t encode_all(const void *x, const float *smooth, const void *codebooks,
+                          int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                          int32_t sub_dim, int32_t head_dim, int32_t dtype, uint32_t *out,
+                          int32_t n_threads)
 {
     if (n_groups < 0 || n_per_group < 0 || n_centroids < 1 || sub_dim < 1)
         return VQO_ERR_INVALID_ARG;
@@ -171,7 +198,8 @@ int32_t vqo_encode_grouped(const void *x, const void *codebooks, int64_t n_group
     if ((int64_t)n_threads > rows)
         n_threads = (int32_t)rows;
     if (n_threads == 1) {
-        encode_rows(x, codebooks, n_per_group, n_centroids, sub_dim, dtype, out, 0, rows);
+        encode_rows(x, codebooks, n_per_group, n_centroids, sub_dim, dtype, smooth, head_dim, out,
+                    0, rows);
         return VQO_OK;
     }
     pthread_t *tid = (pthread_t *)calloc((size_t)n_threads, sizeof *tid);
@@ -184,8 +212,8 @@ int32_t vqo_encode_grouped(const void *x, const void *codebooks, int64_t n_group
     int32_t started = 0;
     int32_t rc = VQO_OK;
     for (int32_t t = 0; t < n_threads; ++t) {
-        jobs[t] = (struct job){x, codebooks, n_per_group, n_centroids, sub_dim, dtype, out,
-                               rows * t / n_threads, rows * (t + 1) / n_threads};
+        jobs[t] = (struct job){x, codebooks, n_per_group, n_centroids, sub_dim, dtype, smooth,
+                               head_dim, out, rows * t / n_threads, rows * (t + 1) / n_threads};
         if (pthread_create(&tid[t], NULL, job_main, &jobs[t]) != 0) {
             rc = VQO_ERR_THREAD;
             break;
@@ -200,6 +228,33 @@ int32_t vqo_encode_grouped(const void *x, const void *codebooks, int64_t n_group
     free(tid);
     free(jobs);
     return VQO_OK;
+}
+
+int32_t vqo_encode_grouped(const void *x, const void *codebooks, int64_t n_groups,
+                           int64_t n_per_group, int32_t n_centroids, int32_t sub_dim,
+                           int32_t dtype, uint32_t *out, int32_t n_threads)
+{
+    return encode_all(x, NULL, codebooks, n_groups, n_per_group, n_centroids, sub_dim, sub_dim,
+                      dtype, out, n_threads);
+}
+
+/* Encode with per-channel smoothing (fused neighbour of the encode: "VecInfer
+ * -- 16x with Metal acceleration" on the same site names per-channel smooth
+ * scaling for outlier channels; read here as key / factor per channel).
+ * smooth: [n_groups][head_dim] fp32; head_dim a multiple of sub_dim and
+ * n_per_group a multiple of head_dim / sub_dim (whole key vectors). */
+int32_t vqo_encode_grouped_smooth(const void *x, const float *smooth, const void *codebooks,
+                                  int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                                  int32_t sub_dim, int32_t head_dim, int32_t dtype, uint32_t *out,
+                                  int32_t n_threads)
+{
+    if (sub_dim < 1 || head_dim < sub_dim || head_dim % sub_dim != 0 || n_per_group < 0 ||
+        n_per_group % (head_dim / sub_dim) != 0)
+        return VQO_ERR_INVALID_ARG;
+    if (n_groups > 0 && n_per_group > 0 && !smooth)
+        return VQO_ERR_INVALID_ARG;
+    return encode_all(x, smooth, codebooks, n_groups, n_per_group, n_centroids, sub_dim, head_dim,
+                      dtype, out, n_threads);
 }
 
 int32_t vqo_encode(const void *x, const void *codebook, int64_t n, int32_t n_centroids,

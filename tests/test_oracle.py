@@ -255,3 +255,62 @@ def test_encode_then_dequantize_round_trips_exact_copies(oracle_mod):
     d_rec = ((rec.astype(np.float64) - x) ** 2).sum(-1)
     d_all = ((x.astype(np.float64)[:, :, None, :] - cb[:, None, :, :]) ** 2).sum(-1)
     assert np.all(d_rec <= d_all.min(-1) * (1 + 1e-6) + 1e-12)
+
+
+# ---------------------------------------------------------------- smoothing
+
+def _smooth_case(seed, groups=3, per_group=96, sub_dim=4, head_dim=16, n_c=64, dtype=np.float16):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((groups, per_group, sub_dim)).astype(dtype)
+    cb = rng.standard_normal((groups, n_c, sub_dim)).astype(dtype)
+    smooth = np.exp(0.5 * rng.standard_normal((groups, head_dim))).astype(np.float32)
+    return x, cb, smooth
+
+
+def test_smooth_ones_is_the_plain_encode(oracle_mod):
+    x, cb, _ = _smooth_case(120)
+    ones = np.ones((3, 16), dtype=np.float32)
+    assert np.array_equal(oracle_mod.encode_smooth(x, ones, cb, 16), oracle_mod.encode(x, cb))
+
+
+def test_smooth_equals_encoding_numpy_divided_rows(oracle_mod):
+    """Division by the channel's factor in IEEE fp32 (numpy's own division),
+    channel (m % (head_dim / sub_dim)) * sub_dim + i of group g, then the plain
+    encode on the fp32 rows: bit-identical indices."""
+    for seed, sub_dim, head_dim in ((121, 4, 16), (122, 8, 128), (123, 4, 256)):
+        x, cb, smooth = _smooth_case(seed, sub_dim=sub_dim, head_dim=head_dim,
+                                     per_group=3 * head_dim // sub_dim)
+        g, m, _ = x.shape
+        ns = head_dim // sub_dim
+        blocks = smooth.reshape(g, ns, sub_dim)[:, np.arange(m) % ns, :]  # [G, M, sub]
+        xs = x.astype(np.float32) / blocks
+        want = oracle_mod.encode(xs, cb.astype(np.float32))
+        assert np.array_equal(oracle_mod.encode_smooth(x, smooth, cb, head_dim), want)
+
+
+def test_smooth_by_powers_of_two_scales_the_codebook(oracle_mod):
+    """A factor 2^k on every channel scales every distance by 4^-k exactly, so
+    the indices equal those of the codebook scaled by 2^k."""
+    x, cb, _ = _smooth_case(124, dtype=np.float32)
+    for k in (-3, 1, 5):
+        s = np.full((3, 16), 2.0 ** k, dtype=np.float32)
+        assert np.array_equal(oracle_mod.encode_smooth(x, s, cb, 16),
+                              oracle_mod.encode(x, (cb * np.float32(2.0 ** k)).astype(np.float32)))
+
+
+def test_smooth_factors_are_per_group(oracle_mod):
+    """Groups use their own factor rows: group 1 with group 0's factors gives
+    other indices."""
+    x, cb, smooth = _smooth_case(125)
+    base = oracle_mod.encode_smooth(x, smooth, cb, 16)
+    swapped = smooth.copy()
+    swapped[1] = smooth[0]
+    other = oracle_mod.encode_smooth(x, swapped, cb, 16)
+    assert np.array_equal(base[0], other[0]) and np.array_equal(base[2], other[2])
+    assert not np.array_equal(base[1], other[1])
+
+
+def test_smooth_rejects_partial_key_vectors(oracle_mod):
+    x, cb, smooth = _smooth_case(126, per_group=10)  # 10 rows, 4 per key vector
+    with pytest.raises(RuntimeError):
+        oracle_mod.encode_smooth(x, smooth, cb, 16)

@@ -41,6 +41,13 @@ MUTATIONS = {
     "finite_init": ("float best = INFINITY;", "float best = 1e30f;"),
     # squared difference replaced by absolute difference
     "abs_distance": ("float sq = d * d;", "float sq = fabsf(d);"),
+    # smoothing multiplies instead of dividing
+    "smooth_multiply": ("xs[i] = load_elem(xn, dtype, i) / f[i];",
+                        "xs[i] = load_elem(xn, dtype, i) * f[i];"),
+    # smoothing reads the factors of the wrong channel block
+    "smooth_block": ("% (head_dim / sub_dim);", "/ (head_dim / sub_dim) % (head_dim / sub_dim);"),
+    # every group smoothed with group 0's factors
+    "smooth_group": ("smooth + (size_t)g * (size_t)head_dim", "smooth + 0 * (size_t)g"),
 }
 
 
@@ -62,6 +69,10 @@ def _pins(lib):
     yield lambda: pins.test_permuting_codebook_rows_permutes_indices(lib)
     yield lambda: pins.test_chunking_grouping_and_threads_do_not_change_results(lib)
     yield lambda: pins.test_special_values(lib)
+    yield lambda: pins.test_smooth_ones_is_the_plain_encode(lib)
+    yield lambda: pins.test_smooth_equals_encoding_numpy_divided_rows(lib)
+    yield lambda: pins.test_smooth_by_powers_of_two_scales_the_codebook(lib)
+    yield lambda: pins.test_smooth_factors_are_per_group(lib)
 
 
 def test_unmutated_source_passes_every_pin():
