@@ -413,6 +413,64 @@ def bench_dequantize(args) -> None:
     print(json.dumps(line))
 
 
+def bench_smooth(args) -> None:
+    """Encode fused with per-channel smoothing (uint8 codes out), one
+    ``vq_encode_grouped_smooth`` per step, against the FP32 CUDA-core peak
+    with the same per-sub-vector accounting as the plain encode."""
+    import torch
+
+    from product_vq_kv_gb300.build import build
+
+    build()
+    import product_vq_kv_gb300 as vq
+
+    dev = torch.device("cuda", 0)
+    w = workloads.WORKLOADS[args.workload]
+    head_dim = w.sub_vectors_per_head * w.sub_dim
+    x, smooth, cb = workloads.generate_smooth(args.workload)
+    xd, sd, cbd = (torch.from_numpy(a).to(dev) for a in (x, smooth, cb))
+    out = torch.empty(x.shape[:2], dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        vq.vq_encode_grouped_smooth(xd, sd, cbd, head_dim, index_bytes=1, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(0) as clocks:
+        for k in range(args.steps):
+            flush.zero_()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    props = torch.cuda.get_device_properties(dev)
+    clk = clocks.summary()
+    sm_max = measured_peaks().get("sm_max_mhz") or clk["sm_max_mhz"] or 2070.0
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    achieved = flops_per_subvector(w) * w.n / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "smoothed sub-vectors encoded to 8-bit codes/sec (1xGB300)",
+        "value": w.n / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "op": "smooth",
+        "config": dict(config_block(w, args, 1), head_dim=head_dim, index_bytes=1),
+        "gpu_launches": args.steps,
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "flops_per_unit": flops_per_subvector(w), "units_per_launch": w.n},
+        "e2e": None,
+    }
+    print(json.dumps(line))
+
+
 def bench_attention(args) -> None:
     """Decode attention over the 8-bit product-VQ KV cache of the Llama-shape
     workload (one ``vq_attention_decode`` per step: table build, scores,
@@ -522,7 +580,8 @@ def main() -> None:
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="falcon_prefill")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--op", choices=["encode", "dequantize", "attention"], default="encode")
+    p.add_argument("--op", choices=["encode", "dequantize", "attention", "smooth"],
+                   default="encode")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -532,6 +591,8 @@ def main() -> None:
         bench_dequantize(args)
     elif args.op == "attention":
         bench_attention(args)
+    elif args.op == "smooth":
+        bench_smooth(args)
     else:
         bench_ours(args)
 

@@ -132,6 +132,30 @@ vq_status vq_encode_grouped_u8(const void *x, const void *codebooks, int64_t n_g
                                vq_dtype dtype, uint8_t *out_idx, vq_stream_t stream);
 
 /*
+ * vq_encode_grouped_smooth -- the grouped encode fused with per-channel
+ * smoothing of the keys ("VecInfer -- 16x with Metal acceleration": per-channel
+ * smooth scaling tames the outlier channels that defeat plain VQ).  Each
+ * element is divided by its channel's factor in fp32, rounded to nearest, and
+ * the divided row is encoded by the exact formula of vq_encode (same indices
+ * as encoding the divided rows).  The query side is the caller's: attention
+ * over these codes takes the query multiplied by the same factors.
+ *   x          [n_groups][n_per_group][sub_dim]   device, dtype; row m of a
+ *              group holds channels (m % (head_dim / sub_dim)) * sub_dim + i
+ *              of a key vector, so n_per_group is a multiple of
+ *              head_dim / sub_dim
+ *   smooth     [n_groups][head_dim]               device, fp32 factors
+ *   codebooks  [n_groups][n_centroids][sub_dim]   device, dtype
+ *   out_idx    [n_groups][n_per_group]            device, uint32 (index_bytes
+ *              4) or uint8 codes (index_bytes 1, n_centroids <= 256)
+ * sub_dim 4 or 8 and x aligned to its row (up to 16 bytes), else
+ * VQ_ERR_UNSUPPORTED.  Other rules and asynchrony as vq_encode_grouped.
+ */
+vq_status vq_encode_grouped_smooth(const void *x, const float *smooth, const void *codebooks,
+                                   int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                                   int32_t sub_dim, int32_t head_dim, vq_dtype dtype, void *out_idx,
+                                   int32_t index_bytes, vq_stream_t stream);
+
+/*
  * vq_dequantize_grouped -- decode ("dequantize_vq"): rebuild each sub-vector
  * as a copy of its codebook row ("I Wrote a Metal Kernel to Stop My Mac From
  * OOMing", section "Mistake 1: I Wrote the Dequant Kernel First": indices in,

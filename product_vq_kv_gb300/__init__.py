@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     vq_encode,
     vq_encode_grouped,
     vq_encode_grouped_host,
+    vq_encode_grouped_smooth,
     vq_encode_grouped_u8,
     vq_status_string,
 )

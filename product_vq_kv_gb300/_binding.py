@@ -62,6 +62,9 @@ def load_library() -> ctypes.CDLL:
         lib.vq_attention_decode_static.restype = i32
         lib.vq_attention_decode_static.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i64, i32,
                                                    i32, i32, i64, ctypes.c_float, i32, vp, vp]
+        lib.vq_encode_grouped_smooth.restype = i32
+        lib.vq_encode_grouped_smooth.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, vp,
+                                                 i32, vp]
         lib.vq_attention_workspace_bytes.restype = ctypes.c_size_t
         lib.vq_attention_workspace_bytes.argtypes = [i64, i32, i32, i64, i32, i32, i32, i64]
         lib.vq_status_string.restype = ctypes.c_char_p
@@ -182,6 +185,40 @@ def vq_encode_grouped_u8(x: torch.Tensor, codebooks: torch.Tensor,
                                              codebooks.shape[1], sub, _dtype_code(x),
                                              out.data_ptr(), _stream_handle(stream, x.device))
     _check(st, "vq_encode_grouped_u8")
+    return out
+
+
+def vq_encode_grouped_smooth(x: torch.Tensor, smooth: torch.Tensor, codebooks: torch.Tensor,
+                             head_dim: int, index_bytes: int = 1, out: torch.Tensor | None = None,
+                             stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Grouped encode of smoothed keys: every element of ``x`` ``[G, M,
+    sub_dim]`` divided by its channel's factor in ``smooth`` ``[G, head_dim]``
+    (float32; row ``m`` holds channels ``(m % (head_dim // sub_dim)) * sub_dim
+    + i``) before the encode.  Returns ``[G, M]`` uint8 codes
+    (``index_bytes=1``) or uint32 indices (``index_bytes=4``)."""
+    _device_tensor(x, "x")
+    _device_tensor(smooth, "smooth")
+    _device_tensor(codebooks, "codebooks")
+    if (x.dim() != 3 or codebooks.dim() != 3 or x.shape[0] != codebooks.shape[0]
+            or x.shape[2] != codebooks.shape[2]):
+        raise ValueError(f"expected x [G, M, sub_dim] and codebooks [G, n_centroids, sub_dim], "
+                         f"got {tuple(x.shape)} and {tuple(codebooks.shape)}")
+    if x.dtype != codebooks.dtype:
+        raise TypeError("x and codebooks must share a dtype")
+    if smooth.dtype != torch.float32 or tuple(smooth.shape) != (x.shape[0], head_dim):
+        raise ValueError("smooth must be float32 of shape [G, head_dim]")
+    if index_bytes not in (1, 4):
+        raise ValueError("index_bytes must be 1 or 4")
+    g, m, sub = x.shape
+    odt = torch.uint8 if index_bytes == 1 else torch.uint32
+    if out is None:
+        out = torch.empty((g, m), dtype=odt, device=x.device)
+    elif out.dtype != odt or out.shape != (g, m) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {odt} tensor of shape [G, M]")
+    st = load_library().vq_encode_grouped_smooth(
+        x.data_ptr(), smooth.data_ptr(), codebooks.data_ptr(), g, m, codebooks.shape[1], sub,
+        head_dim, _dtype_code(x), out.data_ptr(), index_bytes, _stream_handle(stream, x.device))
+    _check(st, "vq_encode_grouped_smooth")
     return out
 
 

@@ -120,6 +120,8 @@ struct Args {
     void *out;
     cudaStream_t stream;
     int out_bytes = 4;  // index width: 4 (uint32) or 1 (uint8 codes)
+    const float *smooth = nullptr;  // per-channel smooth factors [n_groups][head_dim]
+    int32_t head_dim = 0;
 };
 
 size_t elem_size(vq_dtype d) { return d == VQ_F32 ? 4 : 2; }
@@ -244,10 +246,10 @@ vq_status launch_tc(const Args &a, const Plan &p)
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
-template <typename T, int SUB, typename OutT>
+template <typename T, int SUB, typename OutT, bool SMOOTH = false>
 vq_status launch_filter(const Args &a, const Plan &p)
 {
-    auto kernel = vqk::encode_filter<T, SUB, kFRows, kFThreads, kFGroup, OutT>;
+    auto kernel = vqk::encode_filter<T, SUB, kFRows, kFThreads, kFGroup, OutT, SMOOTH>;
     if (p.smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)p.smem) != cudaSuccess)
@@ -255,7 +257,8 @@ vq_status launch_filter(const Args &a, const Plan &p)
     }
     kernel<<<(unsigned)p.blocks, p.threads, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
-        p.tiles_per_group, 1.0f, static_cast<OutT *>(a.out));
+        p.tiles_per_group, 1.0f, static_cast<OutT *>(a.out), a.smooth,
+        SMOOTH ? a.head_dim / SUB : 0);
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
@@ -319,6 +322,44 @@ vq_status run(const Args &a)
     const Plan p = make_plan(a);
     if (p.blocks > 0x7fffffffLL) return VQ_ERR_UNSUPPORTED;
     return a.out_bytes == 1 ? launch_dtype<uint8_t>(a, p) : launch_dtype<uint32_t>(a, p);
+}
+
+template <typename OutT, int SUB>
+vq_status launch_smooth_typed(const Args &a, const Plan &p)
+{
+    switch (a.dtype) {
+    case VQ_F16: return launch_filter<__half, SUB, OutT, true>(a, p);
+    case VQ_BF16: return launch_filter<__nv_bfloat16, SUB, OutT, true>(a, p);
+    case VQ_F32: return launch_filter<float, SUB, OutT, true>(a, p);
+    }
+    return VQ_ERR_INTERNAL;
+}
+
+// Encode with per-channel smoothing: always the filter kernel, whose bound
+// holds for any fp32 row (the divided rows are not fp16 values).
+vq_status run_smooth(const Args &a)
+{
+    if (a.head_dim < a.sub_dim || a.sub_dim < 1 || a.head_dim % a.sub_dim) return VQ_ERR_INVALID_ARG;
+    if (a.n_per_group >= 0 && a.n_per_group % (a.head_dim / a.sub_dim)) return VQ_ERR_INVALID_ARG;
+    vq_status s = validate(a, true);
+    if (s != VQ_OK) return s;
+    if (a.n_groups * a.n_per_group == 0) return VQ_OK;
+    if (a.sub_dim != 4 && a.sub_dim != 8) return VQ_ERR_UNSUPPORTED;
+    if (!a.smooth || (uintptr_t)a.smooth % sizeof(float)) return VQ_ERR_INVALID_ARG;
+    const size_t row_bytes = (size_t)a.sub_dim * elem_size(a.dtype);
+    if ((uintptr_t)a.x % (row_bytes < 16 ? row_bytes : 16)) return VQ_ERR_UNSUPPORTED;
+    Plan p{};
+    p.kind = kFilter;
+    p.smem = a.sub_dim == 4 ? filter_smem<4>(a.n_centroids) : filter_smem<8>(a.n_centroids);
+    if (p.smem > kMaxFastSmem) return VQ_ERR_UNSUPPORTED;
+    const int64_t tile = (int64_t)kFThreads * kFRows;
+    p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
+    p.blocks = a.n_groups * p.tiles_per_group;
+    p.threads = kFThreads;
+    if (p.blocks > 0x7fffffffLL) return VQ_ERR_UNSUPPORTED;
+    if (a.out_bytes == 1)
+        return a.sub_dim == 4 ? launch_smooth_typed<uint8_t, 4>(a, p) : launch_smooth_typed<uint8_t, 8>(a, p);
+    return a.sub_dim == 4 ? launch_smooth_typed<uint32_t, 4>(a, p) : launch_smooth_typed<uint32_t, 8>(a, p);
 }
 
 const char *dtype_name(vq_dtype d)
@@ -502,6 +543,20 @@ vq_status vq_encode_grouped_u8(const void *x, const void *codebooks, int64_t n_g
            reinterpret_cast<cudaStream_t>(stream)};
     a.out_bytes = 1;
     return run(a);
+}
+
+vq_status vq_encode_grouped_smooth(const void *x, const float *smooth, const void *codebooks,
+                                   int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
+                                   int32_t sub_dim, int32_t head_dim, vq_dtype dtype, void *out_idx,
+                                   int32_t index_bytes, vq_stream_t stream)
+{
+    if (index_bytes != 1 && index_bytes != 4) return VQ_ERR_INVALID_ARG;
+    Args a{x, codebooks, n_groups, n_per_group, n_centroids, sub_dim, dtype, out_idx,
+           reinterpret_cast<cudaStream_t>(stream)};
+    a.out_bytes = index_bytes;
+    a.smooth = smooth;
+    a.head_dim = head_dim;
+    return run_smooth(a);
 }
 
 vq_status vq_dequantize_grouped(const void *idx, int32_t index_bytes, const void *codebooks,

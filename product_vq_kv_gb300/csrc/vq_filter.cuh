@@ -71,14 +71,33 @@ __device__ __forceinline__ float gamma_u(int k)
     return k * 5.9604645e-8f / (1.0f - k * 5.9604645e-8f);
 }
 
+// Row `row` of group g divided element-wise by its channels' smooth factors
+// (SMOOTH only): channels (row % smooth_ns) * SUB + i of smooth[g][.], fp32
+// division rounded to nearest.
+template <int SUB, bool SMOOTH>
+__device__ __forceinline__ void smooth_row(float (&v)[SUB], const float *__restrict__ sg,
+                                           int64_t row, int32_t smooth_ns)
+{
+    if constexpr (SMOOTH) {
+        const float *f = sg + (size_t)(row % smooth_ns) * SUB;
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) v[i] = __fdiv_rn(v[i], __ldg(f + i));
+    }
+}
+
 // Launch: grid.x = n_groups * tiles_per_group, block = THREADS, dynamic shared
 // memory = FilterLayout<SUB, GC>::bytes(n_centroids, THREADS * R); `one` =
-// 1.0f.  Same tiling and alignment requirements as encode_fast.
-template <typename T, int SUB, int R, int THREADS, int GC, typename OutT = uint32_t>
+// 1.0f.  Same tiling and alignment requirements as encode_fast.  With SMOOTH,
+// every row is first divided by its per-channel smooth factors (`smooth`
+// [n_groups][smooth_ns * SUB]; groups are whole key vectors of smooth_ns
+// rows); the bound below then holds for the divided row, which is what is
+// encoded.  Without SMOOTH, `smooth` and `smooth_ns` are unused.
+template <typename T, int SUB, int R, int THREADS, int GC, typename OutT = uint32_t,
+          bool SMOOTH = false>
 __global__ void __launch_bounds__(THREADS)
     encode_filter(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
                   int32_t n_centroids, int64_t tiles_per_group, float one,
-                  OutT *__restrict__ out)
+                  OutT *__restrict__ out, const float *__restrict__ smooth, int32_t smooth_ns)
 {
     static_assert(R % 2 == 0 && SUB % 4 == 0 && GC % 2 == 0, "layout constraints");
     using L = FilterLayout<SUB, GC>;
@@ -99,6 +118,7 @@ __global__ void __launch_bounds__(THREADS)
     const T *__restrict__ cb = codebooks + (size_t)g * (size_t)n_centroids * SUB;
     const T *__restrict__ xg = x + (size_t)g * (size_t)n_per_group * SUB;
     OutT *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
+    const float *__restrict__ sg = SMOOTH ? smooth + (size_t)g * (size_t)smooth_ns * SUB : nullptr;
     const int64_t row0 = tile * (int64_t)kTile + threadIdx.x;
 
     // Rows of this thread: row0 + r * THREADS, rows 2rp and 2rp+1 packed in
@@ -111,12 +131,14 @@ __global__ void __launch_bounds__(THREADS)
         const int64_t rb = ra + THREADS;
         if (ra < n_per_group) {
             load_row<T, SUB>(xg + (size_t)ra * SUB, a);
+            smooth_row<SUB, SMOOTH>(a, sg, ra, smooth_ns);
         } else {
 #pragma unroll
             for (int i = 0; i < SUB; ++i) a[i] = 0.f;
         }
         if (rb < n_per_group) {
             load_row<T, SUB>(xg + (size_t)rb * SUB, b);
+            smooth_row<SUB, SMOOTH>(b, sg, rb, smooth_ns);
         } else {
 #pragma unroll
             for (int i = 0; i < SUB; ++i) b[i] = 0.f;
@@ -287,6 +309,7 @@ __global__ void __launch_bounds__(THREADS)
         float xr[SUB];
 #pragma unroll
         for (int i = 0; i < SUB; ++i) xr[i] = widen(xg[(size_t)row * SUB + i]);
+        smooth_row<SUB, SMOOTH>(xr, sg, row, smooth_ns);
         float best = kInf;
         uint32_t id = kQueued;
         for (int c = lane; c < n_centroids; c += 32) {

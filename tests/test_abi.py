@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     for required in ("vq_encode", "vq_encode_grouped", "vq_encode_grouped_host",
                      "vq_encode_grouped_u8", "vq_dequantize_grouped",
                      "vq_status_string", "vq_describe_launch", "vq_abi_version",
-                     "vq_attention_decode", "vq_attention_workspace_bytes"):
+                     "vq_attention_decode", "vq_attention_workspace_bytes",
+                     "vq_encode_grouped_smooth"):
         assert required in names
 
 
@@ -139,6 +140,31 @@ def test_attention_argument_errors(lib, shape, status):
     p = P + off
     assert _attention(lib)(p, P, p, P, p, b, hq, hkv, t, d, sub, nc, window, 0.0, dtype, p, P, ws,
                            None) == status
+
+
+def _smooth(lib):
+    f = lib.vq_encode_grouped_smooth
+    f.restype = ctypes.c_int32
+    i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    f.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, vp, i32, vp]
+    return f
+
+
+# (x, smooth, cb, G, M, n_c, sub, head_dim, dtype, out, index_bytes) -> status
+@pytest.mark.parametrize("args,status", [
+    ((P, P, P, 2, 64, 256, 4, 16, 0, P, 2), 1),      # index width neither 1 nor 4
+    ((P, P, P, 2, 66, 256, 4, 16, 0, P, 4), 1),      # partial key vector in a group
+    ((P, P, P, 2, 64, 256, 4, 18, 0, P, 4), 1),      # head_dim not a multiple of sub_dim
+    ((P, P, P, 2, 64, 256, 4, 2, 0, P, 4), 1),       # head_dim below sub_dim
+    ((P, None, P, 2, 64, 256, 4, 16, 0, P, 4), 1),   # no factors
+    ((P, P + 2, P, 2, 64, 256, 4, 16, 0, P, 4), 1),  # factors not 4-byte aligned
+    ((P, P, P, 2, 64, 300, 4, 16, 0, P, 1), 2),      # 8-bit codes, 300 centroids
+    ((P, P, P, 2, 60, 256, 6, 12, 0, P, 4), 2),      # sub_dim 6
+    ((P + 2, P, P, 2, 64, 256, 4, 16, 0, P, 4), 2),  # x not aligned to its row
+    ((None, None, None, 2, 0, 256, 4, 16, 0, None, 4), 0),  # empty groups
+])
+def test_smooth_argument_errors(lib, args, status):
+    assert _smooth(lib)(*args, None) == status
 
 
 def test_attention_workspace_bytes(lib):

@@ -136,6 +136,33 @@ def generate(name: str, tokens: int | None = None):
     return x, cb
 
 
+SMOOTH_SEED = 18
+
+
+def generate_smooth(name: str, tokens: int | None = None):
+    """``(x, smooth, codebooks)`` for the smoothed encode of workload ``name``:
+    ``smooth`` is ``[G, head_dim]`` float32, one factor per channel.
+
+    For ``long_context`` the factors are the workload's own per-(head,
+    channel) outlier scales, so the smoothed keys are about N(0, 1), and the
+    codebooks are N(0, 1) rows (a codebook of the smoothed space).  For the
+    other workloads x and the codebooks are those of :func:`generate` and the
+    factors are exp(0.5 z), z ~ N(0, 1), per (group, channel).
+    """
+    w = WORKLOADS[name]
+    head_dim = w.sub_vectors_per_head * w.sub_dim
+    x, cb = generate(name, tokens)
+    if name == "long_context":
+        g = w.n_groups
+        seeds = SEEDS[name]
+        smooth = np.exp(np.float32(0.5) * _normal(seeds[2], (g, w.sub_vectors_per_head, w.sub_dim)))
+        smooth = smooth.astype(np.float32).reshape(g, head_dim)
+        cb = _normal(SMOOTH_SEED, cb.shape).astype(np.float16)
+        return x, smooth, cb
+    smooth = np.exp(np.float32(0.5) * _normal(SMOOTH_SEED, (w.n_groups, head_dim))).astype(np.float32)
+    return x, smooth, cb
+
+
 def _long_context(w, tokens, x_shape, cb_shape, seeds):
     """Keys with per-(head, channel) scale s = exp(0.5 z), z ~ N(0, 1), so a few
     channels are outliers; each head's codebook row r is N(0, 1) scaled by the
