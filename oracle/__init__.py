@@ -94,6 +94,17 @@ class OracleLib:
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
             ctypes.c_int32]
+        lib.vqo_scalar_quantize.restype = ctypes.c_int32
+        lib.vqo_scalar_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                            ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+        lib.vqo_hadamard_rotate.restype = ctypes.c_int32
+        lib.vqo_hadamard_rotate.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                            ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                            ctypes.c_void_p]
+        lib.vqo_hadamard_quantize.restype = ctypes.c_int32
+        lib.vqo_hadamard_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                              ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                              ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
         self.path = path
         self._lib = lib
 
@@ -145,6 +156,51 @@ class OracleLib:
                                           out.ctypes.data, int(n_threads))
         if rc != 0:
             raise RuntimeError(f"oracle encode failed with status {rc}")
+        return out
+
+    def scalar_quantize(self, x: np.ndarray, centroids: np.ndarray, *,
+                        bf16: bool = False) -> np.ndarray:
+        """Scalar (sub_dim = 1) quantize: index of the nearest fp32 centroid of
+        every element of ``x`` (any shape), as uint32 of the same shape."""
+        x = np.ascontiguousarray(x)
+        c = np.ascontiguousarray(centroids, dtype=np.float32).reshape(-1)
+        out = np.zeros(x.shape, dtype=np.uint32)
+        rc = self._lib.vqo_scalar_quantize(x.ctypes.data, _dtype_code(x, bf16), x.size,
+                                           c.ctypes.data, c.size, out.ctypes.data)
+        if rc != 0:
+            raise RuntimeError(f"oracle scalar quantize failed with status {rc}")
+        return out
+
+    def hadamard_rotate(self, x: np.ndarray, diag: np.ndarray, *, scale: float | None = None,
+                        bf16: bool = False) -> np.ndarray:
+        """Randomised Hadamard rotation of the rows of ``x`` ``[..., D]``:
+        float32 ``[..., D]``.  ``scale`` defaults to fp32(1/sqrt(D))."""
+        x = np.ascontiguousarray(x)
+        dim = x.shape[-1]
+        d = np.ascontiguousarray(diag, dtype=np.float32).reshape(-1)
+        scale = hadamard_scale(dim) if scale is None else np.float32(scale)
+        y = np.zeros(x.shape, dtype=np.float32)
+        rc = self._lib.vqo_hadamard_rotate(x.ctypes.data, _dtype_code(x, bf16), d.ctypes.data,
+                                           x.size // dim, dim, float(scale), y.ctypes.data)
+        if rc != 0:
+            raise RuntimeError(f"oracle hadamard rotate failed with status {rc}")
+        return y
+
+    def hadamard_quantize(self, x: np.ndarray, diag: np.ndarray, centroids: np.ndarray, *,
+                          scale: float | None = None, bf16: bool = False) -> np.ndarray:
+        """Rotation then scalar quantize of every rotated element: uint32 of
+        ``x``'s shape."""
+        x = np.ascontiguousarray(x)
+        dim = x.shape[-1]
+        d = np.ascontiguousarray(diag, dtype=np.float32).reshape(-1)
+        c = np.ascontiguousarray(centroids, dtype=np.float32).reshape(-1)
+        scale = hadamard_scale(dim) if scale is None else np.float32(scale)
+        out = np.zeros(x.shape, dtype=np.uint32)
+        rc = self._lib.vqo_hadamard_quantize(x.ctypes.data, _dtype_code(x, bf16), d.ctypes.data,
+                                             x.size // dim, dim, float(scale), c.ctypes.data,
+                                             c.size, out.ctypes.data)
+        if rc != 0:
+            raise RuntimeError(f"oracle hadamard quantize failed with status {rc}")
         return out
 
     def encode_smooth(self, x: np.ndarray, smooth: np.ndarray, codebooks: np.ndarray,
@@ -256,6 +312,24 @@ def bf16_to_f32(bits: int) -> float:
 
 def distance(x, c, bf16: bool = False):
     return default().distance(x, c, bf16=bf16)
+
+
+def hadamard_scale(dim: int) -> np.float32:
+    """fp32 value of 1/sqrt(dim), correctly rounded (dim a power of two: the
+    double value 2^(-k/2) rounds to fp32 without double-rounding trouble)."""
+    return np.float32(1.0 / np.sqrt(np.float64(dim)))
+
+
+def scalar_quantize(x, centroids, *, bf16: bool = False):
+    return default().scalar_quantize(x, centroids, bf16=bf16)
+
+
+def hadamard_rotate(x, diag, *, scale=None, bf16: bool = False):
+    return default().hadamard_rotate(x, diag, scale=scale, bf16=bf16)
+
+
+def hadamard_quantize(x, diag, centroids, *, scale=None, bf16: bool = False):
+    return default().hadamard_quantize(x, diag, centroids, scale=scale, bf16=bf16)
 
 
 def encode_smooth(x, smooth, codebooks, head_dim, *, bf16: bool = False, n_threads: int = 1):

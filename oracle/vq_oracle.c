@@ -264,3 +264,100 @@ int32_t vqo_encode(const void *x, const void *codebook, int64_t n, int32_t n_cen
         return VQO_ERR_INVALID_ARG;
     return vqo_encode_grouped(x, codebook, 1, n, n_centroids, sub_dim, dtype, out, n_threads);
 }
+
+/* ------------------------------------------------------------------------
+ * Sibling encoders on the same argmin (the page of five hand-tuned Metal
+ * compute kernels for TurboQuant, sections "Kernel 2: Scalar Quantize /
+ * Dequantize" and "Kernel 3: Fused Hadamard + Quantize").
+ * ---------------------------------------------------------------------- */
+
+/* Nearest scalar centroid of one fp32 value: d = val - c[j], dist = d * d
+ * (fp32, round to nearest, separately rounded), strict "<" over ascending j
+ * from (+inf, 0). */
+static uint32_t scalar_nearest(float val, const float *centroids, int32_t n_centroids)
+{
+    float best_dist = INFINITY;
+    uint32_t best = 0;
+    for (int32_t j = 0; j < n_centroids; ++j) {
+        float d = val - centroids[j];
+        float dist = d * d;
+        if (dist < best_dist) {
+            best_dist = dist;
+            best = (uint32_t)j;
+        }
+    }
+    return best;
+}
+
+/* Scalar (sub_dim = 1) quantize of n elements against one fp32 codebook
+ * ("Kernel 2"): out[e] = index of the nearest centroid of float(x[e]). */
+int32_t vqo_scalar_quantize(const void *x, int32_t dtype, int64_t n, const float *centroids,
+                            int32_t n_centroids, uint32_t *out)
+{
+    if (n < 0 || n_centroids < 1 || (dtype != VQO_F16 && dtype != VQO_BF16 && dtype != VQO_F32))
+        return VQO_ERR_INVALID_ARG;
+    for (int64_t e = 0; e < n; ++e)
+        out[e] = scalar_nearest(load_elem(x, dtype, e), centroids, n_centroids);
+    return VQO_OK;
+}
+
+/* Randomised Hadamard rotation of rows of length dim (a power of two)
+ * ("Kernel 3", steps 1-3): v = float(x) * diag (fp32); for stride = 1, 2,
+ * ..., dim/2 every pair (e, e + stride) with e % (2 stride) < stride becomes
+ * (v[e] + v[e + stride], v[e] - v[e + stride]) from the previous pass's
+ * values (fp32); finally y = v * scale with scale the fp32 value of
+ * 1/sqrt(dim) (correctly rounded; the page's rsqrt(float(D))). */
+static void hadamard_row(const void *x, int32_t dtype, int64_t row, const float *diag,
+                         int32_t dim, float scale, float *v)
+{
+    for (int32_t e = 0; e < dim; ++e)
+        v[e] = load_elem(x, dtype, row * dim + e) * diag[e];
+    for (int32_t stride = 1; stride < dim; stride <<= 1) {
+        for (int32_t e = 0; e < dim; ++e) {
+            if (e % (2 * stride) < stride) {
+                const float a = v[e], b = v[e + stride];
+                v[e] = a + b;
+                v[e + stride] = a - b;
+            }
+        }
+    }
+    for (int32_t e = 0; e < dim; ++e)
+        v[e] = v[e] * scale;
+}
+
+static int dim_ok(int32_t dim)
+{
+    return dim >= 1 && dim <= 65536 && (dim & (dim - 1)) == 0;
+}
+
+/* The rotated rows y [n_rows][dim] (fp32). */
+int32_t vqo_hadamard_rotate(const void *x, int32_t dtype, const float *diag, int64_t n_rows,
+                            int32_t dim, float scale, float *y)
+{
+    if (n_rows < 0 || !dim_ok(dim) || (dtype != VQO_F16 && dtype != VQO_BF16 && dtype != VQO_F32))
+        return VQO_ERR_INVALID_ARG;
+    for (int64_t r = 0; r < n_rows; ++r)
+        hadamard_row(x, dtype, r, diag, dim, scale, y + (size_t)r * (size_t)dim);
+    return VQO_OK;
+}
+
+/* Fused rotation and scalar quantize ("Kernel 3", step 4): out[r][e] = index
+ * of the nearest centroid of y[r][e]. */
+int32_t vqo_hadamard_quantize(const void *x, int32_t dtype, const float *diag, int64_t n_rows,
+                              int32_t dim, float scale, const float *centroids,
+                              int32_t n_centroids, uint32_t *out)
+{
+    if (n_rows < 0 || !dim_ok(dim) || n_centroids < 1 ||
+        (dtype != VQO_F16 && dtype != VQO_BF16 && dtype != VQO_F32))
+        return VQO_ERR_INVALID_ARG;
+    float *v = (float *)malloc((size_t)dim * sizeof(float));
+    if (!v)
+        return VQO_ERR_THREAD;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        hadamard_row(x, dtype, r, diag, dim, scale, v);
+        for (int32_t e = 0; e < dim; ++e)
+            out[(size_t)r * (size_t)dim + (size_t)e] = scalar_nearest(v[e], centroids, n_centroids);
+    }
+    free(v);
+    return VQO_OK;
+}

@@ -153,3 +153,54 @@ def test_attention_mutation_is_caught(name):
             caught += 1
             break
     assert caught, f"no pin caught the '{name}' mutation"
+
+
+# ---- sibling encoders (scalar quantize, Hadamard rotation) in the C source
+
+SIBLING_MUTATIONS = {
+    # ties go to the higher index
+    "scalar_tie": ("if (dist < best_dist) {", "if (dist <= best_dist) {"),
+    # the value is rounded to fp16 precision before the subtraction
+    "scalar_half": ("float d = val - centroids[j];",
+                    "float d = (float)(_Float16)val - centroids[j];"),
+    # butterfly with the difference the wrong way round
+    "butterfly_sign": ("v[e + stride] = a - b;", "v[e + stride] = b - a;"),
+    # the random sign flip dropped
+    "no_diag": ("load_elem(x, dtype, row * dim + e) * diag[e];",
+                "load_elem(x, dtype, row * dim + e);"),
+    # the butterfly pairs elements one stride too far
+    "butterfly_partner": ("const float a = v[e], b = v[e + stride];",
+                          "const float a = v[e], b = v[(e + 2 * stride) % dim];"),
+    # scaling skipped
+    "no_scale": ("v[e] = v[e] * scale;", "v[e] = v[e];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SIBLING_MUTATIONS))
+def test_sibling_mutation_is_caught(name):
+    import test_oracle_siblings as spins
+
+    before, after = SIBLING_MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, f"mutation anchor for {name} not found exactly once"
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "mutant.c")
+        with open(path, "w") as f:
+            f.write(src.replace(before, after))
+        lib = oracle.OracleLib(oracle.compile_source(path, os.path.join(tmp, "mutant.so")))
+        caught = 0
+        for pin in spins.PINS:
+            try:
+                pin(lib)
+            except (AssertionError, RuntimeError, ValueError):
+                caught += 1
+                break
+        assert caught, f"no pin caught the '{name}' mutation"
+
+
+def test_unmutated_sibling_source_passes_every_pin():
+    import test_oracle_siblings as spins
+
+    lib = oracle.default()
+    for pin in spins.PINS:
+        pin(lib)
