@@ -471,6 +471,72 @@ def bench_smooth(args) -> None:
     print(json.dumps(line))
 
 
+def bench_sibling(args, fused: bool) -> None:
+    """Scalar (sub_dim = 1) quantize of one layer's key cache against a 4-bit
+    Lloyd-Max codebook (``--op scalar``: the 64 KiB table pass), or the
+    randomised Hadamard rotation fused with it (``--op hadamard``); one launch
+    per step (plus the table build for the scalar pass), against the HBM
+    roofline of 2 bytes in and 1 byte out per element."""
+    import torch
+
+    from product_vq_kv_gb300.build import build
+
+    build()
+    import product_vq_kv_gb300 as vq
+
+    dev = torch.device("cuda", 0)
+    sw = workloads.SCALAR_WORKLOADS["turboquant_keys"]
+    x, c, diag = workloads.generate_scalar(sw.name)
+    xd, cd, dd = (torch.from_numpy(a).to(dev) for a in (x, c, diag))
+    out = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+    ws = torch.empty(65536, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if fused:
+            vq.vq_hadamard_quantize(xd, dd, cd, out=out, stream=stream)
+        else:
+            vq.vq_scalar_quantize(xd, cd, out=out, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(0) as clocks:
+        for k in range(args.steps):
+            flush.zero_()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    algo_bytes = 3 * sw.n
+    achieved = algo_bytes / (ms * 1e-3) / 1e9
+    peak = measured_peaks().get("hbm_gbs") or 6800.0
+    clk = clocks.summary()
+    line = {
+        "metric": ("key elements rotated and quantized/sec (1xGB300)" if fused
+                   else "key elements scalar-quantized/sec (1xGB300)"),
+        "value": sw.n / (ms * 1e-3), "unit": "elements/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "op": "hadamard" if fused else "scalar",
+        "config": {"workload": sw.name, "batch": sw.batch, "heads": sw.heads,
+                   "tokens": sw.tokens, "head_dim": sw.head_dim, "bits": sw.bits,
+                   "l2": "flushed before every step (256 MiB write)"},
+        "gpu_launches": args.steps * (1 if fused else 2),
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "bytes_per_launch": algo_bytes,
+                     "timed": "whole step" + ("" if fused else " (table build + lookup pass)")},
+        "e2e": None,
+    }
+    print(json.dumps(line))
+
+
 def bench_attention(args) -> None:
     """Decode attention over the 8-bit product-VQ KV cache of the Llama-shape
     workload (one ``vq_attention_decode`` per step: table build, scores,
@@ -580,8 +646,8 @@ def main() -> None:
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="falcon_prefill")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--op", choices=["encode", "dequantize", "attention", "smooth"],
-                   default="encode")
+    p.add_argument("--op", choices=["encode", "dequantize", "attention", "smooth", "scalar",
+                                    "hadamard"], default="encode")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -593,6 +659,8 @@ def main() -> None:
         bench_attention(args)
     elif args.op == "smooth":
         bench_smooth(args)
+    elif args.op in ("scalar", "hadamard"):
+        bench_sibling(args, fused=args.op == "hadamard")
     else:
         bench_ours(args)
 

@@ -240,6 +240,57 @@ vq_status vq_attention_decode_static(const void *q, const uint8_t *k_codes,
                                      int32_t sub_dim, int32_t n_centroids, int64_t window,
                                      float scale, vq_dtype dtype, void *out, vq_stream_t stream);
 
+/*
+ * Sibling encoders on the same nearest-centroid rule (the page of five
+ * hand-tuned Metal compute kernels for TurboQuant, "Kernel 2: Scalar Quantize
+ * / Dequantize" and "Kernel 3: Fused Hadamard + Quantize").  One fp32
+ * codebook `centroids` [n_centroids] (1..256, device) serves every element;
+ * indices are uint8.
+ *
+ * vq_scalar_quantize -- out[e] = the j minimising fl(fl(float(x[e]) -
+ * centroids[j])^2), lowest j on ties, NaN never winning, 0 when nothing wins.
+ *   x          [n]  device, dtype
+ *   out        [n]  device, uint8, written
+ *   workspace  device scratch of the caller, 16-byte aligned.  With fp16 /
+ *              bf16 input and at least vq_scalar_quantize_workspace_bytes
+ *              (65536) bytes, the rule is evaluated once for each of the
+ *              65,536 input bit patterns and the pass becomes a table lookup
+ *              (same indices); otherwise (fp32 input, or NULL / smaller
+ *              workspace) every element scans the codebook.
+ */
+size_t vq_scalar_quantize_workspace_bytes(vq_dtype dtype);
+vq_status vq_scalar_quantize(const void *x, vq_dtype dtype, int64_t n, const float *centroids,
+                             int32_t n_centroids, uint8_t *out, void *workspace,
+                             size_t workspace_bytes, vq_stream_t stream);
+
+/*
+ * vq_scalar_dequantize -- out[e] = centroids[idx[e]] rounded to nearest in the
+ * output dtype (the page's half(centroids[idx])); an index >= n_centroids
+ * gives 0.  idx [n] uint8, out [n] dtype, both device.
+ */
+vq_status vq_scalar_dequantize(const uint8_t *idx, int64_t n, const float *centroids,
+                               int32_t n_centroids, vq_dtype dtype, void *out,
+                               vq_stream_t stream);
+
+/*
+ * vq_hadamard_rotate -- randomised Hadamard rotation of each row of dim
+ * elements (dim a power of two, 1..1024): v = float(x) * diag (fp32); for
+ * stride = 1, 2, ..., dim/2 every pair (e, e + stride) with e % (2 stride) <
+ * stride becomes (v[e] + v[e+stride], v[e] - v[e+stride]); y = v * s with s
+ * the fp32 value of 1/sqrt(dim) (correctly rounded).  Every step is one
+ * rounded fp32 operation in exactly this order.
+ *   x     [n_rows][dim]  device, dtype        diag  [dim]  device, fp32
+ *   y     [n_rows][dim]  device, fp32, written
+ * vq_hadamard_quantize -- the same rotation fused with vq_scalar_quantize of
+ * every rotated value; out [n_rows][dim] uint8 (4-byte aligned when dim >=
+ * 128).  Neither writes the rotated keys to memory in the fused form.
+ */
+vq_status vq_hadamard_rotate(const void *x, vq_dtype dtype, const float *diag, int64_t n_rows,
+                             int32_t dim, float *y, vq_stream_t stream);
+vq_status vq_hadamard_quantize(const void *x, vq_dtype dtype, const float *diag, int64_t n_rows,
+                               int32_t dim, const float *centroids, int32_t n_centroids,
+                               uint8_t *out, vq_stream_t stream);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char *vq_status_string(vq_status status);
 

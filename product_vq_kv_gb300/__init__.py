@@ -27,6 +27,10 @@ from ._binding import (  # noqa: F401
     vq_encode_grouped,
     vq_encode_grouped_host,
     vq_encode_grouped_smooth,
+    vq_hadamard_quantize,
+    vq_hadamard_rotate,
+    vq_scalar_dequantize,
+    vq_scalar_quantize,
     vq_encode_grouped_u8,
     vq_status_string,
 )

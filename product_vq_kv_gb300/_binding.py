@@ -65,6 +65,16 @@ def load_library() -> ctypes.CDLL:
         lib.vq_encode_grouped_smooth.restype = i32
         lib.vq_encode_grouped_smooth.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, vp,
                                                  i32, vp]
+        lib.vq_scalar_quantize_workspace_bytes.restype = ctypes.c_size_t
+        lib.vq_scalar_quantize_workspace_bytes.argtypes = [i32]
+        lib.vq_scalar_quantize.restype = i32
+        lib.vq_scalar_quantize.argtypes = [vp, i32, i64, vp, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.vq_scalar_dequantize.restype = i32
+        lib.vq_scalar_dequantize.argtypes = [vp, i64, vp, i32, i32, vp, vp]
+        lib.vq_hadamard_rotate.restype = i32
+        lib.vq_hadamard_rotate.argtypes = [vp, i32, vp, i64, i32, vp, vp]
+        lib.vq_hadamard_quantize.restype = i32
+        lib.vq_hadamard_quantize.argtypes = [vp, i32, vp, i64, i32, vp, i32, vp, vp]
         lib.vq_attention_workspace_bytes.restype = ctypes.c_size_t
         lib.vq_attention_workspace_bytes.argtypes = [i64, i32, i32, i64, i32, i32, i32, i64]
         lib.vq_status_string.restype = ctypes.c_char_p
@@ -219,6 +229,96 @@ def vq_encode_grouped_smooth(x: torch.Tensor, smooth: torch.Tensor, codebooks: t
         x.data_ptr(), smooth.data_ptr(), codebooks.data_ptr(), g, m, codebooks.shape[1], sub,
         head_dim, _dtype_code(x), out.data_ptr(), index_bytes, _stream_handle(stream, x.device))
     _check(st, "vq_encode_grouped_smooth")
+    return out
+
+
+def _f32_vector(t: torch.Tensor, name: str) -> None:
+    _device_tensor(t, name)
+    if t.dtype != torch.float32 or t.dim() != 1:
+        raise ValueError(f"{name} must be a 1-D float32 device tensor")
+
+
+def vq_scalar_quantize(x: torch.Tensor, centroids: torch.Tensor, out: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, use_table: bool = True,
+                       stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Scalar (sub_dim = 1) quantize of every element of ``x`` against the
+    float32 ``centroids``: uint8 indices of ``x``'s shape.  For fp16 / bf16
+    input a 64 KiB ``workspace`` enables the table pass (allocated here when
+    omitted and ``use_table``)."""
+    _device_tensor(x, "x")
+    _f32_vector(centroids, "centroids")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    elif out.dtype != torch.uint8 or out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous uint8 tensor of x's shape")
+    code = _dtype_code(x)
+    lib = load_library()
+    need = int(lib.vq_scalar_quantize_workspace_bytes(code))
+    if workspace is None and use_table and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.vq_scalar_quantize(x.data_ptr(), code, x.numel(), centroids.data_ptr(),
+                                centroids.numel(), out.data_ptr(), ws_ptr, ws_bytes,
+                                _stream_handle(stream, x.device))
+    _check(st, "vq_scalar_quantize")
+    return out
+
+
+def vq_scalar_dequantize(idx: torch.Tensor, centroids: torch.Tensor,
+                         dtype: torch.dtype = torch.float16, out: torch.Tensor | None = None,
+                         stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """``centroids[idx]`` in ``dtype`` (round to nearest); out-of-range
+    indices give 0."""
+    _device_tensor(idx, "idx")
+    _f32_vector(centroids, "centroids")
+    if idx.dtype != torch.uint8:
+        raise TypeError("idx must be uint8")
+    if out is None:
+        out = torch.empty(idx.shape, dtype=dtype, device=idx.device)
+    st = load_library().vq_scalar_dequantize(idx.data_ptr(), idx.numel(), centroids.data_ptr(),
+                                             centroids.numel(), _dtype_code(out), out.data_ptr(),
+                                             _stream_handle(stream, idx.device))
+    _check(st, "vq_scalar_dequantize")
+    return out
+
+
+def vq_hadamard_rotate(x: torch.Tensor, diag: torch.Tensor, out: torch.Tensor | None = None,
+                       stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Randomised Hadamard rotation of the rows of ``x`` ``[..., D]``:
+    float32 of the same shape."""
+    _device_tensor(x, "x")
+    _f32_vector(diag, "diag")
+    dim = x.shape[-1]
+    if diag.numel() != dim:
+        raise ValueError("diag must have one entry per column")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    st = load_library().vq_hadamard_rotate(x.data_ptr(), _dtype_code(x), diag.data_ptr(),
+                                           x.numel() // dim, dim, out.data_ptr(),
+                                           _stream_handle(stream, x.device))
+    _check(st, "vq_hadamard_rotate")
+    return out
+
+
+def vq_hadamard_quantize(x: torch.Tensor, diag: torch.Tensor, centroids: torch.Tensor,
+                         out: torch.Tensor | None = None,
+                         stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Rotation fused with the scalar quantize: uint8 indices of ``x``'s
+    shape."""
+    _device_tensor(x, "x")
+    _f32_vector(diag, "diag")
+    _f32_vector(centroids, "centroids")
+    dim = x.shape[-1]
+    if diag.numel() != dim:
+        raise ValueError("diag must have one entry per column")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    st = load_library().vq_hadamard_quantize(x.data_ptr(), _dtype_code(x), diag.data_ptr(),
+                                             x.numel() // dim, dim, centroids.data_ptr(),
+                                             centroids.numel(), out.data_ptr(),
+                                             _stream_handle(stream, x.device))
+    _check(st, "vq_hadamard_quantize")
     return out
 
 

@@ -1,0 +1,218 @@
+// vq_scalar.cuh -- sibling encoders on the same nearest-centroid rule (the
+// page of five hand-tuned Metal compute kernels for TurboQuant, sections
+// "Kernel 2: Scalar Quantize / Dequantize" and "Kernel 3: Fused Hadamard +
+// Quantize"):
+//   scalar quantize   idx[e] = argmin_j fl(fl(float(x[e]) - c[j])^2), strict
+//                     "<" over ascending j from (+inf, 0), one fp32 codebook;
+//   Hadamard rotate   v = float(x) * diag; butterfly passes stride 1, 2, ...,
+//                     D/2: (lo, hi) -> (lo + hi, lo - hi); y = v * scale;
+//   fused quantize    idx = scalar quantize of y.
+// Every operation is an explicitly rounded fp32 intrinsic, so no compiler
+// contraction can change a result.
+//
+// GB300 shape.  16-bit inputs have only 65,536 values: scalar_table
+// evaluates the formula once for each bit pattern into a 64 KiB table (the
+// caller's workspace), and scalar_lookup stages that table in shared memory
+// and turns the pass into a coalesced 2-byte-in / 1-byte-out stream with one
+// shared-memory lookup per element (HBM-bound, bit-identical to the scan).
+// fp32 inputs use scalar_scan (the scan itself, codebook in shared memory,
+// broadcast reads).  The rotation runs one row per warp (or several rows of
+// D < 32 per warp): a lane holds E = D/32 contiguous elements, so butterfly
+// strides below E stay in registers and larger ones are shfl.xor exchanges;
+// no shared memory and no barriers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+namespace vqs {
+
+__device__ __forceinline__ float widen16(uint16_t bits, bool bf16)
+{
+    return bf16 ? __uint_as_float((uint32_t)bits << 16) : __half2float(__ushort_as_half(bits));
+}
+__device__ __forceinline__ float widen_elem(float v) { return v; }
+__device__ __forceinline__ float widen_elem(__half v) { return __half2float(v); }
+__device__ __forceinline__ float widen_elem(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// The nearest-centroid rule for one fp32 value, codebook c[0..n_c) in shared
+// memory (every lane reads the same entry: broadcast).
+__device__ __forceinline__ uint32_t nearest(float val, const float *c, int n_c)
+{
+    float best_dist = __int_as_float(0x7f800000);
+    uint32_t best = 0;
+    for (int j = 0; j < n_c; ++j) {
+        const float d = __fsub_rn(val, c[j]);
+        const float dist = __fmul_rn(d, d);
+        if (dist < best_dist) {
+            best_dist = dist;
+            best = (uint32_t)j;
+        }
+    }
+    return best;
+}
+
+// table[p] = nearest index of the 16-bit pattern p (fp16 or bf16).  Launch:
+// 65536 threads in blocks of 256; dynamic shared memory n_c * 4 bytes.
+__global__ void scalar_table(const float *__restrict__ centroids, int32_t n_c, bool bf16,
+                             uint8_t *__restrict__ table)
+{
+    extern __shared__ float sc_tab[];
+    for (int j = threadIdx.x; j < n_c; j += blockDim.x) sc_tab[j] = centroids[j];
+    __syncthreads();
+    const uint32_t p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p < 65536u) table[p] = (uint8_t)nearest(widen16((uint16_t)p, bf16), sc_tab, n_c);
+}
+
+// out[e] = table[x[e]].  Launch: any grid of 256-thread blocks, dynamic
+// shared memory 65536 bytes; grid-stride over 8-element units when `vec`
+// (x 16-byte and out 8-byte aligned), the remaining elements one by one.
+__global__ void __launch_bounds__(256)
+    scalar_lookup(const uint16_t *__restrict__ x, int64_t n, const uint8_t *__restrict__ table,
+                  bool vec, uint8_t *__restrict__ out)
+{
+    extern __shared__ __align__(16) uint8_t sl_tab[];
+    const uint4 *t4 = reinterpret_cast<const uint4 *>(table);
+    for (int k = threadIdx.x; k < 65536 / 16; k += blockDim.x)
+        reinterpret_cast<uint4 *>(sl_tab)[k] = __ldg(t4 + k);
+    __syncthreads();
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t units = vec ? n / 8 : 0;
+    for (int64_t u = tid; u < units; u += nthreads) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(x) + u);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            lo |= (uint32_t)sl_tab[w[k] & 0xffffu] << (16 * k);
+            lo |= (uint32_t)sl_tab[w[k] >> 16] << (16 * k + 8);
+            hi |= (uint32_t)sl_tab[w[k + 2] & 0xffffu] << (16 * k);
+            hi |= (uint32_t)sl_tab[w[k + 2] >> 16] << (16 * k + 8);
+        }
+        __stcs(reinterpret_cast<uint2 *>(out) + u, make_uint2(lo, hi));
+    }
+    for (int64_t e = units * 8 + tid; e < n; e += nthreads) out[e] = sl_tab[x[e]];
+}
+
+// The scan itself (any input type), codebook in shared memory.  Launch: any
+// grid of 256-thread blocks, dynamic shared memory n_c * 4 bytes.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
+                int32_t n_c, uint8_t *__restrict__ out)
+{
+    extern __shared__ float ss_cb[];
+    for (int j = threadIdx.x; j < n_c; j += blockDim.x) ss_cb[j] = centroids[j];
+    __syncthreads();
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += nthreads)
+        out[e] = (uint8_t)nearest(widen_elem(x[e]), ss_cb, n_c);
+}
+
+// Randomised Hadamard rotation of rows of D = LPR * E elements, optionally
+// fused with the scalar quantize.  LPR = min(D, 32) lanes per row, 32 / LPR
+// rows per warp; lane l of a row holds elements l*E .. l*E + E - 1.
+// Launch: blockDim.x = 256, grid = ceil(n_rows / (8 * 32 / LPR)); dynamic
+// shared memory n_c * 4 bytes (QUANT) or 0.  x rows contiguous; y / idx
+// [n_rows][D].
+template <typename T, int E, bool QUANT>
+__global__ void __launch_bounds__(256)
+    hadamard_rows(const T *__restrict__ x, const float *__restrict__ diag, int64_t n_rows,
+                  int32_t lanes_per_row, float scale, const float *__restrict__ centroids,
+                  int32_t n_c, float *__restrict__ y, uint8_t *__restrict__ idx)
+{
+    extern __shared__ float hq_cb[];
+    if constexpr (QUANT) {
+        for (int j = threadIdx.x; j < n_c; j += blockDim.x) hq_cb[j] = centroids[j];
+        __syncthreads();
+    }
+    const int lane = threadIdx.x & 31;
+    const int lpr = lanes_per_row;
+    const int rows_per_warp = 32 / lpr;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int sub = lane / lpr;   // row within the warp
+    const int l = lane - sub * lpr;  // lane within the row
+    const int64_t row = warp * rows_per_warp + sub;
+    const bool live = row < n_rows;
+    const int d = lpr * E;
+    float v[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        const int e = l * E + j;
+        v[j] = live ? __fmul_rn(widen_elem(x[(size_t)row * d + e]), __ldg(diag + e)) : 0.f;
+    }
+    // strides below E: pairs inside the lane's registers
+#pragma unroll
+    for (int s = 1; s < E; s <<= 1) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            if ((j & s) == 0) {
+                const float a = v[j], b = v[j + s];
+                v[j] = __fadd_rn(a, b);
+                v[j + s] = __fsub_rn(a, b);
+            }
+        }
+    }
+    // strides E .. D/2: the partner element sits in lane l ^ (s / E)
+    for (int ls = 1; ls < lpr; ls <<= 1) {
+        const bool upper = (l & ls) != 0;
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            const float p = __shfl_xor_sync(0xffffffffu, v[j], ls);
+            v[j] = upper ? __fsub_rn(p, v[j]) : __fadd_rn(v[j], p);
+        }
+    }
+    if (!live) return;
+#pragma unroll
+    for (int j = 0; j < E; ++j) v[j] = __fmul_rn(v[j], scale);
+    if constexpr (QUANT) {
+        uint8_t *o = idx + (size_t)row * d + (size_t)l * E;
+        if constexpr (E % 4 == 0) {
+#pragma unroll
+            for (int j = 0; j < E; j += 4) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) w |= nearest(v[j + k], hq_cb, n_c) << (8 * k);
+                *reinterpret_cast<uint32_t *>(o + j) = w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < E; ++j) o[j] = (uint8_t)nearest(v[j], hq_cb, n_c);
+        }
+    } else {
+        float *o = y + (size_t)row * d + (size_t)l * E;
+#pragma unroll
+        for (int j = 0; j < E; ++j) o[j] = v[j];
+    }
+}
+
+}  // namespace vqs
+
+namespace vqs {
+
+// out[e] = centroids[idx[e]] converted to the output type (round to
+// nearest); an index >= n_c gives 0.  Launch: any grid, grid-stride.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    scalar_dequant(const uint8_t *__restrict__ idx, int64_t n, const float *__restrict__ centroids,
+                   int32_t n_c, T *__restrict__ out)
+{
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += nthreads) {
+        const uint32_t k = idx[e];
+        const float v = k < (uint32_t)n_c ? __ldg(centroids + k) : 0.f;
+        if constexpr (sizeof(T) == 4) {
+            out[e] = v;
+        } else if constexpr (std::is_same<T, __half>::value) {
+            out[e] = __float2half_rn(v);
+        } else {
+            out[e] = __float2bfloat16_rn(v);
+        }
+    }
+}
+
+}  // namespace vqs

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
                      "vq_encode_grouped_u8", "vq_dequantize_grouped",
                      "vq_status_string", "vq_describe_launch", "vq_abi_version",
                      "vq_attention_decode", "vq_attention_workspace_bytes",
-                     "vq_encode_grouped_smooth"):
+                     "vq_encode_grouped_smooth", "vq_scalar_quantize", "vq_scalar_dequantize",
+                     "vq_hadamard_rotate", "vq_hadamard_quantize"):
         assert required in names
 
 
@@ -165,6 +166,32 @@ def _smooth(lib):
 ])
 def test_smooth_argument_errors(lib, args, status):
     assert _smooth(lib)(*args, None) == status
+
+
+def test_sibling_argument_errors(lib):
+    i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    sq = lib.vq_scalar_quantize
+    sq.restype, sq.argtypes = i32, [vp, i32, i64, vp, i32, vp, vp, ctypes.c_size_t, vp]
+    assert sq(P, 0, -1, P, 16, P, None, 0, None) == 1       # negative n
+    assert sq(P, 5, 10, P, 16, P, None, 0, None) == 1       # unknown dtype
+    assert sq(P, 0, 10, P, 0, P, None, 0, None) == 2        # no centroids
+    assert sq(P, 0, 10, P, 257, P, None, 0, None) == 2      # more than 8-bit codes
+    assert sq(P + 1, 0, 10, P, 16, P, None, 0, None) == 1   # x not aligned to its element
+    assert sq(None, 0, 0, None, 16, None, None, 0, None) == 0  # nothing to do
+    hr = lib.vq_hadamard_rotate
+    hr.restype, hr.argtypes = i32, [vp, i32, vp, i64, i32, vp, vp]
+    assert hr(P, 0, P, 10, 96, P, None) == 1                # not a power of two
+    assert hr(P, 0, P, 10, 0, P, None) == 1
+    assert hr(P, 0, P, 10, 2048, P, None) == 2              # above 1024
+    assert hr(P, 0, P, -1, 128, P, None) == 1
+    assert hr(None, 0, None, 0, 128, None, None) == 0
+    hq = lib.vq_hadamard_quantize
+    hq.restype, hq.argtypes = i32, [vp, i32, vp, i64, i32, vp, i32, vp, vp]
+    assert hq(P, 0, P, 10, 128, P, 300, P, None) == 2       # more than 8-bit codes
+    assert hq(P, 0, P, 10, 128, P, 16, P + 2, None) == 1    # 4-byte index stores
+    ws = lib.vq_scalar_quantize_workspace_bytes
+    ws.restype, ws.argtypes = ctypes.c_size_t, [i32]
+    assert (ws(0), ws(1), ws(2)) == (65536, 65536, 0)
 
 
 def test_attention_workspace_bytes(lib):

@@ -1,0 +1,121 @@
+"""GPU parity of the sibling encoders: scalar (sub_dim = 1) quantize and
+dequantize, and the randomised Hadamard rotation with its fused quantize.
+Indices and rotated values are compared bit for bit with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vq():
+    from product_vq_kv_gb300.build import build
+
+    build()
+    import product_vq_kv_gb300 as m
+
+    m.load_library()
+    return m
+
+
+def to_dev(x, dtype):
+    """(host array the oracle takes, its bf16 flag, device tensor)."""
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+        return t.view(torch.int16).numpy().view(np.uint16), True, t.cuda()
+    a = np.ascontiguousarray(x, dtype=np.float16 if dtype == "f16" else np.float32)
+    return a, False, torch.from_numpy(a).cuda()
+
+
+def codebook(rng, n_c):
+    c = rng.standard_normal(n_c).astype(np.float32)
+    if n_c > 2:
+        c[n_c // 2] = c[1]  # a duplicate: ties go to the lower index
+    return c
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("n_c", [2, 16, 256])
+def test_scalar_every_16_bit_pattern(vq, oracle_mod, dtype, n_c):
+    """All 65,536 bit patterns (NaN, inf, subnormals included), table and scan."""
+    rng = np.random.default_rng(n_c)
+    c = codebook(rng, n_c)
+    bits = np.arange(65536, dtype=np.uint16)
+    if dtype == "f16":
+        host, bf, dev = bits.view(np.float16), False, torch.from_numpy(bits.view(np.int16)).cuda().view(torch.float16)
+    else:
+        host, bf, dev = bits, True, torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    want = oracle_mod.scalar_quantize(host, c, bf16=bf)
+    cd = torch.from_numpy(c).cuda()
+    for use_table in (True, False):
+        got = vq.vq_scalar_quantize(dev, cd, use_table=use_table).cpu().numpy()
+        assert np.array_equal(got.astype(np.uint32), want), use_table
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("n", [0, 1, 7, 8, 4099, 1 << 20])
+def test_scalar_sizes_and_alignment(vq, oracle_mod, dtype, n):
+    rng = np.random.default_rng(n + 3)
+    c = codebook(rng, 16)
+    x = 2.0 * rng.standard_normal(n + 3)
+    x[: min(3, n)] = [np.inf, -np.nan, 1e-7][: min(3, n)]
+    host, bf, dev = to_dev(x, dtype)
+    cd = torch.from_numpy(c).cuda()
+    for off in (0, 1, 3):  # unaligned starts take the element-wise path
+        want = oracle_mod.scalar_quantize(host[off:off + n], c, bf16=bf)
+        got = vq.vq_scalar_quantize(dev[off:off + n], cd).cpu().numpy()
+        assert np.array_equal(got.astype(np.uint32), want)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_scalar_dequantize(vq, dtype):
+    rng = np.random.default_rng(7)
+    c = (3 * rng.standard_normal(16)).astype(np.float32)
+    idx = rng.integers(0, 20, 10001).astype(np.uint8)  # 16..19 are out of range
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+    got = vq.vq_scalar_dequantize(torch.from_numpy(idx).cuda(), torch.from_numpy(c).cuda(),
+                                  dtype=tdt).cpu()
+    padded = np.concatenate([c, np.zeros(256 - 16, dtype=np.float32)])
+    want = torch.from_numpy(padded[idx]).to(tdt)  # round to nearest
+    assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("dim", [1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024])
+def test_hadamard_rotate_bit_exact(vq, oracle_mod, dtype, dim):
+    rng = np.random.default_rng(dim)
+    rows = 1001 if dim <= 256 else 97
+    host, bf, dev = to_dev(rng.standard_normal((rows, dim)), dtype)
+    diag = rng.choice([-1.0, 1.0], dim).astype(np.float32)
+    diag[0] = 0.75  # any fp32 factor, not only signs
+    want = oracle_mod.hadamard_rotate(host, diag, bf16=bf)
+    got = vq.vq_hadamard_rotate(dev, torch.from_numpy(diag).cuda()).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("dim,n_c", [(4, 2), (32, 16), (128, 16), (128, 256), (256, 4), (1024, 16)])
+def test_hadamard_quantize_bit_exact(vq, oracle_mod, dtype, dim, n_c):
+    rng = np.random.default_rng(dim * 1000 + n_c)
+    rows = 777 if dim <= 256 else 65
+    host, bf, dev = to_dev(rng.standard_normal((rows, dim)), dtype)
+    diag = rng.choice([-1.0, 1.0], dim).astype(np.float32)
+    c = np.sort(codebook(rng, n_c))
+    want = oracle_mod.hadamard_quantize(host, diag, c, bf16=bf)
+    got = vq.vq_hadamard_quantize(dev, torch.from_numpy(diag).cuda(),
+                                  torch.from_numpy(c).cuda()).cpu().numpy()
+    assert np.array_equal(got.astype(np.uint32), want)
+
+
+def test_full_turboquant_keys(vq, oracle_mod):
+    """The benchmarked cache (8 heads x 32768 tokens x 128, 4-bit codebook):
+    every index of the scalar and of the fused Hadamard quantize."""
+    x, c, diag = workloads.generate_scalar("turboquant_keys")
+    xd, cd, dd = (torch.from_numpy(a).cuda() for a in (x, c, diag))
+    got = vq.vq_scalar_quantize(xd, cd).cpu().numpy()
+    assert np.array_equal(got.astype(np.uint32), oracle_mod.scalar_quantize(x, c))
+    got = vq.vq_hadamard_quantize(xd, dd, cd).cpu().numpy()
+    assert np.array_equal(got.astype(np.uint32), oracle_mod.hadamard_quantize(x, diag, c))

@@ -136,6 +136,67 @@ def generate(name: str, tokens: int | None = None):
     return x, cb
 
 
+@dataclasses.dataclass(frozen=True)
+class ScalarWorkload:
+    """Keys quantized element by element (sub_dim = 1) against one Lloyd-Max
+    codebook, optionally after a randomised Hadamard rotation of each
+    head_dim row."""
+
+    name: str
+    description: str
+    batch: int
+    heads: int
+    tokens: int
+    head_dim: int
+    bits: int
+
+    @property
+    def n(self) -> int:
+        return self.batch * self.heads * self.tokens * self.head_dim
+
+    @property
+    def rows(self) -> int:
+        return self.batch * self.heads * self.tokens
+
+
+SCALAR_WORKLOADS = {
+    # one layer's keys of a Llama-3.1-8B-shape cache (8 KV heads, head_dim 128)
+    # at 32768 tokens, 4-bit codebook
+    "turboquant_keys": ScalarWorkload("turboquant_keys", "Llama-3.1-8B-shape key cache, one layer, "
+                                      "8 KV heads x 32768 tokens x 128, 4-bit Lloyd-Max codebook",
+                                      batch=1, heads=8, tokens=32768, head_dim=128, bits=4),
+}
+
+SCALAR_SEEDS = {"turboquant_keys": (19, 20, 21)}  # keys, codebook sample, signs
+
+
+def lloyd_max_gaussian(bits: int, seed: int, samples: int = 1 << 18, iters: int = 60):
+    """Sorted float32 Lloyd-Max centroids of N(0, 1) for 2^bits levels, fitted
+    by Lloyd iterations on a seeded sample (an input of the quantizer, not part
+    of its arithmetic)."""
+    z = np.sort(_normal(seed, (samples,)).astype(np.float64))
+    k = 1 << bits
+    c = np.quantile(z, (np.arange(k) + 0.5) / k)
+    for _ in range(iters):
+        edges = np.concatenate([[-np.inf], (c[:-1] + c[1:]) / 2, [np.inf]])
+        idx = np.searchsorted(edges, z) - 1
+        c = np.array([z[idx == j].mean() for j in range(k)])
+    return c.astype(np.float32)
+
+
+def generate_scalar(name: str, tokens: int | None = None):
+    """``(x, centroids, diag)``: fp16 keys ``[B, H, S, D]`` ~ N(0, 1), the
+    Lloyd-Max codebook, and random +-1 signs of the Hadamard rotation."""
+    w = SCALAR_WORKLOADS[name]
+    tokens = w.tokens if tokens is None else int(tokens)
+    s = SCALAR_SEEDS[name]
+    x = _normal(s[0], (w.batch, w.heads, tokens, w.head_dim)).astype(np.float16)
+    c = lloyd_max_gaussian(w.bits, s[1])
+    signs = np.random.Generator(np.random.PCG64(s[2])).integers(0, 2, w.head_dim)
+    diag = np.where(signs == 1, 1.0, -1.0).astype(np.float32)
+    return x, c, diag
+
+
 SMOOTH_SEED = 18
 
 
