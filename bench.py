@@ -42,8 +42,8 @@ PAGES_FALCON_SUBVEC_PER_S = 1_048_576 / 7.98e-3
 # ncu capture, keyed by the exact launch description it was taken on; a
 # kernel that has changed since reports null (see profiles/).
 MEASURED_TRAFFIC = {
-    "kernel=encode_filter dtype=f16 sub_dim=4 rows_per_thread=8 threads=128 "
-    "centroid_group=16 grid=1024 smem=18712": 8_446_720,
+    "kernel=encode_tc dtype=f16 sub_dim=4 tmem_cols=64 tiles_per_block=7 centroid_group=16 "
+    "grid=1171 smem=26965": 8_422_912,
 }
 L2_FLUSH_BYTES = 256 << 20
 FP32_LANES_PER_SM = 128
