@@ -279,7 +279,8 @@ vq_status vq_scalar_dequantize(const uint8_t *idx, int64_t n, const float *centr
  * stride becomes (v[e] + v[e+stride], v[e] - v[e+stride]); y = v * s with s
  * the fp32 value of 1/sqrt(dim) (correctly rounded).  Every step is one
  * rounded fp32 operation in exactly this order.
- *   x     [n_rows][dim]  device, dtype        diag  [dim]  device, fp32
+ *   x     [n_rows][dim]  device, dtype, aligned to min(dim/32 elements, 16
+ *         bytes) (one element for dim <= 32)   diag  [dim]  device, fp32
  *   y     [n_rows][dim]  device, fp32, written
  * vq_hadamard_quantize -- the same rotation fused with vq_scalar_quantize of
  * every rotated value; out [n_rows][dim] uint8 (4-byte aligned when dim >=

@@ -44,18 +44,37 @@ vq_status launch_scan(const void *x, int64_t n, const float *c, int32_t n_c, uin
     return launched();
 }
 
-template <typename T, int E, bool QUANT>
-vq_status launch_hadamard_e(const void *x, const float *diag, int64_t n_rows, int32_t dim,
-                            float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,
-                            cudaStream_t st)
+template <typename T, int E, bool QUANT, int NC>
+vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, int32_t dim,
+                             float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,
+                             cudaStream_t st)
 {
     const int lpr = dim < 32 ? dim : 32;
     const int64_t rows_per_block = (int64_t)(kThreads / 32) * (32 / lpr);
     const int64_t blocks = (n_rows + rows_per_block - 1) / rows_per_block;
     if (blocks > 0x7fffffffLL) return VQ_ERR_UNSUPPORTED;
-    vqs::hadamard_rows<T, E, QUANT><<<(unsigned)blocks, kThreads, QUANT ? (size_t)n_c * 4 : 0, st>>>(
+    const size_t smem = QUANT && NC == 0 ? (size_t)n_c * 4 : 0;
+    vqs::hadamard_rows<T, E, QUANT, NC><<<(unsigned)blocks, kThreads, smem, st>>>(
         static_cast<const T *>(x), diag, n_rows, lpr, scale, c, n_c, y, idx);
     return launched();
+}
+
+// Codebooks of 2, 4, 8 or 16 entries (the pages' 1- to 4-bit Lloyd-Max
+// codebooks) are held in registers; others are read from shared memory.
+template <typename T, int E, bool QUANT>
+vq_status launch_hadamard_e(const void *x, const float *diag, int64_t n_rows, int32_t dim,
+                            float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,
+                            cudaStream_t st)
+{
+    if constexpr (QUANT) {
+        switch (n_c) {
+        case 2: return launch_hadamard_nc<T, E, true, 2>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
+        case 4: return launch_hadamard_nc<T, E, true, 4>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
+        case 8: return launch_hadamard_nc<T, E, true, 8>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
+        case 16: return launch_hadamard_nc<T, E, true, 16>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
+        }
+    }
+    return launch_hadamard_nc<T, E, QUANT, 0>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
 }
 
 template <typename T, bool QUANT>
@@ -88,6 +107,10 @@ vq_status hadamard(const void *x, vq_dtype dtype, const float *diag, int64_t n_r
         (!QUANT && (uintptr_t)y % 4) || (QUANT && dim >= 128 && (uintptr_t)idx % 4))
         return VQ_ERR_INVALID_ARG;
     if (n_rows > INT64_MAX / dim) return VQ_ERR_INVALID_ARG;
+    {  // the rotation kernel reads each lane's run of dim/32 elements as vectors
+        const size_t run = (size_t)(dim >= 32 ? dim / 32 : 1) * elem_size(dtype);
+        if ((uintptr_t)x % (run < 16 ? run : 16)) return VQ_ERR_INVALID_ARG;
+    }
     // fp32 value of 1/sqrt(dim), correctly rounded (2^(-k/2) for dim = 2^k)
     const float scale = (float)(1.0 / std::sqrt((double)dim));
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

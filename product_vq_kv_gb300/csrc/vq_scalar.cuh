@@ -67,6 +67,21 @@ __global__ void scalar_table(const float *__restrict__ centroids, int32_t n_c, b
     if (p < 65536u) table[p] = (uint8_t)nearest(widen16((uint16_t)p, bf16), sc_tab, n_c);
 }
 
+// Eight 16-bit patterns -> their eight table bytes.
+__device__ __forceinline__ uint2 lookup8(const uint8_t *tab, uint4 v)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        lo |= (uint32_t)tab[w[k] & 0xffffu] << (16 * k);
+        lo |= (uint32_t)tab[w[k] >> 16] << (16 * k + 8);
+        hi |= (uint32_t)tab[w[k + 2] & 0xffffu] << (16 * k);
+        hi |= (uint32_t)tab[w[k + 2] >> 16] << (16 * k + 8);
+    }
+    return make_uint2(lo, hi);
+}
+
 // out[e] = table[x[e]].  Launch: any grid of 256-thread blocks, dynamic
 // shared memory 65536 bytes; grid-stride over 8-element units when `vec`
 // (x 16-byte and out 8-byte aligned), the remaining elements one by one.
@@ -82,19 +97,20 @@ __global__ void __launch_bounds__(256)
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t units = vec ? n / 8 : 0;
-    for (int64_t u = tid; u < units; u += nthreads) {
-        const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(x) + u);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t lo = 0, hi = 0;
+    // four 16-byte loads in flight per thread before any lookup
+    constexpr int U = 4;
+    int64_t u = tid;
+    for (; u + (U - 1) * nthreads < units; u += U * nthreads) {
+        uint4 v[U];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            lo |= (uint32_t)sl_tab[w[k] & 0xffffu] << (16 * k);
-            lo |= (uint32_t)sl_tab[w[k] >> 16] << (16 * k + 8);
-            hi |= (uint32_t)sl_tab[w[k + 2] & 0xffffu] << (16 * k);
-            hi |= (uint32_t)sl_tab[w[k + 2] >> 16] << (16 * k + 8);
-        }
-        __stcs(reinterpret_cast<uint2 *>(out) + u, make_uint2(lo, hi));
+        for (int k = 0; k < U; ++k) v[k] = __ldcs(reinterpret_cast<const uint4 *>(x) + u + k * nthreads);
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+            __stcs(reinterpret_cast<uint2 *>(out) + u + k * nthreads, lookup8(sl_tab, v[k]));
     }
+    for (; u < units; u += nthreads)
+        __stcs(reinterpret_cast<uint2 *>(out) + u,
+               lookup8(sl_tab, __ldcs(reinterpret_cast<const uint4 *>(x) + u)));
     for (int64_t e = units * 8 + tid; e < n; e += nthreads) out[e] = sl_tab[x[e]];
 }
 
@@ -113,20 +129,64 @@ __global__ void __launch_bounds__(256)
         out[e] = (uint8_t)nearest(widen_elem(x[e]), ss_cb, n_c);
 }
 
+// E consecutive elements of one row as fp32 (vector loads where E and the
+// element size allow; rows are E-element aligned).
+template <typename T, int E>
+__device__ __forceinline__ void load_run(const T *p, float (&v)[E])
+{
+    constexpr int kBytes = E * (int)sizeof(T);
+    if constexpr (kBytes >= 16 && kBytes % 16 == 0) {
+        constexpr int kPer = 16 / (int)sizeof(T);
+#pragma unroll
+        for (int k = 0; k < E / kPer; ++k) {
+            const uint4 q = __ldcs(reinterpret_cast<const uint4 *>(p) + k);
+            const T *t = reinterpret_cast<const T *>(&q);
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) v[k * kPer + i] = widen_elem(t[i]);
+        }
+    } else if constexpr (kBytes == 8) {
+        const uint2 q = __ldcs(reinterpret_cast<const uint2 *>(p));
+        const T *t = reinterpret_cast<const T *>(&q);
+#pragma unroll
+        for (int i = 0; i < E; ++i) v[i] = widen_elem(t[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < E; ++i) v[i] = widen_elem(p[i]);
+    }
+}
+
+// The nearest-centroid rule with NC centroids in registers.
+template <int NC>
+__device__ __forceinline__ uint32_t nearest_reg(float val, const float (&c)[NC])
+{
+    float best_dist = __int_as_float(0x7f800000);
+    uint32_t best = 0;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+        const float d = __fsub_rn(val, c[j]);
+        const float dist = __fmul_rn(d, d);
+        const bool p = dist < best_dist;
+        best_dist = p ? dist : best_dist;
+        best = p ? (uint32_t)j : best;
+    }
+    return best;
+}
+
 // Randomised Hadamard rotation of rows of D = LPR * E elements, optionally
 // fused with the scalar quantize.  LPR = min(D, 32) lanes per row, 32 / LPR
 // rows per warp; lane l of a row holds elements l*E .. l*E + E - 1.
 // Launch: blockDim.x = 256, grid = ceil(n_rows / (8 * 32 / LPR)); dynamic
-// shared memory n_c * 4 bytes (QUANT) or 0.  x rows contiguous; y / idx
-// [n_rows][D].
-template <typename T, int E, bool QUANT>
+// shared memory n_c * 4 bytes when QUANT with NC == 0, else 0.  With NC > 0
+// the codebook has exactly NC entries and lives in registers.  x rows
+// contiguous and E-element aligned; y / idx [n_rows][D].
+template <typename T, int E, bool QUANT, int NC>
 __global__ void __launch_bounds__(256)
     hadamard_rows(const T *__restrict__ x, const float *__restrict__ diag, int64_t n_rows,
                   int32_t lanes_per_row, float scale, const float *__restrict__ centroids,
                   int32_t n_c, float *__restrict__ y, uint8_t *__restrict__ idx)
 {
     extern __shared__ float hq_cb[];
-    if constexpr (QUANT) {
+    if constexpr (QUANT && NC == 0) {
         for (int j = threadIdx.x; j < n_c; j += blockDim.x) hq_cb[j] = centroids[j];
         __syncthreads();
     }
@@ -140,11 +200,14 @@ __global__ void __launch_bounds__(256)
     const bool live = row < n_rows;
     const int d = lpr * E;
     float v[E];
+    if (live) {
+        load_run<T, E>(x + (size_t)row * d + (size_t)l * E, v);
+    } else {
 #pragma unroll
-    for (int j = 0; j < E; ++j) {
-        const int e = l * E + j;
-        v[j] = live ? __fmul_rn(widen_elem(x[(size_t)row * d + e]), __ldg(diag + e)) : 0.f;
+        for (int j = 0; j < E; ++j) v[j] = 0.f;
     }
+#pragma unroll
+    for (int j = 0; j < E; ++j) v[j] = __fmul_rn(v[j], __ldg(diag + l * E + j));
     // strides below E: pairs inside the lane's registers
 #pragma unroll
     for (int s = 1; s < E; s <<= 1) {
@@ -170,18 +233,26 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int j = 0; j < E; ++j) v[j] = __fmul_rn(v[j], scale);
     if constexpr (QUANT) {
+        uint32_t code[E];
+        if constexpr (NC > 0) {
+            float c[NC];
+#pragma unroll
+            for (int k = 0; k < NC; ++k) c[k] = __ldg(centroids + k);
+#pragma unroll
+            for (int j = 0; j < E; ++j) code[j] = nearest_reg<NC>(v[j], c);
+        } else {
+#pragma unroll
+            for (int j = 0; j < E; ++j) code[j] = nearest(v[j], hq_cb, n_c);
+        }
         uint8_t *o = idx + (size_t)row * d + (size_t)l * E;
         if constexpr (E % 4 == 0) {
 #pragma unroll
-            for (int j = 0; j < E; j += 4) {
-                uint32_t w = 0;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) w |= nearest(v[j + k], hq_cb, n_c) << (8 * k);
-                *reinterpret_cast<uint32_t *>(o + j) = w;
-            }
+            for (int j = 0; j < E; j += 4)
+                *reinterpret_cast<uint32_t *>(o + j) =
+                    code[j] | code[j + 1] << 8 | code[j + 2] << 16 | code[j + 3] << 24;
         } else {
 #pragma unroll
-            for (int j = 0; j < E; ++j) o[j] = (uint8_t)nearest(v[j], hq_cb, n_c);
+            for (int j = 0; j < E; ++j) o[j] = (uint8_t)code[j];
         }
     } else {
         float *o = y + (size_t)row * d + (size_t)l * E;
