@@ -56,18 +56,18 @@ vq_status attn_validate(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_
 // tables and the final merge).
 vq_status attn_plan(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_t tokens,
                     int32_t head_dim, int32_t sub_dim, int32_t n_centroids, int64_t window,
-                    float scale, AttnPlan *p)
+                    float scale, int elem, AttnPlan *p)
 {
     const int qpk = heads_q / heads_kv;
     const int ns = head_dim / sub_dim;
     int gpb = 0;
     for (int g = 8; g >= 1; g /= 2)
-        if (qpk % g == 0 && vqk::attn_smem(g, ns, sub_dim).total <= kAttnMaxSmem) {
+        if (qpk % g == 0 && vqk::attn_smem(g, ns, sub_dim, elem).total <= kAttnMaxSmem) {
             gpb = g;
             break;
         }
     if (gpb == 0) return VQ_ERR_UNSUPPORTED;
-    const size_t smem = vqk::attn_smem(gpb, ns, sub_dim).total;
+    const size_t smem = vqk::attn_smem(gpb, ns, sub_dim, elem).total;
     const int chunk = vqk::attn_chunk(ns);
     const int64_t first = window > 0 && window < tokens ? tokens - window : 0;
     const int64_t chunks = (tokens - first + chunk - 1) / chunk;
@@ -189,11 +189,16 @@ size_t vq_attention_workspace_bytes(int64_t batch, int32_t heads_q, int32_t head
     if (attn_validate(batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids, window) !=
         VQ_OK)
         return 0;
-    AttnPlan p;
-    if (attn_plan(batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids, window, 0.f,
-                  &p) != VQ_OK)
-        return 0;
-    return p.part_bytes_per_split * (size_t)p.sh.splits;
+    size_t most = 0;
+    for (int elem = 2; elem <= 4; elem += 2) {  // the plan of 16-bit and of fp32 inputs
+        AttnPlan p;
+        if (attn_plan(batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids, window,
+                      0.f, elem, &p) != VQ_OK)
+            return 0;
+        const size_t bytes = p.part_bytes_per_split * (size_t)p.sh.splits;
+        if (bytes > most) most = bytes;
+    }
+    return most;
 }
 
 vq_status vq_attention_decode(const void *q, const uint8_t *k_codes, const void *k_codebooks,
@@ -218,7 +223,7 @@ vq_status vq_attention_decode(const void *q, const uint8_t *k_codes, const void 
         return VQ_ERR_INVALID_ARG;
     AttnPlan p;
     if ((s = attn_plan(batch, heads_q, heads_kv, tokens, head_dim, sub_dim, n_centroids, window,
-                       scale, &p)) != VQ_OK)
+                       scale, (int)es, &p)) != VQ_OK)
         return s;
     // fewer token slices if the workspace holds fewer partials
     const int64_t fit = (int64_t)(workspace_bytes / p.part_bytes_per_split);

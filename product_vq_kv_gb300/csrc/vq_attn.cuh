@@ -24,11 +24,15 @@
 //     register accumulators are rescaled), and the weights 2^(score - max)
 //     and the value code rows go to shared memory;
 //   phase B, one thread per (4-column slice of the head, token stream): the
-//     value rows are gathered from the fp32 codebook in shared memory and
-//     accumulated with the weights of every head in registers (no atomics).
-// Shared-memory random gathers bound this kernel (about 8 random 4-byte or 3
-// random 16-byte lane accesses per clock per SM, with bank conflicts), not
-// HBM.  Each block writes a partial (max, sum, out[D]) per query head to the
+//     value rows are gathered from the value codebook in shared memory (kept
+//     in the input type, widened in registers) and accumulated with the
+//     weights of every head in registers (no atomics).  The codebook is held
+//     in bank-disjoint copies, sub-space s reading copy s % ncopies, where a
+//     copy owns one (row bytes)-wide slot of every 128-byte line: the lanes
+//     that share a shared-memory wavefront (consecutive sub-spaces of one
+//     token) never hit the same banks, whatever the codes.
+// Shared-memory gathers bound this kernel (random table lookups in phase A,
+// about 3 random 16-byte lane accesses per clock per SM), not HBM.  Each block writes a partial (max, sum, out[D]) per query head to the
 // caller's workspace; attn_combine merges the partials (flash-decoding).
 // A code >= n_centroids reads a zero table entry and a zero value row (the
 // decode of such a code is a zero row).
@@ -40,7 +44,7 @@
 
 namespace vqk {
 
-constexpr int kLutStride = 260;  // table row stride (>= 256 codes), in vectors
+constexpr int kLutStride = 256;  // table row stride (one entry per 8-bit code), in vectors
 constexpr int kAttnThreads = 256;
 constexpr int kAttnVw = 4;       // value columns per phase-B thread
 
@@ -62,31 +66,59 @@ __device__ __forceinline__ void from_f32(__half &d, float v) { d = __float2half_
 __device__ __forceinline__ void from_f32(__nv_bfloat16 &d, float v) { d = __float2bfloat16_rn(v); }
 
 // Tokens per phase-A thread and per chunk, by sub-space count.
-__host__ __device__ constexpr int attn_tok_per_thread(int ns) { return ns <= 16 ? 4 : ns == 32 ? 2 : 1; }
+__host__ __device__ constexpr int attn_tok_per_thread(int ns) { return ns <= 16 ? 2 : 1; }
 __host__ __device__ constexpr int attn_chunk(int ns) { return kAttnThreads * attn_tok_per_thread(ns); }
 
-// Shared-memory layout (floats unless noted), in order:
-//   lut  [GPB / GP][NS][kLutStride][GP]   GP = min(GPB, 4) heads per vector
-//   vcb  [256][SUB]                       value codebook, fp32, zero past n_c
-//   pw   [CHUNK][GPB]                     weights of the chunk
-//   red  [3][GPB][32]                     block maxima (two buffers), sums
-//   vtile[CHUNK][NS] bytes                value codes of the chunk
-// After the last chunk, the lut region holds the per-stream accumulators
-// [streams][GPB][D] (it is at least that large).
+// Value-codebook copies: rows of rb = sub * elem bytes; ncopies copies, each
+// owning one rb-byte slot of every 128-byte line (one copy when rb >= 128).
+__host__ __device__ inline int attn_vcopies(int sub, int elem)
+{
+    const int rb = sub * elem;
+    return rb >= 128 ? 1 : 128 / rb;
+}
+
+// Shared-memory layout, in order (bytes):
+//   lut  [GPB / GP][NS][kLutStride][GP] fp32   GP = min(GPB, 4) heads per vector;
+//        after the last chunk it holds the per-stream accumulators
+//        [streams][GPB][D] fp32 (the region is sized for both)
+//   vcb  [256][ncopies] rows of `sub` elements of T, zero past n_c
+//   pw   [CHUNK][GPB] fp32                     weights of the chunk
+//   red  [3][GPB][NW] fp32                     block maxima (two buffers), sums
+//   vtile[CHUNK][NS] bytes                     value codes of the chunk
 struct AttnSmem {
     size_t lut, vcb, pw, red, vtile, total;
 };
-__host__ __device__ inline AttnSmem attn_smem(int gpb, int ns, int sub)
+__host__ __device__ inline AttnSmem attn_smem(int gpb, int ns, int sub, int elem)
 {
     AttnSmem m;
     const int chunk = attn_chunk(ns);
+    const size_t lut_bytes = (size_t)gpb * ns * kLutStride * 4;
+    const size_t acc_bytes = (size_t)kAttnThreads * kAttnVw * gpb * 4;  // streams * GPB * D floats
     m.lut = 0;
-    m.vcb = m.lut + (size_t)gpb * ns * kLutStride * 4;
-    m.pw = m.vcb + (size_t)256 * sub * 4;
+    m.vcb = m.lut + (lut_bytes > acc_bytes ? lut_bytes : acc_bytes);
+    m.pw = m.vcb + (size_t)256 * attn_vcopies(sub, elem) * sub * elem;
+    m.pw = (m.pw + 15) / 16 * 16;
     m.red = m.pw + (size_t)chunk * gpb * 4;
-    m.vtile = m.red + (size_t)3 * gpb * 32 * 4;
+    m.vtile = m.red + (size_t)3 * gpb * (kAttnThreads / 32) * 4;
+    m.vtile = (m.vtile + 15) / 16 * 16;
     m.total = m.vtile + (size_t)chunk * ns;
     return m;
+}
+
+// Four consecutive elements of a value row in shared memory, widened.
+__device__ __forceinline__ float4 load4_f32(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 load4_f32(const __half *p)
+{
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float4 load4_f32(const __nv_bfloat16 *p)
+{
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
 }
 
 // Code row of one token as 32-bit words (NS bytes, NS % 4 == 0, row address
@@ -162,7 +194,7 @@ __device__ __forceinline__ void load_vec(const float *p, float (&v)[GP])
 }
 
 // Launch: grid.x = batch * heads_kv * (heads_q / heads_kv / GPB) * splits,
-// block = kAttnThreads, dynamic shared memory attn_smem(GPB, NS, SUB).total.
+// block = kAttnThreads, dynamic shared memory attn_smem(GPB, NS, SUB, sizeof(T)).total.
 // NS = head_dim / sub_dim in {4, 8, 16, 32, 64}; sub_dim % 4 == 0; code rows
 // are NS bytes apart and the code arrays aligned to min(NS, 16) bytes.
 // Partial of (b, hq, split) at part[((b * heads_q + hq) * splits + split) *
@@ -185,9 +217,10 @@ __global__ void __launch_bounds__(kAttnThreads)
     const int sub = sh.sub_dim;
     const int d = sh.head_dim;
     const int nc = sh.n_centroids;
-    const AttnSmem lay = attn_smem(GPB, NS, sub);
+    const AttnSmem lay = attn_smem(GPB, NS, sub, (int)sizeof(T));
+    const int ncopies = attn_vcopies(sub, (int)sizeof(T));
     float *lut = reinterpret_cast<float *>(smem_raw + lay.lut);
-    float *vcs = reinterpret_cast<float *>(smem_raw + lay.vcb);
+    T *vcs = reinterpret_cast<T *>(smem_raw + lay.vcb);
     float *pw = reinterpret_cast<float *>(smem_raw + lay.pw);
     float *red = reinterpret_cast<float *>(smem_raw + lay.red);
     uint8_t *vtile = smem_raw + lay.vtile;
@@ -209,25 +242,39 @@ __global__ void __launch_bounds__(kAttnThreads)
     const uint8_t *kb = kcodes + cache_off;
     const uint8_t *vb = vcodes + cache_off;
 
-    // ---- tables (kappa folded in, zero past n_centroids), value codebook
-    {
-        const int entries = GPB * NS * kLutStride;
-        for (int e = threadIdx.x; e < entries; e += THREADS) {
-            const int gi = e % GP;                    // head within the pack
-            const int c = (e / GP) % kLutStride;
-            const int s = (e / (GP * kLutStride)) % NS;
-            const int pk = e / (GP * kLutStride * NS);
-            const int g = pk * GP + gi;
-            float acc = 0.f;
-            if (c < nc) {
-                const T *qv = q + ((size_t)b * sh.heads_q + hq0 + g) * d + (size_t)s * sub;
-                const T *cv = kc + (size_t)c * sub;
-                for (int i = 0; i < sub; ++i) acc = fmaf(to_f32(qv[i]), to_f32(cv[i]), acc);
+    // ---- tables (kappa folded in, zero past n_centroids): thread c owns
+    // centroid c and writes the GP heads of a pack as one vector; the value
+    // codebook goes to its bank-disjoint copies
+    for (int c = threadIdx.x; c < kLutStride; c += THREADS) {
+        const T *cv = kc + (size_t)c * sub;
+#pragma unroll
+        for (int pk = 0; pk < NPACK; ++pk) {
+            for (int s = 0; s < NS; ++s) {
+                float acc[GP];
+#pragma unroll
+                for (int gi = 0; gi < GP; ++gi) acc[gi] = 0.f;
+                if (c < nc) {
+                    for (int i = 0; i < sub; ++i) {
+                        const float kv = to_f32(cv[i]);
+#pragma unroll
+                        for (int gi = 0; gi < GP; ++gi) {
+                            const T *qv = q + ((size_t)b * sh.heads_q + hq0 + pk * GP + gi) * d;
+                            acc[gi] = fmaf(to_f32(qv[(size_t)s * sub + i]), kv, acc[gi]);
+                        }
+                    }
+                }
+                float *dst = lut + ((size_t)(pk * NS + s) * kLutStride + c) * GP;
+#pragma unroll
+                for (int gi = 0; gi < GP; ++gi) dst[gi] = acc[gi] * sh.kappa;
             }
-            lut[e] = acc * sh.kappa;
         }
-        for (int e = threadIdx.x; e < 256 * sub; e += THREADS)
-            vcs[e] = e < nc * sub ? to_f32(vc[e]) : 0.f;
+    }
+    for (int e = threadIdx.x; e < 256 * ncopies * sub; e += THREADS) {
+        const int i = e % sub;
+        const int k = (e / sub) % ncopies;
+        const int c = e / (sub * ncopies);
+        (void)k;
+        vcs[e] = c < nc ? vc[(size_t)c * sub + i] : T(0.f);
     }
     __syncthreads();
 
@@ -240,6 +287,9 @@ __global__ void __launch_bounds__(kAttnThreads)
     const bool b_active = stream < streams;
     const int bs = (col * VW) / sub;            // sub-space of the slice
     const int bi = (col * VW) - bs * sub;       // first element in the row
+    // this slice's columns in copy bs % ncopies of code 0; code c adds c rows
+    const T *vrow0 = vcs + (size_t)(bs % ncopies) * sub + bi;
+    const size_t vstride = (size_t)ncopies * sub;
     float2 acc[GPB][VW / 2];  // columns (0, 1) and (2, 3) of the slice
 #pragma unroll
     for (int g = 0; g < GPB; ++g)
@@ -304,20 +354,20 @@ __global__ void __launch_bounds__(kAttnThreads)
         // block maximum of the chunk (alternating buffers).  This barrier
         // also ends the previous chunk's phase B, so the weights and value
         // codes below may be overwritten after it.
-        float *rmax = red + (size_t)(ch & 1) * GPB * 32;
+        float *rmax = red + (size_t)(ch & 1) * GPB * NW;
 #pragma unroll
         for (int g = 0; g < GPB; ++g) {
             float m = cm[g];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0) rmax[g * 32 + warp] = m;
+            if (lane == 0) rmax[g * NW + warp] = m;
         }
         __syncthreads();
 #pragma unroll
         for (int g = 0; g < GPB; ++g) {
             float m = m_run[g];
 #pragma unroll
-            for (int k = 0; k < NW; ++k) m = fmaxf(m, rmax[g * 32 + k]);
+            for (int k = 0; k < NW; ++k) m = fmaxf(m, rmax[g * NW + k]);
             if (m > m_run[g] && m_run[g] > kNegInf) {  // rescale what is accumulated
                 const float f = exp2f(m_run[g] - m);
                 l_run[g] *= f;
@@ -363,8 +413,7 @@ __global__ void __launch_bounds__(kAttnThreads)
                 for (int u = 0; u < U; ++u) code[u] = vtile[(size_t)(tl + u * streams) * NS + bs];
                 float4 row[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    row[u] = *reinterpret_cast<const float4 *>(vcs + (size_t)code[u] * sub + bi);
+                for (int u = 0; u < U; ++u) row[u] = load4_f32(vrow0 + (size_t)code[u] * vstride);
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     float p[GPB];
@@ -384,7 +433,7 @@ __global__ void __launch_bounds__(kAttnThreads)
             }
             for (; tl < n_chunk; tl += streams) {
                 const int code = vtile[(size_t)tl * NS + bs];
-                const float4 row = *reinterpret_cast<const float4 *>(vcs + (size_t)code * sub + bi);
+                const float4 row = load4_f32(vrow0 + (size_t)code * vstride);
                 float p[GPB];
 #pragma unroll
                 for (int pk = 0; pk < NPACK; ++pk) {
@@ -404,13 +453,13 @@ __global__ void __launch_bounds__(kAttnThreads)
     __syncthreads();  // the tables are reused below
 
     // ---- block sums and the merge of the token streams
-    float *rsum = red + (size_t)2 * GPB * 32;
+    float *rsum = red + (size_t)2 * GPB * NW;
 #pragma unroll
     for (int g = 0; g < GPB; ++g) {
         float l = l_run[g];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        if (lane == 0) rsum[g * 32 + warp] = l;
+        if (lane == 0) rsum[g * NW + warp] = l;
     }
     float *accs = lut;  // [streams][GPB][D]; the tables are no longer read
     if (b_active) {
@@ -429,7 +478,7 @@ __global__ void __launch_bounds__(kAttnThreads)
         pp[2 + j] = o;
         if (j == 0) {
             float l = 0.f, m = m_run[0];
-            for (int k = 0; k < NW; ++k) l += rsum[g * 32 + k];
+            for (int k = 0; k < NW; ++k) l += rsum[g * NW + k];
 #pragma unroll
             for (int gg = 1; gg < GPB; ++gg)
                 if (gg == g) m = m_run[gg];  // static register index

@@ -34,12 +34,12 @@ import workloads
 pytestmark = pytest.mark.gpu
 
 U = 2.0 ** -24
-CHUNK = 1024  # tokens per chunk of the kernel for up to 16 sub-spaces
+CHUNK = 512  # tokens per chunk of the kernel for up to 16 sub-spaces
 
 
 def chunk_tokens(ns):
-    """Tokens per chunk: 256 threads x (4, 2 or 1) tokens."""
-    return 256 * (4 if ns <= 16 else 2 if ns == 32 else 1)
+    """Tokens per chunk: 256 threads x (2 or 1) tokens."""
+    return 256 * (2 if ns <= 16 else 1)
 
 
 @pytest.fixture(scope="module")
