@@ -44,6 +44,7 @@ vq_status launch_scan(const void *x, int64_t n, const float *c, int32_t n_c, uin
     return launched();
 }
 
+// A persistent grid: up to 8 blocks of 256 threads per SM stride over the rows.
 template <typename T, int E, bool QUANT, int NC>
 vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, int32_t dim,
                              float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,
@@ -51,16 +52,17 @@ vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, i
 {
     const int lpr = dim < 32 ? dim : 32;
     const int64_t rows_per_block = (int64_t)(kThreads / 32) * (32 / lpr);
-    const int64_t blocks = (n_rows + rows_per_block - 1) / rows_per_block;
-    if (blocks > 0x7fffffffLL) return VQ_ERR_UNSUPPORTED;
-    const size_t smem = QUANT && NC == 0 ? (size_t)n_c * 4 : 0;
+    int64_t blocks = (n_rows + rows_per_block - 1) / rows_per_block;
+    const int sms = vqh_device_sms() > 0 ? vqh_device_sms() : 152;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    const size_t smem = QUANT && NC == 0 ? vqs::hadamard_smem(n_c) : 0;
     vqs::hadamard_rows<T, E, QUANT, NC><<<(unsigned)blocks, kThreads, smem, st>>>(
         static_cast<const T *>(x), diag, n_rows, lpr, scale, c, n_c, y, idx);
     return launched();
 }
 
 // Codebooks of 2, 4, 8 or 16 entries (the pages' 1- to 4-bit Lloyd-Max
-// codebooks) are held in registers; others are read from shared memory.
+// codebooks) are scanned from registers; others through the sorted view.
 template <typename T, int E, bool QUANT>
 vq_status launch_hadamard_e(const void *x, const float *diag, int64_t n_rows, int32_t dim,
                             float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,

@@ -129,6 +129,87 @@ __global__ void __launch_bounds__(256)
         out[e] = (uint8_t)nearest(widen_elem(x[e]), ss_cb, n_c);
 }
 
+// ---- exact nearest centroid through the sorted codebook
+//
+// For a finite value y and finite centroids, let u_0 < ... < u_{m-1} be the
+// distinct centroid values and rep[k] the lowest index j with c_j == u_k.
+// D(u) = fl(fl(y - u)^2) is non-increasing in u up to y and non-decreasing
+// after it (fl is monotone), so the distances equal to the least one form a
+// run of consecutive u_k around y, and the rule's answer (lowest index among
+// the least distances; none below +inf gives 0) is the least rep[k] over that
+// run.  With L the last u_k <= y and R = L + 1, the least distance is
+// min(D(u_L), D(u_R)); when the neighbours outside the pair are strictly
+// larger, the run is {L}, {R} or {L, R}.  Anything else -- equal distances
+// beyond the pair, or a non-finite value -- takes the scan of the rule itself.
+struct SortedCb {
+    const float *u;    // [m] distinct values, ascending
+    const int *rep;    // [m] lowest original index of each value
+    int m;
+    int top;           // largest power of two <= m
+};
+
+// Build the sorted view in shared memory (all threads of the block; c[n_c]
+// already in shared memory).  Returns false if a centroid is not finite (the
+// scan is used for everything then).  u and rep need n_c entries, scratch
+// (ints) n_c entries.
+__device__ __forceinline__ bool build_sorted(const float *c, int n_c, float *u, int *rep,
+                                             int *first, int *m_out)
+{
+    bool finite = true;
+    for (int t = threadIdx.x; t < n_c; t += blockDim.x) {
+        const float v = c[t];
+        if (!(fabsf(v) <= 3.402823466e38f)) finite = false;
+        int f = 1;
+        for (int j = 0; j < t; ++j) f &= c[j] != v;  // the lowest index of its value
+        first[t] = f;
+    }
+    finite = __syncthreads_and(finite) != 0;
+    if (!finite) return false;
+    for (int t = threadIdx.x; t < n_c; t += blockDim.x) {
+        if (first[t]) {
+            const float v = c[t];
+            int rank = 0;
+            for (int j = 0; j < n_c; ++j) rank += first[j] && c[j] < v;
+            u[rank] = v;
+            rep[rank] = t;
+        }
+    }
+    if (threadIdx.x == 0) {
+        int m = 0;
+        for (int j = 0; j < n_c; ++j) m += first[j];
+        *m_out = m;
+    }
+    __syncthreads();
+    return true;
+}
+
+__device__ __forceinline__ float dist_to(float y, float u)
+{
+    const float d = __fsub_rn(y, u);
+    return __fmul_rn(d, d);
+}
+
+// Nearest index of y by the sorted view, or -1 if the scan must decide.
+__device__ __forceinline__ int nearest_sorted(float y, const SortedCb &cb)
+{
+    if (!(fabsf(y) <= 3.402823466e38f)) return 0;  // NaN or inf: every distance NaN or inf
+    int pos = 0;  // number of u_k <= y
+    for (int step = cb.top; step > 0; step >>= 1)
+        if (pos + step <= cb.m && cb.u[pos + step - 1] <= y) pos += step;
+    const int L = pos - 1, R = pos;
+    const float inf = __int_as_float(0x7f800000);
+    const float dl = L >= 0 ? dist_to(y, cb.u[L]) : inf;
+    const float dr = R < cb.m ? dist_to(y, cb.u[R]) : inf;
+    const float best = fminf(dl, dr);
+    if (best == inf) return 0;  // nothing below +inf
+    const float dll = L >= 1 ? dist_to(y, cb.u[L - 1]) : inf;
+    const float drr = R + 1 < cb.m ? dist_to(y, cb.u[R + 1]) : inf;
+    const bool left = dl == best, right = dr == best;
+    if ((left && !(dll > best)) || (right && !(drr > best))) return -1;  // a longer run
+    if (left && right) return min(cb.rep[L], cb.rep[R]);
+    return left ? cb.rep[L] : cb.rep[R];
+}
+
 // E consecutive elements of one row as fp32 (vector loads where E and the
 // element size allow; rows are E-element aligned).
 template <typename T, int E>
@@ -155,7 +236,8 @@ __device__ __forceinline__ void load_run(const T *p, float (&v)[E])
     }
 }
 
-// The nearest-centroid rule with NC centroids in registers.
+// The nearest-centroid rule with NC centroids in registers (the scan itself:
+// cheaper than the sorted search for up to 16 centroids).
 template <int NC>
 __device__ __forceinline__ uint32_t nearest_reg(float val, const float (&c)[NC])
 {
@@ -174,90 +256,121 @@ __device__ __forceinline__ uint32_t nearest_reg(float val, const float (&c)[NC])
 
 // Randomised Hadamard rotation of rows of D = LPR * E elements, optionally
 // fused with the scalar quantize.  LPR = min(D, 32) lanes per row, 32 / LPR
-// rows per warp; lane l of a row holds elements l*E .. l*E + E - 1.
-// Launch: blockDim.x = 256, grid = ceil(n_rows / (8 * 32 / LPR)); dynamic
-// shared memory n_c * 4 bytes when QUANT with NC == 0, else 0.  With NC > 0
-// the codebook has exactly NC entries and lives in registers.  x rows
-// contiguous and E-element aligned; y / idx [n_rows][D].
+// rows per warp; lane l of a row holds elements l*E .. l*E + E - 1.  Warps
+// stride over the rows (a persistent grid).  The quantize scans NC > 0
+// centroids held in registers (codebooks of exactly NC entries), or, with
+// NC == 0, searches the block's sorted view of the codebook (any size up to
+// 256).  Launch: blockDim.x = 256, any grid; dynamic shared memory
+// hadamard_smem(n_c) when QUANT and NC == 0, else 0.  x rows contiguous and
+// E-element aligned; y / idx [n_rows][D].
+__host__ __device__ inline size_t hadamard_smem(int n_c) { return (size_t)n_c * 16 + 16; }
+
 template <typename T, int E, bool QUANT, int NC>
 __global__ void __launch_bounds__(256)
     hadamard_rows(const T *__restrict__ x, const float *__restrict__ diag, int64_t n_rows,
                   int32_t lanes_per_row, float scale, const float *__restrict__ centroids,
                   int32_t n_c, float *__restrict__ y, uint8_t *__restrict__ idx)
 {
-    extern __shared__ float hq_cb[];
+    extern __shared__ float hq_sm[];
+    SortedCb scb{nullptr, nullptr, 0, 0};
+    const float *hq_cb = hq_sm;
+    bool sorted_ok = false;
+    float creg[NC > 0 ? NC : 1];
+    if constexpr (QUANT && NC > 0) {
+#pragma unroll
+        for (int k = 0; k < NC; ++k) creg[k] = __ldg(centroids + k);
+    }
     if constexpr (QUANT && NC == 0) {
-        for (int j = threadIdx.x; j < n_c; j += blockDim.x) hq_cb[j] = centroids[j];
+        float *c = hq_sm;                                            // [n_c] as given
+        float *u = c + n_c;                                          // [n_c] sorted distinct
+        int *rep = reinterpret_cast<int *>(u + n_c);                 // [n_c]
+        int *first = rep + n_c;                                      // [n_c]
+        int *mcount = first + n_c;
+        for (int j = threadIdx.x; j < n_c; j += blockDim.x) c[j] = centroids[j];
         __syncthreads();
+        sorted_ok = build_sorted(c, n_c, u, rep, first, mcount);
+        if (sorted_ok) {
+            scb.u = u;
+            scb.rep = rep;
+            scb.m = *mcount;
+            int top = 1;
+            while (top * 2 <= scb.m) top *= 2;
+            scb.top = top;
+        }
     }
     const int lane = threadIdx.x & 31;
     const int lpr = lanes_per_row;
     const int rows_per_warp = 32 / lpr;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int sub = lane / lpr;   // row within the warp
+    const int sub = lane / lpr;      // row within the warp
     const int l = lane - sub * lpr;  // lane within the row
-    const int64_t row = warp * rows_per_warp + sub;
-    const bool live = row < n_rows;
     const int d = lpr * E;
-    float v[E];
-    if (live) {
-        load_run<T, E>(x + (size_t)row * d + (size_t)l * E, v);
-    } else {
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    float dg[E];
 #pragma unroll
-        for (int j = 0; j < E; ++j) v[j] = 0.f;
-    }
+    for (int j = 0; j < E; ++j) dg[j] = __ldg(diag + l * E + j);
+    for (int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+         warp * rows_per_warp < n_rows; warp += warps) {  // warp-uniform
+        const int64_t row = warp * rows_per_warp + sub;
+        const bool live = row < n_rows;
+        float v[E];
+        if (live) {
+            load_run<T, E>(x + (size_t)row * d + (size_t)l * E, v);
+        } else {
 #pragma unroll
-    for (int j = 0; j < E; ++j) v[j] = __fmul_rn(v[j], __ldg(diag + l * E + j));
-    // strides below E: pairs inside the lane's registers
+            for (int j = 0; j < E; ++j) v[j] = 0.f;
+        }
 #pragma unroll
-    for (int s = 1; s < E; s <<= 1) {
+        for (int j = 0; j < E; ++j) v[j] = __fmul_rn(v[j], dg[j]);
+        // strides below E: pairs inside the lane's registers
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-            if ((j & s) == 0) {
-                const float a = v[j], b = v[j + s];
-                v[j] = __fadd_rn(a, b);
-                v[j + s] = __fsub_rn(a, b);
+        for (int s = 1; s < E; s <<= 1) {
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                if ((j & s) == 0) {
+                    const float a = v[j], b = v[j + s];
+                    v[j] = __fadd_rn(a, b);
+                    v[j + s] = __fsub_rn(a, b);
+                }
             }
         }
-    }
-    // strides E .. D/2: the partner element sits in lane l ^ (s / E)
-    for (int ls = 1; ls < lpr; ls <<= 1) {
-        const bool upper = (l & ls) != 0;
+        // strides E .. D/2: the partner element sits in lane l ^ (s / E)
+        for (int ls = 1; ls < lpr; ls <<= 1) {
+            const bool upper = (l & ls) != 0;
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-            const float p = __shfl_xor_sync(0xffffffffu, v[j], ls);
-            v[j] = upper ? __fsub_rn(p, v[j]) : __fadd_rn(v[j], p);
+            for (int j = 0; j < E; ++j) {
+                const float p = __shfl_xor_sync(0xffffffffu, v[j], ls);
+                v[j] = upper ? __fsub_rn(p, v[j]) : __fadd_rn(v[j], p);
+            }
         }
-    }
-    if (!live) return;
+        if (!live) continue;
 #pragma unroll
-    for (int j = 0; j < E; ++j) v[j] = __fmul_rn(v[j], scale);
-    if constexpr (QUANT) {
-        uint32_t code[E];
-        if constexpr (NC > 0) {
-            float c[NC];
+        for (int j = 0; j < E; ++j) v[j] = __fmul_rn(v[j], scale);
+        if constexpr (QUANT) {
+            uint32_t code[E];
 #pragma unroll
-            for (int k = 0; k < NC; ++k) c[k] = __ldg(centroids + k);
+            for (int j = 0; j < E; ++j) {
+                if constexpr (NC > 0) {
+                    code[j] = nearest_reg<NC>(v[j], creg);
+                } else {
+                    const int k = sorted_ok ? nearest_sorted(v[j], scb) : -1;
+                    code[j] = k >= 0 ? (uint32_t)k : nearest(v[j], hq_cb, n_c);
+                }
+            }
+            uint8_t *o = idx + (size_t)row * d + (size_t)l * E;
+            if constexpr (E % 4 == 0) {
 #pragma unroll
-            for (int j = 0; j < E; ++j) code[j] = nearest_reg<NC>(v[j], c);
+                for (int j = 0; j < E; j += 4)
+                    *reinterpret_cast<uint32_t *>(o + j) =
+                        code[j] | code[j + 1] << 8 | code[j + 2] << 16 | code[j + 3] << 24;
+            } else {
+#pragma unroll
+                for (int j = 0; j < E; ++j) o[j] = (uint8_t)code[j];
+            }
         } else {
+            float *o = y + (size_t)row * d + (size_t)l * E;
 #pragma unroll
-            for (int j = 0; j < E; ++j) code[j] = nearest(v[j], hq_cb, n_c);
+            for (int j = 0; j < E; ++j) o[j] = v[j];
         }
-        uint8_t *o = idx + (size_t)row * d + (size_t)l * E;
-        if constexpr (E % 4 == 0) {
-#pragma unroll
-            for (int j = 0; j < E; j += 4)
-                *reinterpret_cast<uint32_t *>(o + j) =
-                    code[j] | code[j + 1] << 8 | code[j + 2] << 16 | code[j + 3] << 24;
-        } else {
-#pragma unroll
-            for (int j = 0; j < E; ++j) o[j] = (uint8_t)code[j];
-        }
-    } else {
-        float *o = y + (size_t)row * d + (size_t)l * E;
-#pragma unroll
-        for (int j = 0; j < E; ++j) o[j] = v[j];
     }
 }
 

@@ -119,3 +119,41 @@ def test_full_turboquant_keys(vq, oracle_mod):
     assert np.array_equal(got.astype(np.uint32), oracle_mod.scalar_quantize(x, c))
     got = vq.vq_hadamard_quantize(xd, dd, cd).cpu().numpy()
     assert np.array_equal(got.astype(np.uint32), oracle_mod.hadamard_quantize(x, diag, c))
+
+
+@pytest.mark.parametrize("case", ["unsorted_duplicates", "plateaus", "signed_zeros", "non_finite",
+                                  "one_centroid", "all_equal", "wide_256"])
+def test_hadamard_quantize_codebook_edge_cases(vq, oracle_mod, case):
+    """The sorted-codebook search against the rule: duplicates in any order,
+    centroids whose fp32 distances tie for large keys, +-0, an infinite
+    centroid (the kernel falls back to the scan), degenerate codebooks."""
+    rng = np.random.default_rng(sum(map(ord, case)))
+    dim, rows = 128, 300
+    x = rng.standard_normal((rows, dim)).astype(np.float32)
+    if case == "unsorted_duplicates":
+        c = rng.standard_normal(16).astype(np.float32)
+        c[[3, 9, 14]] = c[5]
+        c[[0, 11]] = c[7]
+    elif case == "plateaus":
+        base = np.float32(1.0)
+        c = (base + np.arange(16, dtype=np.float32) * np.float32(2.0 ** -22)).astype(np.float32)
+        rng.shuffle(c)
+        x *= np.float32(1e4)  # |y - c| ~ 1e3: the ulp of y swamps the centroid gaps
+    elif case == "signed_zeros":
+        c = np.array([0.0, -0.0, 1.0, -1.0, -0.0, 0.5, 0.0, -0.5], dtype=np.float32)
+        x[:, :16] = 0.0
+    elif case == "non_finite":
+        c = rng.standard_normal(8).astype(np.float32)
+        c[2] = np.inf
+    elif case == "one_centroid":
+        c = np.array([0.25], dtype=np.float32)
+    elif case == "all_equal":
+        c = np.full(16, 0.75, dtype=np.float32)
+    else:
+        c = rng.standard_normal(256).astype(np.float32)
+        c[rng.integers(0, 256, 40)] = c[rng.integers(0, 256, 40)]
+    diag = rng.choice([-1.0, 1.0], dim).astype(np.float32)
+    want = oracle_mod.hadamard_quantize(x, diag, c)
+    got = vq.vq_hadamard_quantize(torch.from_numpy(x).cuda(), torch.from_numpy(diag).cuda(),
+                                  torch.from_numpy(c).cuda()).cpu().numpy()
+    assert np.array_equal(got.astype(np.uint32), want)
