@@ -24,6 +24,10 @@
 // memory, so thread t of the block owns row t of the tile: it reads its own
 // row's scores (tcgen05.ld) and reduces them without any exchange.
 //
+// A wait that gives up (bounded polls) marks every row the block has not
+// encoded with 0xFFFFFFFF, waits once more (bounded) for the MMA in flight
+// and frees the tensor memory.
+//
 // Launch: block = 128 threads; dynamic shared memory = TcLayout::bytes(...)
 // (at least 512/NCOL CTAs' worth of a 228 KiB SM, which caps the CTAs per SM
 // at the tensor-memory budget: NCOL columns each); grid.x = n_groups *
@@ -342,7 +346,12 @@ __global__ void __launch_bounds__(128, MINB)
             tc_fence_after();
         }
         if (!alive) {
-            if (row < n_per_group) store_index(og + row, kQueued);
+            // the MMA whose completion was not seen: wait once more (bounded)
+            // before its accumulator memory is freed; record the tile
+            if (tid == 0) {
+                (void)mbar_wait(bar, phase ^ 1u);
+                *qcount = (uint32_t)tile;
+            }
             break;
         }
 
@@ -452,7 +461,14 @@ __global__ void __launch_bounds__(128, MINB)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 0 && alive)
+    if (!alive) {
+        // a wait gave up: mark the rows of the failed tile and of every later one
+        for (int t = (int)*qcount; t < tiles_per_block; ++t) {
+            const int64_t r = row_base + (int64_t)t * 128 + tid;
+            if (r < n_per_group) store_index(og + r, kQueued);
+        }
+    }
+    if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOL));
 }
 
