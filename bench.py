@@ -187,9 +187,28 @@ def cpu_baseline(w_name: str, x: np.ndarray, cb: np.ndarray, budget_s: float = 1
         oracle.encode(xs, cb[:1], n_threads=cores)
         times.append(time.perf_counter() - t0)
     med = statistics.median(times)
+    # the same oracle on one core, over a tenth of the sample
+    rows1 = max(1, rows // 10)
+    t0 = time.perf_counter()
+    oracle.encode(np.ascontiguousarray(x[:1, :rows1]), cb[:1], n_threads=1)
+    one_core = rows1 / max(time.perf_counter() - t0, 1e-9)
     return {"value": rows / med, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {rows} of {w.n} sub-vectors of {w_name} (codebook 0), "
-                      f"median of 3 runs, {cores} threads", "seconds": med}
+                      f"median of 3 runs, {cores} threads", "seconds": med,
+            "value_1_core": one_core, "cpu_model": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (or its implementer / part on Arm)."""
+    try:
+        text = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "CPU part"):
+        for line in text.splitlines():
+            if line.split(":")[0].strip() == key:
+                return f"{key}: {line.split(':', 1)[1].strip()}"
+    return "unknown"
 
 
 def bench_reference(args) -> None:
@@ -267,8 +286,16 @@ def bench_ours(args) -> None:
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        vq.vq_encode_grouped(xd, cbd, out=out, stream=stream)
+    if args.per_layer:
+        # the pages' per-layer dispatch: one vq_encode launch per group
+        views = [(xd[g], cbd[g], out[g]) for g in range(x.shape[0])]
+
+        def step():
+            for xg, cg, og in views:
+                vq.vq_encode(xg, cg, out=og, stream=stream)
+    else:
+        def step():
+            vq.vq_encode_grouped(xd, cbd, out=out, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -345,8 +372,9 @@ def bench_ours(args) -> None:
         "vs_baseline": (value / world / PAGES_FALCON_SUBVEC_PER_S
                         if args.workload == "falcon_prefill" else None),
         "dtype": "f32", "data": "synthetic (seeded N(0,1) fp16 keys and codebooks)",
-        "config": dict(config_block(w, args, world), timed_region_s=region_s),
-        "gpu_launches": args.steps,
+        "config": dict(config_block(w, args, world), timed_region_s=region_s,
+                       dispatch="one vq_encode per group" if args.per_layer else "one grouped launch"),
+        "gpu_launches": args.steps * (x.shape[0] if args.per_layer else 1),
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": roofline,
         "e2e": {"value": job_throughput(units * e2e_steps, world, e2e_s), "unit": UNIT,
@@ -646,6 +674,8 @@ def main() -> None:
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="falcon_prefill")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--per-layer", action="store_true",
+                   help="encode: one vq_encode launch per group instead of one grouped launch")
     p.add_argument("--op", choices=["encode", "dequantize", "attention", "smooth", "scalar",
                                     "hadamard"], default="encode")
     args = p.parse_args()
