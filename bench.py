@@ -280,8 +280,15 @@ def bench_ours(args) -> None:
     vq.load_library()
     w = workloads.WORKLOADS[args.workload]
     x, cb = workloads.generate(args.workload)
-    xd = torch.from_numpy(x).to(dev)
-    cbd = torch.from_numpy(cb).to(dev)
+    if args.centroids:  # a smaller codebook: its first rows
+        cb = np.ascontiguousarray(cb[:, : args.centroids])
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[args.dtype]
+    xd = torch.from_numpy(x).to(dev).to(tdt)
+    cbd = torch.from_numpy(cb).to(dev).to(tdt)
+    if args.misalign:  # x one element off its natural alignment: the any-layout kernel
+        buf = torch.empty(xd.numel() + 1, dtype=tdt, device=dev)
+        buf[1:].copy_(xd.reshape(-1))
+        xd = buf[1:].view(xd.shape)
     out = torch.empty(x.shape[:2], dtype=torch.uint32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -322,19 +329,20 @@ def bench_ours(args) -> None:
     kernel_ms = sum(step_ms) / len(step_ms)
     kernel_ms, region_s = reduce_max([kernel_ms, region_s], dev)
 
+    variant = args.dtype != "f16" or args.centroids or args.misalign or args.per_layer
     # end to end through the host entry point: pinned host in, pinned host out
     xh = torch.from_numpy(x).pin_memory()
     cbh = torch.from_numpy(cb).pin_memory()
     outh = torch.empty(x.shape[:2], dtype=torch.uint32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 200))
-    for _ in range(3):
+    e2e_steps = 0 if variant else max(3, min(args.steps, 200))
+    for _ in range(3 if e2e_steps else 0):
         vq.vq_encode_grouped_host(xh, cbh, outh, xd, cbd, out, stream=stream)
     if world > 1:
         dist.barrier()
     e0 = time.perf_counter()
     for _ in range(e2e_steps):
         vq.vq_encode_grouped_host(xh, cbh, outh, xd, cbd, out, stream=stream)
-    e2e_s = time.perf_counter() - e0
+    e2e_s = max(time.perf_counter() - e0, 1e-12)
     (e2e_s,) = reduce_max([e2e_s], dev)
     if world > 1:
         dist.barrier()
@@ -346,19 +354,20 @@ def bench_ours(args) -> None:
 
     props = torch.cuda.get_device_properties(dev)
     peaks = measured_peaks()
-    desc = vq.vq_describe_launch(x.shape[0], x.shape[1], cb.shape[1], x.shape[2], torch.float16,
+    desc = vq.vq_describe_launch(x.shape[0], x.shape[1], cb.shape[1], x.shape[2], tdt,
                                  xd.data_ptr())
     clk = clocks.summary()
     sm_max = peaks.get("sm_max_mhz") or clk["sm_max_mhz"] or 2070.0
     peak_tflops = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
     units = w.n
     value = job_throughput(units, world, kernel_ms * 1e-3)
-    achieved = flops_per_subvector(w) * units / (kernel_ms * 1e-3) / 1e12
+    flops_unit = cb.shape[1] * 3 * w.sub_dim  # as flops_per_subvector, for the codebook used
+    achieved = flops_unit * units / (kernel_ms * 1e-3) / 1e12
     roofline = {
         "bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
         "frac": achieved / peak_tflops, "traffic": MEASURED_TRAFFIC.get(desc),
         "kernel": desc,
-        "flops_per_unit": flops_per_subvector(w), "units_per_launch": units,
+        "flops_per_unit": flops_unit, "units_per_launch": units,
         "peak_basis": f"{props.multi_processor_count} SMs x {FP32_LANES_PER_SM} FP32 lanes x "
                       f"2 (FMA) x {sm_max:.0f} MHz",
         "hbm_gbs": bytes_per_subvector(w) * units / (kernel_ms * 1e-3) / 1e9,
@@ -370,20 +379,22 @@ def bench_ours(args) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": kernel_ms,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / world / PAGES_FALCON_SUBVEC_PER_S
-                        if args.workload == "falcon_prefill" else None),
+                        if args.workload == "falcon_prefill" and not variant else None),
         "dtype": "f32", "data": "synthetic (seeded N(0,1) fp16 keys and codebooks)",
         "config": dict(config_block(w, args, world), timed_region_s=region_s,
+                       n_centroids=int(cb.shape[1]), input_dtype=args.dtype,
+                       x_misaligned=bool(args.misalign),
                        dispatch="one vq_encode per group" if args.per_layer else "one grouped launch"),
         "gpu_launches": args.steps * (x.shape[0] if args.per_layer else 1),
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": roofline,
-        "e2e": {"value": job_throughput(units * e2e_steps, world, e2e_s), "unit": UNIT,
+        "e2e": None if variant else {"value": job_throughput(units * e2e_steps, world, e2e_s), "unit": UNIT,
                 "h2d_bytes_per_step": x.nbytes + cb.nbytes,
                 "d2h_bytes_per_step": int(units * 4),
                 "path": "vq_encode_grouped_host with pinned host buffers: the kernel reads x and "
                         "writes the indices across the CPU-GPU link; codebooks copied"},
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not variant:
         line["cpu_baseline"] = cpu_baseline(args.workload, x, cb)
     print(json.dumps(line))
     if world > 1:
@@ -674,6 +685,12 @@ def main() -> None:
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="falcon_prefill")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--dtype", choices=["f16", "bf16", "f32"], default="f16",
+                   help="encode: input type (f32 takes the CUDA-core filter kernel)")
+    p.add_argument("--centroids", type=int, default=0,
+                   help="encode: use only the first N codebook rows (below 64: brute force)")
+    p.add_argument("--misalign", action="store_true",
+                   help="encode: x one element off alignment (the any-layout kernel)")
     p.add_argument("--per-layer", action="store_true",
                    help="encode: one vq_encode launch per group instead of one grouped launch")
     p.add_argument("--op", choices=["encode", "dequantize", "attention", "smooth", "scalar",
