@@ -134,6 +134,10 @@ CASES = [
     (2, 6, 2, 2049, 64, 4, 256, "bf16"),    # GQA 3 (three heads per block)
     (1, 32, 2, 2000, 128, 8, 256, "f16"),   # GQA 16: two head groups per KV head
     (3, 4, 4, 777, 128, 8, 100, "f32"),     # 100 centroids; codes up to 99
+    (1, 8, 1, 2000, 512, 8, 256, "f16"),    # head_dim 512 (the maximum), 64 sub-spaces
+    (1, 4, 4, 1000, 512, 32, 256, "bf16"),  # head_dim 512, sub_dim 32
+    (2, 16, 2, 1500, 64, 16, 256, "f32"),   # 4 sub-spaces of 16, GQA 8
+    (1, 64, 8, 700, 128, 8, 256, "f16"),    # 64 query heads
 ]
 
 
@@ -201,6 +205,13 @@ def test_small_workspace_uses_fewer_slices(vq, oracle_mod):
     with pytest.raises(vq.VQError):
         vq.vq_attention_decode(*dev, workspace=torch.empty(per_slice - 16, dtype=torch.uint8,
                                                            device="cuda"))
+
+
+def test_long_cache_many_slices(vq, oracle_mod):
+    """A quarter-million-token cache of one sequence: hundreds of chunks,
+    many token slices merged."""
+    host, dev = make_case(51, 1, 8, 2, 262144, 128, 8, 256, "f16")
+    check(vq, oracle_mod, host, dev, "f16")
 
 
 def test_repeated_calls_agree(vq):
