@@ -527,6 +527,8 @@ def bench_sibling(args, fused: bool) -> None:
     sw = workloads.SCALAR_WORKLOADS["turboquant_keys"]
     x, c, diag = workloads.generate_scalar(sw.name)
     xd, cd, dd = (torch.from_numpy(a).to(dev) for a in (x, c, diag))
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[args.dtype]
+    xd = xd.to(tdt)  # fp32 keys take the per-element exact search instead of the table
     out = torch.empty(x.shape, dtype=torch.uint8, device=dev)
     ws = torch.empty(65536, dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -552,7 +554,7 @@ def bench_sibling(args, fused: bool) -> None:
             ends[k].record(stream)
         torch.cuda.synchronize(dev)
     ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
-    algo_bytes = 3 * sw.n
+    algo_bytes = (xd.element_size() + 1) * sw.n
     achieved = algo_bytes / (ms * 1e-3) / 1e9
     peak = measured_peaks().get("hbm_gbs") or 6800.0
     clk = clocks.summary()
@@ -565,6 +567,7 @@ def bench_sibling(args, fused: bool) -> None:
         "op": "hadamard" if fused else "scalar",
         "config": {"workload": sw.name, "batch": sw.batch, "heads": sw.heads,
                    "tokens": sw.tokens, "head_dim": sw.head_dim, "bits": sw.bits,
+                   "input_dtype": args.dtype,
                    "l2": "flushed before every step (256 MiB write)"},
         "gpu_launches": args.steps * (1 if fused else 2),
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},

@@ -35,16 +35,29 @@ int64_t stream_blocks(int64_t work_items, int per_sm)
 
 vq_status launched() { return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA; }
 
-template <typename T>
-vq_status launch_scan(const void *x, int64_t n, const float *c, int32_t n_c, uint8_t *out,
-                      cudaStream_t st)
+template <typename T, int NC>
+vq_status launch_scan_nc(const void *x, int64_t n, const float *c, int32_t n_c, uint8_t *out,
+                         cudaStream_t st)
 {
-    vqs::scalar_scan<T><<<(unsigned)stream_blocks(n, 8), kThreads, (size_t)n_c * 4, st>>>(
+    const size_t smem = NC == 0 ? vqs::hadamard_smem(n_c) : 0;
+    vqs::scalar_scan<T, NC><<<(unsigned)stream_blocks(n, 8), kThreads, smem, st>>>(
         static_cast<const T *>(x), n, c, n_c, out);
     return launched();
 }
 
-// A persistent grid: up to 8 blocks of 256 threads per SM stride over the rows.
+template <typename T>
+vq_status launch_scan(const void *x, int64_t n, const float *c, int32_t n_c, uint8_t *out,
+                      cudaStream_t st)
+{
+    switch (n_c) {
+    case 2: return launch_scan_nc<T, 2>(x, n, c, n_c, out, st);
+    case 4: return launch_scan_nc<T, 4>(x, n, c, n_c, out, st);
+    case 8: return launch_scan_nc<T, 8>(x, n, c, n_c, out, st);
+    case 16: return launch_scan_nc<T, 16>(x, n, c, n_c, out, st);
+    }
+    return launch_scan_nc<T, 0>(x, n, c, n_c, out, st);
+}
+
 template <typename T, int E, bool QUANT, int NC>
 vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, int32_t dim,
                              float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,

@@ -114,21 +114,6 @@ __global__ void __launch_bounds__(256)
     for (int64_t e = units * 8 + tid; e < n; e += nthreads) out[e] = sl_tab[x[e]];
 }
 
-// The scan itself (any input type), codebook in shared memory.  Launch: any
-// grid of 256-thread blocks, dynamic shared memory n_c * 4 bytes.
-template <typename T>
-__global__ void __launch_bounds__(256)
-    scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
-                int32_t n_c, uint8_t *__restrict__ out)
-{
-    extern __shared__ float ss_cb[];
-    for (int j = threadIdx.x; j < n_c; j += blockDim.x) ss_cb[j] = centroids[j];
-    __syncthreads();
-    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += nthreads)
-        out[e] = (uint8_t)nearest(widen_elem(x[e]), ss_cb, n_c);
-}
-
 // ---- exact nearest centroid through the sorted codebook
 //
 // For a finite value y and finite centroids, let u_0 < ... < u_{m-1} be the
@@ -265,6 +250,19 @@ __device__ __forceinline__ uint32_t nearest_reg(float val, const float (&c)[NC])
 // E-element aligned; y / idx [n_rows][D].
 __host__ __device__ inline size_t hadamard_smem(int n_c) { return (size_t)n_c * 16 + 16; }
 
+// The scalar quantize of any input type without a table: codebooks of 2, 4,
+// 8 or 16 entries (NC) scanned from registers, others (NC == 0) through the
+// block's sorted view, every element falling back to the scan of the rule
+// where the view cannot decide.  A persistent grid strides over the
+// elements.  Launch: any grid of 256-thread blocks; dynamic shared memory
+// hadamard_smem(n_c) when NC == 0, else 0.
+template <typename T, int NC>
+__global__ void __launch_bounds__(256)
+    scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
+                int32_t n_c, uint8_t *__restrict__ out);
+
+
+
 template <typename T, int E, bool QUANT, int NC>
 __global__ void __launch_bounds__(256)
     hadamard_rows(const T *__restrict__ x, const float *__restrict__ diag, int64_t n_rows,
@@ -396,6 +394,50 @@ __global__ void __launch_bounds__(256)
         } else {
             out[e] = __float2bfloat16_rn(v);
         }
+    }
+}
+
+template <typename T, int NC>
+__global__ void __launch_bounds__(256)
+    scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
+                int32_t n_c, uint8_t *__restrict__ out)
+{
+    extern __shared__ float ss_sm[];
+    float creg[NC > 0 ? NC : 1];
+    SortedCb scb{nullptr, nullptr, 0, 0};
+    bool sorted_ok = false;
+    if constexpr (NC > 0) {
+#pragma unroll
+        for (int k = 0; k < NC; ++k) creg[k] = __ldg(centroids + k);
+    } else {
+        float *c = ss_sm;
+        float *u = c + n_c;
+        int *rep = reinterpret_cast<int *>(u + n_c);
+        int *first = rep + n_c;
+        int *mcount = first + n_c;
+        for (int j = threadIdx.x; j < n_c; j += blockDim.x) c[j] = centroids[j];
+        __syncthreads();
+        sorted_ok = build_sorted(c, n_c, u, rep, first, mcount);
+        if (sorted_ok) {
+            scb.u = u;
+            scb.rep = rep;
+            scb.m = *mcount;
+            int top = 1;
+            while (top * 2 <= scb.m) top *= 2;
+            scb.top = top;
+        }
+    }
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += nthreads) {
+        const float v = widen_elem(x[e]);
+        uint32_t k;
+        if constexpr (NC > 0) {
+            k = nearest_reg<NC>(v, creg);
+        } else {
+            const int ks = sorted_ok ? nearest_sorted(v, scb) : -1;
+            k = ks >= 0 ? (uint32_t)ks : nearest(v, ss_sm, n_c);
+        }
+        out[e] = (uint8_t)k;
     }
 }
 

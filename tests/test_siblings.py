@@ -157,3 +157,20 @@ def test_hadamard_quantize_codebook_edge_cases(vq, oracle_mod, case):
     got = vq.vq_hadamard_quantize(torch.from_numpy(x).cuda(), torch.from_numpy(diag).cuda(),
                                   torch.from_numpy(c).cuda()).cpu().numpy()
     assert np.array_equal(got.astype(np.uint32), want)
+
+
+@pytest.mark.parametrize("n_c", [1, 2, 3, 8, 16, 100, 256])
+@pytest.mark.parametrize("kind", ["random", "duplicates", "non_finite"])
+def test_scalar_scan_paths(vq, oracle_mod, n_c, kind):
+    """fp32 keys (no table): the register scan (2, 4, 8, 16 entries) and the
+    sorted-view search (other sizes, with its fallback) against the rule."""
+    rng = np.random.default_rng(n_c * 7 + len(kind))
+    x = (3.0 * rng.standard_normal(50001)).astype(np.float32)
+    x[:6] = [np.nan, np.inf, -np.inf, 0.0, -0.0, 3e38]
+    c = rng.standard_normal(n_c).astype(np.float32)
+    if kind == "duplicates" and n_c > 2:
+        c[rng.integers(0, n_c, n_c // 2)] = c[0]
+    if kind == "non_finite":
+        c[n_c // 2] = np.inf
+    got = vq.vq_scalar_quantize(torch.from_numpy(x).cuda(), torch.from_numpy(c).cuda()).cpu().numpy()
+    assert np.array_equal(got.astype(np.uint32), oracle_mod.scalar_quantize(x, c))
