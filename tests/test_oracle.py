@@ -314,3 +314,30 @@ def test_smooth_rejects_partial_key_vectors(oracle_mod):
     x, cb, smooth = _smooth_case(126, per_group=10)  # 10 rows, 4 per key vector
     with pytest.raises(RuntimeError):
         oracle_mod.encode_smooth(x, smooth, cb, 16)
+
+
+# ---------------------------------------------------------------- fp16 arithmetic vs the rule
+
+def test_fp16_subtract_variant_differs_rarely_at_equal_error(oracle_mod):
+    """The pages contrast the fp32 rule (widen, then subtract) with an fp16
+    path ("Correctness": about 0.1 % of indices differ, reconstruction MSE the
+    same to 3 digits, on their calibrated codebook).  The kind of result, on
+    synthetic keys: an fp16 subtract-square-sum variant (numpy float16, written
+    here, not the oracle) disagrees with the oracle on a small nonzero fraction
+    of indices, and the two reconstructions have the same MSE to within 1 %."""
+    rng = np.random.default_rng(130)
+    x = rng.standard_normal((1, 16384, 8)).astype(np.float16)
+    cb = rng.standard_normal((1, 256, 8)).astype(np.float16)
+    exact = oracle_mod.encode(x, cb)[0].astype(np.int64)
+    d16 = x[0][:, None, :] - cb[0][None, :, :]          # float16 subtract
+    dist16 = (d16 * d16).sum(axis=-1, dtype=np.float16)  # float16 squares and sums
+    half = np.argmin(dist16, axis=1)
+    frac = float((half != exact).mean())
+    assert 0.0 < frac < 0.05, frac
+    x64 = x[0].astype(np.float64)
+    mse = lambda idx: float(((cb[0][idx].astype(np.float64) - x64) ** 2).mean())
+    assert abs(mse(half) - mse(exact)) / mse(exact) < 0.01
+    # the exact rule is never worse row by row (in float64)
+    d_exact = ((cb[0][exact].astype(np.float64) - x64) ** 2).sum(-1)
+    d_half = ((cb[0][half].astype(np.float64) - x64) ** 2).sum(-1)
+    assert np.all(d_exact <= d_half * (1 + 1e-6) + 1e-12)
