@@ -24,9 +24,11 @@
 // memory, so thread t of the block owns row t of the tile: it reads its own
 // row's scores (tcgen05.ld) and reduces them without any exchange.
 //
-// A wait that gives up (bounded polls) marks every row the block has not
-// encoded with 0xFFFFFFFF, waits once more (bounded) for the MMA in flight
-// and frees the tensor memory.
+// Every thread waits for each MMA on the mbarrier (bounded polls); the block
+// agrees once per tile, after the tile's passes, on whether all waits
+// completed.  If one gave up, the block marks every row it has not encoded
+// with 0xFFFFFFFF, waits once more (bounded) for the last MMA and frees the
+// tensor memory.
 //
 // Launch: block = 128 threads; dynamic shared memory = TcLayout::bytes(...)
 // (at least 512/NCOL CTAs' worth of a 228 KiB SM, which caps the CTAs per SM
@@ -97,14 +99,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32])
+// 32 consecutive fp32 columns, without waiting: the registers are valid only
+// after tmem_wait_ld.
+__device__ __forceinline__ void tmem_load32_async(uint32_t taddr, uint32_t *r)
 {
-    uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
@@ -112,8 +113,27 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32])
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
+}
+
+// Wait for this thread's outstanding tensor-memory loads.  The empty
+// statements make every loaded register an output of the wait, so no use of
+// one can be scheduled above it.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[N])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    for (int j = 0; j < N; ++j) asm volatile("" : "+r"(r[j]));
+}
+
+// Least of GC consecutive scores.
+template <int GC>
+__device__ __forceinline__ float group_min(const uint32_t *u)
+{
+    float a = min3(__uint_as_float(u[0]), __uint_as_float(u[1]), __uint_as_float(u[2]));
+#pragma unroll
+    for (int k = 3; k + 1 < GC; k += 2) a = min3(a, __uint_as_float(u[k]), __uint_as_float(u[k + 1]));
+    return fminf(a, __uint_as_float(u[GC - 1]));
 }
 
 // Keep the top 10 bits of an fp32 significand (the tf32 value, exactly).
@@ -286,7 +306,8 @@ __global__ void __launch_bounds__(128, MINB)
     load_x(row_base + tid, xr);
 
     uint32_t phase = 0;
-    bool alive = true;
+    bool alive = true;        // block-wide: every wait so far completed
+    bool alive_here = true;   // this thread's waits
     for (int tile = 0; tile < tiles_per_block; ++tile) {
         const int64_t row = row_base + (int64_t)tile * 128 + tid;
         if (row_base + (int64_t)tile * 128 >= n_per_group) break;  // block-uniform
@@ -319,40 +340,33 @@ __global__ void __launch_bounds__(128, MINB)
                 }
                 umma_commit(bar);
             }
-            const bool done = mbar_wait(bar, phase);
+            // a wait that gives up is agreed on once per tile, below; the
+            // scores it leaves unread are never used
+            alive_here &= mbar_wait(bar, phase);
             phase ^= 1u;
             tc_fence_after();
-            if (!__syncthreads_and(done)) {
-                alive = false;
-                break;
-            }
+            if (NCOL == 64 && ncols == 64) {  // block-uniform
+                uint32_t v[64];
+                tmem_load32_async(tmem + lane_base, v);
+                tmem_load32_async(tmem + lane_base + 32u, v + 32);
+                tmem_wait_ld(v);
 #pragma unroll
-            for (int j = 0; j < NCOL; j += 32) {
-                if (j < ncols) {  // block-uniform
-                    float v[32];
-                    tmem_load32(tmem + lane_base + (uint32_t)j, v);
+                for (int q = 0; q < 64 / kGC; ++q) gmin[c0 / kGC + q] = group_min<kGC>(v + q * kGC);
+            } else {
 #pragma unroll
-                    for (int q = 0; q < 32 / kGC; ++q) {
-                        const float *w = v + q * kGC;
-                        float a = min3(w[0], w[1], w[2]);
+                for (int j = 0; j < NCOL; j += 32) {
+                    if (j < ncols) {  // block-uniform
+                        uint32_t v[32];
+                        tmem_load32_async(tmem + lane_base + (uint32_t)j, v);
+                        tmem_wait_ld(v);
 #pragma unroll
-                        for (int k = 3; k + 1 < kGC; k += 2) a = min3(a, w[k], w[k + 1]);
-                        gmin[(c0 + j) / kGC + q] = fminf(a, w[kGC - 1]);
+                        for (int q = 0; q < 32 / kGC; ++q) gmin[(c0 + j) / kGC + q] = group_min<kGC>(v + q * kGC);
                     }
                 }
             }
             tc_fence_before();
             __syncthreads();  // tensor memory is read before the next MMA writes it
             tc_fence_after();
-        }
-        if (!alive) {
-            // the MMA whose completion was not seen: wait once more (bounded)
-            // before its accumulator memory is freed; record the tile
-            if (tid == 0) {
-                (void)mbar_wait(bar, phase ^ 1u);
-                *qcount = (uint32_t)tile;
-            }
-            break;
         }
 
         // next tile's row, in flight during the bookkeeping below
@@ -381,7 +395,17 @@ __global__ void __launch_bounds__(128, MINB)
         const int ga = __ffs(mask) - 1;
         const int gb = cnt > 1 ? __ffs(mask & (mask - 1)) - 1 : -1;
         if (tid == 0) *qcount = 0u;
-        __syncthreads();
+        if (!__syncthreads_and(alive_here)) {
+            // a wait gave up: wait once more (bounded) for the last MMA, whose
+            // completion may not have been seen, before its accumulator memory
+            // is freed; record the tile
+            alive = false;
+            if (tid == 0) {
+                (void)mbar_wait(bar, phase ^ 1u);
+                *qcount = (uint32_t)tile;
+            }
+            break;
+        }
         uint32_t id = 0;
         if (!ok || cnt > 2 || cnt == 0) {
             id = kQueued;
