@@ -167,8 +167,8 @@ def dist_env():
 
 def cpu_baseline(w_name: str, x: np.ndarray, cb: np.ndarray, budget_s: float = 12.0) -> dict:
     """The CPU oracle on this host's cores over a bounded sample of the same
-    workload: the first rows of group 0 (about ``budget_s`` seconds in all),
-    median of 3 runs."""
+    workload: the first rows of group 0, encoded repeatedly (at least 3 runs)
+    until about ``budget_s`` seconds of CPU work are done; the median run."""
     import oracle  # test infrastructure: used here only for the CPU baseline
 
     oracle.build()
@@ -180,9 +180,10 @@ def cpu_baseline(w_name: str, x: np.ndarray, cb: np.ndarray, budget_s: float = 1
     oracle.encode(x[:1, :probe], cb[:1], n_threads=cores)
     rate = probe / max(time.perf_counter() - t0, 1e-6)
     rows = int(min(m, max(probe, rate * budget_s / 3)))
+    runs = int(min(30, max(3, round(budget_s * rate / rows))))
     xs = np.ascontiguousarray(x[:1, :rows])
     times = []
-    for _ in range(3):
+    for _ in range(runs):
         t0 = time.perf_counter()
         oracle.encode(xs, cb[:1], n_threads=cores)
         times.append(time.perf_counter() - t0)
@@ -194,7 +195,8 @@ def cpu_baseline(w_name: str, x: np.ndarray, cb: np.ndarray, budget_s: float = 1
     one_core = rows1 / max(time.perf_counter() - t0, 1e-9)
     return {"value": rows / med, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {rows} of {w.n} sub-vectors of {w_name} (codebook 0), "
-                      f"median of 3 runs, {cores} threads", "seconds": med,
+                      f"median of {runs} runs ({sum(times):.1f} s in all), {cores} threads",
+            "seconds": med,
             "value_1_core": one_core, "cpu_model": cpu_model()}
 
 
