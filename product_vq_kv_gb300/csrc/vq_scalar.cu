@@ -40,8 +40,9 @@ vq_status launch_scan_nc(const void *x, int64_t n, const float *c, int32_t n_c, 
                          cudaStream_t st)
 {
     const size_t smem = NC == 0 ? vqs::hadamard_smem(n_c) : 0;
-    vqs::scalar_scan<T, NC><<<(unsigned)stream_blocks(n, 8), kThreads, smem, st>>>(
-        static_cast<const T *>(x), n, c, n_c, out);
+    const bool vec = (uintptr_t)x % 16 == 0 && (uintptr_t)out % 8 == 0;
+    vqs::scalar_scan<T, NC><<<(unsigned)stream_blocks((n + 7) / 8, 8), kThreads, smem, st>>>(
+        static_cast<const T *>(x), n, c, n_c, vec, out);
     return launched();
 }
 

@@ -253,13 +253,15 @@ __host__ __device__ inline size_t hadamard_smem(int n_c) { return (size_t)n_c * 
 // The scalar quantize of any input type without a table: codebooks of 2, 4,
 // 8 or 16 entries (NC) scanned from registers, others (NC == 0) through the
 // block's sorted view, every element falling back to the scan of the rule
-// where the view cannot decide.  A persistent grid strides over the
-// elements.  Launch: any grid of 256-thread blocks; dynamic shared memory
+// where the view cannot decide.  A persistent grid strides over 8-element
+// units (16-byte loads, two units in flight per thread, 8-byte stores) when
+// `vec` (x 16-byte and out 8-byte aligned), then over the remaining elements
+// one by one.  Launch: any grid of 256-thread blocks; dynamic shared memory
 // hadamard_smem(n_c) when NC == 0, else 0.
 template <typename T, int NC>
 __global__ void __launch_bounds__(256)
     scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
-                int32_t n_c, uint8_t *__restrict__ out);
+                int32_t n_c, bool vec, uint8_t *__restrict__ out);
 
 
 
@@ -302,72 +304,85 @@ __global__ void __launch_bounds__(256)
     const int sub = lane / lpr;      // row within the warp
     const int l = lane - sub * lpr;  // lane within the row
     const int d = lpr * E;
+    // R row groups per warp step, all loaded before any is rotated, so that
+    // R loads per lane are in flight
+    constexpr int R = E <= 8 ? 4 : E == 16 ? 2 : 1;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     float dg[E];
 #pragma unroll
     for (int j = 0; j < E; ++j) dg[j] = __ldg(diag + l * E + j);
     for (int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-         warp * rows_per_warp < n_rows; warp += warps) {  // warp-uniform
-        const int64_t row = warp * rows_per_warp + sub;
-        const bool live = row < n_rows;
-        float v[E];
-        if (live) {
-            load_run<T, E>(x + (size_t)row * d + (size_t)l * E, v);
-        } else {
+         warp * R * rows_per_warp < n_rows; warp += warps) {  // warp-uniform
+        float v[R][E];
 #pragma unroll
-            for (int j = 0; j < E; ++j) v[j] = 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < E; ++j) v[j] = __fmul_rn(v[j], dg[j]);
-        // strides below E: pairs inside the lane's registers
-#pragma unroll
-        for (int s = 1; s < E; s <<= 1) {
-#pragma unroll
-            for (int j = 0; j < E; ++j) {
-                if ((j & s) == 0) {
-                    const float a = v[j], b = v[j + s];
-                    v[j] = __fadd_rn(a, b);
-                    v[j + s] = __fsub_rn(a, b);
-                }
-            }
-        }
-        // strides E .. D/2: the partner element sits in lane l ^ (s / E)
-        for (int ls = 1; ls < lpr; ls <<= 1) {
-            const bool upper = (l & ls) != 0;
-#pragma unroll
-            for (int j = 0; j < E; ++j) {
-                const float p = __shfl_xor_sync(0xffffffffu, v[j], ls);
-                v[j] = upper ? __fsub_rn(p, v[j]) : __fadd_rn(v[j], p);
-            }
-        }
-        if (!live) continue;
-#pragma unroll
-        for (int j = 0; j < E; ++j) v[j] = __fmul_rn(v[j], scale);
-        if constexpr (QUANT) {
-            uint32_t code[E];
-#pragma unroll
-            for (int j = 0; j < E; ++j) {
-                if constexpr (NC > 0) {
-                    code[j] = nearest_reg<NC>(v[j], creg);
-                } else {
-                    const int k = sorted_ok ? nearest_sorted(v[j], scb) : -1;
-                    code[j] = k >= 0 ? (uint32_t)k : nearest(v[j], hq_cb, n_c);
-                }
-            }
-            uint8_t *o = idx + (size_t)row * d + (size_t)l * E;
-            if constexpr (E % 4 == 0) {
-#pragma unroll
-                for (int j = 0; j < E; j += 4)
-                    *reinterpret_cast<uint32_t *>(o + j) =
-                        code[j] | code[j + 1] << 8 | code[j + 2] << 16 | code[j + 3] << 24;
+        for (int r = 0; r < R; ++r) {
+            const int64_t row = (warp * R + r) * rows_per_warp + sub;
+            if (row < n_rows) {
+                load_run<T, E>(x + (size_t)row * d + (size_t)l * E, v[r]);
             } else {
 #pragma unroll
-                for (int j = 0; j < E; ++j) o[j] = (uint8_t)code[j];
+                for (int j = 0; j < E; ++j) v[r][j] = 0.f;
             }
-        } else {
-            float *o = y + (size_t)row * d + (size_t)l * E;
+        }
 #pragma unroll
-            for (int j = 0; j < E; ++j) o[j] = v[j];
+        for (int r = 0; r < R; ++r) {
+            const int64_t row = (warp * R + r) * rows_per_warp + sub;
+            float *w = v[r];
+#pragma unroll
+            for (int j = 0; j < E; ++j) w[j] = __fmul_rn(w[j], dg[j]);
+            // strides below E: pairs inside the lane's registers
+#pragma unroll
+            for (int s = 1; s < E; s <<= 1) {
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    if ((j & s) == 0) {
+                        const float a = w[j], b = w[j + s];
+                        w[j] = __fadd_rn(a, b);
+                        w[j + s] = __fsub_rn(a, b);
+                    }
+                }
+            }
+            // strides E .. D/2: the partner element sits in lane l ^ (s / E)
+            // (lower lane: own + partner; upper lane: partner - own, as
+            // fma(-1, own, partner): the product is exact, so the one rounding
+            // is that of the sum, bit for bit the add or subtract)
+            for (int ls = 1; ls < lpr; ls <<= 1) {
+                const float sg = (l & ls) != 0 ? -1.0f : 1.0f;
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const float q = __shfl_xor_sync(0xffffffffu, w[j], ls);
+                    w[j] = __fmaf_rn(sg, w[j], q);
+                }
+            }
+            if (row >= n_rows) continue;
+#pragma unroll
+            for (int j = 0; j < E; ++j) w[j] = __fmul_rn(w[j], scale);
+            if constexpr (QUANT) {
+                uint32_t code[E];
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    if constexpr (NC > 0) {
+                        code[j] = nearest_reg<NC>(w[j], creg);
+                    } else {
+                        const int k = sorted_ok ? nearest_sorted(w[j], scb) : -1;
+                        code[j] = k >= 0 ? (uint32_t)k : nearest(w[j], hq_cb, n_c);
+                    }
+                }
+                uint8_t *o = idx + (size_t)row * d + (size_t)l * E;
+                if constexpr (E % 4 == 0) {
+#pragma unroll
+                    for (int j = 0; j < E; j += 4)
+                        *reinterpret_cast<uint32_t *>(o + j) =
+                            code[j] | code[j + 1] << 8 | code[j + 2] << 16 | code[j + 3] << 24;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < E; ++j) o[j] = (uint8_t)code[j];
+                }
+            } else {
+                float *o = y + (size_t)row * d + (size_t)l * E;
+#pragma unroll
+                for (int j = 0; j < E; ++j) o[j] = w[j];
+            }
         }
     }
 }
@@ -397,10 +412,26 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Eight consecutive elements (16-byte aligned) as fp32.
+template <typename T>
+__device__ __forceinline__ void load8(const T *p, float (&v)[8])
+{
+    if constexpr (sizeof(T) == 4) {
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+        const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+        v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+    } else {
+        const uint4 q = __ldcs(reinterpret_cast<const uint4 *>(p));
+        const T *t = reinterpret_cast<const T *>(&q);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = widen_elem(t[i]);
+    }
+}
+
 template <typename T, int NC>
 __global__ void __launch_bounds__(256)
     scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
-                int32_t n_c, uint8_t *__restrict__ out)
+                int32_t n_c, bool vec, uint8_t *__restrict__ out)
 {
     extern __shared__ float ss_sm[];
     float creg[NC > 0 ? NC : 1];
@@ -427,18 +458,43 @@ __global__ void __launch_bounds__(256)
             scb.top = top;
         }
     }
-    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += nthreads) {
-        const float v = widen_elem(x[e]);
-        uint32_t k;
+    auto quant = [&](float v) -> uint32_t {
         if constexpr (NC > 0) {
-            k = nearest_reg<NC>(v, creg);
+            return nearest_reg<NC>(v, creg);
         } else {
-            const int ks = sorted_ok ? nearest_sorted(v, scb) : -1;
-            k = ks >= 0 ? (uint32_t)ks : nearest(v, ss_sm, n_c);
+            const int k = sorted_ok ? nearest_sorted(v, scb) : -1;
+            return k >= 0 ? (uint32_t)k : nearest(v, ss_sm, n_c);
         }
-        out[e] = (uint8_t)k;
+    };
+    auto quant8 = [&](const float (&v)[8]) -> uint2 {
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo |= quant(v[i]) << (8 * i);
+            hi |= quant(v[i + 4]) << (8 * i);
+        }
+        return make_uint2(lo, hi);
+    };
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    // 8-element units (x 16-byte and out 8-byte aligned when `vec`), two
+    // units' loads in flight per thread; then the remaining elements
+    const int64_t units = vec ? n / 8 : 0;
+    constexpr int U = 2;
+    int64_t u = tid;
+    for (; u + (U - 1) * nthreads < units; u += U * nthreads) {
+        float v[U][8];
+#pragma unroll
+        for (int k = 0; k < U; ++k) load8<T>(x + (u + k * nthreads) * 8, v[k]);
+#pragma unroll
+        for (int k = 0; k < U; ++k) __stcs(reinterpret_cast<uint2 *>(out) + u + k * nthreads, quant8(v[k]));
     }
+    for (; u < units; u += nthreads) {
+        float v[8];
+        load8<T>(x + u * 8, v);
+        __stcs(reinterpret_cast<uint2 *>(out) + u, quant8(v));
+    }
+    for (int64_t e = units * 8 + tid; e < n; e += nthreads) out[e] = (uint8_t)quant(widen_elem(x[e]));
 }
 
 }  // namespace vqs

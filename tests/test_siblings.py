@@ -174,3 +174,66 @@ def test_scalar_scan_paths(vq, oracle_mod, n_c, kind):
         c[n_c // 2] = np.inf
     got = vq.vq_scalar_quantize(torch.from_numpy(x).cuda(), torch.from_numpy(c).cuda()).cpu().numpy()
     assert np.array_equal(got.astype(np.uint32), oracle_mod.scalar_quantize(x, c))
+
+
+def value_sweep_keys(seed: int) -> np.ndarray:
+    """Every fp32 value whose low 16 bits are all 0, all 1 or random: every
+    sign, exponent and top-7-bit mantissa prefix at both ends and inside,
+    NaN, inf and subnormals included."""
+    rng = np.random.default_rng(seed)
+    top = np.arange(65536, dtype=np.uint32) << 16
+    low = rng.integers(0, 65536, 65536, dtype=np.uint32)
+    return np.concatenate([top, top | 0xFFFF, top | low]).view(np.float32)
+
+
+@pytest.mark.parametrize("case", ["normal_3", "normal_5", "normal_100", "normal_256", "scaled_tiny",
+                                  "scaled_huge", "negative_only", "close_pairs", "duplicates",
+                                  "subnormal", "powers_of_two"])
+def test_scalar_scan_value_sweep(vq, oracle_mod, case):
+    """fp32 keys over the whole float range against the rule, for codebooks
+    of several sizes, scales and shapes (register scan and sorted-view search
+    with its fallback)."""
+    rng = np.random.default_rng(sum(map(ord, case)))
+    if case.startswith("normal_"):
+        c = rng.standard_normal(int(case.split("_")[1])).astype(np.float32)
+    elif case == "scaled_tiny":
+        c = (rng.standard_normal(12) * 1e-30).astype(np.float32)
+    elif case == "scaled_huge":
+        c = (rng.standard_normal(12) * 1e30).astype(np.float32)
+    elif case == "negative_only":
+        c = -np.abs(rng.standard_normal(9)).astype(np.float32) - 1.0
+    elif case == "close_pairs":  # centroids closer than 2^-10 relative
+        base = rng.standard_normal(6).astype(np.float32)
+        c = np.concatenate([base, base * np.float32(1 + 2 ** -12), base * np.float32(1 - 2 ** -10)])
+    elif case == "duplicates":
+        c = rng.standard_normal(20).astype(np.float32)
+        c[[2, 7, 11]] = c[15]
+        c[[0, 19]] = c[4]
+    elif case == "subnormal":
+        c = np.array([1e-45, -3e-45, 2e-40, 0.0, -1e-39, 5e-42], dtype=np.float32)
+    else:
+        c = np.float32(2.0) ** np.arange(-8, 9, 2, dtype=np.float32)
+        c = np.concatenate([c, -c])
+    x = value_sweep_keys(len(case))
+    got = vq.vq_scalar_quantize(torch.from_numpy(x).cuda(), torch.from_numpy(c).cuda()).cpu().numpy()
+    assert np.array_equal(got.astype(np.uint32), oracle_mod.scalar_quantize(x, c))
+
+
+@pytest.mark.parametrize("n_c", [8, 16, 256])
+def test_hadamard_quantize_value_sweep(vq, oracle_mod, n_c):
+    """The fused quantize on rotated rows spread over the float range: the
+    rotation (diag = 1) maps v * sqrt(D) * e_0 to the constant row v, plus a
+    little noise from the other columns."""
+    rng = np.random.default_rng(n_c)
+    c = np.sort(rng.standard_normal(n_c).astype(np.float32))
+    dim = 32
+    vals = value_sweep_keys(n_c)
+    vals = vals[np.isfinite(vals) & (np.abs(vals) < 1e30)]
+    x = np.zeros((vals.size, dim), dtype=np.float32)
+    x[:, 0] = vals * np.float32(np.sqrt(dim))  # y = H e_0 * v: every element equal to v (up to rounding)
+    x[:, 1:] = rng.standard_normal((vals.size, dim - 1)).astype(np.float32) * np.float32(1e-3)
+    diag = np.ones(dim, dtype=np.float32)
+    want = oracle_mod.hadamard_quantize(x, diag, c)
+    got = vq.vq_hadamard_quantize(torch.from_numpy(x).cuda(), torch.from_numpy(diag).cuda(),
+                                  torch.from_numpy(c).cuda()).cpu().numpy()
+    assert np.array_equal(got.astype(np.uint32), want)
