@@ -163,27 +163,32 @@ size_t fast_smem(int32_t n_centroids)
     return vqk::CbLayout<SUB, kGroupCentroids>::bytes(n_centroids);
 }
 
-template <int SUB>
+// With SMOOTH the A operand holds the three tf32 pieces of each divided row.
+template <int SUB, bool SMOOTH = false>
 size_t tc_smem(int32_t n_centroids)
 {
     using C = TcConfig<SUB>;
-    return vqk::TcLayout<SUB, C::kCols, C::kGroup>::bytes(n_centroids);
+    return vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH ? 3 : 1>::bytes(n_centroids);
 }
 
-template <typename T, int SUB, typename OutT = uint32_t>
+template <typename T, int SUB, typename OutT = uint32_t, bool SMOOTH = false>
 auto tc_kernel()
 {
     using C = TcConfig<SUB>;
-    return vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks, OutT>;
+    return vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks, OutT, SMOOTH>;
 }
 
 // Resident tensor-core CTAs on the device: the register budget of the launch
-// bounds admits kMinBlocks per SM, and the shared-memory request caps them at
-// the tensor-memory budget (512 / kCols), which is not smaller.
-int tc_slots(int sub_dim)
+// bounds admits kMinBlocks per SM, the tensor memory 512 / kCols, and the
+// shared memory of an SM (228 KiB, 1 KiB reserved per block) what `smem`
+// allows.
+int tc_slots(int sub_dim, size_t smem)
 {
     const int sms = device_sms();
-    const int per_sm = sub_dim == 4 ? TcConfig<4>::kMinBlocks : TcConfig<8>::kMinBlocks;
+    int per_sm = sub_dim == 4 ? TcConfig<4>::kMinBlocks : TcConfig<8>::kMinBlocks;
+    const int by_smem = (int)((size_t)228 * 1024 / (smem + 1024));
+    if (by_smem < per_sm) per_sm = by_smem;
+    if (per_sm < 1) per_sm = 1;
     return (sms > 0 ? sms : 152) * per_sm;
 }
 
@@ -216,7 +221,7 @@ Plan make_plan(const Args &a)
         if (p.smem <= kMaxFastSmem) p.kind = kBrute;
     }
     if (p.kind == kTc) {
-        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim), &p.tiles_per_group, &p.tc_tiles);
+        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, p.smem), &p.tiles_per_group, &p.tc_tiles);
         p.blocks = a.n_groups * p.tiles_per_group;
         p.threads = 128;
     } else if (p.kind != kGeneral) {
@@ -233,16 +238,17 @@ Plan make_plan(const Args &a)
     return p;
 }
 
-template <typename T, int SUB, typename OutT>
+template <typename T, int SUB, typename OutT, bool SMOOTH = false>
 vq_status launch_tc(const Args &a, const Plan &p)
 {
-    auto kernel = tc_kernel<T, SUB, OutT>();
+    auto kernel = tc_kernel<T, SUB, OutT, SMOOTH>();
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
         return VQ_ERR_CUDA;
     kernel<<<(unsigned)p.blocks, 128, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
-        p.tiles_per_group, p.tc_tiles, 1.0f, static_cast<OutT *>(a.out));
+        p.tiles_per_group, p.tc_tiles, 1.0f, static_cast<OutT *>(a.out), a.smooth,
+        SMOOTH ? (int32_t)(a.head_dim / a.sub_dim) : 1);
     return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
 }
 
@@ -327,6 +333,13 @@ vq_status run(const Args &a)
 template <typename OutT, int SUB>
 vq_status launch_smooth_typed(const Args &a, const Plan &p)
 {
+    if (p.kind == kTc) {
+        switch (a.dtype) {
+        case VQ_F16: return launch_tc<__half, SUB, OutT, true>(a, p);
+        case VQ_BF16: return launch_tc<__nv_bfloat16, SUB, OutT, true>(a, p);
+        default: return VQ_ERR_INTERNAL;
+        }
+    }
     switch (a.dtype) {
     case VQ_F16: return launch_filter<__half, SUB, OutT, true>(a, p);
     case VQ_BF16: return launch_filter<__nv_bfloat16, SUB, OutT, true>(a, p);
@@ -335,8 +348,10 @@ vq_status launch_smooth_typed(const Args &a, const Plan &p)
     return VQ_ERR_INTERNAL;
 }
 
-// Encode with per-channel smoothing: always the filter kernel, whose bound
-// holds for any fp32 row (the divided rows are not fp16 values).
+// Encode with per-channel smoothing.  fp16 and bf16 codebooks of 64..256
+// centroids take the tensor-core kernel with the divided rows split into
+// three exact tf32 pieces; others the filter kernel, whose bound holds for
+// any fp32 row.
 vq_status run_smooth(const Args &a)
 {
     if (a.head_dim < a.sub_dim || a.sub_dim < 1 || a.head_dim % a.sub_dim) return VQ_ERR_INVALID_ARG;
@@ -349,13 +364,21 @@ vq_status run_smooth(const Args &a)
     const size_t row_bytes = (size_t)a.sub_dim * elem_size(a.dtype);
     if ((uintptr_t)a.x % (row_bytes < 16 ? row_bytes : 16)) return VQ_ERR_UNSUPPORTED;
     Plan p{};
-    p.kind = kFilter;
-    p.smem = a.sub_dim == 4 ? filter_smem<4>(a.n_centroids) : filter_smem<8>(a.n_centroids);
-    if (p.smem > kMaxFastSmem) return VQ_ERR_UNSUPPORTED;
-    const int64_t tile = (int64_t)kFThreads * kFRows;
-    p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
-    p.blocks = a.n_groups * p.tiles_per_group;
-    p.threads = kFThreads;
+    if (a.dtype != VQ_F32 && a.n_centroids >= kFilterMinCentroids && a.n_centroids <= 256) {
+        p.kind = kTc;
+        p.smem = a.sub_dim == 4 ? tc_smem<4, true>(a.n_centroids) : tc_smem<8, true>(a.n_centroids);
+        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, p.smem), &p.tiles_per_group, &p.tc_tiles);
+        p.blocks = a.n_groups * p.tiles_per_group;
+        p.threads = 128;
+    } else {
+        p.kind = kFilter;
+        p.smem = a.sub_dim == 4 ? filter_smem<4>(a.n_centroids) : filter_smem<8>(a.n_centroids);
+        if (p.smem > kMaxFastSmem) return VQ_ERR_UNSUPPORTED;
+        const int64_t tile = (int64_t)kFThreads * kFRows;
+        p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
+        p.blocks = a.n_groups * p.tiles_per_group;
+        p.threads = kFThreads;
+    }
     if (p.blocks > 0x7fffffffLL) return VQ_ERR_UNSUPPORTED;
     if (a.out_bytes == 1)
         return a.sub_dim == 4 ? launch_smooth_typed<uint8_t, 4>(a, p) : launch_smooth_typed<uint8_t, 8>(a, p);

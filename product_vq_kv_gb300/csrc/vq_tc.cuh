@@ -20,6 +20,19 @@
 // follow as in vq_filter.cuh.  fp32 inputs are not exact in tf32 and use
 // encode_filter instead.
 //
+// With SMOOTH, each row is first divided by its per-channel smooth factors
+// (fp32, rounded to nearest), and the divided row -- an fp32 value, not
+// exact in tf32 -- is what is encoded.  It is split exactly into three tf32
+// pieces, x_i = hi_i + mid_i + lo_i (hi keeps the top 11 significant bits,
+// mid the next 11 of the exact remainder, lo the last 2), and three
+// accumulating MMAs multiply A_hi = [hi, 1, 1, 1, 0 ...], A_mid = [mid, 0 ...]
+// and A_lo = [lo, 0 ...] by the same B, so every product is still exact.  The
+// sum of the terms' magnitudes grows to at most (1 + 2^-9) times its bound
+// above (|hi| + |mid| + |lo| <= (1 + 2^-10 + 2^-20) |x|), and the kernel uses
+// B(x) = (2 (1 + 2^-9) eps_tc + 2 gamma_SUB) (C2 + sum_i |x_i| A_i); the
+// accumulation now spans 3 K terms, 24 or 48, whose truncating fp32 error
+// (at most 48 x 2^-23 = 2^-17.4 of the magnitudes) eps_tc still covers.
+//
 // The accumulator of a tile is a 128-lane x n_pad-column fp32 block of tensor
 // memory, so thread t of the block owns row t of the tile: it reads its own
 // row's scores (tcgen05.ld) and reduces them without any exchange.
@@ -35,7 +48,9 @@
 // at the tensor-memory budget: NCOL columns each); grid.x = n_groups *
 // blocks_per_group, each block encoding tiles_per_block consecutive 128-row
 // tiles of one group.  Requirements: T is __half or __nv_bfloat16, 64 <= n_centroids <=
-// 256, x aligned to SUB * sizeof(T) bytes.
+// 256, x aligned to SUB * sizeof(T) bytes.  With SMOOTH: `smooth`
+// [n_groups][smooth_ns * SUB] fp32 factors, row m of a group holding channels
+// (m % smooth_ns) * SUB + i; TcLayout's A holds three pieces (NA = 3).
 #pragma once
 
 #include "vq_filter.cuh"
@@ -141,7 +156,7 @@ __device__ __forceinline__ float tf32_trunc(float v) { return __uint_as_float(__
 
 // ------------------------------------------------------------------ layout
 
-template <int SUB, int NCOL, int GC>
+template <int SUB, int NCOL, int GC, int NA = 1>
 struct TcLayout {
     static constexpr int kK = SUB == 4 ? 8 : 16;       // MMA K (tf32 elements), 8 per instruction
     static constexpr int kRowBytes = kK * 4;
@@ -154,8 +169,9 @@ struct TcLayout {
     __host__ __device__ static int padded(int nc) { return (nc + 31) / 32 * 32; }
     __host__ __device__ static int groups(int nc) { return padded(nc) / kGC; }
     // byte offsets
+    static constexpr size_t kABytes = (size_t)128 * kRowBytes;  // one A piece
     __host__ __device__ static size_t a_off() { return 0; }
-    __host__ __device__ static size_t b_off() { return (size_t)128 * kRowBytes; }
+    __host__ __device__ static size_t b_off() { return NA * kABytes; }
     __host__ __device__ static size_t x_off(int nc) { return b_off() + (size_t)256 * kRowBytes; }
     __host__ __device__ static size_t misc_off(int nc)
     {
@@ -173,16 +189,18 @@ struct TcLayout {
 
 // ------------------------------------------------------------------ kernel
 
-template <typename T, int SUB, int NCOL, int GC, int MINB, typename OutT = uint32_t>
+template <typename T, int SUB, int NCOL, int GC, int MINB, typename OutT = uint32_t,
+          bool SMOOTH = false>
 __global__ void __launch_bounds__(128, MINB)
     encode_tc(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
               int32_t n_centroids, int64_t blocks_per_group, int32_t tiles_per_block, float one,
-              OutT *__restrict__ out)
+              OutT *__restrict__ out, const float *__restrict__ smooth, int32_t smooth_ns)
 {
     static_assert(SUB == 4 || SUB == 8, "sub_dim 4 or 8");
     static_assert(NCOL == 32 || NCOL == 64 || NCOL == 128 || NCOL == 256, "tensor-memory columns");
     static_assert(GC == 8 || GC == 16, "centroid group size");
-    using L = TcLayout<SUB, NCOL, GC>;
+    constexpr int kNA = SMOOTH ? 3 : 1;  // A pieces
+    using L = TcLayout<SUB, NCOL, GC, kNA>;
     constexpr int kK = L::kK;
     constexpr int kKB = kK / 4;  // 16-byte core-matrix columns per row
     constexpr int kGC = L::kGC;
@@ -211,6 +229,7 @@ __global__ void __launch_bounds__(128, MINB)
     const T *__restrict__ cb = codebooks + (size_t)g * (size_t)n_centroids * SUB;
     const T *__restrict__ xg = x + (size_t)g * (size_t)n_per_group * SUB;
     OutT *__restrict__ og = out + (size_t)g * (size_t)n_per_group;
+    const float *__restrict__ sg = SMOOTH ? smooth + (size_t)g * (size_t)smooth_ns * SUB : nullptr;
     const int64_t row_base = blk * (int64_t)tiles_per_block * 128;
 
     // ---- set-up: maxima, barrier, tensor memory, constant part of A
@@ -227,11 +246,16 @@ __global__ void __launch_bounds__(128, MINB)
     }
     {
         // A row `tid`: columns SUB.. of the row are the constant [1, 1, 1, 0 ...]
-        float *arow = sa;
+        // in the first piece and zero in the others
 #pragma unroll
-        for (int kb = SUB / 4; kb < kKB; ++kb) {
-            const float4 v = kb == SUB / 4 ? make_float4(1.f, 1.f, 1.f, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4 *>(arow + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) = v;
+        for (int pc = 0; pc < kNA; ++pc) {
+            float *arow = sa + pc * (L::kABytes / 4);
+#pragma unroll
+            for (int kb = SUB / 4; kb < kKB; ++kb) {
+                const float4 v = kb == SUB / 4 && pc == 0 ? make_float4(1.f, 1.f, 1.f, 0.f)
+                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(arow + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) = v;
+            }
         }
     }
     __syncthreads();
@@ -286,7 +310,8 @@ __global__ void __launch_bounds__(128, MINB)
     float amax[SUB];
 #pragma unroll
     for (int i = 0; i < SUB; ++i) amax[i] = __uint_as_float(smax[1 + i]);
-    const float kBtc = 2.0f * 1.5258789e-5f + 2.0f * gamma_u(SUB);  // 2 eps_tc + 2 gamma_SUB
+    // 2 eps_tc + 2 gamma_SUB; with the three-piece split, 2 (1 + 2^-9) eps_tc
+    const float kBtc = (SMOOTH ? 2.00390625f : 2.0f) * 1.5258789e-5f + 2.0f * gamma_u(SUB);
     const float kD = 4.0f * gamma_u(SUB + 2);
     const float kTiny = 7.8886091e-31f;  // 2^-100
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
@@ -298,6 +323,7 @@ __global__ void __launch_bounds__(128, MINB)
     auto load_x = [&](int64_t row, float (&v)[SUB]) {
         if (row < n_per_group) {
             load_row<T, SUB>(xg + (size_t)row * SUB, v);
+            smooth_row<SUB, SMOOTH>(v, sg, row, smooth_ns);
         } else {
 #pragma unroll
             for (int i = 0; i < SUB; ++i) v[i] = 0.f;
@@ -313,10 +339,28 @@ __global__ void __launch_bounds__(128, MINB)
         if (row_base + (int64_t)tile * 128 >= n_per_group) break;  // block-uniform
 
         // A rows of this tile (the MMA of the previous tile has completed)
+        if constexpr (SMOOTH) {
+            float pc3[3][SUB];
 #pragma unroll
-        for (int kb = 0; kb < SUB / 4; ++kb)
-            *reinterpret_cast<float4 *>(sa + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) =
-                make_float4(xr[4 * kb], xr[4 * kb + 1], xr[4 * kb + 2], xr[4 * kb + 3]);
+            for (int i = 0; i < SUB; ++i) {
+                pc3[0][i] = tf32_trunc(xr[i]);
+                const float r1 = xr[i] - pc3[0][i];  // exact: the low bits of xr[i]
+                pc3[1][i] = tf32_trunc(r1);
+                pc3[2][i] = r1 - pc3[1][i];          // exact, at most two bits
+            }
+#pragma unroll
+            for (int pc = 0; pc < 3; ++pc)
+#pragma unroll
+                for (int kb = 0; kb < SUB / 4; ++kb)
+                    *reinterpret_cast<float4 *>(sa + pc * (L::kABytes / 4) +
+                                                ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) =
+                        make_float4(pc3[pc][4 * kb], pc3[pc][4 * kb + 1], pc3[pc][4 * kb + 2], pc3[pc][4 * kb + 3]);
+        } else {
+#pragma unroll
+            for (int kb = 0; kb < SUB / 4; ++kb)
+                *reinterpret_cast<float4 *>(sa + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) =
+                    make_float4(xr[4 * kb], xr[4 * kb + 1], xr[4 * kb + 2], xr[4 * kb + 3]);
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         __syncthreads();
@@ -333,10 +377,14 @@ __global__ void __launch_bounds__(128, MINB)
             if (tid == 0) {
                 const uint32_t idesc = umma_idesc_tf32((uint32_t)ncols);
 #pragma unroll
-                for (int kstep = 0; kstep < kK / 8; ++kstep) {
-                    const uint64_t ad = umma_smem_desc(sa_addr + kstep * 256, 128, kSbo);
-                    const uint64_t bd = umma_smem_desc(sb_addr + (c0 >> 3) * kSbo + kstep * 256, 128, kSbo);
-                    umma_tf32(tmem, ad, bd, idesc, kstep > 0);
+                for (int pc = 0; pc < kNA; ++pc) {
+#pragma unroll
+                    for (int kstep = 0; kstep < kK / 8; ++kstep) {
+                        const uint64_t ad =
+                            umma_smem_desc(sa_addr + pc * (uint32_t)L::kABytes + kstep * 256, 128, kSbo);
+                        const uint64_t bd = umma_smem_desc(sb_addr + (c0 >> 3) * kSbo + kstep * 256, 128, kSbo);
+                        umma_tf32(tmem, ad, bd, idesc, pc > 0 || kstep > 0);
+                    }
                 }
                 umma_commit(bar);
             }
@@ -454,6 +502,7 @@ __global__ void __launch_bounds__(128, MINB)
             float xq[SUB];
 #pragma unroll
             for (int i = 0; i < SUB; ++i) xq[i] = widen(xg[(size_t)qrow * SUB + i]);
+            smooth_row<SUB, SMOOTH>(xq, sg, qrow, smooth_ns);
             float best = __int_as_float(0x7f800000);
             uint32_t bi = kQueued;
             for (int c = lane; c < n_centroids; c += 32) {

@@ -104,3 +104,20 @@ def test_smooth_empty_and_errors(vq):
     x = torch.zeros((2, 10, 4), dtype=torch.float16, device="cuda")  # 10 rows, 4 per key
     with pytest.raises(vq.VQError):
         vq.vq_encode_grouped_smooth(x, s, cb, 16)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("sub,head_dim", [(4, 256), (8, 128)])
+def test_smooth_tensor_core_extreme_factors(vq, oracle_mod, dtype, sub, head_dim):
+    """The tensor-core path (16-bit keys, 64..256 centroids): factors whose
+    quotients are subnormal, huge, infinite or NaN (those rows are queued for
+    the exact scan), and factors like 1/3 or 1/pi whose quotients use every
+    bit of fp32, so all three tf32 pieces of the split are nonzero."""
+    ns = head_dim // sub
+    x, smooth, cb = case(11 + sub, dtype, 2, ns * 300, 200, sub, head_dim)
+    smooth[0, :12] = [1e-30, 1e30, 0.0, -2.0, 1e-38, 3e38, -0.0, 1e-45, 3.0, 7.0, 1 / 3, 1e38]
+    smooth[1] = np.float32(1 / np.pi) * (1 + np.arange(head_dim, dtype=np.float32) / 7)
+    bf = dtype == "bf16"
+    want = oracle_mod.encode_smooth(x, smooth, cb, head_dim, bf16=bf, n_threads=THREADS)
+    assert np.array_equal(run(vq, x, smooth, cb, head_dim, bf, 4), want)
+    assert np.array_equal(run(vq, x, smooth, cb, head_dim, bf, 1), want)
