@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr size_t kTableBytes = 65536;
+constexpr int kLookupThreads = 1024;
 
 bool dtype_ok(vq_dtype d) { return d == VQ_F16 || d == VQ_BF16 || d == VQ_F32; }
 size_t elem_size(vq_dtype d) { return d == VQ_F32 ? 4 : 2; }
@@ -166,17 +167,18 @@ vq_status vq_scalar_quantize(const void *x, vq_dtype dtype, int64_t n, const flo
             centroids, n_centroids, dtype == VQ_BF16, tab);
         if (launched() != VQ_OK) return VQ_ERR_CUDA;
         const bool vec = (uintptr_t)x % 16 == 0 && (uintptr_t)out % 8 == 0;
-        // each block stages the 64 KiB table: give it at least 64 Ki elements
+        // one block of kLookupThreads per SM stages the 64 KiB table once;
+        // give each block at least 64 Ki elements
         int64_t blocks = (n + 65535) / 65536;
         const int sms = vqh_device_sms() > 0 ? vqh_device_sms() : 152;
-        if (blocks > 3LL * sms) blocks = 3LL * sms;
+        if (blocks > sms) blocks = sms;
         if (blocks < 1) blocks = 1;
         auto kp = vqs::scalar_lookup;
         if (cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTableBytes) !=
             cudaSuccess)
             return VQ_ERR_CUDA;
-        kp<<<(unsigned)blocks, kThreads, kTableBytes, st>>>(static_cast<const uint16_t *>(x), n, tab,
-                                                            vec, out);
+        kp<<<(unsigned)blocks, kLookupThreads, kTableBytes, st>>>(static_cast<const uint16_t *>(x), n,
+                                                                  tab, vec, out);
         return launched();
     }
     switch (dtype) {

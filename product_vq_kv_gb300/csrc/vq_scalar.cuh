@@ -82,10 +82,10 @@ __device__ __forceinline__ uint2 lookup8(const uint8_t *tab, uint4 v)
     return make_uint2(lo, hi);
 }
 
-// out[e] = table[x[e]].  Launch: any grid of 256-thread blocks, dynamic
-// shared memory 65536 bytes; grid-stride over 8-element units when `vec`
-// (x 16-byte and out 8-byte aligned), the remaining elements one by one.
-__global__ void __launch_bounds__(256)
+// out[e] = table[x[e]].  Launch: any grid of blocks of up to 1024 threads,
+// dynamic shared memory 65536 bytes; grid-stride over 8-element units when
+// `vec` (x 16-byte and out 8-byte aligned), the remaining elements one by one.
+__global__ void __launch_bounds__(1024)
     scalar_lookup(const uint16_t *__restrict__ x, int64_t n, const uint8_t *__restrict__ table,
                   bool vec, uint8_t *__restrict__ out)
 {

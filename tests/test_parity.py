@@ -101,6 +101,29 @@ def test_full_size_workload_sampled(vq, oracle_mod, name):
         assert_same(got[k, rows], want)
 
 
+@pytest.mark.parametrize("name", ["long_context", "grouped_adversarial"])
+def test_full_size_workload_every_row(vq, oracle_mod, name):
+    """Every row of the two largest workloads at full size (4.2 M and 33.5 M
+    sub-vectors, the benchmark's single grouped launch) against the oracle,
+    and the adversarial invariants on the whole cache: every exact copy of a
+    centroid maps to the lowest index holding that row."""
+    x, cb = workloads.generate(name)
+    got = gpu_encode(vq, x, cb)
+    assert_same(got, oracle_mod.encode(x, cb, n_threads=THREADS))
+    if name == "grouped_adversarial":
+        g, m, sub = x.shape
+        for k in range(0, g, 37):  # a spread of groups: exact-copy rows
+            rows = x[k].view(np.uint16).reshape(m, sub)
+            cbr = cb[k].view(np.uint16).reshape(-1, sub)
+            lut = {}
+            for c in range(cbr.shape[0] - 1, -1, -1):  # lowest index wins
+                lut[cbr[c].tobytes()] = c
+            hits = [(r, lut[rows[r].tobytes()]) for r in range(m) if rows[r].tobytes() in lut]
+            assert len(hits) >= 1000
+            for r, c in hits:
+                assert got[k, r] == c, (k, r, c, got[k, r])
+
+
 # ---------------------------------------------------------------- dtypes and shapes
 
 
