@@ -151,6 +151,28 @@ __device__ __forceinline__ float group_min(const uint32_t *u)
     return fminf(a, __uint_as_float(u[GC - 1]));
 }
 
+// Least of N values by a tree of three-input minima (NaN ignored unless all
+// are NaN, as min3).
+template <int N>
+__device__ __forceinline__ float tree_min_p(const float *w)
+{
+    if constexpr (N == 1) {
+        return w[0];
+    } else if constexpr (N == 2) {
+        return fminf(w[0], w[1]);
+    } else if constexpr (N == 3) {
+        return min3(w[0], w[1], w[2]);
+    } else {
+        constexpr int a = (N + 2) / 3, b = (N - a + 1) / 2, c = N - a - b;
+        return min3(tree_min_p<a>(w), tree_min_p<b>(w + a), tree_min_p<c>(w + a + b));
+    }
+}
+template <int N>
+__device__ __forceinline__ float tree_min(const float (&w)[N])
+{
+    return tree_min_p<N>(&w[0]);
+}
+
 // Keep the top 10 bits of an fp32 significand (the tf32 value, exactly).
 __device__ __forceinline__ float tf32_trunc(float v) { return __uint_as_float(__float_as_uint(v) & 0xffffe000u); }
 
@@ -223,7 +245,6 @@ __global__ void __launch_bounds__(128, MINB)
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int n_pad = L::padded(n_centroids);
-    const int n_groups_c = L::groups(n_centroids);
     const int64_t g = blockIdx.x / blocks_per_group;
     const int64_t blk = blockIdx.x - g * blocks_per_group;
     const T *__restrict__ cb = codebooks + (size_t)g * (size_t)n_centroids * SUB;
@@ -422,9 +443,7 @@ __global__ void __launch_bounds__(128, MINB)
         load_x(row + 128, xn);
 
         // ---- bound, candidate groups, exact re-evaluation
-        float m1 = gmin[0];
-#pragma unroll
-        for (int k = 1; k < kNG; ++k) m1 = fminf(m1, gmin[k]);
+        const float m1 = tree_min<kNG>(gmin);
         float sabs = 0.f, xx = 0.f;
 #pragma unroll
         for (int i = 0; i < SUB; ++i) {
@@ -436,9 +455,15 @@ __global__ void __launch_bounds__(128, MINB)
         const float dmax = fmaxf(0.f, xx + m1 + bnd);
         const float thr = m1 + (2.0f * bnd + kD * dmax + kTiny);
         const bool ok = base < 1e30f && dmax < 1e37f;
-        uint32_t mask = 0;
+        // candidate groups: gmin[k] <= thr exactly when fl(thr - gmin[k]) has a
+        // clear sign bit (rounding keeps the sign of the exact difference and
+        // gives +0 for equal operands); groups past the codebook hold +inf.
+        // The sign bits are gathered with one funnel shift per group.
+        uint32_t out_bits = 0;
 #pragma unroll
-        for (int k = 0; k < kNG; ++k) mask |= (k < n_groups_c && gmin[k] <= thr) ? (1u << k) : 0u;
+        for (int k = kNG - 1; k >= 0; --k)
+            out_bits = __funnelshift_l(__float_as_uint(__fsub_rn(thr, gmin[k])), out_bits, 1);
+        const uint32_t mask = ~out_bits & (kNG == 32 ? 0xffffffffu : (1u << kNG) - 1u);
         const int cnt = __popc(mask);
         const int ga = __ffs(mask) - 1;
         const int gb = cnt > 1 ? __ffs(mask & (mask - 1)) - 1 : -1;
