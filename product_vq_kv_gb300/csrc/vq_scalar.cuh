@@ -239,6 +239,107 @@ __device__ __forceinline__ uint32_t nearest_reg(float val, const float (&c)[NC])
     return best;
 }
 
+// Least of N values by a tree of three-input minima (NaN ignored unless all
+// are NaN).
+__device__ __forceinline__ float min3f(float a, float b, float c)
+{
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+template <int N>
+__device__ __forceinline__ float tree_min3(const float *w)
+{
+    if constexpr (N == 1) {
+        return w[0];
+    } else if constexpr (N == 2) {
+        return fminf(w[0], w[1]);
+    } else if constexpr (N == 3) {
+        return min3f(w[0], w[1], w[2]);
+    } else {
+        constexpr int a = (N + 2) / 3, b = (N - a + 1) / 2, cnt = N - a - b;
+        return min3f(tree_min3<a>(w), tree_min3<b>(w + a), tree_min3<cnt>(w + a + b));
+    }
+}
+
+// Packed fp32 pairs (sm_100 f32x2): each lane rounds exactly as the scalar
+// instruction.
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mov.b64 pc, {%6, %7};\n\tfma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// The same rule for FINITE centroids in fewer instructions.  The NC
+// distances are computed in packed pairs (centroids held negated: val + (-c)
+// is the same rounding as val - c); their least comes from a min3 tree; the
+// lowest index holding it comes from the sign bits of fl(least - d_j),
+// gathered by funnel shifts.  least - d_j is fma(-1, d_j, least) with -1
+// passed in at run time (`neg_one` = (-1, -1)), one rounding of the
+// difference that no compiler can merge with the square.  With finite
+// centroids every distance is finite or +inf when the key is finite, so
+// fl(least - d_j) is +0 exactly for the distances equal to the least and
+// negative for the others: the first clear bit is the scan's strict-"<"
+// answer.  A NaN or infinite key makes every distance NaN or +inf; the rule
+// then answers 0, and so does this (every least - d_j is NaN: the index is 0
+// when all sign bits are clear, and clamped to 0 when none is).
+template <int NC>
+__device__ __forceinline__ uint32_t nearest_reg_finite(float val, const float2 (&cneg)[NC / 2], float2 neg_one)
+{
+    static_assert(NC % 2 == 0, "centroid pairs");
+    float2 d[NC / 2];
+    const float2 v2 = make_float2(val, val);
+#pragma unroll
+    for (int j = 0; j < NC / 2; ++j) {
+        const float2 t = add2_rn(v2, cneg[j]);
+        d[j] = mul2_rn(t, t);
+    }
+    const float least = tree_min3<NC>(reinterpret_cast<const float *>(d));
+    const float2 l2 = make_float2(least, least);
+    uint32_t above = 0;
+#pragma unroll
+    for (int j = NC / 2 - 1; j >= 0; --j) {
+        const float2 e = fma2_rn(neg_one, d[j], l2);
+        above = __funnelshift_l(__float_as_uint(e.y), above, 1);
+        above = __funnelshift_l(__float_as_uint(e.x), above, 1);
+    }
+    const uint32_t low = NC == 32 ? 0xffffffffu : (1u << NC) - 1u;
+    const int k = __ffs(~above & low) - 1;
+    return k < 0 ? 0u : (uint32_t)k;
+}
+
+// Whether all NC register centroids are finite (the finite rule applies).
+template <int NC>
+__device__ __forceinline__ bool all_finite(const float (&c)[NC])
+{
+    bool f = true;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) f = f && fabsf(c[j]) <= 3.402823466e38f;
+    return f;
+}
+
 // Randomised Hadamard rotation of rows of D = LPR * E elements, optionally
 // fused with the scalar quantize.  LPR = min(D, 32) lanes per row, 32 / LPR
 // rows per warp; lane l of a row holds elements l*E .. l*E + E - 1.  Warps
@@ -261,7 +362,7 @@ __host__ __device__ inline size_t hadamard_smem(int n_c) { return (size_t)n_c * 
 template <typename T, int NC>
 __global__ void __launch_bounds__(256)
     scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
-                int32_t n_c, bool vec, uint8_t *__restrict__ out);
+                int32_t n_c, bool vec, float neg_one, uint8_t *__restrict__ out);
 
 
 
@@ -269,17 +370,23 @@ template <typename T, int E, bool QUANT, int NC>
 __global__ void __launch_bounds__(256)
     hadamard_rows(const T *__restrict__ x, const float *__restrict__ diag, int64_t n_rows,
                   int32_t lanes_per_row, float scale, const float *__restrict__ centroids,
-                  int32_t n_c, float *__restrict__ y, uint8_t *__restrict__ idx)
+                  int32_t n_c, float neg_one, float *__restrict__ y, uint8_t *__restrict__ idx)
 {
     extern __shared__ float hq_sm[];
     SortedCb scb{nullptr, nullptr, 0, 0};
     const float *hq_cb = hq_sm;
     bool sorted_ok = false;
     float creg[NC > 0 ? NC : 1];
+    bool creg_finite = false;
+    float2 cneg[NC > 1 ? NC / 2 : 1];
     if constexpr (QUANT && NC > 0) {
 #pragma unroll
         for (int k = 0; k < NC; ++k) creg[k] = __ldg(centroids + k);
+        creg_finite = all_finite<NC>(creg);
+#pragma unroll
+        for (int k = 0; k < NC / 2; ++k) cneg[k] = make_float2(-creg[2 * k], -creg[2 * k + 1]);
     }
+    const float2 neg_one2 = make_float2(neg_one, neg_one);
     if constexpr (QUANT && NC == 0) {
         float *c = hq_sm;                                            // [n_c] as given
         float *u = c + n_c;                                          // [n_c] sorted distinct
@@ -362,7 +469,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
                     if constexpr (NC > 0) {
-                        code[j] = nearest_reg<NC>(w[j], creg);
+                        code[j] = creg_finite ? nearest_reg_finite<NC>(w[j], cneg, neg_one2)
+                                              : nearest_reg<NC>(w[j], creg);
                     } else {
                         const int k = sorted_ok ? nearest_sorted(w[j], scb) : -1;
                         code[j] = k >= 0 ? (uint32_t)k : nearest(w[j], hq_cb, n_c);
@@ -431,15 +539,21 @@ __device__ __forceinline__ void load8(const T *p, float (&v)[8])
 template <typename T, int NC>
 __global__ void __launch_bounds__(256)
     scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
-                int32_t n_c, bool vec, uint8_t *__restrict__ out)
+                int32_t n_c, bool vec, float neg_one, uint8_t *__restrict__ out)
 {
     extern __shared__ float ss_sm[];
     float creg[NC > 0 ? NC : 1];
     SortedCb scb{nullptr, nullptr, 0, 0};
     bool sorted_ok = false;
+    bool creg_finite = false;
+    float2 cneg[NC > 1 ? NC / 2 : 1];
+    const float2 neg_one2 = make_float2(neg_one, neg_one);
     if constexpr (NC > 0) {
 #pragma unroll
         for (int k = 0; k < NC; ++k) creg[k] = __ldg(centroids + k);
+        creg_finite = all_finite<NC>(creg);
+#pragma unroll
+        for (int k = 0; k < NC / 2; ++k) cneg[k] = make_float2(-creg[2 * k], -creg[2 * k + 1]);
     } else {
         float *c = ss_sm;
         float *u = c + n_c;
@@ -460,7 +574,7 @@ __global__ void __launch_bounds__(256)
     }
     auto quant = [&](float v) -> uint32_t {
         if constexpr (NC > 0) {
-            return nearest_reg<NC>(v, creg);
+            return creg_finite ? nearest_reg_finite<NC>(v, cneg, neg_one2) : nearest_reg<NC>(v, creg);
         } else {
             const int k = sorted_ok ? nearest_sorted(v, scb) : -1;
             return k >= 0 ? (uint32_t)k : nearest(v, ss_sm, n_c);
