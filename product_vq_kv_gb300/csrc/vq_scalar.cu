@@ -62,10 +62,9 @@ vq_status launch_scan(const void *x, int64_t n, const float *c, int32_t n_c, uin
 
 template <typename T, int E, bool QUANT, int NC>
 vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, int32_t dim,
-                             float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,
-                             cudaStream_t st)
+                             int lpr, float scale, const float *c, int32_t n_c, float *y,
+                             uint8_t *idx, cudaStream_t st)
 {
-    const int lpr = dim < 32 ? dim : 32;
     const int64_t rows_per_block = (int64_t)(kThreads / 32) * (32 / lpr);
     int64_t blocks = (n_rows + rows_per_block - 1) / rows_per_block;
     const int sms = vqh_device_sms() > 0 ? vqh_device_sms() : 152;
@@ -79,33 +78,43 @@ vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, i
 // Codebooks of 2, 4, 8 or 16 entries (the pages' 1- to 4-bit Lloyd-Max
 // codebooks) are scanned from registers; others through the sorted view.
 template <typename T, int E, bool QUANT>
-vq_status launch_hadamard_e(const void *x, const float *diag, int64_t n_rows, int32_t dim,
+vq_status launch_hadamard_e(const void *x, const float *diag, int64_t n_rows, int32_t dim, int lpr,
                             float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,
                             cudaStream_t st)
 {
     if constexpr (QUANT) {
         switch (n_c) {
-        case 2: return launch_hadamard_nc<T, E, true, 2>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
-        case 4: return launch_hadamard_nc<T, E, true, 4>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
-        case 8: return launch_hadamard_nc<T, E, true, 8>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
-        case 16: return launch_hadamard_nc<T, E, true, 16>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
+        case 2: return launch_hadamard_nc<T, E, true, 2>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+        case 4: return launch_hadamard_nc<T, E, true, 4>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+        case 8: return launch_hadamard_nc<T, E, true, 8>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+        case 16: return launch_hadamard_nc<T, E, true, 16>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
         }
     }
-    return launch_hadamard_nc<T, E, QUANT, 0>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
+    return launch_hadamard_nc<T, E, QUANT, 0>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
 }
 
+// Lanes per row: up to 32 with at least eight elements each (fewer shuffle
+// stages, each stage's set-up spread over more elements) when x and the codes
+// are aligned for runs of that length; otherwise the layout the contract's
+// alignment guarantees: one element per lane up to dim 32, then dim / 32.
 template <typename T, bool QUANT>
 vq_status launch_hadamard_t(const void *x, const float *diag, int64_t n_rows, int32_t dim,
                             float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,
                             cudaStream_t st)
 {
-    switch (dim <= 32 ? 1 : dim / 32) {
-    case 1: return launch_hadamard_e<T, 1, QUANT>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
-    case 2: return launch_hadamard_e<T, 2, QUANT>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
-    case 4: return launch_hadamard_e<T, 4, QUANT>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
-    case 8: return launch_hadamard_e<T, 8, QUANT>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
-    case 16: return launch_hadamard_e<T, 16, QUANT>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
-    case 32: return launch_hadamard_e<T, 32, QUANT>(x, diag, n_rows, dim, scale, c, n_c, y, idx, st);
+    int lpr = dim < 32 ? dim : 32;
+    const int lpr_w = dim >= 8 ? (dim / 8 < 32 ? dim / 8 : 32) : 1;
+    const size_t run_w = (size_t)(dim / lpr_w) * sizeof(T);
+    if ((uintptr_t)x % (run_w < 16 ? run_w : 16) == 0 &&
+        (!QUANT || (dim / lpr_w) % 4 != 0 || (uintptr_t)idx % 4 == 0))
+        lpr = lpr_w;
+    switch (dim / lpr) {
+    case 1: return launch_hadamard_e<T, 1, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+    case 2: return launch_hadamard_e<T, 2, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+    case 4: return launch_hadamard_e<T, 4, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+    case 8: return launch_hadamard_e<T, 8, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+    case 16: return launch_hadamard_e<T, 16, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+    case 32: return launch_hadamard_e<T, 32, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
     }
     return VQ_ERR_INTERNAL;
 }

@@ -221,16 +221,17 @@ __device__ __forceinline__ void load_run(const T *p, float (&v)[E])
     }
 }
 
-// The nearest-centroid rule with NC centroids in registers (the scan itself:
-// cheaper than the sorted search for up to 16 centroids).
+// The nearest-centroid rule with NC centroids in registers, held negated in
+// pairs (val + (-c) rounds exactly as val - c): the scan itself, for
+// codebooks with a non-finite value.
 template <int NC>
-__device__ __forceinline__ uint32_t nearest_reg(float val, const float (&c)[NC])
+__device__ __forceinline__ uint32_t nearest_reg(float val, const float2 (&cneg)[NC / 2])
 {
     float best_dist = __int_as_float(0x7f800000);
     uint32_t best = 0;
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
-        const float d = __fsub_rn(val, c[j]);
+        const float d = __fadd_rn(val, (j & 1) ? cneg[j / 2].y : cneg[j / 2].x);
         const float dist = __fmul_rn(d, d);
         const bool p = dist < best_dist;
         best_dist = p ? dist : best_dist;
@@ -332,12 +333,20 @@ __device__ __forceinline__ uint32_t nearest_reg_finite(float val, const float2 (
 
 // Whether all NC register centroids are finite (the finite rule applies).
 template <int NC>
-__device__ __forceinline__ bool all_finite(const float (&c)[NC])
+__device__ __forceinline__ bool all_finite(const float2 (&cneg)[NC / 2])
 {
     bool f = true;
 #pragma unroll
-    for (int j = 0; j < NC; ++j) f = f && fabsf(c[j]) <= 3.402823466e38f;
+    for (int j = 0; j < NC / 2; ++j) f = f && fabsf(cneg[j].x) <= 3.402823466e38f && fabsf(cneg[j].y) <= 3.402823466e38f;
     return f;
+}
+
+// The NC centroids as negated pairs.
+template <int NC>
+__device__ __forceinline__ void load_cneg(const float *__restrict__ centroids, float2 (&cneg)[NC / 2])
+{
+#pragma unroll
+    for (int k = 0; k < NC / 2; ++k) cneg[k] = make_float2(-__ldg(centroids + 2 * k), -__ldg(centroids + 2 * k + 1));
 }
 
 // Randomised Hadamard rotation of rows of D = LPR * E elements, optionally
@@ -376,15 +385,11 @@ __global__ void __launch_bounds__(256)
     SortedCb scb{nullptr, nullptr, 0, 0};
     const float *hq_cb = hq_sm;
     bool sorted_ok = false;
-    float creg[NC > 0 ? NC : 1];
     bool creg_finite = false;
     float2 cneg[NC > 1 ? NC / 2 : 1];
     if constexpr (QUANT && NC > 0) {
-#pragma unroll
-        for (int k = 0; k < NC; ++k) creg[k] = __ldg(centroids + k);
-        creg_finite = all_finite<NC>(creg);
-#pragma unroll
-        for (int k = 0; k < NC / 2; ++k) cneg[k] = make_float2(-creg[2 * k], -creg[2 * k + 1]);
+        load_cneg<NC>(centroids, cneg);
+        creg_finite = all_finite<NC>(cneg);
     }
     const float2 neg_one2 = make_float2(neg_one, neg_one);
     if constexpr (QUANT && NC == 0) {
@@ -413,7 +418,7 @@ __global__ void __launch_bounds__(256)
     const int d = lpr * E;
     // R row groups per warp step, all loaded before any is rotated, so that
     // R loads per lane are in flight
-    constexpr int R = E <= 8 ? 4 : E == 16 ? 2 : 1;
+    constexpr int R = E <= 4 ? 4 : E <= 16 ? 2 : 1;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     float dg[E];
 #pragma unroll
@@ -470,7 +475,7 @@ __global__ void __launch_bounds__(256)
                 for (int j = 0; j < E; ++j) {
                     if constexpr (NC > 0) {
                         code[j] = creg_finite ? nearest_reg_finite<NC>(w[j], cneg, neg_one2)
-                                              : nearest_reg<NC>(w[j], creg);
+                                              : nearest_reg<NC>(w[j], cneg);
                     } else {
                         const int k = sorted_ok ? nearest_sorted(w[j], scb) : -1;
                         code[j] = k >= 0 ? (uint32_t)k : nearest(w[j], hq_cb, n_c);
@@ -542,18 +547,14 @@ __global__ void __launch_bounds__(256)
                 int32_t n_c, bool vec, float neg_one, uint8_t *__restrict__ out)
 {
     extern __shared__ float ss_sm[];
-    float creg[NC > 0 ? NC : 1];
     SortedCb scb{nullptr, nullptr, 0, 0};
     bool sorted_ok = false;
     bool creg_finite = false;
     float2 cneg[NC > 1 ? NC / 2 : 1];
     const float2 neg_one2 = make_float2(neg_one, neg_one);
     if constexpr (NC > 0) {
-#pragma unroll
-        for (int k = 0; k < NC; ++k) creg[k] = __ldg(centroids + k);
-        creg_finite = all_finite<NC>(creg);
-#pragma unroll
-        for (int k = 0; k < NC / 2; ++k) cneg[k] = make_float2(-creg[2 * k], -creg[2 * k + 1]);
+        load_cneg<NC>(centroids, cneg);
+        creg_finite = all_finite<NC>(cneg);
     } else {
         float *c = ss_sm;
         float *u = c + n_c;
@@ -574,7 +575,7 @@ __global__ void __launch_bounds__(256)
     }
     auto quant = [&](float v) -> uint32_t {
         if constexpr (NC > 0) {
-            return creg_finite ? nearest_reg_finite<NC>(v, cneg, neg_one2) : nearest_reg<NC>(v, creg);
+            return creg_finite ? nearest_reg_finite<NC>(v, cneg, neg_one2) : nearest_reg<NC>(v, cneg);
         } else {
             const int k = sorted_ok ? nearest_sorted(v, scb) : -1;
             return k >= 0 ? (uint32_t)k : nearest(v, ss_sm, n_c);
