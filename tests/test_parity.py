@@ -331,6 +331,25 @@ def test_host_entry_point(vq, oracle_mod, g, m, sub, pinned):
     assert_same(want[:, rows], oracle_mod.encode(x[:, rows], cb, n_threads=THREADS))
 
 
+def test_host_entry_point_pageable_codebooks(vq):
+    """Pinned keys and indices with pageable codebooks: the kernel still
+    reads the keys in place, and the codebooks are copied to the device
+    buffer first."""
+    rng = np.random.default_rng(77)
+    x = rng.standard_normal((4, 50000, 8)).astype(np.float16)
+    cb = rng.standard_normal((4, 256, 8)).astype(np.float16)
+    xh = torch.from_numpy(x).pin_memory()
+    outh = torch.empty((4, 50000), dtype=torch.int32).pin_memory().view(torch.uint32)
+    xd = torch.empty(x.shape, dtype=torch.float16, device="cuda")
+    cbd = torch.zeros(cb.shape, dtype=torch.float16, device="cuda")
+    outd = torch.empty((4, 50000), dtype=torch.int32, device="cuda").view(torch.uint32)
+    want = vq.vq_encode_grouped(torch.from_numpy(x).cuda(), torch.from_numpy(cb).cuda()).cpu().numpy()
+    vq.vq_encode_grouped_host(xh, torch.from_numpy(cb), outh, xd, cbd, outd)
+    assert_same(outh.numpy(), want)
+    torch.cuda.synchronize()
+    assert torch.equal(cbd.cpu(), torch.from_numpy(cb))
+
+
 def test_argument_errors_raise(vq):
     x = torch.zeros((10, 4), dtype=torch.float16, device="cuda")
     cb = torch.zeros((5000, 4), dtype=torch.float16, device="cuda")

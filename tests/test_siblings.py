@@ -237,3 +237,27 @@ def test_hadamard_quantize_value_sweep(vq, oracle_mod, n_c):
     got = vq.vq_hadamard_quantize(torch.from_numpy(x).cuda(), torch.from_numpy(diag).cuda(),
                                   torch.from_numpy(c).cuda()).cpu().numpy()
     assert np.array_equal(got.astype(np.uint32), want)
+
+
+@pytest.mark.parametrize("n_c", [4, 16, 100])
+@pytest.mark.parametrize("dim", [32, 64, 128])
+def test_hadamard_both_lane_layouts(vq, oracle_mod, n_c, dim):
+    """The same rows through the wide lane layout (x 16-byte aligned) and the
+    contract's minimal one (x aligned to dim/32 elements only, here 8 bytes
+    off a 16-byte boundary): both bit-identical to the oracle."""
+    rng = np.random.default_rng(dim + n_c)
+    rows = 999
+    x = rng.standard_normal((rows, dim)).astype(np.float16)
+    diag = rng.choice([-1.0, 1.0], dim).astype(np.float32)
+    c = np.sort(rng.standard_normal(n_c).astype(np.float32))
+    want = oracle_mod.hadamard_quantize(x, diag, c)
+    want_rot = oracle_mod.hadamard_rotate(x, diag)
+    dd, cd = torch.from_numpy(diag).cuda(), torch.from_numpy(c).cuda()
+    buf = torch.zeros(rows * dim + 64, dtype=torch.float16, device="cuda")
+    for off in (0, 4):  # elements: 16-byte aligned, then 8 bytes past
+        xv = buf[off:off + rows * dim].view(rows, dim)
+        xv.copy_(torch.from_numpy(x))
+        got = vq.vq_hadamard_quantize(xv, dd, cd).cpu().numpy()
+        assert np.array_equal(got.astype(np.uint32), want), off
+        rot = vq.vq_hadamard_rotate(xv, dd).cpu().numpy()
+        assert np.array_equal(rot.view(np.uint32), want_rot.view(np.uint32)), off
