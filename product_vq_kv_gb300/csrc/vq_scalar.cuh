@@ -7,19 +7,23 @@
 //   Hadamard rotate   v = float(x) * diag; butterfly passes stride 1, 2, ...,
 //                     D/2: (lo, hi) -> (lo + hi, lo - hi); y = v * scale;
 //   fused quantize    idx = scalar quantize of y.
-// Every operation is an explicitly rounded fp32 intrinsic, so no compiler
-// contraction can change a result.
+// Every operation is an explicitly rounded fp32 intrinsic (or packed f32x2
+// form, each lane rounded alike), arranged so that no compiler contraction
+// can change a result.
 //
 // GB300 shape.  16-bit inputs have only 65,536 values: scalar_table
 // evaluates the formula once for each bit pattern into a 64 KiB table (the
 // caller's workspace), and scalar_lookup stages that table in shared memory
 // and turns the pass into a coalesced 2-byte-in / 1-byte-out stream with one
 // shared-memory lookup per element (HBM-bound, bit-identical to the scan).
-// fp32 inputs use scalar_scan (the scan itself, codebook in shared memory,
-// broadcast reads).  The rotation runs one row per warp (or several rows of
-// D < 32 per warp): a lane holds E = D/32 contiguous elements, so butterfly
-// strides below E stay in registers and larger ones are shfl.xor exchanges;
-// no shared memory and no barriers.
+// Other inputs use scalar_scan: codebooks of 2, 4, 8 or 16 finite entries go
+// through a packed register scan (distances in f32x2 pairs, their least by a
+// min3 tree, the lowest index holding it from sign bits), others through a
+// sorted view of the codebook with the scan as fallback.  The rotation
+// spreads each row over up to 32 lanes: a lane holds E contiguous elements
+// (at least 8 when x is aligned for it), so butterfly strides below E stay
+// in registers and larger ones are shfl.xor exchanges; no shared memory and
+// no barriers.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -350,14 +354,17 @@ __device__ __forceinline__ void load_cneg(const float *__restrict__ centroids, f
 }
 
 // Randomised Hadamard rotation of rows of D = LPR * E elements, optionally
-// fused with the scalar quantize.  LPR = min(D, 32) lanes per row, 32 / LPR
-// rows per warp; lane l of a row holds elements l*E .. l*E + E - 1.  Warps
-// stride over the rows (a persistent grid).  The quantize scans NC > 0
-// centroids held in registers (codebooks of exactly NC entries), or, with
-// NC == 0, searches the block's sorted view of the codebook (any size up to
-// 256).  Launch: blockDim.x = 256, any grid; dynamic shared memory
-// hadamard_smem(n_c) when QUANT and NC == 0, else 0.  x rows contiguous and
-// E-element aligned; y / idx [n_rows][D].
+// fused with the scalar quantize.  LPR = lanes_per_row (a power of two up to
+// 32, chosen by the host), 32 / LPR rows per warp; lane l of a row holds
+// elements l*E .. l*E + E - 1.  Warps stride over groups of rows (a
+// persistent grid), loading R groups before rotating the first.  The
+// quantize scans NC > 0 centroids held in registers as negated pairs
+// (codebooks of exactly NC entries; the packed finite scan when all are
+// finite), or, with NC == 0, searches the block's sorted view of the codebook
+// (any size up to 256).  `neg_one` must be -1.0f.  Launch: blockDim.x = 256,
+// any grid; dynamic shared memory hadamard_smem(n_c) when QUANT and NC == 0,
+// else 0.  x rows contiguous and E-element aligned (E * sizeof(T) up to 16
+// bytes); idx 4-byte aligned when E % 4 == 0; y / idx [n_rows][D].
 __host__ __device__ inline size_t hadamard_smem(int n_c) { return (size_t)n_c * 16 + 16; }
 
 // The scalar quantize of any input type without a table: codebooks of 2, 4,
@@ -366,8 +373,8 @@ __host__ __device__ inline size_t hadamard_smem(int n_c) { return (size_t)n_c * 
 // where the view cannot decide.  A persistent grid strides over 8-element
 // units (16-byte loads, two units in flight per thread, 8-byte stores) when
 // `vec` (x 16-byte and out 8-byte aligned), then over the remaining elements
-// one by one.  Launch: any grid of 256-thread blocks; dynamic shared memory
-// hadamard_smem(n_c) when NC == 0, else 0.
+// one by one.  `neg_one` must be -1.0f.  Launch: any grid of 256-thread
+// blocks; dynamic shared memory hadamard_smem(n_c) when NC == 0, else 0.
 template <typename T, int NC>
 __global__ void __launch_bounds__(256)
     scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
