@@ -163,12 +163,12 @@ size_t fast_smem(int32_t n_centroids)
     return vqk::CbLayout<SUB, kGroupCentroids>::bytes(n_centroids);
 }
 
-// With SMOOTH the A operand holds the three tf32 pieces of each divided row.
+// With SMOOTH the A operand holds two tf32 pieces of each divided row.
 template <int SUB, bool SMOOTH = false>
 size_t tc_smem(int32_t n_centroids)
 {
     using C = TcConfig<SUB>;
-    return vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH ? 3 : 1>::bytes(n_centroids);
+    return vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH ? 2 : 1>::bytes(n_centroids);
 }
 
 template <typename T, int SUB, typename OutT = uint32_t, bool SMOOTH = false>
@@ -349,9 +349,9 @@ vq_status launch_smooth_typed(const Args &a, const Plan &p)
 }
 
 // Encode with per-channel smoothing.  fp16 and bf16 codebooks of 64..256
-// centroids take the tensor-core kernel with the divided rows split into
-// three exact tf32 pieces; others the filter kernel, whose bound holds for
-// any fp32 row.
+// centroids take the tensor-core kernel with the divided rows split into two
+// tf32 pieces (the bound covers the dropped low bits); others the filter
+// kernel, whose bound holds for any fp32 row.
 vq_status run_smooth(const Args &a)
 {
     if (a.head_dim < a.sub_dim || a.sub_dim < 1 || a.head_dim % a.sub_dim) return VQ_ERR_INVALID_ARG;

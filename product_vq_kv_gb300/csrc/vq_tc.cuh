@@ -22,16 +22,16 @@
 //
 // With SMOOTH, each row is first divided by its per-channel smooth factors
 // (fp32, rounded to nearest), and the divided row -- an fp32 value, not
-// exact in tf32 -- is what is encoded.  It is split exactly into three tf32
-// pieces, x_i = hi_i + mid_i + lo_i (hi keeps the top 11 significant bits,
-// mid the next 11 of the exact remainder, lo the last 2), and three
-// accumulating MMAs multiply A_hi = [hi, 1, 1, 1, 0 ...], A_mid = [mid, 0 ...]
-// and A_lo = [lo, 0 ...] by the same B, so every product is still exact.  The
-// sum of the terms' magnitudes grows to at most (1 + 2^-9) times its bound
-// above (|hi| + |mid| + |lo| <= (1 + 2^-10 + 2^-20) |x|), and the kernel uses
-// B(x) = (2 (1 + 2^-9) eps_tc + 2 gamma_SUB) (C2 + sum_i |x_i| A_i); the
-// accumulation now spans 3 K terms, 24 or 48, whose truncating fp32 error
-// (at most 48 x 2^-23 = 2^-17.4 of the magnitudes) eps_tc still covers.
+// exact in tf32 -- is what is encoded.  Each element is x_i = hi_i + mid_i +
+// lo_i exactly (hi keeps the top 11 significant bits, mid the next 11 of the
+// exact remainder, lo the last 2, |lo_i| <= 2^-20 |x_i|).  Two accumulating
+// MMAs multiply A_hi = [hi, 1, 1, 1, 0 ...] and A_mid = [mid, 0 ...] by the
+// same B, so every product is exact; the dropped lo part changes the score
+// by |2 sum_i lo_i c_i| <= 2^-19 sum_i |x_i| A_i.  The magnitudes of the
+// terms add up to at most (1 + 2^-9) times their bound above, and the kernel
+// uses B(x) = (2 (1 + 2^-9) eps_tc + 2 gamma_SUB + 2^-19) (C2 + sum_i |x_i|
+// A_i); the accumulation spans 2 K terms, 16 or 32, whose truncating fp32
+// error (at most 32 x 2^-23 = 2^-18 of the magnitudes) eps_tc still covers.
 //
 // The accumulator of a tile is a 128-lane x n_pad-column fp32 block of tensor
 // memory, so thread t of the block owns row t of the tile: it reads its own
@@ -50,7 +50,7 @@
 // tiles of one group.  Requirements: T is __half or __nv_bfloat16, 64 <= n_centroids <=
 // 256, x aligned to SUB * sizeof(T) bytes.  With SMOOTH: `smooth`
 // [n_groups][smooth_ns * SUB] fp32 factors, row m of a group holding channels
-// (m % smooth_ns) * SUB + i; TcLayout's A holds three pieces (NA = 3).
+// (m % smooth_ns) * SUB + i; TcLayout's A holds two pieces (NA = 2).
 #pragma once
 
 #include "vq_filter.cuh"
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(128, MINB)
     static_assert(SUB == 4 || SUB == 8, "sub_dim 4 or 8");
     static_assert(NCOL == 32 || NCOL == 64 || NCOL == 128 || NCOL == 256, "tensor-memory columns");
     static_assert(GC == 8 || GC == 16, "centroid group size");
-    constexpr int kNA = SMOOTH ? 3 : 1;  // A pieces
+    constexpr int kNA = SMOOTH ? 2 : 1;  // A pieces
     using L = TcLayout<SUB, NCOL, GC, kNA>;
     constexpr int kK = L::kK;
     constexpr int kKB = kK / 4;  // 16-byte core-matrix columns per row
@@ -331,8 +331,10 @@ __global__ void __launch_bounds__(128, MINB)
     float amax[SUB];
 #pragma unroll
     for (int i = 0; i < SUB; ++i) amax[i] = __uint_as_float(smax[1 + i]);
-    // 2 eps_tc + 2 gamma_SUB; with the three-piece split, 2 (1 + 2^-9) eps_tc
-    const float kBtc = (SMOOTH ? 2.00390625f : 2.0f) * 1.5258789e-5f + 2.0f * gamma_u(SUB);
+    // 2 eps_tc + 2 gamma_SUB; with the two-piece split, 2 (1 + 2^-9) eps_tc
+    // and the dropped low part's 2^-19
+    const float kBtc = (SMOOTH ? 2.00390625f : 2.0f) * 1.5258789e-5f + 2.0f * gamma_u(SUB) +
+                       (SMOOTH ? 1.9073486e-6f : 0.0f);
     const float kD = 4.0f * gamma_u(SUB + 2);
     const float kTiny = 7.8886091e-31f;  // 2^-100
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
@@ -361,16 +363,14 @@ __global__ void __launch_bounds__(128, MINB)
 
         // A rows of this tile (the MMA of the previous tile has completed)
         if constexpr (SMOOTH) {
-            float pc3[3][SUB];
+            float pc3[2][SUB];
 #pragma unroll
             for (int i = 0; i < SUB; ++i) {
                 pc3[0][i] = tf32_trunc(xr[i]);
-                const float r1 = xr[i] - pc3[0][i];  // exact: the low bits of xr[i]
-                pc3[1][i] = tf32_trunc(r1);
-                pc3[2][i] = r1 - pc3[1][i];          // exact, at most two bits
+                pc3[1][i] = tf32_trunc(xr[i] - pc3[0][i]);  // of the exact low bits of xr[i]
             }
 #pragma unroll
-            for (int pc = 0; pc < 3; ++pc)
+            for (int pc = 0; pc < 2; ++pc)
 #pragma unroll
                 for (int kb = 0; kb < SUB / 4; ++kb)
                     *reinterpret_cast<float4 *>(sa + pc * (L::kABytes / 4) +
