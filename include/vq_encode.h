@@ -33,6 +33,11 @@
  *     point.
  *   - A launch failure returns VQ_ERR_CUDA; the CUDA error is left for the
  *     caller to inspect (cudaGetLastError) and is not cleared.
+ *   - The tensor-core kernel waits for its matrix units with a bounded
+ *     number of polls.  Should a wait give up (never observed), the rows the
+ *     block has not encoded are written as 0xFFFFFFFF, an index no codebook
+ *     has; with 8-bit codes that marker is 255, which is a valid code when
+ *     n_centroids is 256, so it then cannot be told from one.
  *   - N = 0 (or n_per_group = 0) is valid: VQ_OK, nothing is launched, and
  *     the pointers may be NULL.
  *   - Supported shapes: 1 <= sub_dim <= 32, 1 <= n_centroids <= 4096.
