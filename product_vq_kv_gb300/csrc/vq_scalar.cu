@@ -61,9 +61,9 @@ vq_status launch_scan(const void *x, int64_t n, const float *c, int32_t n_c, uin
 }
 
 template <typename T, int E, bool QUANT, int NC>
-vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, int32_t dim,
-                             int lpr, float scale, const float *c, int32_t n_c, float *y,
-                             uint8_t *idx, cudaStream_t st)
+vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, int lpr,
+                             float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,
+                             cudaStream_t st)
 {
     const int64_t rows_per_block = (int64_t)(kThreads / 32) * (32 / lpr);
     int64_t blocks = (n_rows + rows_per_block - 1) / rows_per_block;
@@ -78,19 +78,18 @@ vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, i
 // Codebooks of 2, 4, 8 or 16 entries (the pages' 1- to 4-bit Lloyd-Max
 // codebooks) are scanned from registers; others through the sorted view.
 template <typename T, int E, bool QUANT>
-vq_status launch_hadamard_e(const void *x, const float *diag, int64_t n_rows, int32_t dim, int lpr,
-                            float scale, const float *c, int32_t n_c, float *y, uint8_t *idx,
-                            cudaStream_t st)
+vq_status launch_hadamard_e(const void *x, const float *diag, int64_t n_rows, int lpr, float scale,
+                            const float *c, int32_t n_c, float *y, uint8_t *idx, cudaStream_t st)
 {
     if constexpr (QUANT) {
         switch (n_c) {
-        case 2: return launch_hadamard_nc<T, E, true, 2>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
-        case 4: return launch_hadamard_nc<T, E, true, 4>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
-        case 8: return launch_hadamard_nc<T, E, true, 8>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
-        case 16: return launch_hadamard_nc<T, E, true, 16>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+        case 2: return launch_hadamard_nc<T, E, true, 2>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
+        case 4: return launch_hadamard_nc<T, E, true, 4>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
+        case 8: return launch_hadamard_nc<T, E, true, 8>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
+        case 16: return launch_hadamard_nc<T, E, true, 16>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
         }
     }
-    return launch_hadamard_nc<T, E, QUANT, 0>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+    return launch_hadamard_nc<T, E, QUANT, 0>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
 }
 
 // Lanes per row: up to 32 with at least eight elements each (fewer shuffle
@@ -109,12 +108,12 @@ vq_status launch_hadamard_t(const void *x, const float *diag, int64_t n_rows, in
         (!QUANT || (dim / lpr_w) % 4 != 0 || (uintptr_t)idx % 4 == 0))
         lpr = lpr_w;
     switch (dim / lpr) {
-    case 1: return launch_hadamard_e<T, 1, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
-    case 2: return launch_hadamard_e<T, 2, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
-    case 4: return launch_hadamard_e<T, 4, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
-    case 8: return launch_hadamard_e<T, 8, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
-    case 16: return launch_hadamard_e<T, 16, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
-    case 32: return launch_hadamard_e<T, 32, QUANT>(x, diag, n_rows, dim, lpr, scale, c, n_c, y, idx, st);
+    case 1: return launch_hadamard_e<T, 1, QUANT>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
+    case 2: return launch_hadamard_e<T, 2, QUANT>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
+    case 4: return launch_hadamard_e<T, 4, QUANT>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
+    case 8: return launch_hadamard_e<T, 8, QUANT>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
+    case 16: return launch_hadamard_e<T, 16, QUANT>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
+    case 32: return launch_hadamard_e<T, 32, QUANT>(x, diag, n_rows, lpr, scale, c, n_c, y, idx, st);
     }
     return VQ_ERR_INTERNAL;
 }

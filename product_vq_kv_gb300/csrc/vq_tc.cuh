@@ -194,7 +194,7 @@ struct TcLayout {
     static constexpr size_t kABytes = (size_t)128 * kRowBytes;  // one A piece
     __host__ __device__ static size_t a_off() { return 0; }
     __host__ __device__ static size_t b_off() { return NA * kABytes; }
-    __host__ __device__ static size_t x_off(int nc) { return b_off() + (size_t)256 * kRowBytes; }
+    __host__ __device__ static size_t x_off(int /*nc: B always holds 256 rows*/) { return b_off() + (size_t)256 * kRowBytes; }
     __host__ __device__ static size_t misc_off(int nc)
     {
         return x_off(nc) + (size_t)groups(nc) * kGroupFloats * 4;
