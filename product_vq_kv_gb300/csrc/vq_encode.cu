@@ -163,12 +163,15 @@ size_t fast_smem(int32_t n_centroids)
     return vqk::CbLayout<SUB, kGroupCentroids>::bytes(n_centroids);
 }
 
-// With SMOOTH the A operand holds two tf32 pieces of each divided row.
+// A holds two tf32 pieces of each row when the rows are not 16-bit values
+// (smoothed or fp32), B two pieces of -2c for fp32 codebooks.
 template <int SUB, bool SMOOTH = false>
-size_t tc_smem(int32_t n_centroids)
+size_t tc_smem(int32_t n_centroids, vq_dtype dtype)
 {
     using C = TcConfig<SUB>;
-    return vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH ? 2 : 1>::bytes(n_centroids);
+    if (dtype == VQ_F32)
+        return vqk::TcLayout<SUB, C::kCols, C::kGroup, 2, 2>::bytes(n_centroids);
+    return vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH ? 2 : 1, 1>::bytes(n_centroids);
 }
 
 template <typename T, int SUB, typename OutT = uint32_t, bool SMOOTH = false>
@@ -206,11 +209,11 @@ Plan make_plan(const Args &a)
     const size_t align = row_bytes < 16 ? row_bytes : 16;
     const bool shape_ok = (a.sub_dim == 4 || a.sub_dim == 8) && ((uintptr_t)a.x % align == 0);
     p.kind = kGeneral;
-    // tf32 holds fp16 and bf16 values exactly, not fp32 ones
-    if (shape_ok && a.dtype != VQ_F32 && a.n_centroids >= kFilterMinCentroids &&
-        a.n_centroids <= 256) {
+    // tf32 holds fp16 and bf16 values exactly; fp32 rows and codebooks are
+    // split into tf32 pieces, the dropped bits covered by the bound
+    if (shape_ok && a.n_centroids >= kFilterMinCentroids && a.n_centroids <= 256) {
         p.kind = kTc;
-        p.smem = a.sub_dim == 4 ? tc_smem<4>(a.n_centroids) : tc_smem<8>(a.n_centroids);
+        p.smem = a.sub_dim == 4 ? tc_smem<4>(a.n_centroids, a.dtype) : tc_smem<8>(a.n_centroids, a.dtype);
     }
     if (shape_ok && p.kind == kGeneral && a.n_centroids >= kFilterMinCentroids) {
         p.smem = a.sub_dim == 4 ? filter_smem<4>(a.n_centroids) : filter_smem<8>(a.n_centroids);
@@ -297,9 +300,7 @@ vq_status launch_typed(const Args &a, const Plan &p)
 {
     switch (p.kind) {
     case kTc:
-        if constexpr (sizeof(T) == 2)
-            return a.sub_dim == 4 ? launch_tc<T, 4, OutT>(a, p) : launch_tc<T, 8, OutT>(a, p);
-        return VQ_ERR_INTERNAL;
+        return a.sub_dim == 4 ? launch_tc<T, 4, OutT>(a, p) : launch_tc<T, 8, OutT>(a, p);
     case kFilter:
         return a.sub_dim == 4 ? launch_filter<T, 4, OutT>(a, p) : launch_filter<T, 8, OutT>(a, p);
     case kBrute:
@@ -337,6 +338,7 @@ vq_status launch_smooth_typed(const Args &a, const Plan &p)
         switch (a.dtype) {
         case VQ_F16: return launch_tc<__half, SUB, OutT, true>(a, p);
         case VQ_BF16: return launch_tc<__nv_bfloat16, SUB, OutT, true>(a, p);
+        case VQ_F32: return launch_tc<float, SUB, OutT, true>(a, p);
         default: return VQ_ERR_INTERNAL;
         }
     }
@@ -348,10 +350,10 @@ vq_status launch_smooth_typed(const Args &a, const Plan &p)
     return VQ_ERR_INTERNAL;
 }
 
-// Encode with per-channel smoothing.  fp16 and bf16 codebooks of 64..256
-// centroids take the tensor-core kernel with the divided rows split into two
-// tf32 pieces (the bound covers the dropped low bits); others the filter
-// kernel, whose bound holds for any fp32 row.
+// Encode with per-channel smoothing.  Codebooks of 64..256 centroids take the
+// tensor-core kernel with the divided rows split into two tf32 pieces (and
+// fp32 codebooks too; the bound covers the dropped low bits); others the
+// filter kernel, whose bound holds for any fp32 row.
 vq_status run_smooth(const Args &a)
 {
     if (a.head_dim < a.sub_dim || a.sub_dim < 1 || a.head_dim % a.sub_dim) return VQ_ERR_INVALID_ARG;
@@ -364,9 +366,9 @@ vq_status run_smooth(const Args &a)
     const size_t row_bytes = (size_t)a.sub_dim * elem_size(a.dtype);
     if ((uintptr_t)a.x % (row_bytes < 16 ? row_bytes : 16)) return VQ_ERR_UNSUPPORTED;
     Plan p{};
-    if (a.dtype != VQ_F32 && a.n_centroids >= kFilterMinCentroids && a.n_centroids <= 256) {
+    if (a.n_centroids >= kFilterMinCentroids && a.n_centroids <= 256) {
         p.kind = kTc;
-        p.smem = a.sub_dim == 4 ? tc_smem<4, true>(a.n_centroids) : tc_smem<8, true>(a.n_centroids);
+        p.smem = a.sub_dim == 4 ? tc_smem<4, true>(a.n_centroids, a.dtype) : tc_smem<8, true>(a.n_centroids, a.dtype);
         tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, p.smem), &p.tiles_per_group, &p.tc_tiles);
         p.blocks = a.n_groups * p.tiles_per_group;
         p.threads = 128;

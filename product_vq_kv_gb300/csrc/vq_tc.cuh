@@ -17,8 +17,14 @@
 // rounding of the fp32 |c|^2 (gamma_SUB) gives the screening bound
 //     B(x) = (2 eps_tc + 2 gamma_SUB) (C2 + sum_i |x_i| A_i),
 // and the threshold, candidate groups, exact re-evaluation and exact queue
-// follow as in vq_filter.cuh.  fp32 inputs are not exact in tf32 and use
-// encode_filter instead.
+// follow as in vq_filter.cuh.
+//
+// fp32 rows and codebooks are not exact in tf32.  The rows are split as
+// below (x = hi + mid + lo), and -2c likewise into b_hi + b_mid + b_lo with
+// a second B piece holding b_mid; three accumulating MMAs form (hi, b_hi),
+// (mid, b_hi) and (hi, b_mid).  The dropped products x_lo (-2c), x b_lo and
+// mid b_mid are each at most 2^-20 |x| |2c|, together 3 x 2^-19 sum_i |x_i|
+// A_i (the kernel adds 2^-17) to the screening bound.
 //
 // With SMOOTH, each row is first divided by its per-channel smooth factors
 // (fp32, rounded to nearest), and the divided row -- an fp32 value, not
@@ -47,11 +53,13 @@
 // (at least 512/NCOL CTAs' worth of a 228 KiB SM, which caps the CTAs per SM
 // at the tensor-memory budget: NCOL columns each); grid.x = n_groups *
 // blocks_per_group, each block encoding tiles_per_block consecutive 128-row
-// tiles of one group.  Requirements: T is __half or __nv_bfloat16, 64 <= n_centroids <=
+// tiles of one group.  Requirements: T is __half, __nv_bfloat16 or float, 64 <= n_centroids <=
 // 256, x aligned to SUB * sizeof(T) bytes.  With SMOOTH: `smooth`
 // [n_groups][smooth_ns * SUB] fp32 factors, row m of a group holding channels
 // (m % smooth_ns) * SUB + i; TcLayout's A holds two pieces (NA = 2).
 #pragma once
+
+#include <type_traits>
 
 #include "vq_filter.cuh"
 #include "vq_kernels.cuh"
@@ -178,7 +186,7 @@ __device__ __forceinline__ float tf32_trunc(float v) { return __uint_as_float(__
 
 // ------------------------------------------------------------------ layout
 
-template <int SUB, int NCOL, int GC, int NA = 1>
+template <int SUB, int NCOL, int GC, int NA = 1, int NB = 1>
 struct TcLayout {
     static constexpr int kK = SUB == 4 ? 8 : 16;       // MMA K (tf32 elements), 8 per instruction
     static constexpr int kRowBytes = kK * 4;
@@ -194,7 +202,7 @@ struct TcLayout {
     static constexpr size_t kABytes = (size_t)128 * kRowBytes;  // one A piece
     __host__ __device__ static size_t a_off() { return 0; }
     __host__ __device__ static size_t b_off() { return NA * kABytes; }
-    __host__ __device__ static size_t x_off(int /*nc: B always holds 256 rows*/) { return b_off() + (size_t)256 * kRowBytes; }
+    __host__ __device__ static size_t x_off(int /*nc: B always holds 256 rows*/) { return b_off() + (size_t)NB * 256 * kRowBytes; }
     __host__ __device__ static size_t misc_off(int nc)
     {
         return x_off(nc) + (size_t)groups(nc) * kGroupFloats * 4;
@@ -221,8 +229,10 @@ __global__ void __launch_bounds__(128, MINB)
     static_assert(SUB == 4 || SUB == 8, "sub_dim 4 or 8");
     static_assert(NCOL == 32 || NCOL == 64 || NCOL == 128 || NCOL == 256, "tensor-memory columns");
     static_assert(GC == 8 || GC == 16, "centroid group size");
-    constexpr int kNA = SMOOTH ? 2 : 1;  // A pieces
-    using L = TcLayout<SUB, NCOL, GC, kNA>;
+    constexpr bool kF32 = std::is_same<T, float>::value;  // fp32 rows and codebook
+    constexpr int kNA = SMOOTH || kF32 ? 2 : 1;  // A pieces: rows not exact in tf32
+    constexpr int kNB = kF32 ? 2 : 1;            // B pieces: -2c not exact in tf32
+    using L = TcLayout<SUB, NCOL, GC, kNA, kNB>;
     constexpr int kK = L::kK;
     constexpr int kKB = kK / 4;  // 16-byte core-matrix columns per row
     constexpr int kGC = L::kGC;
@@ -293,8 +303,13 @@ __global__ void __launch_bounds__(128, MINB)
         float bk[kK];
 #pragma unroll
         for (int k = 0; k < kK; ++k) bk[k] = 0.f;
+        float bm[SUB];  // second piece of -2c (fp32 codebooks)
 #pragma unroll
-        for (int i = 0; i < SUB; ++i) bk[i] = -2.0f * v[i];
+        for (int i = 0; i < SUB; ++i) {
+            const float w = -2.0f * v[i];
+            bk[i] = kF32 ? tf32_trunc(w) : w;
+            bm[i] = kF32 ? tf32_trunc(w - bk[i]) : 0.f;
+        }
         if (real) {
             const float hi = tf32_trunc(nrm);
             const float mid = tf32_trunc(nrm - hi);
@@ -308,6 +323,15 @@ __global__ void __launch_bounds__(128, MINB)
         for (int kb = 0; kb < kKB; ++kb)
             *reinterpret_cast<float4 *>(sb + ((c >> 3) * (kKB * 128) + kb * 128 + (c & 7) * 16) / 4) =
                 make_float4(bk[4 * kb], bk[4 * kb + 1], bk[4 * kb + 2], bk[4 * kb + 3]);
+        if constexpr (kNB == 2) {
+            // second piece: -2c's next 11 bits, nothing in the constant columns
+            float *sb2 = sb + 256 * L::kRowBytes / 4;
+#pragma unroll
+            for (int kb = 0; kb < kKB; ++kb)
+                *reinterpret_cast<float4 *>(sb2 + ((c >> 3) * (kKB * 128) + kb * 128 + (c & 7) * 16) / 4) =
+                    kb < SUB / 4 ? make_float4(bm[4 * kb], bm[4 * kb + 1], bm[4 * kb + 2], bm[4 * kb + 3])
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         if (c < n_pad) {
             float *ex = sx + (c / kGC) * L::kGroupFloats + ((c % kGC) >> 1) * (2 * SUB) + (c & 1);
 #pragma unroll
@@ -331,10 +355,11 @@ __global__ void __launch_bounds__(128, MINB)
     float amax[SUB];
 #pragma unroll
     for (int i = 0; i < SUB; ++i) amax[i] = __uint_as_float(smax[1 + i]);
-    // 2 eps_tc + 2 gamma_SUB; with the two-piece split, 2 (1 + 2^-9) eps_tc
-    // and the dropped low part's 2^-19
-    const float kBtc = (SMOOTH ? 2.00390625f : 2.0f) * 1.5258789e-5f + 2.0f * gamma_u(SUB) +
-                       (SMOOTH ? 1.9073486e-6f : 0.0f);
+    // 2 eps_tc + 2 gamma_SUB; with split rows, 2 (1 + 2^-9) eps_tc and the
+    // dropped low part's 2^-19; with split codebooks too, 2^-17 for the three
+    // dropped products
+    const float kBtc = (kNA == 2 ? 2.00390625f : 2.0f) * 1.5258789e-5f + 2.0f * gamma_u(SUB) +
+                       (kF32 ? 7.6293945e-6f : kNA == 2 ? 1.9073486e-6f : 0.0f);
     const float kD = 4.0f * gamma_u(SUB + 2);
     const float kTiny = 7.8886091e-31f;  // 2^-100
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
@@ -362,7 +387,7 @@ __global__ void __launch_bounds__(128, MINB)
         if (row_base + (int64_t)tile * 128 >= n_per_group) break;  // block-uniform
 
         // A rows of this tile (the MMA of the previous tile has completed)
-        if constexpr (SMOOTH) {
+        if constexpr (kNA == 2) {
             float pc3[2][SUB];
 #pragma unroll
             for (int i = 0; i < SUB; ++i) {
@@ -397,14 +422,18 @@ __global__ void __launch_bounds__(128, MINB)
             const int ncols = n_pad - c0 < NCOL ? n_pad - c0 : NCOL;
             if (tid == 0) {
                 const uint32_t idesc = umma_idesc_tf32((uint32_t)ncols);
+                // (A piece, B piece) products: (hi, hi), (mid, hi), (hi, mid)
 #pragma unroll
-                for (int pc = 0; pc < kNA; ++pc) {
+                for (int pp = 0; pp < kNA + kNB - 1; ++pp) {
+                    const uint32_t pa = pp == 1 && kNA == 2 ? 1u : 0u;
+                    const uint32_t pb = pp == kNA ? 1u : 0u;
 #pragma unroll
                     for (int kstep = 0; kstep < kK / 8; ++kstep) {
                         const uint64_t ad =
-                            umma_smem_desc(sa_addr + pc * (uint32_t)L::kABytes + kstep * 256, 128, kSbo);
-                        const uint64_t bd = umma_smem_desc(sb_addr + (c0 >> 3) * kSbo + kstep * 256, 128, kSbo);
-                        umma_tf32(tmem, ad, bd, idesc, pc > 0 || kstep > 0);
+                            umma_smem_desc(sa_addr + pa * (uint32_t)L::kABytes + kstep * 256, 128, kSbo);
+                        const uint64_t bd = umma_smem_desc(
+                            sb_addr + pb * (uint32_t)(256 * L::kRowBytes) + (c0 >> 3) * kSbo + kstep * 256, 128, kSbo);
+                        umma_tf32(tmem, ad, bd, idesc, pp > 0 || kstep > 0);
                     }
                 }
                 umma_commit(bar);

@@ -218,7 +218,9 @@ def test_describe_launch_picks_kernels(lib):
     assert buf.value.decode().startswith("kernel=encode_tc")
     assert f(256, 131072, 256, 8, 1, P, buf, 512) == 0       # bf16
     assert buf.value.decode().startswith("kernel=encode_tc")
-    assert f(1, 1 << 20, 256, 4, 2, P, buf, 512) == 0        # fp32: CUDA-core screening
+    assert f(1, 1 << 20, 256, 4, 2, P, buf, 512) == 0        # fp32: tensor cores, split into tf32 pieces
+    assert buf.value.decode().startswith("kernel=encode_tc")
+    assert f(1, 1 << 20, 300, 4, 2, P, buf, 512) == 0        # fp32, more than 256: CUDA-core screening
     assert buf.value.decode().startswith("kernel=encode_filter")
     assert f(1, 1 << 20, 1000, 8, 0, P, buf, 512) == 0       # more than 256 centroids
     assert buf.value.decode().startswith("kernel=encode_filter")

@@ -46,7 +46,7 @@ def expected_kernel(dtype, n_c):
         return ""  # large codebooks: whichever exact kernel fits in shared memory
     if n_c < 64:
         return "encode_fast"
-    if dtype in (np.float16, "bf16") and n_c <= 256:
+    if n_c <= 256:
         return "encode_tc"
     return "encode_filter"
 
@@ -60,15 +60,16 @@ def check(vq, oracle_mod, x, cb, kernel=None):
     assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
 
 
+@pytest.mark.parametrize("n_c", [256, 320])
 @pytest.mark.parametrize("dtype", [np.float16, np.float32])
 @pytest.mark.parametrize("sub_dim", [4, 8])
-def test_permuted_coordinate_ties(vq, oracle_mod, sub_dim, dtype):
+def test_permuted_coordinate_ties(vq, oracle_mod, sub_dim, dtype, n_c):
     """Rows x = (a, a, b, b, ...) are exactly equidistant (in real arithmetic)
     from a centroid and its copy with coordinates swapped pairwise; the fp32
     sums differ only by rounding order, so the winner is decided at the last
     bit.  The swapped copies sit in other centroid groups."""
     rng = np.random.default_rng(11 + sub_dim)
-    n_c, m = 256, 20000
+    m = 20000  # 256 centroids: the tensor-core kernel; 320: the filter kernel
     half = n_c // 2
     base = rng.standard_normal((half, sub_dim)).astype(dtype)
     swapped = base.reshape(half, sub_dim // 2, 2)[:, :, ::-1].reshape(half, sub_dim)
@@ -82,13 +83,14 @@ def test_permuted_coordinate_ties(vq, oracle_mod, sub_dim, dtype):
     check(vq, oracle_mod, x[None], cb[None])
 
 
+@pytest.mark.parametrize("n_c", [256, 320])
 @pytest.mark.parametrize("dtype", [np.float16, np.float32])
 @pytest.mark.parametrize("copies", [2, 3, 5])
-def test_duplicated_centroids_across_groups(vq, oracle_mod, copies, dtype):
+def test_duplicated_centroids_across_groups(vq, oracle_mod, copies, dtype, n_c):
     """Exact duplicate centroids in `copies` different groups: with three or
     more, rows near them take the exact queue."""
     rng = np.random.default_rng(20 + copies)
-    n_c, sub = 256, 8
+    sub = 8
     cb = rng.standard_normal((n_c, sub)).astype(dtype)
     for src in range(0, 40, 4):
         for k in range(1, copies):
@@ -99,12 +101,13 @@ def test_duplicated_centroids_across_groups(vq, oracle_mod, copies, dtype):
     check(vq, oracle_mod, x.astype(dtype)[None], cb[None])
 
 
+@pytest.mark.parametrize("n_c", [256, 320])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_extreme_magnitudes(vq, oracle_mod, dtype):
+def test_extreme_magnitudes(vq, oracle_mod, dtype, n_c):
     """Huge rows (queued: the bound would be near overflow) and tiny rows
     (gradual underflow; the bound's absolute term) next to ordinary ones."""
     rng = np.random.default_rng(5)
-    sub, n_c = 4, 256
+    sub = 4
     cb = rng.standard_normal((n_c, sub)).astype(np.float32)
     x = rng.standard_normal((6000, sub)).astype(np.float32)
     x[:1000] *= 1e25
@@ -115,7 +118,7 @@ def test_extreme_magnitudes(vq, oracle_mod, dtype):
         ct = torch.from_numpy(cb).to(torch.bfloat16)
         got = None
         desc = vq.vq_describe_launch(1, x.shape[0], n_c, sub, torch.bfloat16, xt.cuda().data_ptr())
-        assert desc.startswith("kernel=encode_tc")
+        assert desc.startswith("kernel=" + expected_kernel("bf16", n_c))
         got = vq.vq_encode(xt.cuda(), ct.cuda()).cpu().numpy()
         want = oracle_mod.encode(xt.view(torch.int16).numpy().view(np.uint16),
                                  ct.view(torch.int16).numpy().view(np.uint16), bf16=True,
@@ -143,13 +146,14 @@ def test_codebook_sizes_around_the_groups(vq, oracle_mod, n_c, sub_dim):
     check(vq, oracle_mod, x, cb)
 
 
+@pytest.mark.parametrize("n_c", [256, 320])
 @pytest.mark.parametrize("dtype", [np.float16, np.float32])
 @pytest.mark.parametrize("scale", [0.01, 1000.0])
-def test_clustered_keys_near_many_centroids(vq, oracle_mod, dtype, scale):
+def test_clustered_keys_near_many_centroids(vq, oracle_mod, dtype, scale, n_c):
     """Keys concentrated near the origin, where many centroids are at similar
     distances (more candidate groups per row), at small and large scale."""
     rng = np.random.default_rng(8)
-    cb = (rng.standard_normal((256, 8)) * scale).astype(dtype)
+    cb = (rng.standard_normal((n_c, 8)) * scale).astype(dtype)
     x = (rng.standard_normal((20000, 8)) * scale).astype(dtype)
     check(vq, oracle_mod, x[None], cb[None])
 
