@@ -39,6 +39,18 @@
 // A_i); the accumulation spans 2 K terms, 16 or 32, whose truncating fp32
 // error (at most 32 x 2^-23 = 2^-18 of the magnitudes) eps_tc still covers.
 //
+// Underflow.  The relative bounds above hold for normal numbers.  Below
+// 2^-126 a split drops up to 2^-136 absolute (the mask keeps no bit of a
+// subnormal below 2^-136), and the tensor core may flush subnormal operands,
+// products or partial sums.  A flushed or dropped part of x (below 2^-126 per
+// element) costs at most 2^-125 A_i per term, which 2^-100 covers while
+// A_i <= 2^22 and 2^-15 C2 (C2 >= A_i^2 up to rounding) covers beyond.  A
+// flushed or dropped part of -2c (below 2^-125) costs at most 2^-125 |x_i|,
+// which the A_i term covers once A_i is floored at 2^-100 (2^-15 x 2^-100 =
+// 2^-115); a larger bound only widens the candidate set.  Rounding the
+// |c|^2 pieces drops below 2^-136.  Each of these is a few 2^-125 terms
+// next to the 2^-100 that bnd and thr carry.
+//
 // The accumulator of a tile is a 128-lane x n_pad-column fp32 block of tensor
 // memory, so thread t of the block owns row t of the tile: it reads its own
 // row's scores (tcgen05.ld) and reduces them without any exchange.
@@ -352,9 +364,11 @@ __global__ void __launch_bounds__(128, MINB)
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const float c2 = __uint_as_float(smax[0]);
+    // A_i, floored at 2^-100 (compared as bits, so a NaN maximum stays NaN):
+    // the floor covers the tiny-codebook terms the tensor core may flush
     float amax[SUB];
 #pragma unroll
-    for (int i = 0; i < SUB; ++i) amax[i] = __uint_as_float(smax[1 + i]);
+    for (int i = 0; i < SUB; ++i) amax[i] = __uint_as_float(max(smax[1 + i], 0x0d800000u));
     // 2 eps_tc + 2 gamma_SUB; with split rows, 2 (1 + 2^-9) eps_tc and the
     // dropped low part's 2^-19; with split codebooks too, 2^-17 for the three
     // dropped products

@@ -128,6 +128,46 @@ def test_extreme_magnitudes(vq, oracle_mod, dtype, n_c):
         check(vq, oracle_mod, x[None], cb[None])
 
 
+@pytest.mark.parametrize("n_c", [256, 320])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layout", ["all_subnormal", "one_dim_subnormal"])
+def test_subnormal_codebooks(vq, oracle_mod, layout, dtype, n_c):
+    """Codebooks whose coordinates (all, or those of one dimension) are fp32
+    subnormals, against rows at the same scale, rows far below it and rows
+    with a huge coordinate: the regime where splits lose bits below 2^-136
+    and the tensor core may flush operands, covered by the bound's absolute
+    term and its floor on the per-dimension maxima."""
+    rng = np.random.default_rng(31)
+    sub = 4
+    cb = rng.standard_normal((n_c, sub)).astype(np.float32)
+    tiny = np.float32(2.0 ** -132)
+    if layout == "all_subnormal":
+        cb *= tiny
+    else:
+        cb[:, 0] *= tiny
+    src = rng.integers(0, n_c, 8000)
+    x = cb[src] + rng.standard_normal((8000, sub)).astype(np.float32) * (cb.std(axis=0) * 0.3)
+    x[:1000] *= np.float32(2.0 ** -10)
+    x[1000:2000, 0] = rng.standard_normal(1000).astype(np.float32) * np.float32(1e20)
+    x[2000:3000, 0] = rng.standard_normal(1000).astype(np.float32) * np.float32(2.0 ** -100)
+    x = x.astype(np.float32)
+    assert (np.abs(cb[cb != 0]) < 2.0 ** -126).any()
+    if dtype == "bf16":
+        xt = torch.from_numpy(x).to(torch.bfloat16)
+        ct = torch.from_numpy(cb).to(torch.bfloat16)
+        xd = xt.cuda()
+        desc = vq.vq_describe_launch(1, x.shape[0], n_c, sub, torch.bfloat16, xd.data_ptr())
+        assert desc.startswith("kernel=" + expected_kernel("bf16", n_c)), desc
+        got = vq.vq_encode(xd, ct.cuda()).cpu().numpy()
+        want = oracle_mod.encode(xt.view(torch.int16).numpy().view(np.uint16),
+                                 ct.view(torch.int16).numpy().view(np.uint16), bf16=True,
+                                 n_threads=THREADS)
+        bad = np.argwhere(got != want)
+        assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
+    else:
+        check(vq, oracle_mod, x[None], cb[None])
+
+
 @pytest.mark.parametrize("n_c", [200, 300])
 def test_codebook_with_nan_queues_every_row(vq, oracle_mod, n_c):
     rng = np.random.default_rng(6)
