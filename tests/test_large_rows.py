@@ -9,6 +9,10 @@ was written and is a valid index (the output is pre-filled with a value no
 index takes), the 8-bit codes equal the uint32 indices, and the decode is the
 codebook gather.  Against the oracle: sampled rows, among them the first and
 last rows, the rows around 2^31 and 2^30, and the group boundaries.
+The sibling encoders run past 2^31 elements as well: the scalar quantize
+(both paths, every element checked through the oracle's answer for each of
+the 65,536 fp16 bit patterns) with its dequantize, and the Hadamard rotation
+with and without the quantize (sampled rows against the oracle).
 The inputs are seeded N(0, 1) draws made on the device.
 """
 import os
@@ -142,4 +146,79 @@ def test_grouped_offsets_past_2_32_elements(vq, oracle_mod, big):
     assert_all_valid(o)
     check_sampled(oracle_mod, x3, cb, o, seed=81)
     del o, out
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- sibling encoders
+
+N_SCALAR = (1 << 31) + 13        # elements: 16-byte units and a ragged tail
+HD_DIM, HD_ROWS = 128, (1 << 24) + 3   # 2^31 + 384 rotated elements
+
+
+@pytest.fixture(scope="module")
+def centroids16():
+    # sorted, as a Lloyd-Max codebook for N(0, 1) would be
+    return torch.linspace(-2.4, 2.4, 16, dtype=torch.float32, device="cuda")
+
+
+def fp16_normal(n: int, seed: int) -> torch.Tensor:
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    x = torch.empty(n, dtype=torch.float16, device="cuda")
+    for a in range(0, n, CHUNK * SUB):
+        x[a:a + CHUNK * SUB].normal_(generator=gen)
+    return x
+
+
+def test_scalar_quantize_past_2_31_elements(vq, oracle_mod, centroids16):
+    """Both scalar paths (the 64 KiB table and the register scan) and the
+    dequantize.  A 16-bit key's index depends on its bit pattern alone, so
+    the oracle's answer for all 65,536 patterns checks every element."""
+    x = fp16_normal(N_SCALAR, 901)
+    c = centroids16
+    pats = np.arange(1 << 16, dtype=np.uint16).view(np.float16)
+    table = torch.from_numpy(oracle_mod.scalar_quantize(pats, c.cpu().numpy()).astype(np.uint8)).cuda()
+    bits = x.view(torch.int16)
+    got_t = vq.vq_scalar_quantize(x, c)
+    got_s = vq.vq_scalar_quantize(x, c, use_table=False)
+    torch.cuda.synchronize()
+    for a in range(0, N_SCALAR, CHUNK):
+        want = table[bits[a:a + CHUNK].to(torch.int64) & 0xFFFF]
+        assert torch.equal(got_t[a:a + CHUNK], want), a
+        assert torch.equal(got_s[a:a + CHUNK], want), a
+    del got_s
+    dq = vq.vq_scalar_dequantize(got_t, c, dtype=torch.float16)
+    torch.cuda.synchronize()
+    c16 = c.to(torch.float16)
+    for a in range(0, N_SCALAR, CHUNK):
+        assert torch.equal(dq[a:a + CHUNK], c16[got_t[a:a + CHUNK].long()]), a
+    del x, got_t, dq
+    torch.cuda.empty_cache()
+
+
+def test_hadamard_past_2_31_elements(vq, oracle_mod, centroids16):
+    """Rotation and rotation + quantize over 2^24 + 3 rows of 128: sampled
+    rows against the oracle (bit for bit), every code valid."""
+    x = fp16_normal(HD_ROWS * HD_DIM, 902).view(HD_ROWS, HD_DIM)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(903)
+    diag = (torch.randint(0, 2, (HD_DIM,), generator=gen, device="cuda") * 2 - 1).to(torch.float32)
+    c = centroids16
+    codes = vq.vq_hadamard_quantize(x, diag, c)
+    torch.cuda.synchronize()
+    flat = codes.view(-1)
+    for a in range(0, flat.numel(), CHUNK):
+        assert int(flat[a:a + CHUNK].max()) < c.numel(), a
+    rows = torch.from_numpy(sample_rows(HD_ROWS, 904)).cuda()
+    xs = x.index_select(0, rows).cpu().numpy()
+    want = oracle_mod.hadamard_quantize(xs, diag.cpu().numpy(), c.cpu().numpy())
+    got = codes.index_select(0, rows).cpu().numpy()
+    assert np.array_equal(got.astype(np.uint32), want)
+    del codes, flat
+    y = vq.vq_hadamard_rotate(x, diag)
+    torch.cuda.synchronize()
+    want_y = oracle_mod.hadamard_rotate(xs, diag.cpu().numpy())
+    got_y = y.index_select(0, rows).cpu().numpy()
+    assert np.array_equal(got_y.view(np.uint32), want_y.view(np.uint32))
+    del x, y
     torch.cuda.empty_cache()
