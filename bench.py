@@ -384,7 +384,8 @@ def bench_ours(args) -> None:
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / world / PAGES_FALCON_SUBVEC_PER_S
                         if args.workload == "falcon_prefill" and not variant else None),
-        "dtype": "f32", "data": "synthetic (seeded N(0,1) fp16 keys and codebooks)",
+        "dtype": "f32", "data": "synthetic (seeded N(0,1) fp16 keys and codebooks"
+                                + (f", as {args.dtype})" if args.dtype != "f16" else ")"),
         "config": dict(config_block(w, args, world), timed_region_s=region_s,
                        n_centroids=int(cb.shape[1]), input_dtype=args.dtype,
                        x_misaligned=bool(args.misalign),
