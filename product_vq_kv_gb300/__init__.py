@@ -6,6 +6,8 @@ hand-written sm_103a CUDA kernels behind a C ABI (``include/vq_encode.h``).
 This package is the thin Python binding of that library.
 """
 from ._binding import (  # noqa: F401
+    ATTN_STATIC_SCRATCH_BYTES,
+    VQError,
     VQ_BF16,
     VQ_ERR_CUDA,
     VQ_ERR_INTERNAL,
@@ -14,24 +16,22 @@ from ._binding import (  # noqa: F401
     VQ_F16,
     VQ_F32,
     VQ_OK,
-    VQError,
     load_library,
     vq_abi_version,
-    ATTN_STATIC_SCRATCH_BYTES,
     vq_attention_decode,
     vq_attention_decode_static,
     vq_attention_workspace_bytes,
-    vq_describe_launch,
     vq_dequantize_grouped,
+    vq_describe_launch,
     vq_encode,
     vq_encode_grouped,
     vq_encode_grouped_host,
     vq_encode_grouped_smooth,
+    vq_encode_grouped_u8,
     vq_hadamard_quantize,
     vq_hadamard_rotate,
     vq_scalar_dequantize,
     vq_scalar_quantize,
-    vq_encode_grouped_u8,
     vq_status_string,
 )
 from .build import LIB_PATH  # noqa: F401

@@ -271,9 +271,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     }
     for (int e = threadIdx.x; e < 256 * ncopies * sub; e += THREADS) {
         const int i = e % sub;
-        const int k = (e / sub) % ncopies;
-        const int c = e / (sub * ncopies);
-        (void)k;
+        const int c = e / (sub * ncopies);  // every copy holds the same rows
         vcs[e] = c < nc ? vc[(size_t)c * sub + i] : T(0.f);
     }
     __syncthreads();

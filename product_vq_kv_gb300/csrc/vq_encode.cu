@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -23,21 +24,22 @@
 int vqh_device_sms()
 {
     constexpr int kMax = 64;
-    static int cache[kMax] = {};
+    // per device; concurrent first calls store the same value
+    static std::atomic<int> cache[kMax] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMax) {
         (void)cudaGetLastError();
         return 0;
     }
-    if (cache[dev] == 0) {
-        int sms = 0;
+    int sms = cache[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             (void)cudaGetLastError();
             return 0;
         }
-        cache[dev] = sms;
+        cache[dev].store(sms, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return sms;
 }
 
 namespace {
