@@ -244,7 +244,8 @@ def bench_reference(args) -> None:
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_block(w, args, world),
+        "config": dict(config_block(w, args, world),
+                       l2="not applicable: the CPU oracle, wall-clock time over the steps"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"first {rows} of {w.n} sub-vectors of {args.workload} per "
                                    f"step, {cores} threads"},
