@@ -244,3 +244,18 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         b.load_library()
+
+
+def test_bench_launch_matches_the_measured_traffic_key(lib):
+    """The Falcon-shape launch the benchmark times (152 SMs, as on GB300 and
+    as the host assumes without a device) is the launch whose DRAM traffic was
+    measured; a planner change that alters it retires that figure."""
+    import bench
+
+    f = lib.vq_describe_launch
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int32]
+    buf = ctypes.create_string_buffer(512)
+    assert f(1, 1 << 20, 256, 4, 0, 1 << 20, buf, 512) == 0
+    assert buf.value.decode() in bench.MEASURED_TRAFFIC, buf.value.decode()
