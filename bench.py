@@ -695,7 +695,7 @@ def main() -> None:
     p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="falcon_prefill")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--dtype", choices=["f16", "bf16", "f32"], default="f16",
-                   help="encode: input type (f32 takes the CUDA-core filter kernel)")
+                   help="encode: input type (f32 rows and codebooks go to the tensor cores as tf32 pieces)")
     p.add_argument("--centroids", type=int, default=0,
                    help="encode: use only the first N codebook rows (below 64: brute force)")
     p.add_argument("--misalign", action="store_true",
