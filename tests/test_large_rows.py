@@ -4,7 +4,8 @@ which any 32-bit row, tile or element offset would wrap.
 One group of 2^31 + 4099 fp16 sub-vectors (sub_dim 4, 256 centroids: the
 tensor-core kernel, a ragged last tile) is encoded to uint32 indices and to
 8-bit codes, and the codes are decoded; three groups of 2^30 + 77 rows are
-encoded in one grouped launch.  Checks, at full size on the GPU: every output
+encoded in one grouped launch, and 2^31 + 4160 rows with per-channel smoothing.
+Checks, at full size on the GPU: every output
 was written and is a valid index (the output is pre-filled with a value no
 index takes), the 8-bit codes equal the uint32 indices, and the decode is the
 codebook gather.  Against the oracle: sampled rows, among them the first and
@@ -145,6 +146,43 @@ def test_grouped_offsets_past_2_32_elements(vq, oracle_mod, big):
     torch.cuda.synchronize()
     assert_all_valid(o)
     check_sampled(oracle_mod, x3, cb, o, seed=81)
+    del o, out
+    torch.cuda.empty_cache()
+
+
+
+def test_smoothed_encode_past_2_31_rows(vq, oracle_mod, big):
+    """Per-channel smoothing fused into the tensor-core encode over 2^31 + 4160
+    rows (keys of head_dim 256: the channel of a row comes from its index
+    modulo 64).  Every index written and valid; whole sampled keys, among them
+    those around row 2^31, against the oracle."""
+    x, cb = big
+    head_dim = 256
+    spk = head_dim // SUB
+    m = (1 << 31) + 65 * spk
+    x3 = x[:m * SUB].view(1, m, SUB)
+    cb1 = cb[:1].contiguous()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(20252)
+    smooth = torch.exp(0.5 * torch.randn((1, head_dim), generator=gen, device="cuda"))
+    o, out = sentinel_out(1, m)
+    vq.vq_encode_grouped_smooth(x3, smooth, cb1, head_dim, index_bytes=4, out=out)
+    torch.cuda.synchronize()
+    assert_all_valid(o)
+    n_keys = m // spk
+    rng = np.random.default_rng(91)
+    centre = (1 << 31) // spk
+    keys = np.unique(np.concatenate([np.arange(0, 30), np.arange(n_keys - 30, n_keys),
+                                     np.arange(centre - 30, centre + 30),
+                                     rng.integers(0, n_keys, 200)]))
+    rows = (keys[:, None] * spk + np.arange(spk)[None, :]).reshape(-1)
+    ridx = torch.from_numpy(rows).cuda()
+    xs = x3[0].index_select(0, ridx).cpu().numpy()
+    want = oracle_mod.encode_smooth(xs[None], smooth.cpu().numpy(), cb1.cpu().numpy(), head_dim,
+                                    n_threads=THREADS)[0]
+    got = o[0].index_select(0, ridx).cpu().numpy().astype(np.int64)
+    bad = np.nonzero(got != want.astype(np.int64))[0]
+    assert bad.size == 0, f"{bad.size} sampled rows differ, first row {rows[bad[0]]}"
     del o, out
     torch.cuda.empty_cache()
 
