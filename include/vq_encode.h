@@ -237,6 +237,12 @@ size_t vq_attention_workspace_bytes(int64_t batch, int32_t heads_q, int32_t head
  * kernels overlap on the GPU (on different streams, or from several host
  * threads without ordering between them) race on it and give wrong results,
  * so issue them in one stream order.  Nothing in the array needs clearing.
+ * Device: the array used is the CURRENT device's; `stream` and every pointer
+ * must belong to that device (a q on another device returns
+ * VQ_ERR_INVALID_ARG).  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) and keeps it: make that first call
+ * before any stream capture, and do not call cudaDeviceReset on a device
+ * between calls (the kept address would then be stale).
  */
 vq_status vq_attention_decode_static(const void *q, const uint8_t *k_codes,
                                      const void *k_codebooks, const uint8_t *v_codes,

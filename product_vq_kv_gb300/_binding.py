@@ -358,6 +358,51 @@ def vq_attention_workspace_bytes(batch: int, heads_q: int, heads_kv: int, tokens
                                                            window))
 
 
+def _check_attention_args(q, k_codes, k_codebooks, v_codes, v_codebooks):
+    """Validate the tensors of an attention call before any pointer is taken.
+
+    Shapes and dtypes are checked first (so every mismatch is reported the
+    same way whatever the device), then that every tensor is a contiguous CUDA
+    tensor on q's device.  Returns ``(B, Hq, Hkv, T, D, sub_dim, n_c)``.
+    """
+    named = (("q", q), ("k_codes", k_codes), ("k_codebooks", k_codebooks),
+             ("v_codes", v_codes), ("v_codebooks", v_codebooks))
+    for name, t in named:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+    if q.dim() != 3 or k_codes.dim() != 4 or k_codebooks.dim() != 3:
+        raise ValueError(f"expected q [B, Hq, D], k_codes [B, Hkv, T, D/sub_dim] and "
+                         f"k_codebooks [Hkv, n_c, sub_dim], got {tuple(q.shape)}, "
+                         f"{tuple(k_codes.shape)} and {tuple(k_codebooks.shape)}")
+    _dtype_code(q)
+    if k_codes.dtype != torch.uint8 or v_codes.dtype != torch.uint8:
+        raise TypeError("codes must be uint8")
+    if k_codebooks.dtype != q.dtype or v_codebooks.dtype != q.dtype:
+        raise TypeError("codebooks must share q's dtype")
+    b, hq, d = q.shape
+    _, hkv, tokens, ns = k_codes.shape
+    n_c, sub = k_codebooks.shape[1], k_codebooks.shape[2]
+    if (tuple(v_codes.shape) != tuple(k_codes.shape) or k_codes.shape[0] != b or ns * sub != d
+            or tuple(k_codebooks.shape) != (hkv, n_c, sub)
+            or tuple(v_codebooks.shape) != (hkv, n_c, sub)):
+        raise ValueError("inconsistent shapes: q [B, Hq, D], codes [B, Hkv, T, D/sub_dim] (keys "
+                         "and values alike), codebooks [Hkv, n_c, sub_dim] (keys and values alike)")
+    for name, t in named:
+        _device_tensor(t, name)
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+    return b, hq, hkv, tokens, d, sub, n_c
+
+
+def _check_attention_out(out, q):
+    if out is None:
+        return torch.empty_like(q)
+    if (not isinstance(out, torch.Tensor) or out.dtype != q.dtype or out.shape != q.shape
+            or out.device != q.device or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous tensor of q's shape, dtype and device")
+    return out
+
+
 def vq_attention_decode(q: torch.Tensor, k_codes: torch.Tensor, k_codebooks: torch.Tensor,
                         v_codes: torch.Tensor, v_codebooks: torch.Tensor, window: int = 0,
                         scale: float = 0.0, out: torch.Tensor | None = None,
@@ -371,29 +416,22 @@ def vq_attention_decode(q: torch.Tensor, k_codes: torch.Tensor, k_codebooks: tor
     device byte tensor for the per-slice partials; if omitted one of
     :func:`vq_attention_workspace_bytes` bytes is allocated here (by torch).
     """
-    for t, name in ((q, "q"), (k_codes, "k_codes"), (k_codebooks, "k_codebooks"),
-                    (v_codes, "v_codes"), (v_codebooks, "v_codebooks")):
-        _device_tensor(t, name)
-    if k_codes.dtype != torch.uint8 or v_codes.dtype != torch.uint8:
-        raise TypeError("codes must be uint8")
-    if k_codebooks.dtype != q.dtype or v_codebooks.dtype != q.dtype:
-        raise TypeError("codebooks must share q's dtype")
-    b, hq, d = q.shape
-    _, hkv, tokens, ns = k_codes.shape
-    n_c, sub = k_codebooks.shape[1], k_codebooks.shape[2]
-    if (k_codes.shape != v_codes.shape or k_codes.shape[0] != b or ns * sub != d
-            or k_codebooks.shape != (hkv, n_c, sub) or v_codebooks.shape != (hkv, n_c, sub)):
-        raise ValueError("inconsistent shapes")
-    if out is None:
-        out = torch.empty_like(q)
+    b, hq, hkv, tokens, d, sub, n_c = _check_attention_args(q, k_codes, k_codebooks, v_codes,
+                                                            v_codebooks)
+    out = _check_attention_out(out, q)
     if workspace is None:
         nbytes = vq_attention_workspace_bytes(b, hq, hkv, tokens, d, sub, n_c, window)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
-    st = load_library().vq_attention_decode(
-        q.data_ptr(), k_codes.data_ptr(), k_codebooks.data_ptr(), v_codes.data_ptr(),
-        v_codebooks.data_ptr(), b, hq, hkv, tokens, d, sub, n_c, window, scale, _dtype_code(q),
-        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-        _stream_handle(stream, q.device))
+    else:
+        _device_tensor(workspace, "workspace")
+        if workspace.device != q.device:
+            raise ValueError(f"workspace is on {workspace.device}, q on {q.device}")
+    with torch.cuda.device(q.device):
+        st = load_library().vq_attention_decode(
+            q.data_ptr(), k_codes.data_ptr(), k_codebooks.data_ptr(), v_codes.data_ptr(),
+            v_codebooks.data_ptr(), b, hq, hkv, tokens, d, sub, n_c, window, scale,
+            _dtype_code(q), out.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
     _check(st, "vq_attention_decode")
     return out
 
@@ -411,20 +449,20 @@ def vq_attention_decode_static(q: torch.Tensor, k_codes: torch.Tensor, k_codeboo
     allocate device memory per call (a decode loop whose HBM is planned up
     front, host code without a caching allocator).  The library allocates
     nothing; pass ``out`` to allocate nothing here either.  Calls that overlap
-    on the GPU share that array and race: keep them in one stream order."""
-    b, hq, d = q.shape
+    on the GPU share that array and race: keep them in one stream order.  The
+    call runs with q's device current, whose copy of the array it uses."""
+    b, hq, hkv, tokens, d, sub, n_c = _check_attention_args(q, k_codes, k_codebooks, v_codes,
+                                                            v_codebooks)
     if b * hq * (d + 2) * 4 > ATTN_STATIC_SCRATCH_BYTES:
         raise VQError(VQ_ERR_INVALID_ARG,
                       f"vq_attention_decode_static (one token slice needs {b * hq * (d + 2) * 4} "
                       f"bytes of scratch; the built-in array holds {ATTN_STATIC_SCRATCH_BYTES})")
-    if out is None:
-        out = torch.empty_like(q)
-    _, hkv, tokens, _ = k_codes.shape
-    n_c, sub = k_codebooks.shape[1], k_codebooks.shape[2]
-    st = load_library().vq_attention_decode_static(
-        q.data_ptr(), k_codes.data_ptr(), k_codebooks.data_ptr(), v_codes.data_ptr(),
-        v_codebooks.data_ptr(), b, hq, hkv, tokens, d, sub, n_c, window, scale, _dtype_code(q),
-        out.data_ptr(), _stream_handle(stream, q.device))
+    out = _check_attention_out(out, q)
+    with torch.cuda.device(q.device):
+        st = load_library().vq_attention_decode_static(
+            q.data_ptr(), k_codes.data_ptr(), k_codebooks.data_ptr(), v_codes.data_ptr(),
+            v_codebooks.data_ptr(), b, hq, hkv, tokens, d, sub, n_c, window, scale,
+            _dtype_code(q), out.data_ptr(), _stream_handle(stream, q.device))
     _check(st, "vq_attention_decode_static")
     return out
 

@@ -154,18 +154,16 @@ vq_status attn_launch(const AttnPlan &p, const void *q, const uint8_t *kcodes, c
 // All calls on a device share it.
 static __device__ __align__(256) unsigned char g_attn_scratch[VQ_ATTN_STATIC_SCRATCH_BYTES];
 
-// Device address of g_attn_scratch on the current device, looked up once per
-// device; nullptr if the lookup fails.
-void *static_scratch()
+// Device address of g_attn_scratch on the current device, looked up on the
+// first call on that device and kept (a cudaDeviceReset between calls would
+// leave it stale, which the header rules out); nullptr if the lookup fails.
+// `dev` is the current device.
+void *static_scratch(int dev)
 {
     constexpr int kMaxDevices = 64;
     static std::mutex mu;
     static void *addr[kMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        (void)cudaGetLastError();
-        return nullptr;
-    }
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
     if (addr[dev] == nullptr) {
         void *p = nullptr;
@@ -258,7 +256,21 @@ vq_status vq_attention_decode_static(const void *q, const uint8_t *k_codes,
     if ((uint64_t)batch * (uint64_t)heads_q * (uint64_t)(head_dim + 2) * sizeof(float) >
         VQ_ATTN_STATIC_SCRATCH_BYTES)
         return VQ_ERR_INVALID_ARG;
-    void *scratch = static_scratch();
+    // The array used is the current device's, so q must live there: a kernel
+    // on another device would write the partials into this device's copy.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VQ_ERR_CUDA;
+    if (q != nullptr) {
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+            (void)cudaGetLastError();  // not a pointer CUDA knows
+            return VQ_ERR_INVALID_ARG;
+        }
+        if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+            return VQ_ERR_INVALID_ARG;
+        if (at.type == cudaMemoryTypeDevice && at.device != dev) return VQ_ERR_INVALID_ARG;
+    }
+    void *scratch = static_scratch(dev);
     if (scratch == nullptr) return VQ_ERR_CUDA;
     return vq_attention_decode(q, k_codes, k_codebooks, v_codes, v_codebooks, batch, heads_q,
                                heads_kv, tokens, head_dim, sub_dim, n_centroids, window, scale,

@@ -259,3 +259,63 @@ def test_bench_launch_matches_the_measured_traffic_key(lib):
     buf = ctypes.create_string_buffer(512)
     assert f(1, 1 << 20, 256, 4, 0, 1 << 20, buf, 512) == 0
     assert buf.value.decode() in bench.MEASURED_TRAFFIC, buf.value.decode()
+
+
+def _attention_inputs(torch, b=2, hq=8, hkv=2, t=16, d=128, sub=8, n_c=256):
+    q = torch.zeros((b, hq, d), dtype=torch.float16)
+    kc = torch.zeros((b, hkv, t, d // sub), dtype=torch.uint8)
+    cb = torch.zeros((hkv, n_c, sub), dtype=torch.float16)
+    return [q, kc, cb, kc.clone(), cb.clone()]
+
+
+def _bad_attention_inputs(torch):
+    """(description, inputs, exception type, message) cases the Python wrappers
+    must reject before a pointer reaches the library."""
+    cases = []
+
+    def case(name, edit, exc, match):
+        args = _attention_inputs(torch)
+        edit(args)
+        cases.append((name, args, exc, match))
+
+    case("int32 key codes", lambda a: a.__setitem__(1, a[1].to(torch.int32)), TypeError, "uint8")
+    case("int32 value codes", lambda a: a.__setitem__(3, a[3].to(torch.int32)), TypeError, "uint8")
+    case("key codebook dtype", lambda a: a.__setitem__(2, a[2].float()), TypeError, "q's dtype")
+    case("value codebook dtype", lambda a: a.__setitem__(4, a[4].bfloat16()), TypeError, "q's dtype")
+    case("int q", lambda a: a.__setitem__(0, a[0].to(torch.int16)), TypeError, "dtype")
+    case("short value codes", lambda a: a.__setitem__(3, a[3][:, :, :8].contiguous()),
+         ValueError, "inconsistent")
+    case("value codebook rows", lambda a: a.__setitem__(4, a[4][:, :128].contiguous()),
+         ValueError, "inconsistent")
+    case("key codebook sub_dim", lambda a: a.__setitem__(2, torch.zeros((2, 256, 4), dtype=torch.float16)),
+         ValueError, "inconsistent")
+    case("batch mismatch", lambda a: a.__setitem__(0, torch.zeros((3, 8, 128), dtype=torch.float16)),
+         ValueError, "inconsistent")
+    case("2-D q", lambda a: a.__setitem__(0, a[0][0]), ValueError, "expected q")
+    case("host tensors", lambda a: None, ValueError, "CUDA tensor")
+    return cases
+
+
+@pytest.mark.parametrize("entry", ["vq_attention_decode", "vq_attention_decode_static"])
+def test_attention_wrappers_reject_bad_inputs_before_launch(monkeypatch, entry):
+    """Both attention wrappers share one check: wrong code or codebook dtypes,
+    inconsistent key and value shapes, and host or non-contiguous tensors all
+    raise before any pointer is handed to the library."""
+    import torch
+
+    import product_vq_kv_gb300._binding as b
+
+    def no_library():
+        raise AssertionError("the library was reached with bad inputs")
+
+    monkeypatch.setattr(b, "load_library", no_library)
+    fn = getattr(b, entry)
+    for name, args, exc, match in _bad_attention_inputs(torch):
+        with pytest.raises(exc, match=match):
+            fn(*args)
+    # a non-contiguous tensor with consistent shapes is rejected by the device
+    # check (on a machine without a GPU, as a host tensor)
+    args = _attention_inputs(torch)
+    args[0] = torch.zeros((2, 128, 8), dtype=torch.float16).transpose(1, 2)
+    with pytest.raises(ValueError, match="CUDA tensor|contiguous"):
+        fn(*args)
