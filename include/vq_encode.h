@@ -34,10 +34,12 @@
  *   - A launch failure returns VQ_ERR_CUDA; the CUDA error is left for the
  *     caller to inspect (cudaGetLastError) and is not cleared.
  *   - The tensor-core kernel waits for its matrix units with a bounded
- *     number of polls.  Should a wait give up (never observed), the rows the
- *     block has not encoded are written as 0xFFFFFFFF, an index no codebook
- *     has; with 8-bit codes that marker is 255, which is a valid code when
- *     n_centroids is 256, so it then cannot be told from one.
+ *     number of polls.  Should a wait give up (never observed in normal
+ *     use), the rows the block has not encoded are written as 0xFFFFFFFF, an
+ *     index no codebook has, and the device status word records it
+ *     (vq_kernel_status, VQ_KSTATUS_WAIT_GAVE_UP); with 8-bit codes the
+ *     marker is 255, a valid code when n_centroids is 256, so there only the
+ *     status word tells.
  *   - N = 0 (or n_per_group = 0) is valid: VQ_OK, nothing is launched, and
  *     the pointers may be NULL.
  *   - Supported shapes: 1 <= sub_dim <= 32, 1 <= n_centroids <= 4096.
@@ -315,6 +317,27 @@ const char *vq_status_string(vq_status status);
 vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_centroids,
                              int32_t sub_dim, vq_dtype dtype, const void *x, char *buf,
                              int32_t buflen);
+
+/*
+ * vq_kernel_status -- the out-of-band failure record of the library's
+ * kernels on the current device.  Waits for the device to finish all work
+ * (cudaDeviceSynchronize), then sets *bits to the OR of the status bits that
+ * kernels launched on this device have set since the last clear, and resets
+ * them to zero if `clear` is nonzero.  0 means every kernel finished its work
+ * normally.  A bit is needed beside the in-band marker because the marker of
+ * 8-bit codes (255) is a valid code when n_centroids is 256.
+ *   VQ_KSTATUS_WAIT_GAVE_UP   a tensor-core encode's wait for its matrix
+ *                             units gave up; the rows it had not encoded hold
+ *                             0xFFFFFFFF (255 as 8-bit codes)
+ *   VQ_KSTATUS_OUT_OF_BOUNDS  bounds-checked build only: an index fell
+ *                             outside its buffer and the access was skipped
+ * Returns VQ_ERR_INVALID_ARG for a NULL `bits`, VQ_ERR_CUDA if the
+ * synchronisation or the read fails (*bits is then 0).  Not part of the
+ * pages' method; it is this library's failure report.
+ */
+#define VQ_KSTATUS_WAIT_GAVE_UP 0x1u
+#define VQ_KSTATUS_OUT_OF_BOUNDS 0x2u
+vq_status vq_kernel_status(uint32_t *bits, int32_t clear);
 
 /* ABI version of this header (bumped on incompatible changes). */
 #define VQ_ENCODE_ABI_VERSION 1

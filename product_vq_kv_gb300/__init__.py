@@ -15,6 +15,8 @@ from ._binding import (  # noqa: F401
     VQ_ERR_UNSUPPORTED,
     VQ_F16,
     VQ_F32,
+    VQ_KSTATUS_OUT_OF_BOUNDS,
+    VQ_KSTATUS_WAIT_GAVE_UP,
     VQ_OK,
     load_library,
     vq_abi_version,
@@ -30,6 +32,7 @@ from ._binding import (  # noqa: F401
     vq_encode_grouped_u8,
     vq_hadamard_quantize,
     vq_hadamard_rotate,
+    vq_kernel_status,
     vq_scalar_dequantize,
     vq_scalar_quantize,
     vq_status_string,

@@ -83,6 +83,8 @@ def load_library() -> ctypes.CDLL:
         lib.vq_describe_launch.argtypes = [i64, i64, i32, i32, i32, vp, ctypes.c_char_p, i32]
         lib.vq_abi_version.restype = i32
         lib.vq_abi_version.argtypes = []
+        lib.vq_kernel_status.restype = i32
+        lib.vq_kernel_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         _lib = lib
         return lib
 
@@ -93,6 +95,23 @@ def vq_status_string(status: int) -> str:
 
 def vq_abi_version() -> int:
     return int(load_library().vq_abi_version())
+
+
+# Bits of the device status word (vq_kernel_status).
+VQ_KSTATUS_WAIT_GAVE_UP = 0x1
+VQ_KSTATUS_OUT_OF_BOUNDS = 0x2
+
+
+def vq_kernel_status(clear: bool = True, device=None) -> int:
+    """The status bits the library's kernels set on ``device`` (default: the
+    current device) since the last clear, after waiting for that device to
+    finish; 0 means every kernel finished normally.  Clears them if
+    ``clear``."""
+    bits = ctypes.c_uint32(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = load_library().vq_kernel_status(ctypes.byref(bits), 1 if clear else 0)
+    _check(st, "vq_kernel_status")
+    return int(bits.value)
 
 
 def _dtype_code(t: torch.Tensor) -> int:

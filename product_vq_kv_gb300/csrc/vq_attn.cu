@@ -17,6 +17,9 @@
 #include "vq_encode.h"
 #include "vq_attn.cuh"
 #include "vq_host.h"
+#include "vq_status.cuh"
+
+VQH_STATUS_READER(vqh_status_attn)
 
 namespace {
 

@@ -19,6 +19,7 @@
 #include "vq_filter.cuh"
 #include "vq_tc.cuh"
 #include "vq_kernels.cuh"
+#include "vq_status.cuh"
 
 // Declared in vq_host.h.
 int vqh_device_sms()
@@ -42,6 +43,8 @@ int vqh_device_sms()
     return sms;
 }
 
+VQH_STATUS_READER(vqh_status_encode)
+
 namespace {
 
 // Tuning of the exact brute-force kernel (rows per thread, threads per block,
@@ -54,21 +57,8 @@ constexpr int kGroupCentroids = 8;
 constexpr int kFThreads = 128;
 constexpr int kFRows = 8;
 constexpr int kFGroup = 16;
-// Tuning of the tensor-core screening kernel (tensor-memory columns per CTA,
-// 128-row tiles per CTA).
-// Per sub_dim: tensor-memory columns per CTA, 128-row tiles per CTA, centroids
-// per screening group, minimum CTAs per SM (register budget).  Measured best
-// on GB300 for 256-centroid codebooks.
-template <int SUB>
-struct TcConfig;
-template <>
-struct TcConfig<4> {
-    static constexpr int kCols = 64, kGroup = 16, kMinBlocks = 8;
-};
-template <>
-struct TcConfig<8> {
-    static constexpr int kCols = 64, kGroup = 8, kMinBlocks = 6;
-};
+// Tuning of the tensor-core screening kernel: vqk::TcConfig (vq_tc.cuh).
+using vqk::TcConfig;
 
 int device_sms() { return vqh_device_sms(); }
 
@@ -707,5 +697,17 @@ vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_ce
 }
 
 int32_t vq_abi_version(void) { return VQ_ENCODE_ABI_VERSION; }
+
+vq_status vq_kernel_status(uint32_t *bits, int32_t clear)
+{
+    if (!bits) return VQ_ERR_INVALID_ARG;
+    *bits = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return VQ_ERR_CUDA;
+    const bool c = clear != 0;
+    if (vqh_status_encode(bits, c) != cudaSuccess || vqh_status_attn(bits, c) != cudaSuccess ||
+        vqh_status_scalar(bits, c) != cudaSuccess)
+        return VQ_ERR_CUDA;
+    return VQ_OK;
+}
 
 }  // extern "C"

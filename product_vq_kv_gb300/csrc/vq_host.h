@@ -2,6 +2,31 @@
 // (internal; not part of the C ABI).
 #pragma once
 
+#include <cuda_runtime.h>
+#include <stdint.h>
+
 // Streaming multiprocessors of the current device, cached per device; 0 if
 // there is no usable device.
 int vqh_device_sms();
+
+// OR into *bits this translation unit's device status word on the current
+// device (vq_status.cuh), then reset it to zero if `clear`.  The caller has
+// synchronised the device.
+cudaError_t vqh_status_encode(uint32_t *bits, bool clear);
+cudaError_t vqh_status_attn(uint32_t *bits, bool clear);
+cudaError_t vqh_status_scalar(uint32_t *bits, bool clear);
+
+// The body of the three functions above, for the translation unit's own word.
+#define VQH_STATUS_READER(NAME)                                                      \
+    cudaError_t NAME(uint32_t *bits, bool clear)                                     \
+    {                                                                                \
+        uint32_t v = 0;                                                              \
+        cudaError_t e = cudaMemcpyFromSymbol(&v, vqk::g_status_word, sizeof v);      \
+        if (e != cudaSuccess) return e;                                              \
+        *bits |= v;                                                                  \
+        if (clear && v != 0) {                                                       \
+            const uint32_t zero = 0;                                                 \
+            e = cudaMemcpyToSymbol(vqk::g_status_word, &zero, sizeof zero);          \
+        }                                                                            \
+        return e;                                                                    \
+    }

@@ -14,7 +14,10 @@
 
 #include "vq_encode.h"
 #include "vq_host.h"
+#include "vq_status.cuh"
 #include "vq_scalar.cuh"
+
+VQH_STATUS_READER(vqh_status_scalar)
 
 namespace {
 

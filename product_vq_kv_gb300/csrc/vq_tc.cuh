@@ -11,9 +11,11 @@
 // exact; only the accumulation inside the tensor core rounds.  Its error is
 // bounded by eps_tc times the sum of the magnitudes of the terms, which is at
 // most 2 (C2 + sum_i |x_i| A_i).  eps_tc = 2^-16 is taken: 8 times the error
-// of an fp32 accumulator that truncates each of K = 16 partial sums, and 45
-// times the largest error measured on GB300 over 10^8 scores spanning five
-// decades of magnitude (2^-21.5).  Adding the
+// of an fp32 accumulator that truncates each of K = 16 partial sums, and 25
+// times the largest error that tests/test_tc_accumulation.py measures on
+// GB300 through this file's own MMA, descriptors and tensor-memory loads
+// (2^-20.7, chains of up to 6 MMAs, on cancelling, many-decade, split-piece,
+// near-underflow and screening-operand score sets).  Adding the
 // rounding of the fp32 |c|^2 (gamma_SUB) gives the screening bound
 //     B(x) = (2 eps_tc + 2 gamma_SUB) (C2 + sum_i |x_i| A_i),
 // and the threshold, candidate groups, exact re-evaluation and exact queue
@@ -55,11 +57,24 @@
 // memory, so thread t of the block owns row t of the tile: it reads its own
 // row's scores (tcgen05.ld) and reduces them without any exchange.
 //
-// Every thread waits for each MMA on the mbarrier (bounded polls); the block
-// agrees once per tile, after the tile's passes, on whether all waits
-// completed.  If one gave up, the block marks every row it has not encoded
-// with 0xFFFFFFFF, waits once more (bounded) for the last MMA and frees the
-// tensor memory.
+// Every thread waits for each pass's MMA on the mbarrier, polling at most
+// kWaitPolls times; a wait that needed more than POLLS polls, or never
+// completed, counts as given up (in the library POLLS is kWaitPolls, so only
+// the latter; smaller values exist only to test this path).  The block
+// agrees once per tile, after the tile's passes, on whether any wait gave up.
+// A wait that completed late still completed before the thread reads the
+// scores, so no tensor-memory load races an MMA unless a wait never
+// completed.  The waits use the barrier's phase parity, which only tells the
+// last two phases apart, so at most one phase is ever outstanding: thread 0
+// starts a pass's phase only after its own wait for the previous one; once a
+// wait of its own has given up it issues no more MMAs and completes each
+// later pass's phase with a plain arrive instead (so every pass still
+// completes one phase), and once a wait of its own never completed it starts
+// no phase at all.  If a wait gave up, thread 0 waits (kWaitPolls) for the
+// last phase it started, the block marks every row it has not encoded with
+// 0xFFFFFFFF, sets kStatusWaitGaveUp in the device status word and frees the
+// tensor memory: never while an MMA it issued is in flight, unless a wait
+// never completed.
 //
 // Launch: block = 128 threads; dynamic shared memory = TcLayout::bytes(...)
 // (at least 512/NCOL CTAs' worth of a 228 KiB SM, which caps the CTAs per SM
@@ -75,8 +90,16 @@
 
 #include "vq_filter.cuh"
 #include "vq_kernels.cuh"
+#include "vq_status.cuh"
 
 namespace vqk {
+
+#ifdef VQ_TC_STATS
+// Test builds only: rows per screening outcome, [cnt 1, cnt 1 tight, cnt 2,
+// cnt 2 tight, queued]; "tight" = the least excluded group minimum lies
+// within one bound of the threshold.
+static __device__ unsigned long long g_tc_stats[8];
+#endif
 
 // ------------------------------------------------------------------ tcgen05 / mbarrier helpers
 
@@ -116,12 +139,16 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
                  : "memory");
 }
 
-// Wait for the barrier's phase `parity` to complete, giving up after a bounded
-// number of polls; returns whether it completed.
+// Polls of an mbarrier wait before it gives up.
+constexpr int kWaitPolls = 1 << 22;
+
+// Wait for the barrier's phase `parity` to complete, giving up after POLLS
+// polls; returns whether it completed.
+template <int POLLS = kWaitPolls>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t done = 0;
-    for (int it = 0; it < (1 << 22) && !done; ++it) {
+    for (int it = 0; it < POLLS && !done; ++it) {
         asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                      "selp.u32 %0, 1, 0, p;\n\t}"
                      : "=r"(done)
@@ -129,6 +156,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
                      : "memory");
     }
     return done != 0;
+}
+
+// Bits of a thread's wait state.
+constexpr uint32_t kWaitLate = 1u;    // a wait completed only after more than POLLS polls, or not at all
+constexpr uint32_t kWaitFailed = 2u;  // a wait did not complete within the full limit
+
+// Wait for the barrier's phase `parity` to complete, polling up to the full
+// limit whatever POLLS is, and classify the wait: 0 if it completed within
+// POLLS polls, kWaitLate if it completed later, kWaitLate | kWaitFailed if
+// it did not complete.  With POLLS equal to the full limit this is mbar_wait.
+template <int POLLS>
+__device__ __forceinline__ uint32_t mbar_wait_state(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done = 0;
+    int it = 0;
+    for (; it < kWaitPolls && !done; ++it) {
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(smem_addr(bar)), "r"(parity)
+                     : "memory");
+    }
+    if (!done) return kWaitLate | kWaitFailed;
+    if constexpr (POLLS < kWaitPolls) return it > POLLS ? kWaitLate : 0u;
+    return 0u;
+}
+
+// Arrive once on the barrier (completing a phase of arrival count 1).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    uint64_t state;
+    asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];" : "=l"(state) : "r"(smem_addr(bar)) : "memory");
+    (void)state;
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -229,10 +289,24 @@ struct TcLayout {
     }
 };
 
+// Per sub_dim: tensor-memory columns per CTA, centroids per screening group,
+// minimum CTAs per SM (register budget).  Measured best on GB300 for
+// 256-centroid codebooks.
+template <int SUB>
+struct TcConfig;
+template <>
+struct TcConfig<4> {
+    static constexpr int kCols = 64, kGroup = 16, kMinBlocks = 8;
+};
+template <>
+struct TcConfig<8> {
+    static constexpr int kCols = 64, kGroup = 8, kMinBlocks = 6;
+};
+
 // ------------------------------------------------------------------ kernel
 
 template <typename T, int SUB, int NCOL, int GC, int MINB, typename OutT = uint32_t,
-          bool SMOOTH = false>
+          bool SMOOTH = false, int POLLS = kWaitPolls>
 __global__ void __launch_bounds__(128, MINB)
     encode_tc(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
               int32_t n_centroids, int64_t blocks_per_group, int32_t tiles_per_block, float one,
@@ -394,8 +468,10 @@ __global__ void __launch_bounds__(128, MINB)
     load_x(row_base + tid, xr);
 
     uint32_t phase = 0;
-    bool alive = true;        // block-wide: every wait so far completed
-    bool alive_here = true;   // this thread's waits
+    bool alive = true;  // block-wide: every wait so far completed within POLLS polls
+    // this thread's waits: kWaitLate, kWaitFailed; thread 0 also keeps, in
+    // bits 2-3, one more than the parity of the last phase it started (0: none)
+    uint32_t wst = 0;
     for (int tile = 0; tile < tiles_per_block; ++tile) {
         const int64_t row = row_base + (int64_t)tile * 128 + tid;
         if (row_base + (int64_t)tile * 128 >= n_per_group) break;  // block-uniform
@@ -434,7 +510,15 @@ __global__ void __launch_bounds__(128, MINB)
             const int c0 = pass * NCOL;
             if (c0 >= n_pad) break;  // block-uniform
             const int ncols = n_pad - c0 < NCOL ? n_pad - c0 : NCOL;
-            if (tid == 0) {
+            if constexpr (POLLS < kWaitPolls) {
+                // a wait that gave up but completed (possible only when POLLS
+                // is below the full limit): this pass's phase without an MMA
+                if (tid == 0 && (wst & (kWaitLate | kWaitFailed)) == kWaitLate) {
+                    mbar_arrive(bar);
+                    wst = (wst & 3u) | ((phase + 1u) << 2);
+                }
+            }
+            if (tid == 0 && !(wst & kWaitLate)) {  // never a second phase outstanding
                 const uint32_t idesc = umma_idesc_tf32((uint32_t)ncols);
                 // (A piece, B piece) products: (hi, hi), (mid, hi), (hi, mid)
 #pragma unroll
@@ -451,10 +535,12 @@ __global__ void __launch_bounds__(128, MINB)
                     }
                 }
                 umma_commit(bar);
+                wst = (wst & 3u) | ((phase + 1u) << 2);
             }
             // a wait that gives up is agreed on once per tile, below; the
-            // scores it leaves unread are never used
-            alive_here &= mbar_wait(bar, phase);
+            // scores of that tile are never used, but are read only once the
+            // MMA is done
+            wst |= mbar_wait_state<POLLS>(bar, phase);
             phase ^= 1u;
             tc_fence_after();
             if (NCOL == 64 && ncols == 64) {  // block-uniform
@@ -511,17 +597,30 @@ __global__ void __launch_bounds__(128, MINB)
         const int ga = __ffs(mask) - 1;
         const int gb = cnt > 1 ? __ffs(mask & (mask - 1)) - 1 : -1;
         if (tid == 0) *qcount = 0u;
-        if (!__syncthreads_and(alive_here)) {
-            // a wait gave up: wait once more (bounded) for the last MMA, whose
-            // completion may not have been seen, before its accumulator memory
-            // is freed; record the tile
+        if (!__syncthreads_and(!(wst & kWaitLate))) {
+            // a wait gave up: wait once more, with the full limit, for the
+            // last phase thread 0 started (the only one that can be
+            // outstanding) before the accumulator memory is freed; record the
+            // tile
             alive = false;
             if (tid == 0) {
-                (void)mbar_wait(bar, phase ^ 1u);
+                if (wst >> 2) (void)mbar_wait<kWaitPolls>(bar, (wst >> 2) - 1u);
                 *qcount = (uint32_t)tile;
+                raise_status(kStatusWaitGaveUp);
             }
             break;
         }
+#ifdef VQ_TC_STATS
+        if (row < n_per_group) {
+            float excl = __int_as_float(0x7f800000);
+#pragma unroll
+            for (int k = 0; k < kNG; ++k)
+                if (!((mask >> k) & 1u)) excl = fminf(excl, gmin[k]);
+            const bool tight = excl - thr <= bnd;
+            const int b = !ok || cnt > 2 || cnt == 0 ? 4 : (cnt - 1) * 2 + (tight ? 1 : 0);
+            atomicAdd(&g_tc_stats[b], 1ull);
+        }
+#endif
         uint32_t id = 0;
         if (!ok || cnt > 2 || cnt == 0) {
             id = kQueued;
