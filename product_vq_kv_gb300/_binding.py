@@ -33,6 +33,53 @@ class VQError(RuntimeError):
         super().__init__(f"{where}: {vq_status_string(status)}")
 
 
+def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the argument and result types of every entry point on ``lib``
+    (the library, or its bounds-checked build, which has the same ABI)."""
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    lib.vq_encode.restype = i32
+    lib.vq_encode.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp]
+    lib.vq_encode_grouped.restype = i32
+    lib.vq_encode_grouped.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp]
+    lib.vq_encode_grouped_host.restype = i32
+    lib.vq_encode_grouped_host.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp, vp,
+                                           vp, vp]
+    lib.vq_encode_grouped_u8.restype = i32
+    lib.vq_encode_grouped_u8.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp]
+    lib.vq_dequantize_grouped.restype = i32
+    lib.vq_dequantize_grouped.argtypes = [vp, i32, vp, i64, i64, i32, i32, i32, vp, vp]
+    lib.vq_attention_decode.restype = i32
+    lib.vq_attention_decode.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i64, i32, i32, i32,
+                                        i64, ctypes.c_float, i32, vp, vp, ctypes.c_size_t, vp]
+    lib.vq_attention_decode_static.restype = i32
+    lib.vq_attention_decode_static.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i64, i32,
+                                               i32, i32, i64, ctypes.c_float, i32, vp, vp]
+    lib.vq_encode_grouped_smooth.restype = i32
+    lib.vq_encode_grouped_smooth.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, vp,
+                                             i32, vp]
+    lib.vq_scalar_quantize_workspace_bytes.restype = ctypes.c_size_t
+    lib.vq_scalar_quantize_workspace_bytes.argtypes = [i32]
+    lib.vq_scalar_quantize.restype = i32
+    lib.vq_scalar_quantize.argtypes = [vp, i32, i64, vp, i32, vp, vp, ctypes.c_size_t, vp]
+    lib.vq_scalar_dequantize.restype = i32
+    lib.vq_scalar_dequantize.argtypes = [vp, i64, vp, i32, i32, vp, vp]
+    lib.vq_hadamard_rotate.restype = i32
+    lib.vq_hadamard_rotate.argtypes = [vp, i32, vp, i64, i32, vp, vp]
+    lib.vq_hadamard_quantize.restype = i32
+    lib.vq_hadamard_quantize.argtypes = [vp, i32, vp, i64, i32, vp, i32, vp, vp]
+    lib.vq_attention_workspace_bytes.restype = ctypes.c_size_t
+    lib.vq_attention_workspace_bytes.argtypes = [i64, i32, i32, i64, i32, i32, i32, i64]
+    lib.vq_status_string.restype = ctypes.c_char_p
+    lib.vq_status_string.argtypes = [i32]
+    lib.vq_describe_launch.restype = i32
+    lib.vq_describe_launch.argtypes = [i64, i64, i32, i32, i32, vp, ctypes.c_char_p, i32]
+    lib.vq_abi_version.restype = i32
+    lib.vq_abi_version.argtypes = []
+    lib.vq_kernel_status.restype = i32
+    lib.vq_kernel_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    return lib
+
+
 def load_library() -> ctypes.CDLL:
     """Load ``libvqenc.so`` (once).  Raises if it has not been built."""
     global _lib
@@ -43,50 +90,8 @@ def load_library() -> ctypes.CDLL:
             raise RuntimeError(
                 f"{LIB_PATH} is missing; build it with `python -m product_vq_kv_gb300.build` "
                 "(there is no fallback implementation)")
-        lib = ctypes.CDLL(LIB_PATH)
-        i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
-        lib.vq_encode.restype = i32
-        lib.vq_encode.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp]
-        lib.vq_encode_grouped.restype = i32
-        lib.vq_encode_grouped.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp]
-        lib.vq_encode_grouped_host.restype = i32
-        lib.vq_encode_grouped_host.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp, vp,
-                                               vp, vp]
-        lib.vq_encode_grouped_u8.restype = i32
-        lib.vq_encode_grouped_u8.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp]
-        lib.vq_dequantize_grouped.restype = i32
-        lib.vq_dequantize_grouped.argtypes = [vp, i32, vp, i64, i64, i32, i32, i32, vp, vp]
-        lib.vq_attention_decode.restype = i32
-        lib.vq_attention_decode.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i64, i32, i32, i32,
-                                            i64, ctypes.c_float, i32, vp, vp, ctypes.c_size_t, vp]
-        lib.vq_attention_decode_static.restype = i32
-        lib.vq_attention_decode_static.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i64, i32,
-                                                   i32, i32, i64, ctypes.c_float, i32, vp, vp]
-        lib.vq_encode_grouped_smooth.restype = i32
-        lib.vq_encode_grouped_smooth.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, vp,
-                                                 i32, vp]
-        lib.vq_scalar_quantize_workspace_bytes.restype = ctypes.c_size_t
-        lib.vq_scalar_quantize_workspace_bytes.argtypes = [i32]
-        lib.vq_scalar_quantize.restype = i32
-        lib.vq_scalar_quantize.argtypes = [vp, i32, i64, vp, i32, vp, vp, ctypes.c_size_t, vp]
-        lib.vq_scalar_dequantize.restype = i32
-        lib.vq_scalar_dequantize.argtypes = [vp, i64, vp, i32, i32, vp, vp]
-        lib.vq_hadamard_rotate.restype = i32
-        lib.vq_hadamard_rotate.argtypes = [vp, i32, vp, i64, i32, vp, vp]
-        lib.vq_hadamard_quantize.restype = i32
-        lib.vq_hadamard_quantize.argtypes = [vp, i32, vp, i64, i32, vp, i32, vp, vp]
-        lib.vq_attention_workspace_bytes.restype = ctypes.c_size_t
-        lib.vq_attention_workspace_bytes.argtypes = [i64, i32, i32, i64, i32, i32, i32, i64]
-        lib.vq_status_string.restype = ctypes.c_char_p
-        lib.vq_status_string.argtypes = [i32]
-        lib.vq_describe_launch.restype = i32
-        lib.vq_describe_launch.argtypes = [i64, i64, i32, i32, i32, vp, ctypes.c_char_p, i32]
-        lib.vq_abi_version.restype = i32
-        lib.vq_abi_version.argtypes = []
-        lib.vq_kernel_status.restype = i32
-        lib.vq_kernel_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
-        _lib = lib
-        return lib
+        _lib = _configure(ctypes.CDLL(LIB_PATH))
+        return _lib
 
 
 def vq_status_string(status: int) -> str:

@@ -17,10 +17,13 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libvqenc.so")
+# The bounds-checked build (-DVQ_CHECKED, csrc/vq_check.cuh): the same entry
+# points, every kernel index checked, launches waited for; for tests only.
+CHECKED_LIB_PATH = os.path.join(LIB_DIR, "libvqenc_checked.so")
 PTXAS_LOG = os.path.join(LIB_DIR, "ptxas.txt")
 SOURCES = [os.path.join(CSRC, name) for name in ("vq_encode.cu", "vq_attn.cu", "vq_scalar.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, name) for name in (
-    "vq_kernels.cuh", "vq_filter.cuh", "vq_tc.cuh", "vq_decode.cuh", "vq_attn.cuh", "vq_host.h", "vq_scalar.cuh", "vq_status.cuh")] + [
+    "vq_kernels.cuh", "vq_filter.cuh", "vq_tc.cuh", "vq_decode.cuh", "vq_attn.cuh", "vq_host.h", "vq_scalar.cuh", "vq_status.cuh", "vq_check.cuh")] + [
     os.path.join(ROOT, "include", "vq_encode.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -38,27 +41,29 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libvqenc.so")
 
 
-def is_fresh() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_fresh(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    built = os.path.getmtime(LIB_PATH)
+    built = os.path.getmtime(path)
     return all(os.path.getmtime(p) <= built for p in DEPENDS)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
     """Compile the library unless it is newer than all of its sources.
 
     The translation units compile in parallel, then link into one shared
-    library."""
-    if not force and is_fresh():
-        return LIB_PATH
+    library.  ``checked`` builds the bounds-checked variant instead
+    (``libvqenc_checked.so``)."""
+    lib_path = CHECKED_LIB_PATH if checked else LIB_PATH
+    if not force and is_fresh(lib_path):
+        return lib_path
     os.makedirs(LIB_DIR, exist_ok=True)
     with tempfile.TemporaryDirectory(dir=LIB_DIR) as tmpdir:
         jobs = []
         for src in SOURCES:
             obj = os.path.join(tmpdir, os.path.basename(src) + ".o")
-            cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", "-o",
-                   obj, src]
+            cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *(["-DVQ_CHECKED"] if checked else []), "-I",
+                   os.path.join(ROOT, "include"), "-c", "-o", obj, src]
             jobs.append((cmd, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE,
                                                     stderr=subprocess.PIPE, text=True)))
         log = []
@@ -72,13 +77,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
         res = subprocess.run(link, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError("nvcc link failed:\n" + " ".join(link) + "\n" + res.stdout + res.stderr)
-        with open(PTXAS_LOG, "w") as f:
-            f.write("\n".join(log))
+        if not checked:
+            with open(PTXAS_LOG, "w") as f:
+                f.write("\n".join(log))
         if verbose:
             sys.stderr.write("\n".join(log))
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                checked="--checked" in sys.argv))

@@ -114,7 +114,7 @@ vq_status attn_launch_k(const AttnPlan &p, const void *q, const uint8_t *kcodes,
     kp<<<(unsigned)(p.base * p.sh.splits), kAttnThreads, p.smem, st>>>(
         static_cast<const T *>(q), kcodes, static_cast<const T *>(kcb), vcodes,
         static_cast<const T *>(vcb), p.sh, part);
-    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+    return vqh_launched(st, vqh_status_attn);
 }
 
 template <typename T, int NS>
@@ -148,7 +148,7 @@ vq_status attn_launch(const AttnPlan &p, const void *q, const uint8_t *kcodes, c
     const int threads = (p.sh.head_dim + 31) / 32 * 32;
     vqk::attn_combine<T><<<(unsigned)rows, threads, 0, st>>>(part, rows, p.sh.head_dim,
                                                              p.sh.splits, static_cast<T *>(out));
-    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+    return vqh_launched(st, vqh_status_attn);
 }
 
 // Scratch of vq_attention_decode_static: the per-slice partials live in this

@@ -42,6 +42,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "vq_check.cuh"
+
 namespace vqk {
 
 constexpr int kLutStride = 256;  // table row stride (one entry per 8-bit code), in vectors
@@ -242,6 +244,21 @@ __global__ void __launch_bounds__(kAttnThreads)
     const uint8_t *kb = kcodes + cache_off;
     const uint8_t *vb = vcodes + cache_off;
 
+    // buffer extents, for the checked build's bounds checks (vq_check.cuh)
+    const int64_t nq_elems = sh.batch * sh.heads_q * d;
+    const int64_t ncb_elems = (int64_t)sh.heads_kv * nc * sub;
+    const int64_t ncodes = sh.batch * sh.heads_kv * sh.tokens * NS;
+    const int64_t npart = sh.batch * sh.heads_q * sh.splits * (int64_t)(d + 2);
+    const uint64_t lut_floats = (lay.vcb - lay.lut) / 4, vcs_elems = (uint64_t)256 * ncopies * sub;
+    const uint64_t pw_floats = (uint64_t)CHUNK * GPB, red_floats = (uint64_t)3 * GPB * NW;
+    constexpr uint32_t kCodeAlign = NS < 16 ? NS : 16;  // load_code_row, store_code_row
+    if constexpr (kChecked) {
+        // the layout inside the launch's shared memory and the block inside
+        // the grid: else the block does nothing
+        if (!dyn_smem_ok(smem_raw, lay.total, 16) || !index_ok(b, sh.batch) || vcs_elems * sizeof(T) > lay.pw - lay.vcb)
+            return;  // block-uniform
+    }
+
     // ---- tables (kappa folded in, zero past n_centroids): thread c owns
     // centroid c and writes the GP heads of a pack as one vector; the value
     // codebook goes to its bank-disjoint copies
@@ -253,26 +270,30 @@ __global__ void __launch_bounds__(kAttnThreads)
                 float acc[GP];
 #pragma unroll
                 for (int gi = 0; gi < GP; ++gi) acc[gi] = 0.f;
-                if (c < nc) {
+                if (c < nc && VQ_SPAN(cv, sub, kcb, ncb_elems)) {
                     for (int i = 0; i < sub; ++i) {
                         const float kv = to_f32(cv[i]);
 #pragma unroll
                         for (int gi = 0; gi < GP; ++gi) {
                             const T *qv = q + ((size_t)b * sh.heads_q + hq0 + pk * GP + gi) * d;
-                            acc[gi] = fmaf(to_f32(qv[(size_t)s * sub + i]), kv, acc[gi]);
+                            if (VQ_SPAN(qv + (size_t)s * sub + i, 1, q, nq_elems))
+                                acc[gi] = fmaf(to_f32(qv[(size_t)s * sub + i]), kv, acc[gi]);
                         }
                     }
                 }
                 float *dst = lut + ((size_t)(pk * NS + s) * kLutStride + c) * GP;
+                if (VQ_SPAN(dst, GP, lut, lut_floats)) {
 #pragma unroll
-                for (int gi = 0; gi < GP; ++gi) dst[gi] = acc[gi] * sh.kappa;
+                    for (int gi = 0; gi < GP; ++gi) dst[gi] = acc[gi] * sh.kappa;
+                }
             }
         }
     }
     for (int e = threadIdx.x; e < 256 * ncopies * sub; e += THREADS) {
         const int i = e % sub;
         const int c = e / (sub * ncopies);  // every copy holds the same rows
-        vcs[e] = c < nc ? vc[(size_t)c * sub + i] : T(0.f);
+        if (VQ_SPAN(vcs + e, 1, vcs, vcs_elems))
+            vcs[e] = c < nc && VQ_SPAN(vc + (size_t)c * sub + i, 1, vcb, ncb_elems) ? vc[(size_t)c * sub + i] : T(0.f);
     }
     __syncthreads();
 
@@ -308,7 +329,8 @@ __global__ void __launch_bounds__(kAttnThreads)
 #pragma unroll
         for (int r = 0; r < TPT; ++r) {
             const int64_t t = tb + (int64_t)r * THREADS;
-            if (t < sh.tokens) {
+            if (t < sh.tokens && VQ_VSPAN(kb + (size_t)t * NS, NS, kcodes, ncodes, kCodeAlign) &&
+                VQ_VSPAN(vb + (size_t)t * NS, NS, vcodes, ncodes, kCodeAlign)) {
                 load_code_row<NS>(kb + (size_t)t * NS, wk[r]);
                 load_code_row<NS>(vb + (size_t)t * NS, wv[r]);
             }
@@ -337,7 +359,13 @@ __global__ void __launch_bounds__(kAttnThreads)
 #pragma unroll
                     for (int pk = 0; pk < NPACK; ++pk) {
                         float v[GP];
-                        load_vec<GP>(lut + ((size_t)(pk * NS + s) * kLutStride + code) * GP, v);
+                        const float *src = lut + ((size_t)(pk * NS + s) * kLutStride + code) * GP;
+                        if (VQ_VSPAN(src, GP, lut, lut_floats, GP * 4)) {
+                            load_vec<GP>(src, v);
+                        } else {
+#pragma unroll
+                            for (int gi = 0; gi < GP; ++gi) v[gi] = 0.f;
+                        }
 #pragma unroll
                         for (int gi = 0; gi < GP; ++gi) a[pk * GP + gi] += v[gi];
                     }
@@ -358,14 +386,15 @@ __global__ void __launch_bounds__(kAttnThreads)
             float m = cm[g];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0) rmax[g * NW + warp] = m;
+            if (lane == 0 && VQ_SPAN(rmax + g * NW + warp, 1, red, red_floats)) rmax[g * NW + warp] = m;
         }
         __syncthreads();
 #pragma unroll
         for (int g = 0; g < GPB; ++g) {
             float m = m_run[g];
 #pragma unroll
-            for (int k = 0; k < NW; ++k) m = fmaxf(m, rmax[g * NW + k]);
+            for (int k = 0; k < NW; ++k)
+                if (VQ_SPAN(rmax + g * NW + k, 1, red, red_floats)) m = fmaxf(m, rmax[g * NW + k]);
             if (m > m_run[g] && m_run[g] > kNegInf) {  // rescale what is accumulated
                 const float f = exp2f(m_run[g] - m);
                 l_run[g] *= f;
@@ -387,6 +416,7 @@ __global__ void __launch_bounds__(kAttnThreads)
 #pragma unroll
             for (int pk = 0; pk < NPACK; ++pk) {
                 float *dst = pw + (size_t)tl * GPB + pk * GP;
+                if (!VQ_VSPAN(dst, GP, pw, pw_floats, GP * 4)) continue;
                 if constexpr (GP == 4) {
                     *reinterpret_cast<float4 *>(dst) = make_float4(p[pk * 4], p[pk * 4 + 1], p[pk * 4 + 2], p[pk * 4 + 3]);
                 } else if constexpr (GP == 2) {
@@ -395,7 +425,8 @@ __global__ void __launch_bounds__(kAttnThreads)
                     dst[0] = p[pk];
                 }
             }
-            if (tbase + tl < sh.tokens) store_code_row<NS>(vtile + (size_t)tl * NS, wv[r]);
+            if (tbase + tl < sh.tokens && VQ_VSPAN(vtile + (size_t)tl * NS, NS, vtile, (uint64_t)CHUNK * NS, kCodeAlign))
+                store_code_row<NS>(vtile + (size_t)tl * NS, wv[r]);
         }
         if (ch + 1 < c1) load_rows(ch + 1);  // in flight during phase B
         __syncthreads();
@@ -408,16 +439,25 @@ __global__ void __launch_bounds__(kAttnThreads)
             for (; tl + (U - 1) * streams < n_chunk; tl += U * streams) {
                 int code[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) code[u] = vtile[(size_t)(tl + u * streams) * NS + bs];
+                for (int u = 0; u < U; ++u)
+                    code[u] = VQ_SPAN(vtile + (size_t)(tl + u * streams) * NS + bs, 1, vtile, (uint64_t)CHUNK * NS)
+                                  ? vtile[(size_t)(tl + u * streams) * NS + bs] : 0;
                 float4 row[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) row[u] = load4_f32(vrow0 + (size_t)code[u] * vstride);
+                for (int u = 0; u < U; ++u)
+                    row[u] = VQ_VSPAN(vrow0 + (size_t)code[u] * vstride, VW, vcs, vcs_elems, VW * sizeof(T))
+                                 ? load4_f32(vrow0 + (size_t)code[u] * vstride) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     float p[GPB];
 #pragma unroll
                     for (int pk = 0; pk < NPACK; ++pk) {
                         float v[GP];
+                        if (!VQ_VSPAN(pw + (size_t)(tl + u * streams) * GPB + pk * GP, GP, pw, pw_floats, GP * 4)) {
+#pragma unroll
+                            for (int gi = 0; gi < GP; ++gi) p[pk * GP + gi] = 0.f;
+                            continue;
+                        }
                         load_vec<GP>(pw + (size_t)(tl + u * streams) * GPB + pk * GP, v);
 #pragma unroll
                         for (int gi = 0; gi < GP; ++gi) p[pk * GP + gi] = v[gi];
@@ -430,12 +470,19 @@ __global__ void __launch_bounds__(kAttnThreads)
                 }
             }
             for (; tl < n_chunk; tl += streams) {
-                const int code = vtile[(size_t)tl * NS + bs];
-                const float4 row = load4_f32(vrow0 + (size_t)code * vstride);
+                const int code = VQ_SPAN(vtile + (size_t)tl * NS + bs, 1, vtile, (uint64_t)CHUNK * NS)
+                                     ? vtile[(size_t)tl * NS + bs] : 0;
+                const float4 row = VQ_VSPAN(vrow0 + (size_t)code * vstride, VW, vcs, vcs_elems, VW * sizeof(T))
+                                       ? load4_f32(vrow0 + (size_t)code * vstride) : make_float4(0.f, 0.f, 0.f, 0.f);
                 float p[GPB];
 #pragma unroll
                 for (int pk = 0; pk < NPACK; ++pk) {
                     float v[GP];
+                    if (!VQ_VSPAN(pw + (size_t)tl * GPB + pk * GP, GP, pw, pw_floats, GP * 4)) {
+#pragma unroll
+                        for (int gi = 0; gi < GP; ++gi) p[pk * GP + gi] = 0.f;
+                        continue;
+                    }
                     load_vec<GP>(pw + (size_t)tl * GPB + pk * GP, v);
 #pragma unroll
                     for (int gi = 0; gi < GP; ++gi) p[pk * GP + gi] = v[gi];
@@ -457,26 +504,30 @@ __global__ void __launch_bounds__(kAttnThreads)
         float l = l_run[g];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        if (lane == 0) rsum[g * NW + warp] = l;
+        if (lane == 0 && VQ_SPAN(rsum + g * NW + warp, 1, red, red_floats)) rsum[g * NW + warp] = l;
     }
     float *accs = lut;  // [streams][GPB][D]; the tables are no longer read
     if (b_active) {
 #pragma unroll
         for (int g = 0; g < GPB; ++g)
-            *reinterpret_cast<float4 *>(accs + ((size_t)stream * GPB + g) * d + col * VW) =
-                make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+            if (VQ_VSPAN(accs + ((size_t)stream * GPB + g) * d + col * VW, VW, lut, lut_floats, 16))
+                *reinterpret_cast<float4 *>(accs + ((size_t)stream * GPB + g) * d + col * VW) =
+                    make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < GPB * d; e += THREADS) {
         const int g = e / d;
         const int j = e - g * d;
         float o = 0.f;
-        for (int k = 0; k < streams; ++k) o += accs[((size_t)k * GPB + g) * d + j];
+        for (int k = 0; k < streams; ++k)
+            if (VQ_SPAN(accs + ((size_t)k * GPB + g) * d + j, 1, lut, lut_floats)) o += accs[((size_t)k * GPB + g) * d + j];
         float *pp = part + (((size_t)b * sh.heads_q + hq0 + g) * sh.splits + split) * (size_t)(d + 2);
+        if (!VQ_SPAN(pp, d + 2, part, npart)) continue;
         pp[2 + j] = o;
         if (j == 0) {
             float l = 0.f, m = m_run[0];
-            for (int k = 0; k < NW; ++k) l += rsum[g * NW + k];
+            for (int k = 0; k < NW; ++k)
+                if (VQ_SPAN(rsum + g * NW + k, 1, red, red_floats)) l += rsum[g * NW + k];
 #pragma unroll
             for (int gg = 1; gg < GPB; ++gg)
                 if (gg == g) m = m_run[gg];  // static register index
@@ -497,6 +548,9 @@ __global__ void attn_combine(const float *__restrict__ part, int64_t n_rows, int
     const int j = threadIdx.x;
     if (r >= n_rows || j >= head_dim) return;
     const float *pr = part + (size_t)r * splits * (head_dim + 2);
+    if (!VQ_SPAN(pr, (int64_t)splits * (head_dim + 2), part, n_rows * splits * (int64_t)(head_dim + 2)) ||
+        !VQ_SPAN(out + (size_t)r * head_dim + j, 1, out, n_rows * head_dim))
+        return;
     float m = kNegInf;
     for (int k = 0; k < splits; ++k) m = fmaxf(m, pr[(size_t)k * (head_dim + 2)]);
     float l = 0.f, o = 0.f;

@@ -244,7 +244,7 @@ vq_status launch_tc(const Args &a, const Plan &p)
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
         p.tiles_per_group, p.tc_tiles, 1.0f, static_cast<OutT *>(a.out), a.smooth,
         SMOOTH ? (int32_t)(a.head_dim / a.sub_dim) : 1);
-    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+    return vqh_launched(a.stream, vqh_status_encode);
 }
 
 template <typename T, int SUB, typename OutT, bool SMOOTH = false>
@@ -260,7 +260,7 @@ vq_status launch_filter(const Args &a, const Plan &p)
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
         p.tiles_per_group, 1.0f, static_cast<OutT *>(a.out), a.smooth,
         SMOOTH ? a.head_dim / SUB : 0);
-    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+    return vqh_launched(a.stream, vqh_status_encode);
 }
 
 template <typename T, int SUB, typename OutT>
@@ -275,7 +275,7 @@ vq_status launch_fast(const Args &a, const Plan &p)
     kernel<<<(unsigned)p.blocks, p.threads, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
         p.tiles_per_group, 1.0f, static_cast<OutT *>(a.out));
-    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+    return vqh_launched(a.stream, vqh_status_encode);
 }
 
 template <typename T, typename OutT>
@@ -284,7 +284,7 @@ vq_status launch_general(const Args &a, const Plan &p)
     vqk::encode_general<T, OutT><<<(unsigned)p.blocks, p.threads, 0, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_groups, a.n_per_group,
         a.n_centroids, a.sub_dim, 1.0f, static_cast<OutT *>(a.out));
-    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+    return vqh_launched(a.stream, vqh_status_encode);
 }
 
 template <typename T, typename OutT>
@@ -645,7 +645,7 @@ vq_status vq_dequantize_grouped(const void *idx, int32_t index_bytes, const void
                     n_groups, n_per_group, n_centroids, sub_dim, static_cast<uint32_t *>(out));
         }
     }
-    return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+    return vqh_launched(st, vqh_status_encode);
 }
 
 const char *vq_status_string(vq_status status)

@@ -35,6 +35,7 @@
 //      (distance, index), lowest index winning ties).  No global scratch.
 #pragma once
 
+#include "vq_check.cuh"
 #include "vq_kernels.cuh"
 
 namespace vqk {
@@ -121,6 +122,19 @@ __global__ void __launch_bounds__(THREADS)
     const float *__restrict__ sg = SMOOTH ? smooth + (size_t)g * (size_t)smooth_ns * SUB : nullptr;
     const int64_t row0 = tile * (int64_t)kTile + threadIdx.x;
 
+    // buffer extents, for the checked build's bounds checks (vq_check.cuh)
+    const int64_t n_groups_all = gridDim.x / tiles_per_group;
+    const int64_t nx = n_groups_all * n_per_group * SUB, nout = n_groups_all * n_per_group;
+    const uint64_t f4_total = L::f4_total(n_centroids);
+    constexpr uint32_t kRowAlign = SUB * sizeof(T) < 16 ? SUB * sizeof(T) : 16;  // load_row
+    if constexpr (kChecked) {
+        // the layout inside the launch's shared memory, the block inside the
+        // grid, its smooth factors inside theirs: else the block does nothing
+        if (!dyn_smem_ok(smem, L::bytes(n_centroids, kTile), 16) || !index_ok(g, n_groups_all) ||
+            (SMOOTH && !VQ_SPAN(sg, (int64_t)smooth_ns * SUB, smooth, n_groups_all * smooth_ns * SUB)))
+            return;  // block-uniform
+    }
+
     // Rows of this thread: row0 + r * THREADS, rows 2rp and 2rp+1 packed in
     // one float2.  Rows past the end compute on zeros and are not stored.
     float2 xp[R / 2][SUB];
@@ -129,14 +143,14 @@ __global__ void __launch_bounds__(THREADS)
         float a[SUB], b[SUB];
         const int64_t ra = row0 + (int64_t)(2 * rp) * THREADS;
         const int64_t rb = ra + THREADS;
-        if (ra < n_per_group) {
+        if (ra < n_per_group && VQ_VSPAN(xg + (size_t)ra * SUB, SUB, x, nx, kRowAlign)) {
             load_row<T, SUB>(xg + (size_t)ra * SUB, a);
             smooth_row<SUB, SMOOTH>(a, sg, ra, smooth_ns);
         } else {
 #pragma unroll
             for (int i = 0; i < SUB; ++i) a[i] = 0.f;
         }
-        if (rb < n_per_group) {
+        if (rb < n_per_group && VQ_VSPAN(xg + (size_t)rb * SUB, SUB, x, nx, kRowAlign)) {
             load_row<T, SUB>(xg + (size_t)rb * SUB, b);
             smooth_row<SUB, SMOOTH>(b, sg, rb, smooth_ns);
         } else {
@@ -152,23 +166,27 @@ __global__ void __launch_bounds__(THREADS)
     __syncthreads();
     for (int c = threadIdx.x; c < n_pad; c += THREADS) {
         const bool real = c < n_centroids;
+        const bool cb_ok = !real || VQ_SPAN(cb + (size_t)c * SUB, SUB, codebooks, n_groups_all * n_centroids * SUB);
         float v[SUB];
 #pragma unroll
         for (int i = 0; i < SUB; ++i)
-            v[i] = real ? widen(cb[(size_t)c * SUB + i]) : __int_as_float(0x7fc00000);
+            v[i] = real && cb_ok ? widen(cb[(size_t)c * SUB + i]) : __int_as_float(0x7fc00000);
         float nrm = mul_rn(v[0], v[0]);
 #pragma unroll
         for (int i = 1; i < SUB; ++i) nrm = fma_rn(v[i], v[i], nrm);
 #pragma unroll
         for (int k = 0; k < SUB / 2; ++k) {
             const float w0 = -2.0f * v[2 * k], w1 = -2.0f * v[2 * k + 1];
-            sw[(size_t)c * L::kW4 + k] = make_float4(w0, w0, w1, w1);
+            if (VQ_SPAN(sw + (size_t)c * L::kW4 + k, 1, sw, L::n_off(n_centroids)))
+                sw[(size_t)c * L::kW4 + k] = make_float4(w0, w0, w1, w1);
         }
-        reinterpret_cast<float2 *>(sn)[c] = make_float2(nrm, nrm);
+        if (span_ok(reinterpret_cast<float2 *>(sn) + c, 8, sn, (L::x_off(n_centroids) - L::n_off(n_centroids)) * 16, 8))
+            reinterpret_cast<float2 *>(sn)[c] = make_float2(nrm, nrm);
         float4 *ex = sx + (c / GC) * L::kGroupStride + (c % GC) * L::kX4;
 #pragma unroll
         for (int k = 0; k < SUB / 4; ++k)
-            ex[k] = make_float4(-v[4 * k], -v[4 * k + 1], -v[4 * k + 2], -v[4 * k + 3]);
+            if (VQ_SPAN(ex + k, 1, sx, f4_total - L::x_off(n_centroids)))
+                ex[k] = make_float4(-v[4 * k], -v[4 * k + 1], -v[4 * k + 2], -v[4 * k + 3]);
         if (real) {
             // nonnegative floats (and NaN, which sorts above +inf) order as
             // their bit patterns
@@ -195,12 +213,14 @@ __global__ void __launch_bounds__(THREADS)
 #pragma unroll
         for (int cc = 0; cc < GC; cc += 2) {
             const int c = cg * GC + cc;
-            const float4 nn = sn[c / 2];
+            const float4 nn = VQ_SPAN(sn + c / 2, 1, sn, L::x_off(n_centroids) - L::n_off(n_centroids))
+                                  ? sn[c / 2] : make_float4(0.f, 0.f, 0.f, 0.f);
             float2 wa[SUB], wb[SUB];
 #pragma unroll
             for (int k = 0; k < SUB / 2; ++k) {
-                const float4 qa = sw[(size_t)c * L::kW4 + k];
-                const float4 qb = sw[(size_t)(c + 1) * L::kW4 + k];
+                const bool w_ok = VQ_SPAN(sw + (size_t)c * L::kW4 + k, L::kW4 + 1, sw, L::n_off(n_centroids));
+                const float4 qa = w_ok ? sw[(size_t)c * L::kW4 + k] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 qb = w_ok ? sw[(size_t)(c + 1) * L::kW4 + k] : make_float4(0.f, 0.f, 0.f, 0.f);
                 wa[2 * k] = make_float2(qa.x, qa.y);
                 wa[2 * k + 1] = make_float2(qa.z, qa.w);
                 wb[2 * k] = make_float2(qb.x, qb.y);
@@ -264,7 +284,10 @@ __global__ void __launch_bounds__(THREADS)
         uint32_t id = 0;
         if (!ok || m3[r] <= thr) {
             id = kQueued;
-            if (row < n_per_group) queue[atomicAdd(qcount, 1u)] = (uint32_t)(r * THREADS + threadIdx.x);
+            if (row < n_per_group) {
+                const uint32_t k = atomicAdd(qcount, 1u);
+                if (VQ_SPAN(queue + k, 1, queue, kTile)) queue[k] = (uint32_t)(r * THREADS + threadIdx.x);
+            }
         } else {
             const int ga = two ? min(g1[r], g2[r]) : g1[r];
             const int gb = two ? max(g1[r], g2[r]) : -1;
@@ -278,7 +301,8 @@ __global__ void __launch_bounds__(THREADS)
                     float nc[SUB];
 #pragma unroll
                     for (int k = 0; k < SUB / 4; ++k) {
-                        const float4 q = gp[cc * L::kX4 + k];
+                        const float4 q = VQ_SPAN(gp + cc * L::kX4 + k, 1, sx, f4_total - L::x_off(n_centroids))
+                                             ? gp[cc * L::kX4 + k] : make_float4(0.f, 0.f, 0.f, 0.f);
                         nc[4 * k] = q.x;
                         nc[4 * k + 1] = q.y;
                         nc[4 * k + 2] = q.z;
@@ -297,7 +321,8 @@ __global__ void __launch_bounds__(THREADS)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int64_t row = row0 + (int64_t)r * THREADS;
-        if (row < n_per_group && result[r] != kQueued) store_index(og + row, result[r]);
+        if (row < n_per_group && result[r] != kQueued && VQ_SPAN(og + row, 1, out, nout))
+            store_index(og + row, result[r]);
     }
 
     // ---- queued rows: one warp per row, exact scan over all centroids
@@ -305,7 +330,9 @@ __global__ void __launch_bounds__(THREADS)
     const uint32_t nq = *qcount;
     const int lane = threadIdx.x & 31;
     for (uint32_t q = threadIdx.x >> 5; q < nq; q += THREADS / 32) {
+        if (!VQ_SPAN(queue + q, 1, queue, kTile)) break;  // warp-uniform
         const int64_t row = tile * (int64_t)kTile + queue[q];
+        if (!VQ_SPAN(xg + (size_t)row * SUB, SUB, x, nx)) continue;  // warp-uniform
         float xr[SUB];
 #pragma unroll
         for (int i = 0; i < SUB; ++i) xr[i] = widen(xg[(size_t)row * SUB + i]);
@@ -317,7 +344,8 @@ __global__ void __launch_bounds__(THREADS)
             float nc[SUB];
 #pragma unroll
             for (int k = 0; k < SUB / 4; ++k) {
-                const float4 qv = cp[k];
+                const float4 qv = VQ_SPAN(cp + k, 1, sx, f4_total - L::x_off(n_centroids))
+                                      ? cp[k] : make_float4(0.f, 0.f, 0.f, 0.f);
                 nc[4 * k] = qv.x;
                 nc[4 * k + 1] = qv.y;
                 nc[4 * k + 2] = qv.z;
@@ -339,7 +367,7 @@ __global__ void __launch_bounds__(THREADS)
             }
         }
         // no finite, non-NaN distance anywhere: index 0, as the definition gives
-        if (lane == 0) store_index(og + row, id == kQueued ? 0u : id);
+        if (lane == 0 && VQ_SPAN(og + row, 1, out, nout)) store_index(og + row, id == kQueued ? 0u : id);
     }
 }
 

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "vq_encode.h"
+
 // Streaming multiprocessors of the current device, cached per device; 0 if
 // there is no usable device.
 int vqh_device_sms();
@@ -30,3 +32,23 @@ cudaError_t vqh_status_scalar(uint32_t *bits, bool clear);
         }                                                                            \
         return e;                                                                    \
     }
+
+// Status of the launches just made on `stream`: VQ_ERR_CUDA if a launch
+// failed, else VQ_OK.  In the checked build (VQ_CHECKED) the call also waits
+// for them and reports an out-of-bounds bit in this unit's status word (read
+// by `reader`) as VQ_ERR_INTERNAL; the bit stays set until vq_kernel_status()
+// clears it.
+inline vq_status vqh_launched(cudaStream_t stream, cudaError_t (*reader)(uint32_t *, bool))
+{
+    if (cudaPeekAtLastError() != cudaSuccess) return VQ_ERR_CUDA;
+#ifdef VQ_CHECKED
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return VQ_ERR_CUDA;
+    uint32_t bits = 0;
+    if (reader(&bits, false) != cudaSuccess) return VQ_ERR_CUDA;
+    if (bits & VQ_KSTATUS_OUT_OF_BOUNDS) return VQ_ERR_INTERNAL;
+#else
+    (void)stream;
+    (void)reader;
+#endif
+    return VQ_OK;
+}

@@ -37,7 +37,8 @@ int64_t stream_blocks(int64_t work_items, int per_sm)
     return b < 1 ? 1 : b;
 }
 
-vq_status launched() { return cudaPeekAtLastError() == cudaSuccess ? VQ_OK : VQ_ERR_CUDA; }
+// Status of the launches just made on `st` (vq_host.h).
+vq_status launched(cudaStream_t st) { return vqh_launched(st, vqh_status_scalar); }
 
 template <typename T, int NC>
 vq_status launch_scan_nc(const void *x, int64_t n, const float *c, int32_t n_c, uint8_t *out,
@@ -47,7 +48,7 @@ vq_status launch_scan_nc(const void *x, int64_t n, const float *c, int32_t n_c, 
     const bool vec = (uintptr_t)x % 16 == 0 && (uintptr_t)out % 8 == 0;
     vqs::scalar_scan<T, NC><<<(unsigned)stream_blocks((n + 7) / 8, 8), kThreads, smem, st>>>(
         static_cast<const T *>(x), n, c, n_c, vec, -1.0f, out);
-    return launched();
+    return launched(st);
 }
 
 template <typename T>
@@ -75,7 +76,7 @@ vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, i
     const size_t smem = QUANT && NC == 0 ? vqs::hadamard_smem(n_c) : 0;
     vqs::hadamard_rows<T, E, QUANT, NC><<<(unsigned)blocks, kThreads, smem, st>>>(
         static_cast<const T *>(x), diag, n_rows, lpr, scale, c, n_c, -1.0f, y, idx);
-    return launched();
+    return launched(st);
 }
 
 // Codebooks of 2, 4, 8 or 16 entries (the pages' 1- to 4-bit Lloyd-Max
@@ -176,7 +177,8 @@ vq_status vq_scalar_quantize(const void *x, vq_dtype dtype, int64_t n, const flo
         uint8_t *tab = static_cast<uint8_t *>(workspace);
         vqs::scalar_table<<<65536 / kThreads, kThreads, (size_t)n_centroids * 4, st>>>(
             centroids, n_centroids, dtype == VQ_BF16, tab);
-        if (launched() != VQ_OK) return VQ_ERR_CUDA;
+        const vq_status ts = launched(st);
+        if (ts != VQ_OK) return ts;
         const bool vec = (uintptr_t)x % 16 == 0 && (uintptr_t)out % 8 == 0;
         // one block of kLookupThreads per SM stages the 64 KiB table once;
         // give each block at least 64 Ki elements
@@ -190,7 +192,7 @@ vq_status vq_scalar_quantize(const void *x, vq_dtype dtype, int64_t n, const flo
             return VQ_ERR_CUDA;
         kp<<<(unsigned)blocks, kLookupThreads, kTableBytes, st>>>(static_cast<const uint16_t *>(x), n,
                                                                   tab, vec, out);
-        return launched();
+        return launched(st);
     }
     switch (dtype) {
     case VQ_F16: return launch_scan<__half>(x, n, centroids, n_centroids, out, st);
@@ -224,7 +226,7 @@ vq_status vq_scalar_dequantize(const uint8_t *idx, int64_t n, const float *centr
                                                                 static_cast<float *>(out));
         break;
     }
-    return launched();
+    return launched(st);
 }
 
 vq_status vq_hadamard_rotate(const void *x, vq_dtype dtype, const float *diag, int64_t n_rows,

@@ -32,6 +32,8 @@
 
 #include <type_traits>
 
+#include "vq_check.cuh"
+
 namespace vqs {
 
 __device__ __forceinline__ float widen16(uint16_t bits, bool bf16)
@@ -94,9 +96,13 @@ __global__ void __launch_bounds__(1024)
                   bool vec, uint8_t *__restrict__ out)
 {
     extern __shared__ __align__(16) uint8_t sl_tab[];
+    // the table must fit the launch's shared memory, else the block does
+    // nothing (checked build; block-uniform); its lookups take 16-bit
+    // patterns, so they stay inside it
+    if (!vqk::dyn_smem_ok(sl_tab, 65536, 16)) return;
     const uint4 *t4 = reinterpret_cast<const uint4 *>(table);
     for (int k = threadIdx.x; k < 65536 / 16; k += blockDim.x)
-        reinterpret_cast<uint4 *>(sl_tab)[k] = __ldg(t4 + k);
+        if (VQ_SPAN(t4 + k, 1, t4, 4096)) reinterpret_cast<uint4 *>(sl_tab)[k] = __ldg(t4 + k);
     __syncthreads();
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
@@ -107,15 +113,20 @@ __global__ void __launch_bounds__(1024)
     for (; u + (U - 1) * nthreads < units; u += U * nthreads) {
         uint4 v[U];
 #pragma unroll
-        for (int k = 0; k < U; ++k) v[k] = __ldcs(reinterpret_cast<const uint4 *>(x) + u + k * nthreads);
+        for (int k = 0; k < U; ++k)
+            v[k] = VQ_VSPAN(x + (u + k * nthreads) * 8, 8, x, n, 16)
+                       ? __ldcs(reinterpret_cast<const uint4 *>(x) + u + k * nthreads) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int k = 0; k < U; ++k)
-            __stcs(reinterpret_cast<uint2 *>(out) + u + k * nthreads, lookup8(sl_tab, v[k]));
+            if (VQ_VSPAN(out + (u + k * nthreads) * 8, 8, out, n, 8))
+                __stcs(reinterpret_cast<uint2 *>(out) + u + k * nthreads, lookup8(sl_tab, v[k]));
     }
     for (; u < units; u += nthreads)
-        __stcs(reinterpret_cast<uint2 *>(out) + u,
-               lookup8(sl_tab, __ldcs(reinterpret_cast<const uint4 *>(x) + u)));
-    for (int64_t e = units * 8 + tid; e < n; e += nthreads) out[e] = sl_tab[x[e]];
+        if (VQ_VSPAN(x + u * 8, 8, x, n, 16) && VQ_VSPAN(out + u * 8, 8, out, n, 8))
+            __stcs(reinterpret_cast<uint2 *>(out) + u,
+                   lookup8(sl_tab, __ldcs(reinterpret_cast<const uint4 *>(x) + u)));
+    for (int64_t e = units * 8 + tid; e < n; e += nthreads)
+        if (VQ_SPAN(x + e, 1, x, n) && VQ_SPAN(out + e, 1, out, n)) out[e] = sl_tab[x[e]];
 }
 
 // ---- exact nearest centroid through the sorted codebook
@@ -159,8 +170,10 @@ __device__ __forceinline__ bool build_sorted(const float *c, int n_c, float *u, 
             const float v = c[t];
             int rank = 0;
             for (int j = 0; j < n_c; ++j) rank += first[j] && c[j] < v;
-            u[rank] = v;
-            rep[rank] = t;
+            if (vqk::index_ok(rank, n_c)) {
+                u[rank] = v;
+                rep[rank] = t;
+            }
         }
     }
     if (threadIdx.x == 0) {
@@ -186,6 +199,7 @@ __device__ __forceinline__ int nearest_sorted(float y, const SortedCb &cb)
     for (int step = cb.top; step > 0; step >>= 1)
         if (pos + step <= cb.m && cb.u[pos + step - 1] <= y) pos += step;
     const int L = pos - 1, R = pos;
+    if (!vqk::index_ok(pos, cb.m + 1)) return -1;  // the scan decides (checked build)
     const float inf = __int_as_float(0x7f800000);
     const float dl = L >= 0 ? dist_to(y, cb.u[L]) : inf;
     const float dr = R < cb.m ? dist_to(y, cb.u[R]) : inf;
@@ -395,6 +409,9 @@ __global__ void __launch_bounds__(256)
     bool creg_finite = false;
     float2 cneg[NC > 1 ? NC / 2 : 1];
     if constexpr (QUANT && NC > 0) {
+        // a register codebook reads NC <= n_c centroids (checked build:
+        // else the block does nothing)
+        if (!vqk::index_ok(NC - 1, n_c)) return;
         load_cneg<NC>(centroids, cneg);
         creg_finite = all_finite<NC>(cneg);
     }
@@ -405,6 +422,9 @@ __global__ void __launch_bounds__(256)
         int *rep = reinterpret_cast<int *>(u + n_c);                 // [n_c]
         int *first = rep + n_c;                                      // [n_c]
         int *mcount = first + n_c;
+        // the sorted view inside the launch's shared memory (checked build:
+        // else the block does nothing; block-uniform)
+        if (!vqk::dyn_smem_ok(hq_sm, hadamard_smem(n_c), 16)) return;
         for (int j = threadIdx.x; j < n_c; j += blockDim.x) c[j] = centroids[j];
         __syncthreads();
         sorted_ok = build_sorted(c, n_c, u, rep, first, mcount);
@@ -427,16 +447,21 @@ __global__ void __launch_bounds__(256)
     // R loads per lane are in flight
     constexpr int R = E <= 4 ? 4 : E <= 16 ? 2 : 1;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    // the vector width of load_run
+    constexpr uint32_t kRunBytes = E * sizeof(T);
+    constexpr uint32_t kRunAlign = kRunBytes >= 16 && kRunBytes % 16 == 0 ? 16 : kRunBytes == 8 ? 8 : sizeof(T);
+    // the row is lanes_per_row * E = d elements: diag and every row of x and
+    // of the output hold d of them
     float dg[E];
 #pragma unroll
-    for (int j = 0; j < E; ++j) dg[j] = __ldg(diag + l * E + j);
+    for (int j = 0; j < E; ++j) dg[j] = VQ_SPAN(diag + l * E + j, 1, diag, d) ? __ldg(diag + l * E + j) : 0.f;
     for (int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
          warp * R * rows_per_warp < n_rows; warp += warps) {  // warp-uniform
         float v[R][E];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t row = (warp * R + r) * rows_per_warp + sub;
-            if (row < n_rows) {
+            if (row < n_rows && VQ_VSPAN(x + (size_t)row * d + (size_t)l * E, E, x, n_rows * d, kRunAlign)) {
                 load_run<T, E>(x + (size_t)row * d + (size_t)l * E, v[r]);
             } else {
 #pragma unroll
@@ -489,6 +514,7 @@ __global__ void __launch_bounds__(256)
                     }
                 }
                 uint8_t *o = idx + (size_t)row * d + (size_t)l * E;
+                if (!VQ_VSPAN(o, E, idx, n_rows * d, E % 4 == 0 ? 4 : 1)) continue;
                 if constexpr (E % 4 == 0) {
 #pragma unroll
                     for (int j = 0; j < E; j += 4)
@@ -500,6 +526,7 @@ __global__ void __launch_bounds__(256)
                 }
             } else {
                 float *o = y + (size_t)row * d + (size_t)l * E;
+                if (!VQ_SPAN(o, E, y, n_rows * d)) continue;
 #pragma unroll
                 for (int j = 0; j < E; ++j) o[j] = w[j];
             }

@@ -88,6 +88,7 @@
 
 #include <type_traits>
 
+#include "vq_check.cuh"
 #include "vq_filter.cuh"
 #include "vq_kernels.cuh"
 #include "vq_status.cuh"
@@ -183,12 +184,13 @@ __device__ __forceinline__ uint32_t mbar_wait_state(uint64_t *bar, uint32_t pari
     return 0u;
 }
 
-// Arrive once on the barrier (completing a phase of arrival count 1).
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+// Arrive once on the barrier (completing a phase of arrival count 1);
+// returns the barrier state token, which callers may ignore.
+__device__ __forceinline__ uint64_t mbar_arrive(uint64_t *bar)
 {
     uint64_t state;
     asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];" : "=l"(state) : "r"(smem_addr(bar)) : "memory");
-    (void)state;
+    return state;
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -349,6 +351,22 @@ __global__ void __launch_bounds__(128, MINB)
     const float *__restrict__ sg = SMOOTH ? smooth + (size_t)g * (size_t)smooth_ns * SUB : nullptr;
     const int64_t row_base = blk * (int64_t)tiles_per_block * 128;
 
+    // buffer extents, for the checked build's bounds checks (vq_check.cuh)
+    const int64_t n_groups_all = gridDim.x / blocks_per_group;
+    const int64_t nx = n_groups_all * n_per_group * SUB, nout = n_groups_all * n_per_group;
+    constexpr uint64_t kSaBytes = kNA * L::kABytes, kSbBytes = (uint64_t)kNB * 256 * L::kRowBytes;
+    const uint64_t sx_bytes = (uint64_t)L::groups(n_centroids) * L::kGroupFloats * 4;
+    constexpr uint64_t kMiscBytes = 64 + 128 * 4;
+    constexpr uint32_t kRowAlign = SUB * sizeof(T) < 16 ? SUB * sizeof(T) : 16;  // load_row
+    if constexpr (kChecked) {
+        // the layout inside the launch's shared memory, the block inside the
+        // grid, its smooth factors inside theirs: else the block does nothing
+        if (!dyn_smem_ok(sm, L::used(n_centroids), 16) || !span_ok(bar, 8, misc, kMiscBytes, 8) ||
+            !span_ok(queue, 512, misc, kMiscBytes, 4) || !index_ok(g, n_groups_all) ||
+            (SMOOTH && !VQ_SPAN(sg, (int64_t)smooth_ns * SUB, smooth, n_groups_all * smooth_ns * SUB)))
+            return;  // block-uniform
+    }
+
     // ---- set-up: maxima, barrier, tensor memory, constant part of A
     if (tid < SUB + 2) misc[tid] = 0u;
     if (tid == 0) {
@@ -371,7 +389,8 @@ __global__ void __launch_bounds__(128, MINB)
             for (int kb = SUB / 4; kb < kKB; ++kb) {
                 const float4 v = kb == SUB / 4 && pc == 0 ? make_float4(1.f, 1.f, 1.f, 0.f)
                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(arow + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) = v;
+                float4 *dst = reinterpret_cast<float4 *>(arow + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4);
+                if (span_ok(dst, 16, sa, kSaBytes, 16)) *dst = v;
             }
         }
     }
@@ -380,9 +399,10 @@ __global__ void __launch_bounds__(128, MINB)
     // ---- stage the codebook: B operand, exact layout, maxima
     for (int c = tid; c < 256; c += 128) {
         const bool real = c < n_centroids;
+        const bool cb_ok = !real || VQ_SPAN(cb + (size_t)c * SUB, SUB, codebooks, n_groups_all * n_centroids * SUB);
         float v[SUB];
 #pragma unroll
-        for (int i = 0; i < SUB; ++i) v[i] = real ? widen(cb[(size_t)c * SUB + i]) : 0.f;
+        for (int i = 0; i < SUB; ++i) v[i] = real && cb_ok ? widen(cb[(size_t)c * SUB + i]) : 0.f;
         float nrm = mul_rn(v[0], v[0]);
 #pragma unroll
         for (int i = 1; i < SUB; ++i) nrm = fma_rn(v[i], v[i], nrm);
@@ -406,22 +426,26 @@ __global__ void __launch_bounds__(128, MINB)
             bk[SUB] = __int_as_float(0x7f800000);  // padding never screens in
         }
 #pragma unroll
-        for (int kb = 0; kb < kKB; ++kb)
-            *reinterpret_cast<float4 *>(sb + ((c >> 3) * (kKB * 128) + kb * 128 + (c & 7) * 16) / 4) =
-                make_float4(bk[4 * kb], bk[4 * kb + 1], bk[4 * kb + 2], bk[4 * kb + 3]);
+        for (int kb = 0; kb < kKB; ++kb) {
+            float4 *dst = reinterpret_cast<float4 *>(sb + ((c >> 3) * (kKB * 128) + kb * 128 + (c & 7) * 16) / 4);
+            if (span_ok(dst, 16, sb, kSbBytes, 16)) *dst = make_float4(bk[4 * kb], bk[4 * kb + 1], bk[4 * kb + 2], bk[4 * kb + 3]);
+        }
         if constexpr (kNB == 2) {
             // second piece: -2c's next 11 bits, nothing in the constant columns
             float *sb2 = sb + 256 * L::kRowBytes / 4;
 #pragma unroll
-            for (int kb = 0; kb < kKB; ++kb)
-                *reinterpret_cast<float4 *>(sb2 + ((c >> 3) * (kKB * 128) + kb * 128 + (c & 7) * 16) / 4) =
-                    kb < SUB / 4 ? make_float4(bm[4 * kb], bm[4 * kb + 1], bm[4 * kb + 2], bm[4 * kb + 3])
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int kb = 0; kb < kKB; ++kb) {
+                float4 *dst = reinterpret_cast<float4 *>(sb2 + ((c >> 3) * (kKB * 128) + kb * 128 + (c & 7) * 16) / 4);
+                if (span_ok(dst, 16, sb, kSbBytes, 16))
+                    *dst = kb < SUB / 4 ? make_float4(bm[4 * kb], bm[4 * kb + 1], bm[4 * kb + 2], bm[4 * kb + 3])
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         if (c < n_pad) {
             float *ex = sx + (c / kGC) * L::kGroupFloats + ((c % kGC) >> 1) * (2 * SUB) + (c & 1);
 #pragma unroll
-            for (int i = 0; i < SUB; ++i) ex[2 * i] = real ? -v[i] : __int_as_float(0x7fc00000);
+            for (int i = 0; i < SUB; ++i)
+                if (span_ok(ex + 2 * i, 4, sx, sx_bytes, 4)) ex[2 * i] = real ? -v[i] : __int_as_float(0x7fc00000);
         }
         // maxima over the block's centroids: warp reduction, then one atomic per
         // warp (nonnegative floats, and NaN above +inf, order as their bits)
@@ -457,7 +481,7 @@ __global__ void __launch_bounds__(128, MINB)
     // this thread's row of the first tile
     float xr[SUB];
     auto load_x = [&](int64_t row, float (&v)[SUB]) {
-        if (row < n_per_group) {
+        if (row < n_per_group && VQ_VSPAN(xg + (size_t)row * SUB, SUB, x, nx, kRowAlign)) {
             load_row<T, SUB>(xg + (size_t)row * SUB, v);
             smooth_row<SUB, SMOOTH>(v, sg, row, smooth_ns);
         } else {
@@ -487,15 +511,18 @@ __global__ void __launch_bounds__(128, MINB)
 #pragma unroll
             for (int pc = 0; pc < 2; ++pc)
 #pragma unroll
-                for (int kb = 0; kb < SUB / 4; ++kb)
-                    *reinterpret_cast<float4 *>(sa + pc * (L::kABytes / 4) +
-                                                ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) =
-                        make_float4(pc3[pc][4 * kb], pc3[pc][4 * kb + 1], pc3[pc][4 * kb + 2], pc3[pc][4 * kb + 3]);
+                for (int kb = 0; kb < SUB / 4; ++kb) {
+                    float4 *dst = reinterpret_cast<float4 *>(sa + pc * (L::kABytes / 4) +
+                                                             ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4);
+                    if (span_ok(dst, 16, sa, kSaBytes, 16))
+                        *dst = make_float4(pc3[pc][4 * kb], pc3[pc][4 * kb + 1], pc3[pc][4 * kb + 2], pc3[pc][4 * kb + 3]);
+                }
         } else {
 #pragma unroll
-            for (int kb = 0; kb < SUB / 4; ++kb)
-                *reinterpret_cast<float4 *>(sa + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4) =
-                    make_float4(xr[4 * kb], xr[4 * kb + 1], xr[4 * kb + 2], xr[4 * kb + 3]);
+            for (int kb = 0; kb < SUB / 4; ++kb) {
+                float4 *dst = reinterpret_cast<float4 *>(sa + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4);
+                if (span_ok(dst, 16, sa, kSaBytes, 16)) *dst = make_float4(xr[4 * kb], xr[4 * kb + 1], xr[4 * kb + 2], xr[4 * kb + 3]);
+            }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
@@ -514,7 +541,7 @@ __global__ void __launch_bounds__(128, MINB)
                 // a wait that gave up but completed (possible only when POLLS
                 // is below the full limit): this pass's phase without an MMA
                 if (tid == 0 && (wst & (kWaitLate | kWaitFailed)) == kWaitLate) {
-                    mbar_arrive(bar);
+                    (void)mbar_arrive(bar);
                     wst = (wst & 3u) | ((phase + 1u) << 2);
                 }
             }
@@ -531,7 +558,15 @@ __global__ void __launch_bounds__(128, MINB)
                             umma_smem_desc(sa_addr + pa * (uint32_t)L::kABytes + kstep * 256, 128, kSbo);
                         const uint64_t bd = umma_smem_desc(
                             sb_addr + pb * (uint32_t)(256 * L::kRowBytes) + (c0 >> 3) * kSbo + kstep * 256, 128, kSbo);
-                        umma_tf32(tmem, ad, bd, idesc, pp > 0 || kstep > 0);
+                        // the bytes the two operands span (16 or ncols / 8
+                        // groups of 8 rows, kSbo apart, 256 bytes each) and
+                        // the accumulator columns
+                        const bool op_ok =
+                            span_ok(sa + (pa * L::kABytes + kstep * 256) / 4, 15 * kSbo + 256, sa, kSaBytes, 16) &&
+                            span_ok(sb + (pb * 256 * L::kRowBytes + (c0 >> 3) * kSbo + kstep * 256) / 4,
+                                    (ncols / 8 - 1) * kSbo + 256, sb, kSbBytes, 16) &&
+                            index_ok(ncols - 1, NCOL);
+                        if (op_ok) umma_tf32(tmem, ad, bd, idesc, pp > 0 || kstep > 0);
                     }
                 }
                 umma_commit(bar);
@@ -624,7 +659,10 @@ __global__ void __launch_bounds__(128, MINB)
         uint32_t id = 0;
         if (!ok || cnt > 2 || cnt == 0) {
             id = kQueued;
-            if (row < n_per_group) queue[atomicAdd(qcount, 1u)] = (uint32_t)tid;
+            if (row < n_per_group) {
+                const uint32_t k = atomicAdd(qcount, 1u);
+                if (VQ_SPAN(queue + k, 1, queue, 128)) queue[k] = (uint32_t)tid;
+            }
         } else {
             // exact distances, two centroids per packed evaluation, ascending
             // index with a strict "<" (lowest index wins ties)
@@ -642,7 +680,8 @@ __global__ void __launch_bounds__(128, MINB)
                     float2 nc[SUB];
 #pragma unroll
                     for (int k = 0; k < SUB / 2; ++k) {
-                        const float4 q = *reinterpret_cast<const float4 *>(gp + pr * 2 * SUB + 4 * k);
+                        const float4 *src = reinterpret_cast<const float4 *>(gp + pr * 2 * SUB + 4 * k);
+                        const float4 q = span_ok(src, 16, sx, sx_bytes, 16) ? *src : make_float4(0.f, 0.f, 0.f, 0.f);
                         nc[2 * k] = make_float2(q.x, q.y);
                         nc[2 * k + 1] = make_float2(q.z, q.w);
                     }
@@ -659,13 +698,15 @@ __global__ void __launch_bounds__(128, MINB)
                 }
             }
         }
-        if (row < n_per_group && id != kQueued) store_index(og + row, id);
+        if (row < n_per_group && id != kQueued && VQ_SPAN(og + row, 1, out, nout)) store_index(og + row, id);
         __syncthreads();
 
         // ---- queued rows of this tile: one warp per row, exact scan
         const uint32_t nq = *qcount;
         for (uint32_t q = (uint32_t)warp; q < nq; q += 4) {
+            if (!VQ_SPAN(queue + q, 1, queue, 128)) break;  // warp-uniform
             const int64_t qrow = row_base + (int64_t)tile * 128 + queue[q];
+            if (!VQ_SPAN(xg + (size_t)qrow * SUB, SUB, x, nx)) continue;  // warp-uniform
             float xq[SUB];
 #pragma unroll
             for (int i = 0; i < SUB; ++i) xq[i] = widen(xg[(size_t)qrow * SUB + i]);
@@ -676,7 +717,7 @@ __global__ void __launch_bounds__(128, MINB)
                 const float *cp = sx + (c / kGC) * L::kGroupFloats + ((c % kGC) >> 1) * (2 * SUB) + (c & 1);
                 float nc[SUB];
 #pragma unroll
-                for (int i = 0; i < SUB; ++i) nc[i] = cp[2 * i];
+                for (int i = 0; i < SUB; ++i) nc[i] = span_ok(cp + 2 * i, 4, sx, sx_bytes, 4) ? cp[2 * i] : 0.f;
                 const float d = one_dist<SUB>(xq, nc, one);
                 if (d < best) {
                     best = d;
@@ -692,7 +733,7 @@ __global__ void __launch_bounds__(128, MINB)
                     bi = oi;
                 }
             }
-            if (lane == 0) store_index(og + qrow, bi == kQueued ? 0u : bi);
+            if (lane == 0 && VQ_SPAN(og + qrow, 1, out, nout)) store_index(og + qrow, bi == kQueued ? 0u : bi);
         }
 #pragma unroll
         for (int i = 0; i < SUB; ++i) xr[i] = xn[i];
@@ -705,7 +746,7 @@ __global__ void __launch_bounds__(128, MINB)
         // a wait gave up: mark the rows of the failed tile and of every later one
         for (int t = (int)*qcount; t < tiles_per_block; ++t) {
             const int64_t r = row_base + (int64_t)t * 128 + tid;
-            if (r < n_per_group) store_index(og + r, kQueued);
+            if (r < n_per_group && VQ_SPAN(og + r, 1, out, nout)) store_index(og + r, kQueued);
         }
     }
     if (warp == 0)

@@ -10,7 +10,9 @@ of ``libvqenc.so``):
 * ``stats_encode`` -- the library's encode kernel, library configuration, with
   per-row screening statistics;
 * ``polls_encode`` -- the same kernel with a tiny per-pass poll limit, for the
-  wait give-up path.
+  wait give-up path;
+* ``check_probe`` -- the bounds-check primitives of the checked build,
+  evaluated on described spans.
 
 Same compiler flags as the library (``product_vq_kv_gb300.build``); the units
 compile in parallel and are rebuilt only when a source or a library header
@@ -90,6 +92,10 @@ def load() -> ctypes.CDLL:
             lib.polls_encode.argtypes = [i32, i32, i32, vp, vp, i64, i64, i32, i32, vp, vp]
             lib.polls_status.restype = i32
             lib.polls_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+            lib.check_probe.restype = i32
+            lib.check_probe.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, vp]
+            lib.check_status.restype = i32
+            lib.check_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
             _lib = lib
         return _lib
 
@@ -104,6 +110,7 @@ def read_stats(clear: bool = True) -> list:
 
 def status(unit: str, clear: bool = True) -> int:
     bits = ctypes.c_uint32(0)
-    fn = {"stats": load().stats_status, "polls": load().polls_status}[unit]
+    fn = {"stats": load().stats_status, "polls": load().polls_status,
+          "check": load().check_status}[unit]
     assert fn(ctypes.byref(bits), 1 if clear else 0) == 0
     return int(bits.value)

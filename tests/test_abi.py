@@ -44,6 +44,15 @@ def test_library_exports_every_declared_function(lib, name):
     assert hasattr(lib, name), f"{name} declared in include/ but not exported"
 
 
+def test_checked_build_exports_every_declared_function():
+    """The bounds-checked build (-DVQ_CHECKED) compiles and has the same ABI."""
+    from product_vq_kv_gb300.build import build
+
+    checked = ctypes.CDLL(build(checked=True))
+    for name in declared_functions():
+        assert hasattr(checked, name), name
+
+
 def test_abi_version(lib):
     lib.vq_abi_version.restype = ctypes.c_int32
     assert lib.vq_abi_version() == 1
