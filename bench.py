@@ -10,8 +10,12 @@ the launching stream.  Prints one JSON line.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun each rank encodes its own full workload (independent problems,
-no data-path collective: weak scaling); rank 0 prints.  ``--impl reference``
-times the CPU oracle on this host's cores instead (the baseline arm).
+no data-path collective: weak scaling); with ``--partition`` the ranks split
+one workload instead (``vq_partition``: each encodes its share against
+replicated codebooks, no collective: strong scaling).  Rank 0 prints.
+``--impl reference`` times the CPU oracle on this host's cores instead (the
+baseline arm).  The default line also carries ``other_workloads``: the Llama
+decode step, long-context and grouped-adversarial encodes, timed the same way.
 """
 from __future__ import annotations
 
@@ -46,6 +50,13 @@ MEASURED_TRAFFIC = {
     "grid=1171 smem=26965": 8_425_216,
 }
 L2_FLUSH_BYTES = 256 << 20
+# How the encode rooflines count work.
+ENCODE_ACCOUNTING = ("effective: brute-force F = n_centroids * 3 * sub_dim fp32 operations per "
+                     "sub-vector over the measured time; the screening kernels do less "
+                     "arithmetic and return the same index, so frac can exceed 1")
+L2_POLICY = "flushed before every step (256 MiB write); per-step CUDA events on the launching stream"
+# Workloads timed beside the headline one in the default line: (name, steps).
+OTHER_WORKLOADS = (("llama_decode", 300), ("long_context", 100), ("grouped_adversarial", 20))
 FP32_LANES_PER_SM = 128
 CLOCK_REASON_BITS = {
     0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
@@ -242,10 +253,11 @@ def bench_reference(args) -> None:
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "strong" if args.partition else "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(config_block(w, args, world),
-                       l2="not applicable: the CPU oracle, wall-clock time over the steps"),
+        "config": config_block(w, args, world),
+        "timing": {"l2": "not applicable: the CPU oracle, wall-clock time over the steps"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"first {rows} of {w.n} sub-vectors of {args.workload} per "
                                    f"step, {cores} threads"},
@@ -255,12 +267,73 @@ def bench_reference(args) -> None:
 
 
 def config_block(w: workloads.Workload, args, world: int) -> dict:
+    """The workload, identical for both arms (timing details go elsewhere)."""
+    if world == 1:
+        par = "single"
+    else:
+        par = f"partition{world}" if getattr(args, "partition", False) else f"replicas{world}"
     return {"workload": w.name, "description": w.description, "n_subvectors": w.n,
             "n_groups": w.n_groups, "sub_dim": w.sub_dim, "n_centroids": w.n_centroids,
             "input_dtype": "f16", "tokens": w.tokens, "kv_heads": w.kv_heads,
-            "head_dim": w.head_dim, "layers": w.layers,
-            "parallelism": f"replicas{world}" if world > 1 else "single",
-            "l2": "flushed before every step (256 MiB write); per-step CUDA events"}
+            "head_dim": w.head_dim, "layers": w.layers, "parallelism": par}
+
+
+def time_steps(step, steps: int, warmup: int, flush, stream, dev, clock_index=None):
+    """Run `warmup` untimed steps, then `steps` timed ones, each after an L2
+    flush and bracketed by CUDA events on `stream`.  Returns the per-step
+    milliseconds, the wall time of the timed region, and (with clock_index)
+    the sampled clocks."""
+    import torch
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(clock_index) if clock_index is not None else None
+    if sampler:
+        sampler.__enter__()
+    try:
+        region0 = time.perf_counter()
+        for k in range(steps):
+            flush.zero_()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize(dev)
+        region_s = time.perf_counter() - region0
+    finally:
+        if sampler:
+            sampler.__exit__(None, None, None)
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], region_s, (
+        sampler.summary() if sampler else None)
+
+
+def other_workloads(vq, dev, flush, stream, peak_tflops: float) -> dict:
+    """The other encode workloads, one grouped launch per step, timed like
+    the headline one: the Llama decode step, long context, grouped
+    adversarial."""
+    import torch
+
+    out = {}
+    for name, steps in OTHER_WORKLOADS:
+        w = workloads.WORKLOADS[name]
+        x, cb = workloads.generate(name)
+        xd, cbd = torch.from_numpy(x).to(dev), torch.from_numpy(cb).to(dev)
+        idx = torch.empty(x.shape[:2], dtype=torch.uint32, device=dev)
+        ms, _, _ = time_steps(lambda: vq.vq_encode_grouped(xd, cbd, out=idx, stream=stream),
+                              steps, 3, flush, stream, dev)
+        mean = sum(ms) / len(ms)
+        achieved = flops_per_subvector(w) * w.n / (mean * 1e-3) / 1e12
+        out[name] = {"value": w.n / (mean * 1e-3), "unit": UNIT, "ms_per_step": mean,
+                     "ms_median": statistics.median(ms), "steps": steps,
+                     "n_subvectors": w.n, "n_groups": w.n_groups, "sub_dim": w.sub_dim,
+                     "frac": achieved / peak_tflops, "accounting": ENCODE_ACCOUNTING,
+                     "kernel": vq.vq_describe_launch(x.shape[0], x.shape[1], cb.shape[1],
+                                                     x.shape[2], torch.float16, xd.data_ptr())}
+        del xd, cbd, idx
+    return out
 
 
 def bench_ours(args) -> None:
@@ -296,7 +369,16 @@ def bench_ours(args) -> None:
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    if args.per_layer:
+    units = w.n  # sub-vectors this rank encodes per step
+    if args.partition:
+        # this rank's share of the one job (codebooks replicated, no collective)
+        slices = vq.vq_partition(x.shape[0], x.shape[1], world, rank)
+        units = sum(ng * nr for _, ng, _, nr in slices)
+        share = torch.empty(units, dtype=torch.uint32, device=dev)
+
+        def step():
+            vq.vq_encode_partition(xd, cbd, world, rank, out=share, stream=stream)
+    elif args.per_layer:
         # the pages' per-layer dispatch: one vq_encode launch per group
         views = [(xd[g], cbd[g], out[g]) for g in range(x.shape[0])]
 
@@ -311,29 +393,18 @@ def bench_ours(args) -> None:
         flush.zero_()
         step()
     torch.cuda.synchronize(dev)
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clocks:
-        region0 = time.perf_counter()
-        for k in range(args.steps):
-            flush.zero_()
-            starts[k].record(stream)
-            step()
-            ends[k].record(stream)
-        torch.cuda.synchronize(dev)
-        region_s = time.perf_counter() - region0
+    step_ms, region_s, clk = time_steps(step, args.steps, 0, flush, stream, dev, clock_index=local)
     if world > 1:
         dist.barrier()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kernel_ms = sum(step_ms) / len(step_ms)
     median_ms = statistics.median(step_ms)
     kernel_ms, region_s, median_ms = reduce_max([kernel_ms, region_s, median_ms], dev)
 
-    variant = args.dtype != "f16" or args.centroids or args.misalign or args.per_layer
+    variant = (args.dtype != "f16" or args.centroids or args.misalign or args.per_layer
+               or args.partition)
     # end to end through the host entry point: pinned host in, pinned host out
     xh = torch.from_numpy(x).pin_memory()
     cbh = torch.from_numpy(cb).pin_memory()
@@ -360,17 +431,20 @@ def bench_ours(args) -> None:
     peaks = measured_peaks()
     desc = vq.vq_describe_launch(x.shape[0], x.shape[1], cb.shape[1], x.shape[2], tdt,
                                  xd.data_ptr())
-    clk = clocks.summary()
     sm_max = peaks.get("sm_max_mhz") or clk["sm_max_mhz"] or 2070.0
     peak_tflops = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
-    units = w.n
-    value = job_throughput(units, world, kernel_ms * 1e-3)
+    # replicas: every rank encodes the whole workload; partition: the ranks
+    # share one (rank 0's share stands for each rank's launch below)
+    value = (w.n / (kernel_ms * 1e-3) if args.partition
+             else job_throughput(units, world, kernel_ms * 1e-3))
     flops_unit = cb.shape[1] * 3 * w.sub_dim  # as flops_per_subvector, for the codebook used
     achieved = flops_unit * units / (kernel_ms * 1e-3) / 1e12
     roofline = {
         "bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
-        "frac": achieved / peak_tflops, "traffic": MEASURED_TRAFFIC.get(desc),
-        "kernel": desc,
+        "frac": achieved / peak_tflops,
+        "traffic": None if args.partition else MEASURED_TRAFFIC.get(desc),
+        "kernel": desc if not args.partition else f"{desc} (whole job; this rank: {units} rows)",
+        "accounting": ENCODE_ACCOUNTING,
         "flops_per_unit": flops_unit, "units_per_launch": units,
         "peak_basis": f"{props.multi_processor_count} SMs x {FP32_LANES_PER_SM} FP32 lanes x "
                       f"2 (FMA) x {sm_max:.0f} MHz",
@@ -382,16 +456,20 @@ def bench_ours(args) -> None:
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": kernel_ms,
         "ms_median": median_ms,
-        "higher_is_better": True, "scaling": "weak",
+        "higher_is_better": True, "scaling": "strong" if args.partition else "weak",
         "vs_baseline": (value / world / PAGES_FALCON_SUBVEC_PER_S
                         if args.workload == "falcon_prefill" and not variant else None),
         "dtype": "f32", "data": "synthetic (seeded N(0,1) fp16 keys and codebooks"
                                 + (f", as {args.dtype})" if args.dtype != "f16" else ")"),
-        "config": dict(config_block(w, args, world), timed_region_s=region_s,
-                       n_centroids=int(cb.shape[1]), input_dtype=args.dtype,
-                       x_misaligned=bool(args.misalign),
-                       dispatch="one vq_encode per group" if args.per_layer else "one grouped launch"),
-        "gpu_launches": args.steps * (x.shape[0] if args.per_layer else 1),
+        "config": dict(config_block(w, args, world), n_centroids=int(cb.shape[1]),
+                       input_dtype=args.dtype),
+        "timing": {"l2": L2_POLICY, "timed_region_s": region_s,
+                   "x_misaligned": bool(args.misalign),
+                   "dispatch": ("one vq_encode per group" if args.per_layer
+                                else f"vq_encode_partition: {len(slices)} grouped launches"
+                                if args.partition else "one grouped launch")},
+        "gpu_launches": args.steps * (x.shape[0] if args.per_layer
+                                      else len(slices) if args.partition else 1),
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": roofline,
         "e2e": None if variant else {"value": job_throughput(units * e2e_steps, world, e2e_s), "unit": UNIT,
@@ -400,6 +478,9 @@ def bench_ours(args) -> None:
                 "path": "vq_encode_grouped_host with pinned host buffers: the kernel reads x and "
                         "writes the indices across the CPU-GPU link; codebooks copied"},
     }
+    if world == 1 and not variant and args.workload == "falcon_prefill" and not args.no_other:
+        del xd, cbd, out
+        line["other_workloads"] = other_workloads(vq, dev, flush, stream, peak_tflops)
     if world == 1 and not args.no_cpu_baseline and not variant:
         line["cpu_baseline"] = cpu_baseline(args.workload, x, cb)
     print(json.dumps(line))
@@ -452,7 +533,10 @@ def bench_dequantize(args) -> None:
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
-                     "bytes_per_unit": bytes_per_unit, "units_per_launch": w.n},
+                     "bytes_per_unit": bytes_per_unit, "units_per_launch": w.n,
+                     "accounting": "algorithmic bytes: one uint8 code read and one fp16 row "
+                                   "written per sub-vector (codebooks negligible)"},
+        "timing": {"l2": L2_POLICY},
         "e2e": None,
     }
     print(json.dumps(line))
@@ -510,7 +594,9 @@ def bench_smooth(args) -> None:
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
-                     "flops_per_unit": flops_per_subvector(w), "units_per_launch": w.n},
+                     "flops_per_unit": flops_per_subvector(w), "units_per_launch": w.n,
+                     "accounting": ENCODE_ACCOUNTING},
+        "timing": {"l2": L2_POLICY},
         "e2e": None,
     }
     print(json.dumps(line))
@@ -573,13 +659,15 @@ def bench_sibling(args, fused: bool) -> None:
         "op": "hadamard" if fused else "scalar",
         "config": {"workload": sw.name, "batch": sw.batch, "heads": sw.heads,
                    "tokens": sw.tokens, "head_dim": sw.head_dim, "bits": sw.bits,
-                   "input_dtype": args.dtype,
-                   "l2": "flushed before every step (256 MiB write)"},
+                   "input_dtype": args.dtype},
+        "timing": {"l2": L2_POLICY},
         "gpu_launches": args.steps * (1 if fused else 2),
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "bytes_per_launch": algo_bytes,
-                     "timed": "whole step" + ("" if fused else " (table build + lookup pass)")},
+                     "timed": "whole step" + ("" if fused else " (table build + lookup pass)"),
+                     "accounting": "algorithmic bytes: each key element read once and its "
+                                   "uint8 index written once"},
         "e2e": None,
     }
     print(json.dumps(line))
@@ -671,14 +759,16 @@ def bench_attention(args) -> None:
         "data": "synthetic", "op": "attention",
         "config": {"workload": aw.name, "batch": aw.batch, "heads_q": aw.heads_q,
                    "heads_kv": aw.heads_kv, "tokens": aw.tokens, "head_dim": aw.head_dim,
-                   "sub_dim": aw.sub_dim, "n_centroids": aw.n_centroids,
-                   "l2": "flushed before every step (256 MiB write)"},
+                   "sub_dim": aw.sub_dim, "n_centroids": aw.n_centroids},
+        "timing": {"l2": L2_POLICY},
         "gpu_launches": 2 * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
                      "bytes_per_launch": algo_bytes,
-                     "timed": "whole step (partial + combine kernels)"},
+                     "timed": "whole step (partial + combine kernels)",
+                     "accounting": "algorithmic bytes: every key and value code read once "
+                                   "(queries, codebooks and outputs negligible)"},
         "cpu_baseline": cpu,
         "e2e": {"value": scores / e2e_s, "unit": "scores/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -702,6 +792,11 @@ def main() -> None:
                    help="encode: x one element off alignment (the any-layout kernel)")
     p.add_argument("--per-layer", action="store_true",
                    help="encode: one vq_encode launch per group instead of one grouped launch")
+    p.add_argument("--partition", action="store_true",
+                   help="encode under torchrun: the ranks split one workload (strong scaling) "
+                        "instead of each encoding its own (weak scaling)")
+    p.add_argument("--no-other", action="store_true",
+                   help="encode: skip the other workloads of the default line")
     p.add_argument("--op", choices=["encode", "dequantize", "attention", "smooth", "scalar",
                                     "hadamard"], default="encode")
     args = p.parse_args()

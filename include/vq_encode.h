@@ -305,6 +305,39 @@ vq_status vq_hadamard_quantize(const void *x, vq_dtype dtype, const float *diag,
                                int32_t dim, const float *centroids, int32_t n_centroids,
                                uint8_t *out, vq_stream_t stream);
 
+/*
+ * Multi-GPU partition of one encode job.  Every row of a grouped encode is
+ * independent ("What Even Is a KV Cache": each sub-vector is encoded on its
+ * own against its codebook), so a job [n_groups][n_per_group] splits across
+ * `world` GPUs with no exchange: each rank encodes the rows it owns against
+ * replicated codebooks and keeps their indices.
+ *
+ * vq_partition -- the rows rank `rank` of `world` owns: one contiguous range
+ * of the flattened row index g * n_per_group + m, [floor(rank T / world),
+ * floor((rank + 1) T / world)) with T = n_groups * n_per_group (the ranks'
+ * shares differ by at most one row; every row is owned exactly once), cut
+ * into at most three slices, in row order, that each is one grouped encode:
+ * rows [row, row + n_rows) of each of the groups [group, group + n_groups).
+ * A slice with n_groups > 1 covers whole groups (row 0, n_rows =
+ * n_per_group); the others lie in one group.  Its encode is
+ * vq_encode_grouped(x + (group * n_per_group + row) * sub_dim,
+ * codebooks + group * n_centroids * sub_dim, n_groups, n_rows, ...), whose
+ * indices are the next n_groups * n_rows of the rank's share.
+ *   slices     [3] host memory, written (the first *n_slices)
+ *   n_slices   host, written: 0 to 3 (0: the rank owns no row)
+ * world < 1, rank outside [0, world), negative sizes or NULL pointers:
+ * VQ_ERR_INVALID_ARG.  Host arithmetic only: no device is needed.
+ */
+typedef struct {
+    int64_t group;    /* first group */
+    int64_t n_groups; /* groups */
+    int64_t row;      /* first row within each of them */
+    int64_t n_rows;   /* rows of each group */
+} vq_slice;
+
+vq_status vq_partition(int64_t n_groups, int64_t n_per_group, int32_t world, int32_t rank,
+                       vq_slice *slices, int32_t *n_slices);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char *vq_status_string(vq_status status);
 

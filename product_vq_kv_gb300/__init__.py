@@ -30,9 +30,11 @@ from ._binding import (  # noqa: F401
     vq_encode_grouped_host,
     vq_encode_grouped_smooth,
     vq_encode_grouped_u8,
+    vq_encode_partition,
     vq_hadamard_quantize,
     vq_hadamard_rotate,
     vq_kernel_status,
+    vq_partition,
     vq_scalar_dequantize,
     vq_scalar_quantize,
     vq_status_string,

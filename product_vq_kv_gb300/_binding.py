@@ -33,6 +33,12 @@ class VQError(RuntimeError):
         super().__init__(f"{where}: {vq_status_string(status)}")
 
 
+class VqSlice(ctypes.Structure):
+    """``vq_slice``: rows [row, row + n_rows) of groups [group, group + n_groups)."""
+    _fields_ = [("group", ctypes.c_int64), ("n_groups", ctypes.c_int64),
+                ("row", ctypes.c_int64), ("n_rows", ctypes.c_int64)]
+
+
 def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     """Declare the argument and result types of every entry point on ``lib``
     (the library, or its bounds-checked build, which has the same ABI)."""
@@ -77,6 +83,9 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.vq_abi_version.argtypes = []
     lib.vq_kernel_status.restype = i32
     lib.vq_kernel_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    lib.vq_partition.restype = i32
+    lib.vq_partition.argtypes = [i64, i64, i32, i32, ctypes.POINTER(VqSlice),
+                                 ctypes.POINTER(ctypes.c_int32)]
     return lib
 
 
@@ -527,6 +536,54 @@ def vq_encode_grouped_host(x_host: torch.Tensor, codebooks_host: torch.Tensor,
         _stream_handle(stream, x_dev.device))
     _check(st, "vq_encode_grouped_host")
     return out_host
+
+
+def vq_partition(n_groups: int, n_per_group: int, world: int, rank: int) -> list:
+    """The rows of a ``[n_groups, n_per_group]`` encode job that ``rank`` of
+    ``world`` owns, as ``(group, n_groups, row, n_rows)`` slices in row order
+    (see ``vq_partition`` in ``include/vq_encode.h``)."""
+    buf = (VqSlice * 3)()
+    count = ctypes.c_int32(0)
+    st = load_library().vq_partition(n_groups, n_per_group, world, rank, buf, ctypes.byref(count))
+    _check(st, "vq_partition")
+    return [(s.group, s.n_groups, s.row, s.n_rows) for s in buf[:count.value]]
+
+
+def vq_encode_partition(x: torch.Tensor, codebooks: torch.Tensor, world: int, rank: int,
+                        out: torch.Tensor | None = None,
+                        stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Rank ``rank``'s share of the grouped encode of ``x`` ``[G, M, sub_dim]``
+    against the replicated ``codebooks`` ``[G, n_c, sub_dim]``: the indices of
+    the rows :func:`vq_partition` gives it, as a 1-D uint32 tensor in row
+    order (one grouped encode per slice; no collective).  Concatenated over
+    the ranks in rank order they are ``vq_encode_grouped(x, codebooks)``
+    flattened."""
+    _device_tensor(x, "x")
+    _device_tensor(codebooks, "codebooks")
+    if (x.dim() != 3 or codebooks.dim() != 3 or x.shape[0] != codebooks.shape[0]
+            or x.shape[2] != codebooks.shape[2]):
+        raise ValueError(f"expected x [G, M, sub_dim] and codebooks [G, n_centroids, sub_dim], "
+                         f"got {tuple(x.shape)} and {tuple(codebooks.shape)}")
+    if x.dtype != codebooks.dtype:
+        raise TypeError("x and codebooks must share a dtype")
+    g, m, sub = x.shape
+    slices = vq_partition(g, m, world, rank)
+    n = sum(ng * nr for _, ng, _, nr in slices)
+    if out is None:
+        out = torch.empty(n, dtype=torch.uint32, device=x.device)
+    elif out.dtype != torch.uint32 or out.shape != (n,) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous uint32 tensor of shape [{n}]")
+    lib = load_library()
+    handle = _stream_handle(stream, x.device)
+    off = 0
+    for g0, ng, r0, nr in slices:
+        xs = x[g0:g0 + ng, r0:r0 + nr]  # contiguous: one group, or whole groups
+        st = lib.vq_encode_grouped(xs.data_ptr(), codebooks[g0:g0 + ng].data_ptr(), ng, nr,
+                                   codebooks.shape[1], sub, _dtype_code(x),
+                                   out.data_ptr() + off * 4, handle)
+        _check(st, "vq_encode_partition")
+        off += ng * nr
+    return out
 
 
 def vq_describe_launch(n_groups: int, n_per_group: int, n_centroids: int, sub_dim: int,

@@ -648,6 +648,38 @@ vq_status vq_dequantize_grouped(const void *idx, int32_t index_bytes, const void
     return vqh_launched(st, vqh_status_encode);
 }
 
+vq_status vq_partition(int64_t n_groups, int64_t n_per_group, int32_t world, int32_t rank,
+                       vq_slice *slices, int32_t *n_slices)
+{
+    if (!slices || !n_slices || world < 1 || rank < 0 || rank >= world || n_groups < 0 ||
+        n_per_group < 0)
+        return VQ_ERR_INVALID_ARG;
+    if (n_groups != 0 && n_per_group > INT64_MAX / n_groups) return VQ_ERR_INVALID_ARG;
+    *n_slices = 0;
+    const int64_t total = n_groups * n_per_group;
+    // floor(r T / world) without overflow: r (T / world) + floor(r (T % world) / world)
+    const int64_t q = total / world, rem = total % world;
+    auto start = [&](int64_t r) { return r * q + (r * rem) / world; };
+    const int64_t s = start(rank), e = start((int64_t)rank + 1);
+    if (s >= e) return VQ_OK;
+    const int64_t m = n_per_group;
+    const int64_t gs = s / m, rs = s % m, ge = e / m, re = e % m;
+    int32_t k = 0;
+    if (gs == ge) {  // inside one group
+        slices[k++] = vq_slice{gs, 1, rs, re - rs};
+    } else {
+        int64_t full = gs;
+        if (rs > 0) {  // the end of the first group
+            slices[k++] = vq_slice{gs, 1, rs, m - rs};
+            full = gs + 1;
+        }
+        if (ge > full) slices[k++] = vq_slice{full, ge - full, 0, m};  // whole groups
+        if (re > 0) slices[k++] = vq_slice{ge, 1, 0, re};  // the start of the last
+    }
+    *n_slices = k;
+    return VQ_OK;
+}
+
 const char *vq_status_string(vq_status status)
 {
     switch (status) {

@@ -38,3 +38,27 @@ def test_reference_arm_other_ranks_exit_silently():
     res = run_reference({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"})
     assert res.returncode == 0, res.stderr
     assert res.stdout.strip() == ""
+
+
+def test_both_arms_share_one_config_block():
+    """The driver compares the two arms' `config`: the encode arm's, for the
+    default workload, must be exactly the reference arm's (timing details
+    live under `timing`)."""
+    import argparse
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+
+    for name in ("falcon_prefill", "tiny"):
+        w = workloads.WORKLOADS[name]
+        args = argparse.Namespace(partition=False, dtype="f16")
+        ref = bench.config_block(w, args, 1)
+        ours = dict(bench.config_block(w, args, 1), n_centroids=int(w.n_centroids),
+                    input_dtype=args.dtype)
+        assert ours == ref
+        assert "l2" not in ref and "timed_region_s" not in ref
+    res = run_reference({"WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    assert d["config"] == bench.config_block(workloads.WORKLOADS["tiny"],
+                                             argparse.Namespace(partition=False), 1)
