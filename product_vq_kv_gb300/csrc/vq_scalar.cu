@@ -47,7 +47,7 @@ vq_status launch_scan_nc(const void *x, int64_t n, const float *c, int32_t n_c, 
     const size_t smem = NC == 0 ? vqs::hadamard_smem(n_c) : 0;
     const bool vec = (uintptr_t)x % 16 == 0 && (uintptr_t)out % 8 == 0;
     vqs::scalar_scan<T, NC><<<(unsigned)stream_blocks((n + 7) / 8, 8), kThreads, smem, st>>>(
-        static_cast<const T *>(x), n, c, n_c, vec, -1.0f, out);
+        static_cast<const T *>(x), n, c, n_c, vec, out);
     return launched(st);
 }
 
@@ -75,7 +75,7 @@ vq_status launch_hadamard_nc(const void *x, const float *diag, int64_t n_rows, i
     if (blocks > 8LL * sms) blocks = 8LL * sms;
     const size_t smem = QUANT && NC == 0 ? vqs::hadamard_smem(n_c) : 0;
     vqs::hadamard_rows<T, E, QUANT, NC><<<(unsigned)blocks, kThreads, smem, st>>>(
-        static_cast<const T *>(x), diag, n_rows, lpr, scale, c, n_c, -1.0f, y, idx);
+        static_cast<const T *>(x), diag, n_rows, lpr, scale, c, n_c, y, idx);
     return launched(st);
 }
 

@@ -239,132 +239,140 @@ __device__ __forceinline__ void load_run(const T *p, float (&v)[E])
     }
 }
 
-// The nearest-centroid rule with NC centroids in registers, held negated in
-// pairs (val + (-c) rounds exactly as val - c): the scan itself, for
-// codebooks with a non-finite value.
+
+// ---- exact nearest centroid of NC distinct centroids by cut points
+//
+// Let s_0 < ... < s_{NC-1} be the centroids sorted, orig(k) the original
+// index of s_k, and d_j(v) = fl(fl(v - s_j)^2) the rule's distance.  On
+// [s_k, s_{k+1}] d_k never decreases and d_{k+1} never increases as v grows,
+// so "s_{k+1} beats s_k under the rule" (d_{k+1} < d_k, or d_{k+1} <= d_k when
+// orig(k+1) < orig(k): ties go to the lower original index) is false at s_k,
+// true at s_{k+1} and monotone in between.  Its first fp32 value t_k, found by
+// a binary search over the bit patterns of that interval, is the cut point of
+// the pair.  For lo <= v <= hi, k = #{j : t_j <= v} and the answer is
+// orig(k): s_k beats or ties-and-wins against its two neighbours by the cut
+// points, and every farther centroid is strictly farther than the
+// neighbour between them, because the set-up only accepts codebooks whose
+// neighbouring gaps differ by at most 2^15, whose gaps are at least 2^-40 and
+// whose span [lo, hi] (the centroids widened by 2^15 outer gaps) stays below
+// 2^62: a distance ratio of at least 1 + 2^-16 then survives the two
+// roundings, with no underflow or overflow.  Values outside [lo, hi], NaN,
+// and codebooks that fail those conditions take the rule's scan.
 template <int NC>
-__device__ __forceinline__ uint32_t nearest_reg(float val, const float2 (&cneg)[NC / 2])
+struct CutCb {
+    const float *t;   // [NC - 1] cut points, ascending, in shared memory
+    float lo, hi;     // the values they decide
+    uint64_t perm;    // orig(k) in bits 4k .. 4k + 3
+    bool ok;          // the cut points apply (false: the scan for everything)
+};
+
+// Total order of the fp32 values as unsigned keys (finite values; -0 just
+// below +0), and back.
+__device__ __forceinline__ uint32_t f32_key(float f)
 {
-    float best_dist = __int_as_float(0x7f800000);
-    uint32_t best = 0;
-#pragma unroll
-    for (int j = 0; j < NC; ++j) {
-        const float d = __fadd_rn(val, (j & 1) ? cneg[j / 2].y : cneg[j / 2].x);
-        const float dist = __fmul_rn(d, d);
-        const bool p = dist < best_dist;
-        best_dist = p ? dist : best_dist;
-        best = p ? (uint32_t)j : best;
-    }
-    return best;
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float f32_from_key(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Least of N values by a tree of three-input minima (NaN ignored unless all
-// are NaN).
-__device__ __forceinline__ float min3f(float a, float b, float c)
-{
-    float r;
-    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-template <int N>
-__device__ __forceinline__ float tree_min3(const float *w)
-{
-    if constexpr (N == 1) {
-        return w[0];
-    } else if constexpr (N == 2) {
-        return fminf(w[0], w[1]);
-    } else if constexpr (N == 3) {
-        return min3f(w[0], w[1], w[2]);
-    } else {
-        constexpr int a = (N + 2) / 3, b = (N - a + 1) / 2, cnt = N - a - b;
-        return min3f(tree_min3<a>(w), tree_min3<b>(w + a), tree_min3<cnt>(w + a + b));
-    }
-}
-
-// Packed fp32 pairs (sm_100 f32x2): each lane rounds exactly as the scalar
-// instruction.
-__device__ __forceinline__ float2 add2_rn(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "mov.b64 pc, {%6, %7};\n\tfma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return r;
-}
-
-// The same rule for FINITE centroids in fewer instructions.  The NC
-// distances are computed in packed pairs (centroids held negated: val + (-c)
-// is the same rounding as val - c); their least comes from a min3 tree; the
-// lowest index holding it comes from the sign bits of fl(least - d_j),
-// gathered by funnel shifts.  least - d_j is fma(-1, d_j, least) with -1
-// passed in at run time (`neg_one` = (-1, -1)), one rounding of the
-// difference that no compiler can merge with the square.  With finite
-// centroids every distance is finite or +inf when the key is finite, so
-// fl(least - d_j) is +0 exactly for the distances equal to the least and
-// negative for the others: the first clear bit is the scan's strict-"<"
-// answer.  A NaN or infinite key makes every distance NaN or +inf; the rule
-// then answers 0, and so does this (every least - d_j is NaN: the index is 0
-// when all sign bits are clear, and clamped to 0 when none is).
+// Block set-up (every thread of the block calls it; three block barriers).
+// `sm` is shared memory for 4 NC floats; on return sm[NC .. 2 NC) holds the
+// codebook as given, for the rule's scan.  Thread i < NC ranks centroid i;
+// thread k < NC - 1 checks the gaps around pair (k, k + 1) and searches its
+// cut point; every thread then reads the result.
 template <int NC>
-__device__ __forceinline__ uint32_t nearest_reg_finite(float val, const float2 (&cneg)[NC / 2], float2 neg_one)
+__device__ __forceinline__ void build_cut_cb(const float *__restrict__ centroids, float *sm,
+                                             CutCb<NC> &cb)
 {
-    static_assert(NC % 2 == 0, "centroid pairs");
-    float2 d[NC / 2];
-    const float2 v2 = make_float2(val, val);
+    static_assert(NC >= 2 && NC <= 16, "4-bit original indices");
+    float *srt = sm;                                      // [NC] ascending
+    float *cgiven = sm + NC;                              // [NC] as given
+    float *cut = sm + 2 * NC;                             // [NC - 1]
+    int *orig = reinterpret_cast<int *>(sm + 3 * NC);     // [NC]
+    const int t = threadIdx.x;
+    bool ok = true;
+    if (t < NC) {
+        const float ci = __ldg(centroids + t);
+        int rank = 0;
+        bool distinct = true;
 #pragma unroll
-    for (int j = 0; j < NC / 2; ++j) {
-        const float2 t = add2_rn(v2, cneg[j]);
-        d[j] = mul2_rn(t, t);
+        for (int j = 0; j < NC; ++j) {
+            const float cj = __ldg(centroids + j);
+            rank += cj < ci ? 1 : 0;
+            distinct = distinct && (j >= t || cj != ci);
+        }
+        ok = fabsf(ci) <= 3.402823466e38f && distinct;
+        cgiven[t] = ci;
+        if (ok) {  // distinct finite values have distinct ranks 0 .. NC - 1
+            srt[rank] = ci;
+            orig[rank] = t;
+        }
     }
-    const float least = tree_min3<NC>(reinterpret_cast<const float *>(d));
-    const float2 l2 = make_float2(least, least);
-    uint32_t above = 0;
+    ok = __syncthreads_and(ok) != 0;
+    bool pair_ok = true;
+    if (ok && t < NC - 1) {
+        const float a = srt[t], b = srt[t + 1];
+        const float g = __fsub_rn(b, a);
+        pair_ok = g >= 9.094947e-13f;  // 2^-40
+        if (t + 1 < NC - 1) {          // neighbouring gaps within 2^15 of each other
+            const float g2 = __fsub_rn(srt[t + 2], b);
+            pair_ok = pair_ok && g2 <= 32768.f * g && g <= 32768.f * g2;
+        }
+        // the first fp32 value of [a, b] at which b beats a under the rule
+        // (ties go to the lower original index)
+        const bool upper_lower = orig[t + 1] < orig[t];
+        uint32_t klo = f32_key(a), khi = f32_key(b);
+        while (khi - klo > 1u) {  // at most 32 halvings
+            const uint32_t km = klo + (khi - klo) / 2u;
+            const float v = f32_from_key(km);
+            const float da = __fmul_rn(__fsub_rn(v, a), __fsub_rn(v, a));
+            const float db = __fmul_rn(__fsub_rn(v, b), __fsub_rn(v, b));
+            const bool beats = upper_lower ? db <= da : db < da;
+            if (beats) khi = km; else klo = km;
+        }
+        cut[t] = f32_from_key(khi);
+    }
+    ok = __syncthreads_and(ok && pair_ok) != 0;
+    cb.ok = false;
+    cb.lo = 0.f;
+    cb.hi = 0.f;
+    cb.perm = 0;
+    cb.t = cut;
+    if (ok) {
+        const float lo = __fsub_rn(srt[0], __fmul_rn(32768.f, __fsub_rn(srt[1], srt[0])));
+        const float hi = __fadd_rn(srt[NC - 1], __fmul_rn(32768.f, __fsub_rn(srt[NC - 1], srt[NC - 2])));
+        cb.ok = __fsub_rn(hi, lo) <= 4.611686e18f;  // 2^62
+        cb.lo = lo;
+        cb.hi = hi;
 #pragma unroll
-    for (int j = NC / 2 - 1; j >= 0; --j) {
-        const float2 e = fma2_rn(neg_one, d[j], l2);
-        above = __funnelshift_l(__float_as_uint(e.y), above, 1);
-        above = __funnelshift_l(__float_as_uint(e.x), above, 1);
+        for (int k = 0; k < NC; ++k) cb.perm |= (uint64_t)(uint32_t)orig[k] << (4 * k);
     }
-    const uint32_t low = NC == 32 ? 0xffffffffu : (1u << NC) - 1u;
-    const int k = __ffs(~above & low) - 1;
-    return k < 0 ? 0u : (uint32_t)k;
 }
 
-// Whether all NC register centroids are finite (the finite rule applies).
+// Whether the cut points decide v (false for NaN, for values outside
+// [lo, hi] and for codebooks that failed the set-up's conditions).
 template <int NC>
-__device__ __forceinline__ bool all_finite(const float2 (&cneg)[NC / 2])
+__device__ __forceinline__ bool cut_decides(float v, const CutCb<NC> &cb)
 {
-    bool f = true;
-#pragma unroll
-    for (int j = 0; j < NC / 2; ++j) f = f && fabsf(cneg[j].x) <= 3.402823466e38f && fabsf(cneg[j].y) <= 3.402823466e38f;
-    return f;
+    return cb.ok && v >= cb.lo && v <= cb.hi;
 }
 
-// The NC centroids as negated pairs.
+// The rule's answer for v through the cut points, valid when cut_decides(v):
+// the original index of the k-th smallest centroid, k the number of cut
+// points at or below v, by a branch-free binary search over the cut points
+// in shared memory (the lanes read among NC - 1 consecutive words: no bank
+// conflicts).  Callers take the rule's scan separately for the rare values
+// the cut points do not decide.
 template <int NC>
-__device__ __forceinline__ void load_cneg(const float *__restrict__ centroids, float2 (&cneg)[NC / 2])
+__device__ __forceinline__ uint32_t cut_code(float v, const CutCb<NC> &cb)
 {
+    int k = 0;
 #pragma unroll
-    for (int k = 0; k < NC / 2; ++k) cneg[k] = make_float2(-__ldg(centroids + 2 * k), -__ldg(centroids + 2 * k + 1));
+    for (int step = NC / 2; step > 0; step >>= 1) k += v >= cb.t[k + step - 1] ? step : 0;
+    return (uint32_t)(cb.perm >> (4 * k)) & 15u;
 }
 
 // Randomised Hadamard rotation of rows of D = LPR * E elements, optionally
@@ -372,27 +380,26 @@ __device__ __forceinline__ void load_cneg(const float *__restrict__ centroids, f
 // 32, chosen by the host), 32 / LPR rows per warp; lane l of a row holds
 // elements l*E .. l*E + E - 1.  Warps stride over groups of rows (a
 // persistent grid), loading R groups before rotating the first.  The
-// quantize scans NC > 0 centroids held in registers as negated pairs
-// (codebooks of exactly NC entries; the packed finite scan when all are
-// finite), or, with NC == 0, searches the block's sorted view of the codebook
-// (any size up to 256).  `neg_one` must be -1.0f.  Launch: blockDim.x = 256,
+// quantize of a codebook of exactly NC > 0 entries (2 to 16) counts the
+// block's cut points (CutCb); with NC == 0 it searches the block's sorted
+// view of the codebook (any size up to 256).  Launch: blockDim.x = 256,
 // any grid; dynamic shared memory hadamard_smem(n_c) when QUANT and NC == 0,
 // else 0.  x rows contiguous and E-element aligned (E * sizeof(T) up to 16
 // bytes); idx 4-byte aligned when E % 4 == 0; y / idx [n_rows][D].
 __host__ __device__ inline size_t hadamard_smem(int n_c) { return (size_t)n_c * 16 + 16; }
 
 // The scalar quantize of any input type without a table: codebooks of 2, 4,
-// 8 or 16 entries (NC) scanned from registers, others (NC == 0) through the
-// block's sorted view, every element falling back to the scan of the rule
-// where the view cannot decide.  A persistent grid strides over 8-element
-// units (16-byte loads, two units in flight per thread, 8-byte stores) when
-// `vec` (x 16-byte and out 8-byte aligned), then over the remaining elements
-// one by one.  `neg_one` must be -1.0f.  Launch: any grid of 256-thread
-// blocks; dynamic shared memory hadamard_smem(n_c) when NC == 0, else 0.
+// 8 or 16 entries (NC) through the block's cut points, others (NC == 0)
+// through the block's sorted view, every element falling back to the scan of
+// the rule where they cannot decide.  A persistent grid strides over
+// 8-element units (16-byte loads, two units in flight per thread, 8-byte
+// stores) when `vec` (x 16-byte and out 8-byte aligned), then over the
+// remaining elements one by one.  Launch: any grid of 256-thread blocks;
+// dynamic shared memory hadamard_smem(n_c) when NC == 0, else 0.
 template <typename T, int NC>
 __global__ void __launch_bounds__(256)
     scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
-                int32_t n_c, bool vec, float neg_one, uint8_t *__restrict__ out);
+                int32_t n_c, bool vec, uint8_t *__restrict__ out);
 
 
 
@@ -400,22 +407,21 @@ template <typename T, int E, bool QUANT, int NC>
 __global__ void __launch_bounds__(256)
     hadamard_rows(const T *__restrict__ x, const float *__restrict__ diag, int64_t n_rows,
                   int32_t lanes_per_row, float scale, const float *__restrict__ centroids,
-                  int32_t n_c, float neg_one, float *__restrict__ y, uint8_t *__restrict__ idx)
+                  int32_t n_c, float *__restrict__ y, uint8_t *__restrict__ idx)
 {
     extern __shared__ float hq_sm[];
     SortedCb scb{nullptr, nullptr, 0, 0};
     const float *hq_cb = hq_sm;
     bool sorted_ok = false;
-    bool creg_finite = false;
-    float2 cneg[NC > 1 ? NC / 2 : 1];
+    // NC centroids (2 to 16): their cut points, set up once per block
+    __shared__ float cut_sm[4 * 16];
+    CutCb<(NC > 1 ? NC : 2)> cut;
     if constexpr (QUANT && NC > 0) {
-        // a register codebook reads NC <= n_c centroids (checked build:
-        // else the block does nothing)
+        // the set-up reads NC <= n_c centroids (checked build: else the
+        // block does nothing)
         if (!vqk::index_ok(NC - 1, n_c)) return;
-        load_cneg<NC>(centroids, cneg);
-        creg_finite = all_finite<NC>(cneg);
+        build_cut_cb<NC>(centroids, cut_sm, cut);
     }
-    const float2 neg_one2 = make_float2(neg_one, neg_one);
     if constexpr (QUANT && NC == 0) {
         float *c = hq_sm;                                            // [n_c] as given
         float *u = c + n_c;                                          // [n_c] sorted distinct
@@ -506,11 +512,21 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
                     if constexpr (NC > 0) {
-                        code[j] = creg_finite ? nearest_reg_finite<NC>(w[j], cneg, neg_one2)
-                                              : nearest_reg<NC>(w[j], cneg);
+                        code[j] = cut_code<NC>(w[j], cut);
                     } else {
                         const int k = sorted_ok ? nearest_sorted(w[j], scb) : -1;
                         code[j] = k >= 0 ? (uint32_t)k : nearest(w[j], hq_cb, n_c);
+                    }
+                }
+                if constexpr (NC > 0) {
+                    // values the cut points do not decide (rare): the rule's scan
+                    bool all = true;
+#pragma unroll
+                    for (int j = 0; j < E; ++j) all = all && cut_decides<NC>(w[j], cut);
+                    if (!all) {
+#pragma unroll
+                        for (int j = 0; j < E; ++j)
+                            if (!cut_decides<NC>(w[j], cut)) code[j] = nearest(w[j], cut_sm + NC, NC);
                     }
                 }
                 uint8_t *o = idx + (size_t)row * d + (size_t)l * E;
@@ -578,17 +594,15 @@ __device__ __forceinline__ void load8(const T *p, float (&v)[8])
 template <typename T, int NC>
 __global__ void __launch_bounds__(256)
     scalar_scan(const T *__restrict__ x, int64_t n, const float *__restrict__ centroids,
-                int32_t n_c, bool vec, float neg_one, uint8_t *__restrict__ out)
+                int32_t n_c, bool vec, uint8_t *__restrict__ out)
 {
     extern __shared__ float ss_sm[];
     SortedCb scb{nullptr, nullptr, 0, 0};
     bool sorted_ok = false;
-    bool creg_finite = false;
-    float2 cneg[NC > 1 ? NC / 2 : 1];
-    const float2 neg_one2 = make_float2(neg_one, neg_one);
+    __shared__ float cut_sm[4 * 16];
+    CutCb<(NC > 1 ? NC : 2)> cut;
     if constexpr (NC > 0) {
-        load_cneg<NC>(centroids, cneg);
-        creg_finite = all_finite<NC>(cneg);
+        build_cut_cb<NC>(centroids, cut_sm, cut);
     } else {
         float *c = ss_sm;
         float *u = c + n_c;
@@ -609,7 +623,7 @@ __global__ void __launch_bounds__(256)
     }
     auto quant = [&](float v) -> uint32_t {
         if constexpr (NC > 0) {
-            return creg_finite ? nearest_reg_finite<NC>(v, cneg, neg_one2) : nearest_reg<NC>(v, cneg);
+            return cut_decides<NC>(v, cut) ? cut_code<NC>(v, cut) : nearest(v, cut_sm + NC, NC);
         } else {
             const int k = sorted_ok ? nearest_sorted(v, scb) : -1;
             return k >= 0 ? (uint32_t)k : nearest(v, ss_sm, n_c);
@@ -617,6 +631,21 @@ __global__ void __launch_bounds__(256)
     };
     auto quant8 = [&](const float (&v)[8]) -> uint2 {
         uint32_t lo = 0, hi = 0;
+        if constexpr (NC > 0) {
+            // branch-free for the values the cut points decide; the rule's
+            // scan (rare) only when one of the eight is not
+            bool all = true;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) all = all && cut_decides<NC>(v[i], cut);
+            if (all) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    lo |= cut_code<NC>(v[i], cut) << (8 * i);
+                    hi |= cut_code<NC>(v[i + 4], cut) << (8 * i);
+                }
+                return make_uint2(lo, hi);
+            }
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             lo |= quant(v[i]) << (8 * i);

@@ -261,3 +261,68 @@ def test_hadamard_both_lane_layouts(vq, oracle_mod, n_c, dim):
         assert np.array_equal(got.astype(np.uint32), want), off
         rot = vq.vq_hadamard_rotate(xv, dd).cpu().numpy()
         assert np.array_equal(rot.view(np.uint32), want_rot.view(np.uint32)), off
+
+
+def cut_point_codebooks(n_c):
+    """Codebooks of 2 to 16 entries for the cut-point path: exact fp32 ties
+    at every midpoint (dyadic values) in sorted, reversed and shuffled
+    original order (both tie-break directions), random normal ones sorted and
+    not, and gap ratios just inside and just outside the set-up's 2^15 limit
+    (the latter take the rule's scan)."""
+    rng = np.random.default_rng(300 + n_c)
+    dyadic = (np.arange(n_c, dtype=np.float32) * np.float32(0.5) - np.float32(1.0)).astype(np.float32)
+    out = {"dyadic_sorted": dyadic, "dyadic_reversed": dyadic[::-1].copy()}
+    shuffled = dyadic.copy()
+    rng.shuffle(shuffled)
+    out["dyadic_shuffled"] = shuffled
+    normal = rng.standard_normal(n_c).astype(np.float32)
+    out["normal_sorted"] = np.sort(normal)
+    out["normal_unsorted"] = normal
+    if n_c >= 4:
+        for name, ratio in (("gap_ratio_inside", 2.0 ** 14), ("gap_ratio_outside", 2.0 ** 17)):
+            gaps = np.ones(n_c - 1)
+            gaps[n_c // 2] = 1.0 / ratio  # one narrow gap beside wide ones
+            out[name] = np.concatenate([[0.0], np.cumsum(gaps)]).astype(np.float32)
+    return out
+
+
+def cut_point_keys(c):
+    """Keys within 300 ulps of every exact midpoint of neighbouring centroids
+    and of the ends of the range the cut points decide (32768 outer gaps
+    beyond the extreme centroids), plus the whole-range value sweep."""
+    s = np.unique(c.astype(np.float64))
+    marks = list((s[:-1] + s[1:]) / 2)
+    if s.size > 1:
+        marks += [s[0] - 32768 * (s[1] - s[0]), s[-1] + 32768 * (s[-1] - s[-2])]
+    keys = []
+    for m in marks:
+        m32 = np.float32(m)
+        bits = np.int64(m32.view(np.int32))
+        around = (bits + np.arange(-300, 301)).astype(np.int64)
+        around = around[(around >= -(2 ** 31)) & (around < 2 ** 31)].astype(np.int32)
+        keys.append(around.view(np.float32))
+    keys.append(value_sweep_keys(len(c)))
+    return np.concatenate(keys).astype(np.float32)
+
+
+@pytest.mark.parametrize("n_c", [2, 4, 8, 16])
+def test_cut_points_match_the_rule_where_they_decide(vq, oracle_mod, n_c):
+    """The 2- to 16-entry quantize (cut points counted by a binary search,
+    the rule's scan where they cannot decide) against the rule, for fp32
+    keys (scalar quantize) and for rotated rows (Hadamard quantize, a
+    constant row per key: diag 1 maps v * sqrt(D) e_0 to v in every column)."""
+    for name, c in cut_point_codebooks(n_c).items():
+        x = cut_point_keys(c)
+        cd = torch.from_numpy(c).cuda()
+        got = vq.vq_scalar_quantize(torch.from_numpy(x).cuda(), cd).cpu().numpy()
+        want = oracle_mod.scalar_quantize(x, c)
+        bad = np.flatnonzero(got.astype(np.uint32) != want)
+        assert bad.size == 0, f"{name}: {bad.size} keys differ, first {x[bad[:4]]}"
+        dim = 32
+        fin = x[np.isfinite(x) & (np.abs(x) < 1e30)]
+        rows = np.zeros((fin.size, dim), dtype=np.float32)
+        rows[:, 0] = fin * np.float32(np.sqrt(dim))
+        diag = np.ones(dim, dtype=np.float32)
+        got = vq.vq_hadamard_quantize(torch.from_numpy(rows).cuda(), torch.from_numpy(diag).cuda(),
+                                      cd).cpu().numpy()
+        assert np.array_equal(got.astype(np.uint32), oracle_mod.hadamard_quantize(rows, diag, c)), name
