@@ -102,11 +102,11 @@ vq_status attn_plan(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_t to
     return VQ_OK;
 }
 
-template <typename T, int NS, int GPB>
+template <typename T, int NS, int GPB, int VW>
 vq_status attn_launch_k(const AttnPlan &p, const void *q, const uint8_t *kcodes, const void *kcb,
                         const uint8_t *vcodes, const void *vcb, float *part, cudaStream_t st)
 {
-    auto kp = vqk::attn_partial<T, NS, GPB>;
+    auto kp = vqk::attn_partial<T, NS, GPB, VW>;
     if (p.smem > 48 * 1024 &&
         cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
             cudaSuccess)
@@ -117,17 +117,28 @@ vq_status attn_launch_k(const AttnPlan &p, const void *q, const uint8_t *kcodes,
     return vqh_launched(st, vqh_status_attn);
 }
 
+template <typename T, int NS, int VW>
+vq_status attn_launch_vw(const AttnPlan &p, const void *q, const uint8_t *kcodes, const void *kcb,
+                         const uint8_t *vcodes, const void *vcb, float *part, cudaStream_t st)
+{
+    switch (p.gpb) {
+    case 1: return attn_launch_k<T, NS, 1, VW>(p, q, kcodes, kcb, vcodes, vcb, part, st);
+    case 2: return attn_launch_k<T, NS, 2, VW>(p, q, kcodes, kcb, vcodes, vcb, part, st);
+    case 4: return attn_launch_k<T, NS, 4, VW>(p, q, kcodes, kcb, vcodes, vcb, part, st);
+    case 8: return attn_launch_k<T, NS, 8, VW>(p, q, kcodes, kcb, vcodes, vcb, part, st);
+    }
+    return VQ_ERR_INTERNAL;
+}
+
 template <typename T, int NS>
 vq_status attn_launch_ns(const AttnPlan &p, const void *q, const uint8_t *kcodes, const void *kcb,
                          const uint8_t *vcodes, const void *vcb, float *part, cudaStream_t st)
 {
-    switch (p.gpb) {
-    case 1: return attn_launch_k<T, NS, 1>(p, q, kcodes, kcb, vcodes, vcb, part, st);
-    case 2: return attn_launch_k<T, NS, 2>(p, q, kcodes, kcb, vcodes, vcb, part, st);
-    case 4: return attn_launch_k<T, NS, 4>(p, q, kcodes, kcb, vcodes, vcb, part, st);
-    case 8: return attn_launch_k<T, NS, 8>(p, q, kcodes, kcb, vcodes, vcb, part, st);
+    if constexpr (sizeof(T) == 2) {
+        if (vqk::attn_vw(p.sh.sub_dim, 2) == 8)
+            return attn_launch_vw<T, NS, 8>(p, q, kcodes, kcb, vcodes, vcb, part, st);
     }
-    return VQ_ERR_INTERNAL;
+    return attn_launch_vw<T, NS, vqk::kAttnVw>(p, q, kcodes, kcb, vcodes, vcb, part, st);
 }
 
 template <typename T>

@@ -48,7 +48,12 @@ namespace vqk {
 
 constexpr int kLutStride = 256;  // table row stride (one entry per 8-bit code), in vectors
 constexpr int kAttnThreads = 256;
-constexpr int kAttnVw = 4;       // value columns per phase-B thread
+constexpr int kAttnVw = 4;       // value columns per phase-B thread, at least
+
+// Value columns per phase-B thread: a whole 16-byte piece of a 16-bit value
+// row (8 columns) when the sub-space width allows, else 4.  Wider slices
+// halve the gathers of codes and weights per value column.
+__host__ __device__ constexpr int attn_vw(int sub, int elem) { return elem == 2 && sub % 8 == 0 ? 8 : kAttnVw; }
 
 struct AttnShape {
     int64_t batch;
@@ -80,7 +85,8 @@ __host__ __device__ inline int attn_vcopies(int sub, int elem)
 }
 
 // Shared-memory layout, in order (bytes):
-//   lut  [GPB / GP][NS][kLutStride][GP] fp32   GP = min(GPB, 4) heads per vector;
+//   lut  [GPB / GP][NS / Q][kLutStride][Q][GP] fp32   GP = min(GPB, 4) heads per
+//        vector, Q = attn_lut_q(GP, NS) sub-spaces side by side in a row;
 //        after the last chunk it holds the per-stream accumulators
 //        [streams][GPB][D] fp32 (the region is sized for both)
 //   vcb  [256][ncopies] rows of `sub` elements of T, zero past n_c
@@ -95,7 +101,7 @@ __host__ __device__ inline AttnSmem attn_smem(int gpb, int ns, int sub, int elem
     AttnSmem m;
     const int chunk = attn_chunk(ns);
     const size_t lut_bytes = (size_t)gpb * ns * kLutStride * 4;
-    const size_t acc_bytes = (size_t)kAttnThreads * kAttnVw * gpb * 4;  // streams * GPB * D floats
+    const size_t acc_bytes = (size_t)kAttnThreads * attn_vw(sub, elem) * gpb * 4;  // >= streams * GPB * D floats
     m.lut = 0;
     m.vcb = m.lut + (lut_bytes > acc_bytes ? lut_bytes : acc_bytes);
     m.pw = m.vcb + (size_t)256 * attn_vcopies(sub, elem) * sub * elem;
@@ -105,6 +111,37 @@ __host__ __device__ inline AttnSmem attn_smem(int gpb, int ns, int sub, int elem
     m.vtile = (m.vtile + 15) / 16 * 16;
     m.total = m.vtile + (size_t)chunk * ns;
     return m;
+}
+
+// Table layout.  Entry (s, code) of a pack sits in row (s / Q) * 256 + code,
+// slot s % Q, a row being Q entries of GP floats (128 bytes when NS allows).
+// Phase A thread with lane l visits the sub-spaces in the order
+// s = i ^ (l % Q), i = 0, 1, ...: the Q lanes that share a shared-memory
+// wavefront then read Q different slots, so their lookups never meet in a
+// bank whatever the codes are.
+__host__ __device__ constexpr int attn_lut_q(int gp, int ns) { return 32 / gp < ns ? 32 / gp : ns; }
+
+// The code bytes of a token reordered so that byte i of `p` is byte i ^ lq of
+// `w` (lq < Q <= NS; `sel` is the __byte_perm selector of lq % 4).
+template <int NS, int Q>
+__device__ __forceinline__ void xor_order_codes(const uint32_t (&w)[NS / 4], uint32_t (&p)[NS / 4],
+                                                uint32_t lq, uint32_t sel)
+{
+#pragma unroll
+    for (int m = 0; m < NS / 4; ++m) p[m] = w[m];
+#pragma unroll
+    for (int bit = 0; (4 << bit) < Q; ++bit) {  // word index: m -> m ^ (lq / 4)
+        const bool flip = (lq >> (2 + bit)) & 1u;
+#pragma unroll
+        for (int m = 0; m < NS / 4; ++m) {
+            if (m & (1 << bit)) continue;
+            const uint32_t x = p[m], y = p[m | (1 << bit)];
+            p[m] = flip ? y : x;
+            p[m | (1 << bit)] = flip ? x : y;
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < NS / 4; ++m) p[m] = __byte_perm(p[m], 0u, sel);  // byte: t -> t ^ (lq % 4)
 }
 
 // Four consecutive elements of a value row in shared memory, widened.
@@ -121,6 +158,31 @@ __device__ __forceinline__ float4 load4_f32(const __nv_bfloat16 *p)
     const uint2 u = *reinterpret_cast<const uint2 *>(p);
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
+// Two 16-bit elements packed in a word, widened (element 0 in the low half).
+__device__ __forceinline__ float2 pair_f32(uint32_t w, const __half *)
+{
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+__device__ __forceinline__ float2 pair_f32(uint32_t w, const __nv_bfloat16 *)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// VW consecutive elements of a value row in shared memory, widened, as
+// column pairs: VW = 4 (any T) or 8 (16-bit T, one 16-byte load).
+template <int VW, typename T>
+__device__ __forceinline__ void load_row(const T *p, float2 (&r)[VW / 2])
+{
+    if constexpr (VW == 4) {
+        const float4 a = load4_f32(p);
+        r[0] = make_float2(a.x, a.y), r[1] = make_float2(a.z, a.w);
+    } else {
+        static_assert(VW == 8 && sizeof(T) == 2, "8-column slices are for 16-bit values");
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        r[0] = pair_f32(u.x, p), r[1] = pair_f32(u.y, p), r[2] = pair_f32(u.z, p), r[3] = pair_f32(u.w, p);
+    }
 }
 
 // Code row of one token as 32-bit words (NS bytes, NS % 4 == 0, row address
@@ -168,16 +230,7 @@ __device__ __forceinline__ uint32_t code_at(uint32_t w, int k) { return (w >> (8
 // once as fmaf would.
 __device__ __forceinline__ float2 fma2_bcast(float2 a, float b, float2 c)
 {
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
-        "mov.b64 pa, {%2, %3};\n\t"
-        "mov.b64 pb, {%4, %4};\n\t"
-        "mov.b64 pc, {%5, %6};\n\t"
-        "fma.rn.f32x2 pd, pa, pb, pc;\n\t"
-        "mov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b), "f"(c.x), "f"(c.y));
-    return r;
+    return __ffma2_rn(a, make_float2(b, b), c);
 }
 
 // GP consecutive floats from shared memory (GP = 1, 2 or 4, aligned).
@@ -196,12 +249,13 @@ __device__ __forceinline__ void load_vec(const float *p, float (&v)[GP])
 }
 
 // Launch: grid.x = batch * heads_kv * (heads_q / heads_kv / GPB) * splits,
-// block = kAttnThreads, dynamic shared memory attn_smem(GPB, NS, SUB, sizeof(T)).total.
+// block = kAttnThreads, dynamic shared memory attn_smem(GPB, NS, SUB, sizeof(T)).total,
+// VW = attn_vw(SUB, sizeof(T)).
 // NS = head_dim / sub_dim in {4, 8, 16, 32, 64}; sub_dim % 4 == 0; code rows
 // are NS bytes apart and the code arrays aligned to min(NS, 16) bytes.
 // Partial of (b, hq, split) at part[((b * heads_q + hq) * splits + split) *
 // (D + 2)]: {0: max (log2 domain), 1: sum, 2..: unnormalised out}.
-template <typename T, int NS, int GPB>
+template <typename T, int NS, int GPB, int VW>
 __global__ void __launch_bounds__(kAttnThreads)
     attn_partial(const T *__restrict__ q, const uint8_t *__restrict__ kcodes,
                  const T *__restrict__ kcb, const uint8_t *__restrict__ vcodes,
@@ -212,8 +266,9 @@ __global__ void __launch_bounds__(kAttnThreads)
     constexpr int CHUNK = attn_chunk(NS);
     constexpr int GP = GPB < 4 ? GPB : 4;
     constexpr int NPACK = GPB / GP;
+    constexpr int Q = attn_lut_q(GP, NS);
+    static_assert(NS % Q == 0 && (Q & (Q - 1)) == 0, "table rows hold a power-of-two divisor of NS");
     constexpr int NW = THREADS / 32;
-    constexpr int VW = kAttnVw;
     constexpr float kNegInf = -__builtin_huge_valf();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int sub = sh.sub_dim;
@@ -255,18 +310,22 @@ __global__ void __launch_bounds__(kAttnThreads)
     if constexpr (kChecked) {
         // the layout inside the launch's shared memory and the block inside
         // the grid: else the block does nothing
-        if (!dyn_smem_ok(smem_raw, lay.total, 16) || !index_ok(b, sh.batch) || vcs_elems * sizeof(T) > lay.pw - lay.vcb)
+        if (!dyn_smem_ok(smem_raw, lay.total, 16) || !index_ok(b, sh.batch) || vcs_elems * sizeof(T) > lay.pw - lay.vcb ||
+            attn_vw(sub, (int)sizeof(T)) != VW)
             return;  // block-uniform
     }
 
     // ---- tables (kappa folded in, zero past n_centroids): thread c owns
-    // centroid c and writes the GP heads of a pack as one vector; the value
-    // codebook goes to its bank-disjoint copies
+    // centroid c and writes the GP heads of a pack as one vector, visiting
+    // the sub-spaces in the order i ^ (c % Q) so that the stores of a warp
+    // spread over the slots; the value codebook goes to its bank-disjoint
+    // copies
     for (int c = threadIdx.x; c < kLutStride; c += THREADS) {
         const T *cv = kc + (size_t)c * sub;
 #pragma unroll
         for (int pk = 0; pk < NPACK; ++pk) {
-            for (int s = 0; s < NS; ++s) {
+            for (int si = 0; si < NS; ++si) {
+                const int s = si ^ (c & (Q - 1));
                 float acc[GP];
 #pragma unroll
                 for (int gi = 0; gi < GP; ++gi) acc[gi] = 0.f;
@@ -281,7 +340,7 @@ __global__ void __launch_bounds__(kAttnThreads)
                         }
                     }
                 }
-                float *dst = lut + ((size_t)(pk * NS + s) * kLutStride + c) * GP;
+                float *dst = lut + (((size_t)pk * NS + (s / Q) * Q) * kLutStride + (size_t)c * Q + s % Q) * GP;
                 if (VQ_SPAN(dst, GP, lut, lut_floats)) {
 #pragma unroll
                     for (int gi = 0; gi < GP; ++gi) dst[gi] = acc[gi] * sh.kappa;
@@ -297,8 +356,8 @@ __global__ void __launch_bounds__(kAttnThreads)
     }
     __syncthreads();
 
-    // phase-B role: 4-column slice `col` (columns col*4 .. col*4+3 of the
-    // head), token stream `stream` of `streams`
+    // phase-B role: VW-column slice `col` (columns col*VW .. col*VW+VW-1 of
+    // the head, inside one sub-space), token stream `stream` of `streams`
     const int ncols = d / VW;
     const int streams = THREADS / ncols;
     const int col = threadIdx.x % ncols;
@@ -309,13 +368,17 @@ __global__ void __launch_bounds__(kAttnThreads)
     // this slice's columns in copy bs % ncopies of code 0; code c adds c rows
     const T *vrow0 = vcs + (size_t)(bs % ncopies) * sub + bi;
     const size_t vstride = (size_t)ncopies * sub;
-    float2 acc[GPB][VW / 2];  // columns (0, 1) and (2, 3) of the slice
+    float2 acc[GPB][VW / 2];  // column pairs (0, 1), (2, 3), ... of the slice
 #pragma unroll
     for (int g = 0; g < GPB; ++g)
 #pragma unroll
         for (int i = 0; i < VW / 2; ++i) acc[g][i] = make_float2(0.f, 0.f);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // phase-A sub-space order (see attn_lut_q)
+    const uint32_t lq = (uint32_t)lane & (Q - 1);
+    const int lq_f = (int)lq * GP;
+    const uint32_t lq_sel = 0x3210u ^ ((lq & 3u) * 0x1111u);
     float m_run[GPB], l_run[GPB];
 #pragma unroll
     for (int g = 0; g < GPB; ++g) m_run[g] = kNegInf, l_run[g] = 0.f;
@@ -353,21 +416,34 @@ __global__ void __launch_bounds__(kAttnThreads)
                 float a[GPB];
 #pragma unroll
                 for (int g = 0; g < GPB; ++g) a[g] = 0.f;
+                uint32_t wq[NS / 4];  // byte i = code of sub-space i ^ lq
+                xor_order_codes<NS, Q>(wk[r], wq, lq, lq_sel);
 #pragma unroll
-                for (int s = 0; s < NS; ++s) {
-                    const int code = (int)code_at(wk[r][s / 4], s % 4);
+                for (int i = 0; i < NS; ++i) {
+                    const int code = (int)code_at(wq[i / 4], i % 4);
+                    // slot (i % Q) ^ lq of row (i / Q) * 256 + code
+                    const int slot_f = ((i % Q) * GP) ^ lq_f;
 #pragma unroll
                     for (int pk = 0; pk < NPACK; ++pk) {
                         float v[GP];
-                        const float *src = lut + ((size_t)(pk * NS + s) * kLutStride + code) * GP;
+                        const float *src = lut + ((size_t)pk * NS + (i / Q) * Q) * kLutStride * GP +
+                                           code * (Q * GP) + slot_f;
                         if (VQ_VSPAN(src, GP, lut, lut_floats, GP * 4)) {
                             load_vec<GP>(src, v);
                         } else {
 #pragma unroll
                             for (int gi = 0; gi < GP; ++gi) v[gi] = 0.f;
                         }
+                        if constexpr (GP >= 2) {  // head pairs as packed adds
 #pragma unroll
-                        for (int gi = 0; gi < GP; ++gi) a[pk * GP + gi] += v[gi];
+                            for (int gi = 0; gi < GP; gi += 2) {
+                                const float2 t2 = __fadd2_rn(make_float2(a[pk * GP + gi], a[pk * GP + gi + 1]),
+                                                             make_float2(v[gi], v[gi + 1]));
+                                a[pk * GP + gi] = t2.x, a[pk * GP + gi + 1] = t2.y;
+                            }
+                        } else {
+                            a[pk] += v[0];
+                        }
                     }
                 }
 #pragma unroll
@@ -442,11 +518,16 @@ __global__ void __launch_bounds__(kAttnThreads)
                 for (int u = 0; u < U; ++u)
                     code[u] = VQ_SPAN(vtile + (size_t)(tl + u * streams) * NS + bs, 1, vtile, (uint64_t)CHUNK * NS)
                                   ? vtile[(size_t)(tl + u * streams) * NS + bs] : 0;
-                float4 row[U];
+                float2 row[U][VW / 2];
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    row[u] = VQ_VSPAN(vrow0 + (size_t)code[u] * vstride, VW, vcs, vcs_elems, VW * sizeof(T))
-                                 ? load4_f32(vrow0 + (size_t)code[u] * vstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int u = 0; u < U; ++u) {
+                    if (VQ_VSPAN(vrow0 + (size_t)code[u] * vstride, VW, vcs, vcs_elems, VW * sizeof(T))) {
+                        load_row<VW>(vrow0 + (size_t)code[u] * vstride, row[u]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < VW / 2; ++i) row[u][i] = make_float2(0.f, 0.f);
+                    }
+                }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     float p[GPB];
@@ -463,17 +544,21 @@ __global__ void __launch_bounds__(kAttnThreads)
                         for (int gi = 0; gi < GP; ++gi) p[pk * GP + gi] = v[gi];
                     }
 #pragma unroll
-                    for (int g = 0; g < GPB; ++g) {
-                        acc[g][0] = fma2_bcast(make_float2(row[u].x, row[u].y), p[g], acc[g][0]);
-                        acc[g][1] = fma2_bcast(make_float2(row[u].z, row[u].w), p[g], acc[g][1]);
-                    }
+                    for (int g = 0; g < GPB; ++g)
+#pragma unroll
+                        for (int i = 0; i < VW / 2; ++i) acc[g][i] = fma2_bcast(row[u][i], p[g], acc[g][i]);
                 }
             }
             for (; tl < n_chunk; tl += streams) {
                 const int code = VQ_SPAN(vtile + (size_t)tl * NS + bs, 1, vtile, (uint64_t)CHUNK * NS)
                                      ? vtile[(size_t)tl * NS + bs] : 0;
-                const float4 row = VQ_VSPAN(vrow0 + (size_t)code * vstride, VW, vcs, vcs_elems, VW * sizeof(T))
-                                       ? load4_f32(vrow0 + (size_t)code * vstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+                float2 row[VW / 2];
+                if (VQ_VSPAN(vrow0 + (size_t)code * vstride, VW, vcs, vcs_elems, VW * sizeof(T))) {
+                    load_row<VW>(vrow0 + (size_t)code * vstride, row);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < VW / 2; ++i) row[i] = make_float2(0.f, 0.f);
+                }
                 float p[GPB];
 #pragma unroll
                 for (int pk = 0; pk < NPACK; ++pk) {
@@ -488,10 +573,9 @@ __global__ void __launch_bounds__(kAttnThreads)
                     for (int gi = 0; gi < GP; ++gi) p[pk * GP + gi] = v[gi];
                 }
 #pragma unroll
-                for (int g = 0; g < GPB; ++g) {
-                    acc[g][0] = fma2_bcast(make_float2(row.x, row.y), p[g], acc[g][0]);
-                    acc[g][1] = fma2_bcast(make_float2(row.z, row.w), p[g], acc[g][1]);
-                }
+                for (int g = 0; g < GPB; ++g)
+#pragma unroll
+                    for (int i = 0; i < VW / 2; ++i) acc[g][i] = fma2_bcast(row[i], p[g], acc[g][i]);
             }
         }
     }
@@ -510,9 +594,12 @@ __global__ void __launch_bounds__(kAttnThreads)
     if (b_active) {
 #pragma unroll
         for (int g = 0; g < GPB; ++g)
-            if (VQ_VSPAN(accs + ((size_t)stream * GPB + g) * d + col * VW, VW, lut, lut_floats, 16))
-                *reinterpret_cast<float4 *>(accs + ((size_t)stream * GPB + g) * d + col * VW) =
-                    make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+            if (VQ_VSPAN(accs + ((size_t)stream * GPB + g) * d + col * VW, VW, lut, lut_floats, 16)) {
+#pragma unroll
+                for (int i = 0; i < VW / 4; ++i)
+                    reinterpret_cast<float4 *>(accs + ((size_t)stream * GPB + g) * d + col * VW)[i] =
+                        make_float4(acc[g][2 * i].x, acc[g][2 * i].y, acc[g][2 * i + 1].x, acc[g][2 * i + 1].y);
+            }
     }
     __syncthreads();
     for (int e = threadIdx.x; e < GPB * d; e += THREADS) {
