@@ -70,7 +70,11 @@ vq_status attn_plan(int64_t batch, int32_t heads_q, int32_t heads_kv, int64_t to
             break;
         }
     if (gpb == 0) return VQ_ERR_UNSUPPORTED;
-    const size_t smem = vqk::attn_smem(gpb, ns, sub_dim, elem).total;
+    const vqk::AttnSmem lay = vqk::attn_smem(gpb, ns, sub_dim, elem);
+    const size_t smem = lay.total;
+    // the queries are staged in the value-codebook region before it is filled
+    if (((size_t)gpb * head_dim + (size_t)4 * ns) * sizeof(float) > lay.pw - lay.vcb)
+        return VQ_ERR_INTERNAL;
     const int chunk = vqk::attn_chunk(ns);
     const int64_t first = window > 0 && window < tokens ? tokens - window : 0;
     const int64_t chunks = (tokens - first + chunk - 1) / chunk;

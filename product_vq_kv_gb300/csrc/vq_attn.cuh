@@ -315,28 +315,79 @@ __global__ void __launch_bounds__(kAttnThreads)
             return;  // block-uniform
     }
 
+    // ---- the block's queries, widened to fp32 and transposed, staged in
+    // the value-codebook region, which is not in use yet: element s * sub + i
+    // of head g at qT[s * qs_stride + i * GPB + g].  The 4-float pad per
+    // sub-space puts the rows that the lanes of a wavefront read (different
+    // sub-spaces, below) in different banks.  At most 17 KiB; the region
+    // holds at least 18 KiB (attn_plan checks).
+    float *qT = reinterpret_cast<float *>(smem_raw + lay.vcb);
+    const int qs_stride = sub * GPB + 4;
+    const uint64_t qT_floats = (uint64_t)NS * qs_stride;
+    for (int e = threadIdx.x; e < GPB * d; e += THREADS) {
+        const int g = e / d, j = e - g * d;
+        const int sj = j / sub, ij = j - sj * sub;
+        const T *src = q + ((size_t)b * sh.heads_q + hq0 + g) * d + j;
+        float *dst = qT + (size_t)sj * qs_stride + (size_t)ij * GPB + g;
+        if (VQ_SPAN(dst, 1, qT, (lay.pw - lay.vcb) / 4))
+            *dst = VQ_SPAN(src, 1, q, nq_elems) ? to_f32(*src) : 0.f;
+    }
+    __syncthreads();
+
     // ---- tables (kappa folded in, zero past n_centroids): thread c owns
     // centroid c and writes the GP heads of a pack as one vector, visiting
     // the sub-spaces in the order i ^ (c % Q) so that the stores of a warp
-    // spread over the slots; the value codebook goes to its bank-disjoint
-    // copies
+    // spread over the slots.  A 16-byte codebook row is read once into
+    // registers; other widths are read element by element.
+    constexpr int KR = 16 / (int)sizeof(T);  // elements in a 16-byte row
+    const bool row16 = sub == KR && ((uintptr_t)kc & 15u) == 0;
     for (int c = threadIdx.x; c < kLutStride; c += THREADS) {
         const T *cv = kc + (size_t)c * sub;
+        const bool live = c < nc && VQ_SPAN(cv, sub, kcb, ncb_elems);
+        float kr[KR];
+#pragma unroll
+        for (int i = 0; i < KR; ++i) kr[i] = 0.f;
+        if (row16 && live && VQ_VSPAN(cv, KR, kcb, ncb_elems, 16)) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(cv);
+            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if constexpr (sizeof(T) == 4) {
+                    kr[k] = __uint_as_float(uw[k]);
+                } else {
+                    const float2 f = pair_f32(uw[k], cv);
+                    kr[2 * k] = f.x, kr[2 * k + 1] = f.y;
+                }
+            }
+        }
 #pragma unroll
         for (int pk = 0; pk < NPACK; ++pk) {
             for (int si = 0; si < NS; ++si) {
                 const int s = si ^ (c & (Q - 1));
+                const float *qs = qT + (size_t)s * qs_stride + pk * GP;  // query element s * sub
                 float acc[GP];
 #pragma unroll
                 for (int gi = 0; gi < GP; ++gi) acc[gi] = 0.f;
-                if (c < nc && VQ_SPAN(cv, sub, kcb, ncb_elems)) {
-                    for (int i = 0; i < sub; ++i) {
-                        const float kv = to_f32(cv[i]);
+                if (live) {
+                    if (row16) {
 #pragma unroll
-                        for (int gi = 0; gi < GP; ++gi) {
-                            const T *qv = q + ((size_t)b * sh.heads_q + hq0 + pk * GP + gi) * d;
-                            if (VQ_SPAN(qv + (size_t)s * sub + i, 1, q, nq_elems))
-                                acc[gi] = fmaf(to_f32(qv[(size_t)s * sub + i]), kv, acc[gi]);
+                        for (int i = 0; i < KR; ++i) {
+                            float qv[GP];
+                            if (VQ_VSPAN(qs + (size_t)i * GPB, GP, qT, qT_floats, GP * 4)) {
+                                load_vec<GP>(qs + (size_t)i * GPB, qv);
+#pragma unroll
+                                for (int gi = 0; gi < GP; ++gi) acc[gi] = fmaf(qv[gi], kr[i], acc[gi]);
+                            }
+                        }
+                    } else {
+                        for (int i = 0; i < sub; ++i) {
+                            const float kv = to_f32(cv[i]);
+                            float qv[GP];
+                            if (VQ_VSPAN(qs + (size_t)i * GPB, GP, qT, qT_floats, GP * 4)) {
+                                load_vec<GP>(qs + (size_t)i * GPB, qv);
+#pragma unroll
+                                for (int gi = 0; gi < GP; ++gi) acc[gi] = fmaf(qv[gi], kv, acc[gi]);
+                            }
                         }
                     }
                 }
@@ -348,11 +399,36 @@ __global__ void __launch_bounds__(kAttnThreads)
             }
         }
     }
-    for (int e = threadIdx.x; e < 256 * ncopies * sub; e += THREADS) {
-        const int i = e % sub;
-        const int c = e / (sub * ncopies);  // every copy holds the same rows
-        if (VQ_SPAN(vcs + e, 1, vcs, vcs_elems))
-            vcs[e] = c < nc && VQ_SPAN(vc + (size_t)c * sub + i, 1, vcb, ncb_elems) ? vc[(size_t)c * sub + i] : T(0.f);
+    __syncthreads();  // the staged queries are read no more
+
+    // ---- the value codebook in its bank-disjoint copies (zero past
+    // n_centroids): 16-byte pieces where the rows allow, each piece stored
+    // to every copy, starting at copy c % ncopies so that a warp's stores
+    // spread over the copies; else element by element
+    const int rbytes = sub * (int)sizeof(T);
+    if (rbytes % 16 == 0 && ((uintptr_t)vc & 15u) == 0) {
+        const int pieces = rbytes / 16;
+        for (int e = threadIdx.x; e < kLutStride * pieces; e += THREADS) {
+            const int c = e / pieces, w = e - c * pieces;
+            const T *src = vc + (size_t)c * sub + (size_t)w * KR;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (c < nc && VQ_VSPAN(src, KR, vcb, ncb_elems, 16)) v = *reinterpret_cast<const uint4 *>(src);
+            int j = c % ncopies;
+            for (int k = 0; k < ncopies; ++k) {
+                T *dst = vcs + ((size_t)c * ncopies + j) * sub + (size_t)w * KR;
+                if (VQ_VSPAN(dst, KR, vcs, vcs_elems, 16)) *reinterpret_cast<uint4 *>(dst) = v;
+                j = j + 1 == ncopies ? 0 : j + 1;
+            }
+        }
+    } else {
+        for (int c = threadIdx.x; c < kLutStride; c += THREADS) {
+            for (int i = 0; i < sub; ++i) {
+                const T v = c < nc && VQ_SPAN(vc + (size_t)c * sub + i, 1, vcb, ncb_elems) ? vc[(size_t)c * sub + i] : T(0.f);
+                for (int j = 0; j < ncopies; ++j)
+                    if (VQ_SPAN(vcs + ((size_t)c * ncopies + j) * sub + i, 1, vcs, vcs_elems))
+                        vcs[((size_t)c * ncopies + j) * sub + i] = v;
+            }
+        }
     }
     __syncthreads();
 
