@@ -23,7 +23,7 @@ CHECKED_LIB_PATH = os.path.join(LIB_DIR, "libvqenc_checked.so")
 PTXAS_LOG = os.path.join(LIB_DIR, "ptxas.txt")
 SOURCES = [os.path.join(CSRC, name) for name in ("vq_encode.cu", "vq_attn.cu", "vq_scalar.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, name) for name in (
-    "vq_kernels.cuh", "vq_filter.cuh", "vq_tc.cuh", "vq_decode.cuh", "vq_attn.cuh", "vq_host.h", "vq_scalar.cuh", "vq_status.cuh", "vq_check.cuh")] + [
+    "vq_kernels.cuh", "vq_filter.cuh", "vq_tc.cuh", "vq_decode.cuh", "vq_attn.cuh", "vq_host.h", "vq_scalar.cuh", "vq_status.cuh", "vq_check.cuh", "vq_umma.cuh")] + [
     os.path.join(ROOT, "include", "vq_encode.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

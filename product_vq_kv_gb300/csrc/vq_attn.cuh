@@ -42,6 +42,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "vq_check.cuh"
 
 namespace vqk {
@@ -84,12 +86,18 @@ __host__ __device__ inline int attn_vcopies(int sub, int elem)
     return rb >= 128 ? 1 : 128 / rb;
 }
 
+// Bytes per element of the value-codebook copies for inputs of `elem` bytes:
+// with 8-column slices (attn_vw) the 16-bit values are widened to fp32 once,
+// when the copies are built, instead of at every gather.
+__host__ __device__ constexpr int attn_vstore(int sub, int elem) { return attn_vw(sub, elem) == 8 ? 4 : elem; }
+
 // Shared-memory layout, in order (bytes):
 //   lut  [GPB / GP][NS / Q][kLutStride][Q][GP] fp32   GP = min(GPB, 4) heads per
 //        vector, Q = attn_lut_q(GP, NS) sub-spaces side by side in a row;
 //        after the last chunk it holds the per-stream accumulators
 //        [streams][GPB][D] fp32 (the region is sized for both)
-//   vcb  [256][ncopies] rows of `sub` elements of T, zero past n_c
+//   vcb  [256][ncopies] rows of `sub` elements (of T, fp32 with 8-column
+//        slices: attn_vstore), zero past n_c
 //   pw   [CHUNK][GPB] fp32                     weights of the chunk
 //   red  [3][GPB][NW] fp32                     block maxima (two buffers), sums
 //   vtile[CHUNK][NS] bytes                     value codes of the chunk
@@ -104,7 +112,8 @@ __host__ __device__ inline AttnSmem attn_smem(int gpb, int ns, int sub, int elem
     const size_t acc_bytes = (size_t)kAttnThreads * attn_vw(sub, elem) * gpb * 4;  // >= streams * GPB * D floats
     m.lut = 0;
     m.vcb = m.lut + (lut_bytes > acc_bytes ? lut_bytes : acc_bytes);
-    m.pw = m.vcb + (size_t)256 * attn_vcopies(sub, elem) * sub * elem;
+    const int ve = attn_vstore(sub, elem);
+    m.pw = m.vcb + (size_t)256 * attn_vcopies(sub, ve) * sub * ve;
     m.pw = (m.pw + 15) / 16 * 16;
     m.red = m.pw + (size_t)chunk * gpb * 4;
     m.vtile = m.red + (size_t)3 * gpb * (kAttnThreads / 32) * 4;
@@ -168,6 +177,17 @@ __device__ __forceinline__ float2 pair_f32(uint32_t w, const __half *)
 __device__ __forceinline__ float2 pair_f32(uint32_t w, const __nv_bfloat16 *)
 {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Eight consecutive fp32 elements of a value row in shared memory as column
+// pairs, the half h (columns 4h .. 4h+3) first: r[0], r[1] hold columns
+// 4h .. 4h+3, r[2], r[3] the other four.
+__device__ __forceinline__ void load_row(const float *p, int h, float2 (&r)[4])
+{
+    const float4 a = *reinterpret_cast<const float4 *>(p + 4 * h);
+    const float4 b = *reinterpret_cast<const float4 *>(p + 4 - 4 * h);
+    r[0] = make_float2(a.x, a.y), r[1] = make_float2(a.z, a.w);
+    r[2] = make_float2(b.x, b.y), r[3] = make_float2(b.z, b.w);
 }
 
 // VW consecutive elements of a value row in shared memory, widened, as
@@ -248,72 +268,75 @@ __device__ __forceinline__ void load_vec(const float *p, float (&v)[GP])
     }
 }
 
-// Launch: grid.x = batch * heads_kv * (heads_q / heads_kv / GPB) * splits,
-// block = kAttnThreads, dynamic shared memory attn_smem(GPB, NS, SUB, sizeof(T)).total,
-// VW = attn_vw(SUB, sizeof(T)).
-// NS = head_dim / sub_dim in {4, 8, 16, 32, 64}; sub_dim % 4 == 0; code rows
-// are NS bytes apart and the code arrays aligned to min(NS, 16) bytes.
-// Partial of (b, hq, split) at part[((b * heads_q + hq) * splits + split) *
-// (D + 2)]: {0: max (log2 domain), 1: sum, 2..: unnormalised out}.
-template <typename T, int NS, int GPB, int VW>
-__global__ void __launch_bounds__(kAttnThreads)
-    attn_partial(const T *__restrict__ q, const uint8_t *__restrict__ kcodes,
-                 const T *__restrict__ kcb, const uint8_t *__restrict__ vcodes,
-                 const T *__restrict__ vcb, AttnShape sh, float *__restrict__ part)
+// Scores of one token for the block's GPB heads (phase A): its key code
+// row `wk` (NS bytes), looked up in the slot-ordered tables, sub-spaces in
+// the order i ^ lq (lq = lane % Q; lq_sel the byte selector of lq % 4).
+template <int NS, int GPB>
+__device__ __forceinline__ void attn_token_scores(const uint32_t (&wk)[NS / 4], const float *lut,
+                                                  uint64_t lut_floats, uint32_t lq, uint32_t lq_sel,
+                                                  float (&a)[GPB])
 {
-    constexpr int THREADS = kAttnThreads;
-    constexpr int TPT = attn_tok_per_thread(NS);
-    constexpr int CHUNK = attn_chunk(NS);
     constexpr int GP = GPB < 4 ? GPB : 4;
     constexpr int NPACK = GPB / GP;
     constexpr int Q = attn_lut_q(GP, NS);
-    static_assert(NS % Q == 0 && (Q & (Q - 1)) == 0, "table rows hold a power-of-two divisor of NS");
-    constexpr int NW = THREADS / 32;
-    constexpr float kNegInf = -__builtin_huge_valf();
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lq_f = (int)lq * GP;
+    (void)lut_floats;
+#pragma unroll
+    for (int g = 0; g < GPB; ++g) a[g] = 0.f;
+    uint32_t wq[NS / 4];  // byte i = code of sub-space i ^ lq
+    xor_order_codes<NS, Q>(wk, wq, lq, lq_sel);
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        const int code = (int)code_at(wq[i / 4], i % 4);
+        // slot (i % Q) ^ lq of row (i / Q) * 256 + code
+        const int slot_f = ((i % Q) * GP) ^ lq_f;
+#pragma unroll
+        for (int pk = 0; pk < NPACK; ++pk) {
+            float v[GP];
+            const float *src =
+                lut + ((size_t)pk * NS + (i / Q) * Q) * kLutStride * GP + code * (Q * GP) + slot_f;
+            if (VQ_VSPAN(src, GP, lut, lut_floats, GP * 4)) {
+                load_vec<GP>(src, v);
+            } else {
+#pragma unroll
+                for (int gi = 0; gi < GP; ++gi) v[gi] = 0.f;
+            }
+            if constexpr (GP >= 2) {  // head pairs as packed adds
+#pragma unroll
+                for (int gi = 0; gi < GP; gi += 2) {
+                    const float2 t2 = __fadd2_rn(make_float2(a[pk * GP + gi], a[pk * GP + gi + 1]),
+                                                 make_float2(v[gi], v[gi + 1]));
+                    a[pk * GP + gi] = t2.x, a[pk * GP + gi + 1] = t2.y;
+                }
+            } else {
+                a[pk] += v[0];
+            }
+        }
+    }
+}
+
+// The block's tables and value-codebook copies (attn_partial):
+// stage the queries of heads hq0 .. hq0 + GPB - 1 of batch row b, build the
+// GP-interleaved, slot-ordered key tables in `lut` (lut_floats floats) and
+// the value codebook's `ncopies` copies in `vcs` as VT (T, or fp32 for
+// 16-bit T) (a region of region_bytes bytes, vcs_elems elements used).  kc, vc: the KV head's codebooks.  Ends
+// with a block barrier.
+template <typename T, typename VT, int NS, int GPB, int THREADS>
+__device__ __forceinline__ void attn_setup(const T *__restrict__ q, const T *__restrict__ kcb,
+                                           const T *__restrict__ vcb, const AttnShape &sh, int64_t b,
+                                           int hq0, const T *kc, const T *vc, float *lut,
+                                           uint64_t lut_floats, VT *vcs, uint64_t vcs_elems,
+                                           uint64_t region_bytes, int ncopies)
+{
+    constexpr int GP = GPB < 4 ? GPB : 4;
+    constexpr int NPACK = GPB / GP;
+    constexpr int Q = attn_lut_q(GP, NS);
     const int sub = sh.sub_dim;
     const int d = sh.head_dim;
     const int nc = sh.n_centroids;
-    const AttnSmem lay = attn_smem(GPB, NS, sub, (int)sizeof(T));
-    const int ncopies = attn_vcopies(sub, (int)sizeof(T));
-    float *lut = reinterpret_cast<float *>(smem_raw + lay.lut);
-    T *vcs = reinterpret_cast<T *>(smem_raw + lay.vcb);
-    float *pw = reinterpret_cast<float *>(smem_raw + lay.pw);
-    float *red = reinterpret_cast<float *>(smem_raw + lay.red);
-    uint8_t *vtile = smem_raw + lay.vtile;
-
-    const int qpk = sh.heads_q / sh.heads_kv;  // query heads per KV head
-    const int hgroups = qpk / GPB;
-    int64_t bid = blockIdx.x;
-    const int split = (int)(bid % sh.splits);
-    bid /= sh.splits;
-    const int hg = (int)(bid % hgroups);
-    bid /= hgroups;
-    const int hkv = (int)(bid % sh.heads_kv);
-    const int64_t b = bid / sh.heads_kv;
-    const int hq0 = hkv * qpk + hg * GPB;
-
-    const T *kc = kcb + (size_t)hkv * nc * sub;
-    const T *vc = vcb + (size_t)hkv * nc * sub;
-    const size_t cache_off = ((size_t)b * sh.heads_kv + hkv) * (size_t)sh.tokens * NS;
-    const uint8_t *kb = kcodes + cache_off;
-    const uint8_t *vb = vcodes + cache_off;
-
-    // buffer extents, for the checked build's bounds checks (vq_check.cuh)
     const int64_t nq_elems = sh.batch * sh.heads_q * d;
     const int64_t ncb_elems = (int64_t)sh.heads_kv * nc * sub;
-    const int64_t ncodes = sh.batch * sh.heads_kv * sh.tokens * NS;
-    const int64_t npart = sh.batch * sh.heads_q * sh.splits * (int64_t)(d + 2);
-    const uint64_t lut_floats = (lay.vcb - lay.lut) / 4, vcs_elems = (uint64_t)256 * ncopies * sub;
-    const uint64_t pw_floats = (uint64_t)CHUNK * GPB, red_floats = (uint64_t)3 * GPB * NW;
-    constexpr uint32_t kCodeAlign = NS < 16 ? NS : 16;  // load_code_row, store_code_row
-    if constexpr (kChecked) {
-        // the layout inside the launch's shared memory and the block inside
-        // the grid: else the block does nothing
-        if (!dyn_smem_ok(smem_raw, lay.total, 16) || !index_ok(b, sh.batch) || vcs_elems * sizeof(T) > lay.pw - lay.vcb ||
-            attn_vw(sub, (int)sizeof(T)) != VW)
-            return;  // block-uniform
-    }
+    (void)nq_elems, (void)ncb_elems, (void)kcb, (void)vcb;
 
     // ---- the block's queries, widened to fp32 and transposed, staged in
     // the value-codebook region, which is not in use yet: element s * sub + i
@@ -321,7 +344,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     // sub-space puts the rows that the lanes of a wavefront read (different
     // sub-spaces, below) in different banks.  At most 17 KiB; the region
     // holds at least 18 KiB (attn_plan checks).
-    float *qT = reinterpret_cast<float *>(smem_raw + lay.vcb);
+    float *qT = reinterpret_cast<float *>(vcs);
     const int qs_stride = sub * GPB + 4;
     const uint64_t qT_floats = (uint64_t)NS * qs_stride;
     for (int e = threadIdx.x; e < GPB * d; e += THREADS) {
@@ -329,7 +352,7 @@ __global__ void __launch_bounds__(kAttnThreads)
         const int sj = j / sub, ij = j - sj * sub;
         const T *src = q + ((size_t)b * sh.heads_q + hq0 + g) * d + j;
         float *dst = qT + (size_t)sj * qs_stride + (size_t)ij * GPB + g;
-        if (VQ_SPAN(dst, 1, qT, (lay.pw - lay.vcb) / 4))
+        if (VQ_SPAN(dst, 1, qT, region_bytes / 4))
             *dst = VQ_SPAN(src, 1, q, nq_elems) ? to_f32(*src) : 0.f;
     }
     __syncthreads();
@@ -402,9 +425,10 @@ __global__ void __launch_bounds__(kAttnThreads)
     __syncthreads();  // the staged queries are read no more
 
     // ---- the value codebook in its bank-disjoint copies (zero past
-    // n_centroids): 16-byte pieces where the rows allow, each piece stored
-    // to every copy, starting at copy c % ncopies so that a warp's stores
-    // spread over the copies; else element by element
+    // n_centroids): 16-byte pieces of the rows where they allow, each stored
+    // (widened to fp32 when VT is) to every copy, starting at copy
+    // c % ncopies so that a warp's stores spread over the copies; else
+    // element by element
     const int rbytes = sub * (int)sizeof(T);
     if (rbytes % 16 == 0 && ((uintptr_t)vc & 15u) == 0) {
         const int pieces = rbytes / 16;
@@ -415,8 +439,17 @@ __global__ void __launch_bounds__(kAttnThreads)
             if (c < nc && VQ_VSPAN(src, KR, vcb, ncb_elems, 16)) v = *reinterpret_cast<const uint4 *>(src);
             int j = c % ncopies;
             for (int k = 0; k < ncopies; ++k) {
-                T *dst = vcs + ((size_t)c * ncopies + j) * sub + (size_t)w * KR;
-                if (VQ_VSPAN(dst, KR, vcs, vcs_elems, 16)) *reinterpret_cast<uint4 *>(dst) = v;
+                VT *dst = vcs + ((size_t)c * ncopies + j) * sub + (size_t)w * KR;
+                if (VQ_VSPAN(dst, KR, vcs, vcs_elems, 16)) {
+                    if constexpr (std::is_same<VT, T>::value) {
+                        *reinterpret_cast<uint4 *>(dst) = v;
+                    } else {  // eight 16-bit values to fp32
+                        const float2 f0 = pair_f32(v.x, src), f1 = pair_f32(v.y, src);
+                        const float2 f2 = pair_f32(v.z, src), f3 = pair_f32(v.w, src);
+                        reinterpret_cast<float4 *>(dst)[0] = make_float4(f0.x, f0.y, f1.x, f1.y);
+                        reinterpret_cast<float4 *>(dst)[1] = make_float4(f2.x, f2.y, f3.x, f3.y);
+                    }
+                }
                 j = j + 1 == ncopies ? 0 : j + 1;
             }
         }
@@ -425,12 +458,87 @@ __global__ void __launch_bounds__(kAttnThreads)
             for (int i = 0; i < sub; ++i) {
                 const T v = c < nc && VQ_SPAN(vc + (size_t)c * sub + i, 1, vcb, ncb_elems) ? vc[(size_t)c * sub + i] : T(0.f);
                 for (int j = 0; j < ncopies; ++j)
-                    if (VQ_SPAN(vcs + ((size_t)c * ncopies + j) * sub + i, 1, vcs, vcs_elems))
-                        vcs[((size_t)c * ncopies + j) * sub + i] = v;
+                    if (VQ_SPAN(vcs + ((size_t)c * ncopies + j) * sub + i, 1, vcs, vcs_elems)) {
+                        if constexpr (std::is_same<VT, T>::value) {
+                            vcs[((size_t)c * ncopies + j) * sub + i] = v;
+                        } else {
+                            vcs[((size_t)c * ncopies + j) * sub + i] = to_f32(v);
+                        }
+                    }
             }
         }
     }
     __syncthreads();
+}
+
+// Launch: grid.x = batch * heads_kv * (heads_q / heads_kv / GPB) * splits,
+// block = kAttnThreads, dynamic shared memory attn_smem(GPB, NS, SUB, sizeof(T)).total,
+// VW = attn_vw(SUB, sizeof(T)).
+// NS = head_dim / sub_dim in {4, 8, 16, 32, 64}; sub_dim % 4 == 0; code rows
+// are NS bytes apart and the code arrays aligned to min(NS, 16) bytes.
+// Partial of (b, hq, split) at part[((b * heads_q + hq) * splits + split) *
+// (D + 2)]: {0: max (log2 domain), 1: sum, 2..: unnormalised out}.
+template <typename T, int NS, int GPB, int VW>
+__global__ void __launch_bounds__(kAttnThreads)
+    attn_partial(const T *__restrict__ q, const uint8_t *__restrict__ kcodes,
+                 const T *__restrict__ kcb, const uint8_t *__restrict__ vcodes,
+                 const T *__restrict__ vcb, AttnShape sh, float *__restrict__ part)
+{
+    constexpr int THREADS = kAttnThreads;
+    constexpr int TPT = attn_tok_per_thread(NS);
+    constexpr int CHUNK = attn_chunk(NS);
+    constexpr int GP = GPB < 4 ? GPB : 4;
+    constexpr int NPACK = GPB / GP;
+    constexpr int Q = attn_lut_q(GP, NS);
+    static_assert(NS % Q == 0 && (Q & (Q - 1)) == 0, "table rows hold a power-of-two divisor of NS");
+    constexpr int NW = THREADS / 32;
+    constexpr float kNegInf = -__builtin_huge_valf();
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int sub = sh.sub_dim;
+    const int d = sh.head_dim;
+    const int nc = sh.n_centroids;
+    const AttnSmem lay = attn_smem(GPB, NS, sub, (int)sizeof(T));
+    using VT = typename std::conditional<VW == 8, float, T>::type;  // value-copy element (attn_vstore)
+    const int ncopies = attn_vcopies(sub, (int)sizeof(VT));
+    float *lut = reinterpret_cast<float *>(smem_raw + lay.lut);
+    VT *vcs = reinterpret_cast<VT *>(smem_raw + lay.vcb);
+    float *pw = reinterpret_cast<float *>(smem_raw + lay.pw);
+    float *red = reinterpret_cast<float *>(smem_raw + lay.red);
+    uint8_t *vtile = smem_raw + lay.vtile;
+
+    const int qpk = sh.heads_q / sh.heads_kv;  // query heads per KV head
+    const int hgroups = qpk / GPB;
+    int64_t bid = blockIdx.x;
+    const int split = (int)(bid % sh.splits);
+    bid /= sh.splits;
+    const int hg = (int)(bid % hgroups);
+    bid /= hgroups;
+    const int hkv = (int)(bid % sh.heads_kv);
+    const int64_t b = bid / sh.heads_kv;
+    const int hq0 = hkv * qpk + hg * GPB;
+
+    const T *kc = kcb + (size_t)hkv * nc * sub;
+    const T *vc = vcb + (size_t)hkv * nc * sub;
+    const size_t cache_off = ((size_t)b * sh.heads_kv + hkv) * (size_t)sh.tokens * NS;
+    const uint8_t *kb = kcodes + cache_off;
+    const uint8_t *vb = vcodes + cache_off;
+
+    // buffer extents, for the checked build's bounds checks (vq_check.cuh)
+    const int64_t ncodes = sh.batch * sh.heads_kv * sh.tokens * NS;
+    const int64_t npart = sh.batch * sh.heads_q * sh.splits * (int64_t)(d + 2);
+    const uint64_t lut_floats = (lay.vcb - lay.lut) / 4, vcs_elems = (uint64_t)256 * ncopies * sub;
+    const uint64_t pw_floats = (uint64_t)CHUNK * GPB, red_floats = (uint64_t)3 * GPB * NW;
+    constexpr uint32_t kCodeAlign = NS < 16 ? NS : 16;  // load_code_row, store_code_row
+    if constexpr (kChecked) {
+        // the layout inside the launch's shared memory and the block inside
+        // the grid: else the block does nothing
+        if (!dyn_smem_ok(smem_raw, lay.total, 16) || !index_ok(b, sh.batch) || vcs_elems * sizeof(VT) > lay.pw - lay.vcb ||
+            attn_vw(sub, (int)sizeof(T)) != VW)
+            return;  // block-uniform
+    }
+
+    attn_setup<T, VT, NS, GPB, THREADS>(q, kcb, vcb, sh, b, hq0, kc, vc, lut, lut_floats, vcs, vcs_elems,
+                                    lay.pw - lay.vcb, ncopies);
 
     // phase-B role: VW-column slice `col` (columns col*VW .. col*VW+VW-1 of
     // the head, inside one sub-space), token stream `stream` of `streams`
@@ -442,8 +550,11 @@ __global__ void __launch_bounds__(kAttnThreads)
     const int bs = (col * VW) / sub;            // sub-space of the slice
     const int bi = (col * VW) - bs * sub;       // first element in the row
     // this slice's columns in copy bs % ncopies of code 0; code c adds c rows
-    const T *vrow0 = vcs + (size_t)(bs % ncopies) * sub + bi;
+    const VT *vrow0 = vcs + (size_t)(bs % ncopies) * sub + bi;
     const size_t vstride = (size_t)ncopies * sub;
+    // fp32 rows: the two slices that share a copy in one wavefront read
+    // its two 16-byte halves in opposite orders (load_row)
+    const int vh = (bs / ncopies) & 1;
     float2 acc[GPB][VW / 2];  // column pairs (0, 1), (2, 3), ... of the slice
 #pragma unroll
     for (int g = 0; g < GPB; ++g)
@@ -453,7 +564,6 @@ __global__ void __launch_bounds__(kAttnThreads)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // phase-A sub-space order (see attn_lut_q)
     const uint32_t lq = (uint32_t)lane & (Q - 1);
-    const int lq_f = (int)lq * GP;
     const uint32_t lq_sel = 0x3210u ^ ((lq & 3u) * 0x1111u);
     float m_run[GPB], l_run[GPB];
 #pragma unroll
@@ -490,38 +600,7 @@ __global__ void __launch_bounds__(kAttnThreads)
             for (int g = 0; g < GPB; ++g) sc[r][g] = kNegInf;
             if (t < sh.tokens) {
                 float a[GPB];
-#pragma unroll
-                for (int g = 0; g < GPB; ++g) a[g] = 0.f;
-                uint32_t wq[NS / 4];  // byte i = code of sub-space i ^ lq
-                xor_order_codes<NS, Q>(wk[r], wq, lq, lq_sel);
-#pragma unroll
-                for (int i = 0; i < NS; ++i) {
-                    const int code = (int)code_at(wq[i / 4], i % 4);
-                    // slot (i % Q) ^ lq of row (i / Q) * 256 + code
-                    const int slot_f = ((i % Q) * GP) ^ lq_f;
-#pragma unroll
-                    for (int pk = 0; pk < NPACK; ++pk) {
-                        float v[GP];
-                        const float *src = lut + ((size_t)pk * NS + (i / Q) * Q) * kLutStride * GP +
-                                           code * (Q * GP) + slot_f;
-                        if (VQ_VSPAN(src, GP, lut, lut_floats, GP * 4)) {
-                            load_vec<GP>(src, v);
-                        } else {
-#pragma unroll
-                            for (int gi = 0; gi < GP; ++gi) v[gi] = 0.f;
-                        }
-                        if constexpr (GP >= 2) {  // head pairs as packed adds
-#pragma unroll
-                            for (int gi = 0; gi < GP; gi += 2) {
-                                const float2 t2 = __fadd2_rn(make_float2(a[pk * GP + gi], a[pk * GP + gi + 1]),
-                                                             make_float2(v[gi], v[gi + 1]));
-                                a[pk * GP + gi] = t2.x, a[pk * GP + gi + 1] = t2.y;
-                            }
-                        } else {
-                            a[pk] += v[0];
-                        }
-                    }
-                }
+                attn_token_scores<NS, GPB>(wk[r], lut, lut_floats, lq, lq_sel, a);
 #pragma unroll
                 for (int g = 0; g < GPB; ++g) {
                     sc[r][g] = a[g];
@@ -597,8 +676,11 @@ __global__ void __launch_bounds__(kAttnThreads)
                 float2 row[U][VW / 2];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    if (VQ_VSPAN(vrow0 + (size_t)code[u] * vstride, VW, vcs, vcs_elems, VW * sizeof(T))) {
-                        load_row<VW>(vrow0 + (size_t)code[u] * vstride, row[u]);
+                    if (VQ_VSPAN(vrow0 + (size_t)code[u] * vstride, VW, vcs, vcs_elems, VW == 8 ? 16 : VW * sizeof(T))) {
+                        if constexpr (VW == 8)
+                            load_row(vrow0 + (size_t)code[u] * vstride, vh, row[u]);
+                        else
+                            load_row<VW>(vrow0 + (size_t)code[u] * vstride, row[u]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < VW / 2; ++i) row[u][i] = make_float2(0.f, 0.f);
@@ -629,8 +711,11 @@ __global__ void __launch_bounds__(kAttnThreads)
                 const int code = VQ_SPAN(vtile + (size_t)tl * NS + bs, 1, vtile, (uint64_t)CHUNK * NS)
                                      ? vtile[(size_t)tl * NS + bs] : 0;
                 float2 row[VW / 2];
-                if (VQ_VSPAN(vrow0 + (size_t)code * vstride, VW, vcs, vcs_elems, VW * sizeof(T))) {
-                    load_row<VW>(vrow0 + (size_t)code * vstride, row);
+                if (VQ_VSPAN(vrow0 + (size_t)code * vstride, VW, vcs, vcs_elems, VW == 8 ? 16 : VW * sizeof(T))) {
+                    if constexpr (VW == 8)
+                        load_row(vrow0 + (size_t)code * vstride, vh, row);
+                    else
+                        load_row<VW>(vrow0 + (size_t)code * vstride, row);
                 } else {
 #pragma unroll
                     for (int i = 0; i < VW / 2; ++i) row[i] = make_float2(0.f, 0.f);
@@ -672,9 +757,12 @@ __global__ void __launch_bounds__(kAttnThreads)
         for (int g = 0; g < GPB; ++g)
             if (VQ_VSPAN(accs + ((size_t)stream * GPB + g) * d + col * VW, VW, lut, lut_floats, 16)) {
 #pragma unroll
-                for (int i = 0; i < VW / 4; ++i)
-                    reinterpret_cast<float4 *>(accs + ((size_t)stream * GPB + g) * d + col * VW)[i] =
+                for (int i = 0; i < VW / 4; ++i) {
+                    // with fp32 rows, acc[g][0..1] hold columns 4 vh .. 4 vh + 3
+                    const int slot = VW == 8 ? i ^ vh : i;
+                    reinterpret_cast<float4 *>(accs + ((size_t)stream * GPB + g) * d + col * VW)[slot] =
                         make_float4(acc[g][2 * i].x, acc[g][2 * i].y, acc[g][2 * i + 1].x, acc[g][2 * i + 1].y);
+                }
             }
     }
     __syncthreads();
