@@ -268,6 +268,57 @@ __device__ __forceinline__ void load_vec(const float *p, float (&v)[GP])
     }
 }
 
+// Warp maxima of GPB values per lane, with log2(GPB) exchanges that halve
+// the values a lane carries (lanes with bit 16 >> r set keep the upper half
+// in round r) and plain exchanges after: the lanes l with
+// l % (32 / GPB) == 0 return the warp's maximum of value `head`.
+template <int GPB>
+__device__ __forceinline__ float warp_max_heads(const float (&v)[GPB], int lane, int &head)
+{
+    float w[GPB];
+#pragma unroll
+    for (int g = 0; g < GPB; ++g) w[g] = v[g];
+    head = 0;
+#pragma unroll
+    for (int r = 0; (1 << r) < GPB; ++r) {
+        const int off = 16 >> r, half = GPB >> (r + 1);
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < half; ++k) {
+            const float send = upper ? w[k] : w[k + half];
+            const float keep = upper ? w[k + half] : w[k];
+            w[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+        }
+        head += upper ? half : 0;
+    }
+#pragma unroll
+    for (int off = 32 / GPB / 2; off > 0; off >>= 1) w[0] = fmaxf(w[0], __shfl_xor_sync(0xffffffffu, w[0], off));
+    return w[0];
+}
+
+// Block maxima of the GPB heads from the NW warp maxima rmax[g * NW + w]:
+// lane l reads entries l and l + 32, groups of NW lanes reduce, and every
+// lane takes head g's maximum from lane (g % (32 / NW)) * NW.
+template <int GPB, int NW>
+__device__ __forceinline__ void block_max_heads(const float *rmax, const float *red, uint64_t red_floats,
+                                                int lane, float (&bm)[GPB])
+{
+    constexpr float kNegInf = -__builtin_huge_valf();
+    constexpr int ROUNDS = (GPB * NW + 31) / 32;
+    constexpr int HPR = 32 / NW;  // heads per round of 32 entries
+    static_assert(32 % NW == 0, "whole heads per round");
+    float v[ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int e = r * 32 + lane;
+        v[r] = e < GPB * NW && VQ_SPAN(rmax + e, 1, red, red_floats) ? rmax[e] : kNegInf;
+#pragma unroll
+        for (int off = NW / 2; off > 0; off >>= 1) v[r] = fmaxf(v[r], __shfl_xor_sync(0xffffffffu, v[r], off));
+    }
+#pragma unroll
+    for (int g = 0; g < GPB; ++g) bm[g] = __shfl_sync(0xffffffffu, v[g / HPR], (g % HPR) * NW);
+}
+
 // Scores of one token for the block's GPB heads (phase A): its key code
 // row `wk` (NS bytes), looked up in the slot-ordered tables, sub-spaces in
 // the order i ^ lq (lq = lane % Q; lq_sel the byte selector of lq % 4).
@@ -612,20 +663,18 @@ __global__ void __launch_bounds__(kAttnThreads)
         // also ends the previous chunk's phase B, so the weights and value
         // codes below may be overwritten after it.
         float *rmax = red + (size_t)(ch & 1) * GPB * NW;
-#pragma unroll
-        for (int g = 0; g < GPB; ++g) {
-            float m = cm[g];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0 && VQ_SPAN(rmax + g * NW + warp, 1, red, red_floats)) rmax[g * NW + warp] = m;
+        {
+            int head;
+            const float m = warp_max_heads<GPB>(cm, lane, head);
+            if ((lane & (32 / GPB - 1)) == 0 && VQ_SPAN(rmax + head * NW + warp, 1, red, red_floats))
+                rmax[head * NW + warp] = m;
         }
         __syncthreads();
+        float bm[GPB];
+        block_max_heads<GPB, NW>(rmax, red, red_floats, lane, bm);
 #pragma unroll
         for (int g = 0; g < GPB; ++g) {
-            float m = m_run[g];
-#pragma unroll
-            for (int k = 0; k < NW; ++k)
-                if (VQ_SPAN(rmax + g * NW + k, 1, red, red_floats)) m = fmaxf(m, rmax[g * NW + k]);
+            const float m = fmaxf(m_run[g], bm[g]);
             if (m > m_run[g] && m_run[g] > kNegInf) {  // rescale what is accumulated
                 const float f = exp2f(m_run[g] - m);
                 l_run[g] *= f;
