@@ -47,7 +47,16 @@ PAGES_FALCON_SUBVEC_PER_S = 1_048_576 / 7.98e-3
 # kernel that has changed since reports null (see profiles/).
 MEASURED_TRAFFIC = {
     "kernel=encode_tc dtype=f16 sub_dim=4 tmem_cols=64 tiles_per_block=7 centroid_group=16 "
-    "grid=1171 smem=26965": 8_425_216,
+    "grid=1171 smem=26965": 8_425_472,
+    "kernel=encode_tc dtype=f16 sub_dim=8 tmem_cols=64 tiles_per_block=3 centroid_group=8 "
+    "grid=704 smem=34880": 4_364_800,
+}
+# The same for the other ops' dominant kernels, keyed by (op, workload, input dtype):
+# attn_partial, hadamard_rows, scalar_scan.
+MEASURED_OP_TRAFFIC = {
+    ("attention", "llama_attention", "f16"): 67_280_896 + 374_272,
+    ("hadamard", "turboquant_keys", "f16"): 67_156_992 + 4_517_376,
+    ("scalar", "turboquant_keys", "f32"): 134_288_384 + 12_928_256,
 }
 L2_FLUSH_BYTES = 256 << 20
 # How the encode rooflines count work.
@@ -664,7 +673,9 @@ def bench_sibling(args, fused: bool) -> None:
         "gpu_launches": args.steps * (1 if fused else 2),
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "bytes_per_launch": algo_bytes,
+                     "frac": achieved / peak,
+                     "traffic": MEASURED_OP_TRAFFIC.get(("hadamard" if fused else "scalar", sw.name, args.dtype)),
+                     "bytes_per_launch": algo_bytes,
                      "timed": "whole step" + ("" if fused else " (table build + lookup pass)"),
                      "accounting": "algorithmic bytes: each key element read once and its "
                                    "uint8 index written once"},
@@ -764,7 +775,8 @@ def bench_attention(args) -> None:
         "gpu_launches": 2 * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": MEASURED_OP_TRAFFIC.get(("attention", aw.name, "f16")),
                      "bytes_per_launch": algo_bytes,
                      "timed": "whole step (partial + combine kernels)",
                      "accounting": "algorithmic bytes: every key and value code read once "

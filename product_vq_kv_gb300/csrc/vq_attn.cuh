@@ -19,20 +19,23 @@
 // all GPB heads.  Per chunk:
 //   phase A, one thread per token: the key code row is read with vector
 //     loads and its score looked up for every head; the tables of up to four
-//     heads are interleaved so one 16-byte shared load serves four heads.
-//     The chunk maximum raises the running maximum (online softmax: the
-//     register accumulators are rescaled), and the weights 2^(score - max)
-//     and the value code rows go to shared memory;
-//   phase B, one thread per (4-column slice of the head, token stream): the
-//     value rows are gathered from the value codebook in shared memory (kept
-//     in the input type, widened in registers) and accumulated with the
-//     weights of every head in registers (no atomics).  The codebook is held
-//     in bank-disjoint copies, sub-space s reading copy s % ncopies, where a
-//     copy owns one (row bytes)-wide slot of every 128-byte line: the lanes
-//     that share a shared-memory wavefront (consecutive sub-spaces of one
-//     token) never hit the same banks, whatever the codes.
-// Shared-memory gathers bound this kernel (random table lookups in phase A,
-// about 3 random 16-byte lane accesses per clock per SM), not HBM.  Each block writes a partial (max, sum, out[D]) per query head to the
+//     heads are interleaved so one 16-byte shared load serves four heads, and
+//     stored in slot order (attn_lut_q) so that the lanes of a wavefront never
+//     meet in a bank, whatever the codes.  The chunk maximum raises the
+//     running maximum (online softmax: the register accumulators are
+//     rescaled), and the weights 2^(score - max) and the value code rows go
+//     to shared memory;
+//   phase B, one thread per (VW-column slice of the head, token stream): the
+//     value rows are gathered from the value codebook in shared memory (fp32
+//     for 8-column slices, else the input type widened in registers) and
+//     accumulated with the weights of every head in registers (no atomics).
+//     The codebook is held in bank-disjoint copies, sub-space s reading copy
+//     s % ncopies, where a copy owns one (row bytes)-wide slot of every
+//     128-byte line: the lanes that share a shared-memory wavefront
+//     (consecutive sub-spaces of one token) never hit the same banks,
+//     whatever the codes.
+// The shared-memory gathers and the value FMAs bound this kernel, not HBM.
+// Each block writes a partial (max, sum, out[D]) per query head to the
 // caller's workspace; attn_combine merges the partials (flash-decoding).
 // A code >= n_centroids reads a zero table entry and a zero value row (the
 // decode of such a code is a zero row).
