@@ -65,7 +65,8 @@ ENCODE_ACCOUNTING = ("effective: brute-force F = n_centroids * 3 * sub_dim fp32 
                      "arithmetic and return the same index, so frac can exceed 1")
 L2_POLICY = "flushed before every step (256 MiB write); per-step CUDA events on the launching stream"
 # Workloads timed beside the headline one in the default line: (name, steps).
-OTHER_WORKLOADS = (("llama_decode", 300), ("long_context", 100), ("grouped_adversarial", 20))
+OTHER_WORKLOADS = (("tiny", 300), ("llama_decode", 300), ("long_context", 100),
+                   ("grouped_adversarial", 20))
 FP32_LANES_PER_SM = 128
 CLOCK_REASON_BITS = {
     0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
@@ -321,8 +322,8 @@ def time_steps(step, steps: int, warmup: int, flush, stream, dev, clock_index=No
 
 def other_workloads(vq, dev, flush, stream, peak_tflops: float) -> dict:
     """The other encode workloads, one grouped launch per step, timed like
-    the headline one: the Llama decode step, long context, grouped
-    adversarial."""
+    the headline one: the tiny case (launch-bound), the Llama decode step,
+    long context, grouped adversarial."""
     import torch
 
     out = {}

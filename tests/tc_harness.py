@@ -12,7 +12,9 @@ of ``libvqenc.so``):
 * ``polls_encode`` -- the same kernel with a tiny per-pass poll limit, for the
   wait give-up path;
 * ``check_probe`` -- the bounds-check primitives of the checked build,
-  evaluated on described spans.
+  evaluated on described spans;
+* ``probe_link_read`` -- a plain read of a device or pinned host buffer, for
+  the host-link read rate beside the host-buffer encode.
 
 Same compiler flags as the library (``product_vq_kv_gb300.build``); the units
 compile in parallel and are rebuilt only when a source or a library header
@@ -96,6 +98,8 @@ def load() -> ctypes.CDLL:
             lib.check_probe.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, vp]
             lib.check_status.restype = i32
             lib.check_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+            lib.probe_link_read.restype = i32
+            lib.probe_link_read.argtypes = [vp, i64, vp, i32, vp]
             _lib = lib
         return _lib
 

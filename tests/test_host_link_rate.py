@@ -1,0 +1,98 @@
+"""What bounds the end-to-end encode: the CPU-GPU link's read rate.
+
+``vq_encode_grouped_host`` encodes keys that live in pinned host memory: the
+kernel reads them across the CPU-GPU link with its ordinary loads and writes
+the indices back to pinned memory.  On the Falcon prefill workload (8 MiB of
+fp16 keys, 4 MiB of indices) this test measures
+
+  * a plain read kernel over the same pinned buffer and over a device copy
+    (``tests/harness/link_probe.cu``: 16-byte loads, four in flight per
+    thread, one 8-byte store per 16 bytes read);
+  * the host-buffer encode itself, host call to host result.
+
+It checks the probe's output bit for bit and prints the times and the link
+read rate (run with ``-s``).  The encode must read its whole input across
+the link, so it can be no faster than the plain read of that input (a floor,
+checked with 10 % slack for timer resolution), and it is checked to stay
+within 2x of that floor.
+"""
+import ctypes
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vq():
+    from product_vq_kv_gb300.build import build
+
+    build()
+    import product_vq_kv_gb300 as m
+
+    m.load_library()
+    return m
+
+
+def test_host_encode_is_bound_by_the_link_read(vq):
+    import tc_harness
+
+    lib = tc_harness.load()
+    dev = torch.device("cuda")
+    x, cb = workloads.generate("falcon_prefill")
+    xh = torch.from_numpy(x).pin_memory()
+    cbh = torch.from_numpy(cb).pin_memory()
+    outh = torch.empty(x.shape[:2], dtype=torch.uint32).pin_memory()
+    xd, cbd = xh.to(dev), cbh.to(dev)
+    outd = torch.empty(x.shape[:2], dtype=torch.uint32, device=dev)
+    nbytes = xh.numel() * xh.element_size()
+    sink = torch.empty(nbytes // 2, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    handle = ctypes.c_void_p(stream.cuda_stream)
+
+    def probe_us(ptr, reps=30):
+        times = []
+        for i in range(reps + 3):
+            flush.fill_(i & 255)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            assert lib.probe_link_read(ptr, nbytes, sink.data_ptr(), 1216, handle) == 0
+            b.record()
+            times.append((a, b))
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) * 1e3 for a, b in times[3:]]))
+
+    # the probe reads what is there
+    assert lib.probe_link_read(xh.data_ptr(), nbytes, sink.data_ptr(), 1216, handle) == 0
+    torch.cuda.synchronize()
+    words = xh.view(torch.uint32).reshape(-1, 4).numpy()
+    want = np.stack([words[:, 0] ^ words[:, 2], words[:, 1] ^ words[:, 3]], axis=1)
+    assert np.array_equal(sink.view(torch.uint32).cpu().numpy().reshape(-1, 2), want)
+
+    t_dev = probe_us(xd.data_ptr())
+    t_host = probe_us(xh.data_ptr())
+
+    for _ in range(3):
+        vq.vq_encode_grouped_host(xh, cbh, outh, xd, cbd, outd)
+    enc = []
+    for _ in range(30):
+        t0 = time.perf_counter()
+        vq.vq_encode_grouped_host(xh, cbh, outh, xd, cbd, outd)
+        enc.append((time.perf_counter() - t0) * 1e6)
+    t_enc = float(np.median(enc))
+    # the indices are the device encode's
+    ref = vq.vq_encode_grouped(xd, cbd)
+    torch.cuda.synchronize()
+    assert np.array_equal(outh.view(torch.int32).numpy(), ref.view(torch.int32).cpu().numpy())
+
+    print(f"\nplain read of {nbytes / 2**20:.0f} MiB: device {t_dev:.1f} us, pinned host {t_host:.1f} us "
+          f"({nbytes / t_host / 1e3:.0f} GB/s across the link); host-buffer encode {t_enc:.1f} us "
+          f"({t_enc / t_host:.2f}x the pinned read)")
+    assert t_enc >= 0.9 * t_host
+    assert t_enc <= 2.0 * t_host
