@@ -62,11 +62,12 @@ using vqk::TcConfig;
 
 int device_sms() { return vqh_device_sms(); }
 
-// Blocks per group and 128-row tiles per block.  A block's time is taken as
-// its tiles plus half a tile of set-up (codebook staging); the launch's time
-// as waves of `slots` resident blocks times that.  The best of 1..64 tiles per
-// block and the one-wave shape is used.
-void tc_shape(int64_t n_groups, int64_t n_per_group, int slots, int64_t *blocks_per_group,
+// Blocks per group and 128-row tiles per block.  A block works through its
+// tiles `tps` at a time; its time is taken as its steps plus half a step of
+// set-up (codebook staging), the launch's time as waves of `slots` resident
+// blocks times that.  The best of 1..64 tiles per block and the one-wave
+// shape is used.
+void tc_shape(int64_t n_groups, int64_t n_per_group, int slots, int tps, int64_t *blocks_per_group,
               int32_t *tiles_per_block)
 {
     const int64_t tiles = (n_per_group + 127) / 128;
@@ -79,7 +80,7 @@ void tc_shape(int64_t n_groups, int64_t n_per_group, int slots, int64_t *blocks_
         if (t < 1 || t > tiles) return;
         const int64_t blocks = n_groups * ((tiles + t - 1) / t);
         const int64_t waves = (blocks + slots - 1) / slots;
-        const double cost = (double)waves * ((double)t + 0.5);
+        const double cost = (double)waves * ((double)((t + tps - 1) / tps) + 0.5);
         if (cost < best_cost) {
             best_cost = cost;
             best_t = t;
@@ -162,21 +163,24 @@ size_t tc_smem(int32_t n_centroids, vq_dtype dtype)
 {
     using C = TcConfig<SUB>;
     if (dtype == VQ_F32)
-        return vqk::TcLayout<SUB, C::kCols, C::kGroup, 2, 2>::bytes(n_centroids);
-    return vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH ? 2 : 1, 1>::bytes(n_centroids);
+        return vqk::TcLayout<SUB, C::kCols, C::kGroup, 2, 2, C::kTps>::bytes(n_centroids);
+    return vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH ? 2 : 1, 1, C::kTps>::bytes(n_centroids);
 }
 
 template <typename T, int SUB, typename OutT = uint32_t, bool SMOOTH = false>
 auto tc_kernel()
 {
     using C = TcConfig<SUB>;
-    return vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks, OutT, SMOOTH>;
+    return vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks, OutT, SMOOTH, vqk::kWaitPolls, C::kTps>;
 }
 
 // Resident tensor-core CTAs on the device: the register budget of the launch
 // bounds admits kMinBlocks per SM, the tensor memory 512 / kCols, and the
 // shared memory of an SM (228 KiB, 1 KiB reserved per block) what `smem`
 // allows.
+// Tiles per step of the tensor-core kernel.
+int tc_tps(int sub_dim) { return sub_dim == 4 ? TcConfig<4>::kTps : TcConfig<8>::kTps; }
+
 int tc_slots(int sub_dim, size_t smem)
 {
     const int sms = device_sms();
@@ -216,9 +220,10 @@ Plan make_plan(const Args &a)
         if (p.smem <= kMaxFastSmem) p.kind = kBrute;
     }
     if (p.kind == kTc) {
-        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, p.smem), &p.tiles_per_group, &p.tc_tiles);
+        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, p.smem), tc_tps(a.sub_dim), &p.tiles_per_group,
+                 &p.tc_tiles);
         p.blocks = a.n_groups * p.tiles_per_group;
-        p.threads = 128;
+        p.threads = 128 * tc_tps(a.sub_dim);
     } else if (p.kind != kGeneral) {
         const int64_t tile = p.kind == kFilter ? (int64_t)kFThreads * kFRows : (int64_t)kThreads * kRows;
         p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
@@ -240,7 +245,7 @@ vq_status launch_tc(const Args &a, const Plan &p)
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
         return VQ_ERR_CUDA;
-    kernel<<<(unsigned)p.blocks, 128, p.smem, a.stream>>>(
+    kernel<<<(unsigned)p.blocks, 128 * TcConfig<SUB>::kTps, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
         p.tiles_per_group, p.tc_tiles, 1.0f, static_cast<OutT *>(a.out), a.smooth,
         SMOOTH ? (int32_t)(a.head_dim / a.sub_dim) : 1);
@@ -361,9 +366,10 @@ vq_status run_smooth(const Args &a)
     if (a.n_centroids >= kFilterMinCentroids && a.n_centroids <= 256) {
         p.kind = kTc;
         p.smem = a.sub_dim == 4 ? tc_smem<4, true>(a.n_centroids, a.dtype) : tc_smem<8, true>(a.n_centroids, a.dtype);
-        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, p.smem), &p.tiles_per_group, &p.tc_tiles);
+        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, p.smem), tc_tps(a.sub_dim), &p.tiles_per_group,
+                 &p.tc_tiles);
         p.blocks = a.n_groups * p.tiles_per_group;
-        p.threads = 128;
+        p.threads = 128 * tc_tps(a.sub_dim);
     } else {
         p.kind = kFilter;
         p.smem = a.sub_dim == 4 ? filter_smem<4>(a.n_centroids) : filter_smem<8>(a.n_centroids);
@@ -705,9 +711,9 @@ vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_ce
     if (p.kind == kTc)
         snprintf(buf, (size_t)buflen,
                  "kernel=encode_tc dtype=%s sub_dim=%d tmem_cols=%d tiles_per_block=%d "
-                 "centroid_group=%d grid=%lld smem=%zu",
+                 "tiles_per_step=%d centroid_group=%d grid=%lld smem=%zu",
                  dtype_name(dtype), sub_dim, sub_dim == 4 ? TcConfig<4>::kCols : TcConfig<8>::kCols,
-                 (int)p.tc_tiles, sub_dim == 4 ? TcConfig<4>::kGroup : TcConfig<8>::kGroup,
+                 (int)p.tc_tiles, tc_tps(sub_dim), sub_dim == 4 ? TcConfig<4>::kGroup : TcConfig<8>::kGroup,
                  (long long)p.blocks, p.smem);
     else if (p.kind == kFilter)
         snprintf(buf, (size_t)buflen,

@@ -76,11 +76,13 @@
 // tensor memory: never while an MMA it issued is in flight, unless a wait
 // never completed.
 //
-// Launch: block = 128 threads; dynamic shared memory = TcLayout::bytes(...)
-// (at least 512/NCOL CTAs' worth of a 228 KiB SM, which caps the CTAs per SM
-// at the tensor-memory budget: NCOL columns each); grid.x = n_groups *
-// blocks_per_group, each block encoding tiles_per_block consecutive 128-row
-// tiles of one group.  Requirements: T is __half, __nv_bfloat16 or float, 64 <= n_centroids <=
+// Launch: block = 128 * TPS threads; dynamic shared memory =
+// TcLayout::bytes(...) (at least 512/(NCOL * TPS) CTAs' worth of a 228 KiB SM,
+// which caps the CTAs per SM at the tensor-memory budget: NCOL * TPS columns
+// each); grid.x = n_groups * blocks_per_group, each block encoding
+// tiles_per_block consecutive 128-row tiles of one group, TPS at a time (a
+// step): thread t works on tile t / 128 of the step, row t % 128, and the
+// step's tiles share each pass's commit, wait and barrier.  Requirements: T is __half, __nv_bfloat16 or float, 64 <= n_centroids <=
 // 256, x aligned to SUB * sizeof(T) bytes.  With SMOOTH: `smooth`
 // [n_groups][smooth_ns * SUB] fp32 factors, row m of a group holding channels
 // (m % smooth_ns) * SUB + i; TcLayout's A holds two pieces (NA = 2).
@@ -103,30 +105,39 @@ namespace vqk {
 static __device__ unsigned long long g_tc_stats[8];
 #endif
 
-// Least of GC consecutive scores.
-template <int GC>
-__device__ __forceinline__ float group_min(const uint32_t *u)
-{
-    float a = min3(__uint_as_float(u[0]), __uint_as_float(u[1]), __uint_as_float(u[2]));
-#pragma unroll
-    for (int k = 3; k + 1 < GC; k += 2) a = min3(a, __uint_as_float(u[k]), __uint_as_float(u[k + 1]));
-    return fminf(a, __uint_as_float(u[GC - 1]));
-}
-
 // Least of N values by a tree of three-input minima (NaN ignored unless all
-// are NaN, as min3).
-template <int N>
-__device__ __forceinline__ float tree_min_p(const float *w)
+// are NaN, as min3).  W is float, or uint32_t holding float bits.
+template <int N, typename W>
+__device__ __forceinline__ float tree_min_p(const W *w)
 {
+    auto f = [](W v) -> float {
+        if constexpr (std::is_same<W, float>::value) return v;
+        else return __uint_as_float(v);
+    };
     if constexpr (N == 1) {
-        return w[0];
+        return f(w[0]);
     } else if constexpr (N == 2) {
-        return fminf(w[0], w[1]);
+        return fminf(f(w[0]), f(w[1]));
     } else if constexpr (N == 3) {
-        return min3(w[0], w[1], w[2]);
+        return min3(f(w[0]), f(w[1]), f(w[2]));
     } else {
         constexpr int a = (N + 2) / 3, b = (N - a + 1) / 2, c = N - a - b;
         return min3(tree_min_p<a>(w), tree_min_p<b>(w + a), tree_min_p<c>(w + a + b));
+    }
+}
+
+// Least of GC consecutive scores (float bits) by a shallow tree of
+// three-input minima: 8 operations in 3 levels for 16, 4 in 2 for 8.
+template <int GC>
+__device__ __forceinline__ float group_min(const uint32_t *u)
+{
+    auto f = [&](int i) { return __uint_as_float(u[i]); };
+    if constexpr (GC == 16) {
+        const float a = min3(min3(f(0), f(1), f(2)), min3(f(3), f(4), f(5)), min3(f(6), f(7), f(8)));
+        const float b = min3(min3(f(9), f(10), f(11)), min3(f(12), f(13), f(14)), f(15));
+        return fminf(a, b);
+    } else {
+        return tree_min_p<GC>(u);
     }
 }
 template <int N>
@@ -140,7 +151,7 @@ __device__ __forceinline__ float tf32_trunc(float v) { return __uint_as_float(__
 
 // ------------------------------------------------------------------ layout
 
-template <int SUB, int NCOL, int GC, int NA = 1, int NB = 1>
+template <int SUB, int NCOL, int GC, int NA = 1, int NB = 1, int TPS = 1>
 struct TcLayout {
     static constexpr int kK = SUB == 4 ? 8 : 16;       // MMA K (tf32 elements), 8 per instruction
     static constexpr int kRowBytes = kK * 4;
@@ -149,20 +160,20 @@ struct TcLayout {
     // centroids (2p, 2p+1) is the float2 (-c_2p_i, -c_2p+1_i) -- so one packed
     // f32x2 evaluation covers two centroids; one 16-byte pad per group
     static constexpr int kGroupFloats = kGC * SUB + 4;
-    static constexpr int kCtasPerSm = 512 / NCOL;
+    static constexpr int kCtasPerSm = 512 / (NCOL * TPS);
     __host__ __device__ static int padded(int nc) { return (nc + 31) / 32 * 32; }
     __host__ __device__ static int groups(int nc) { return padded(nc) / kGC; }
     // byte offsets
-    static constexpr size_t kABytes = (size_t)128 * kRowBytes;  // one A piece
-    __host__ __device__ static size_t a_off() { return 0; }
-    __host__ __device__ static size_t b_off() { return NA * kABytes; }
+    static constexpr size_t kABytes = (size_t)128 * kRowBytes;  // one A piece of one tile
+    __host__ __device__ static size_t a_off() { return 0; }  // tile h of a step: its NA pieces at h * NA * kABytes
+    __host__ __device__ static size_t b_off() { return TPS * NA * kABytes; }
     __host__ __device__ static size_t x_off(int /*nc: B always holds 256 rows*/) { return b_off() + (size_t)NB * 256 * kRowBytes; }
     __host__ __device__ static size_t misc_off(int nc)
     {
         return x_off(nc) + (size_t)groups(nc) * kGroupFloats * 4;
     }
     // misc: SUB + 1 maxima, queue counter, tensor-memory address, pad, mbarrier (8-aligned), queue
-    __host__ __device__ static size_t used(int nc) { return misc_off(nc) + 64 + 128 * 4; }
+    __host__ __device__ static size_t used(int nc) { return misc_off(nc) + 64 + 128 * TPS * 4; }
     __host__ __device__ static size_t bytes(int nc)
     {
         const size_t cap = (size_t)228 * 1024 / (kCtasPerSm + 1) + 1024;
@@ -171,25 +182,27 @@ struct TcLayout {
     }
 };
 
-// Per sub_dim: tensor-memory columns per CTA, centroids per screening group,
-// minimum CTAs per SM (register budget).  Measured best on GB300 for
-// 256-centroid codebooks.
+// Per sub_dim: tensor-memory columns per tile, centroids per screening group,
+// minimum CTAs per SM (register budget), tiles per step (a CTA has 128 threads
+// per tile of a step and screens the step's tiles with one commit, one wait
+// and one barrier per pass).  Measured best on GB300 for 256-centroid
+// codebooks.
 template <int SUB>
 struct TcConfig;
 template <>
 struct TcConfig<4> {
-    static constexpr int kCols = 64, kGroup = 16, kMinBlocks = 8;
+    static constexpr int kCols = 64, kGroup = 16, kMinBlocks = 4, kTps = 2;
 };
 template <>
 struct TcConfig<8> {
-    static constexpr int kCols = 64, kGroup = 8, kMinBlocks = 6;
+    static constexpr int kCols = 64, kGroup = 8, kMinBlocks = 3, kTps = 2;
 };
 
 // ------------------------------------------------------------------ kernel
 
 template <typename T, int SUB, int NCOL, int GC, int MINB, typename OutT = uint32_t,
-          bool SMOOTH = false, int POLLS = kWaitPolls>
-__global__ void __launch_bounds__(128, MINB)
+          bool SMOOTH = false, int POLLS = kWaitPolls, int TPS = 1>
+__global__ void __launch_bounds__(128 * TPS, MINB)
     encode_tc(const T *__restrict__ x, const T *__restrict__ codebooks, int64_t n_per_group,
               int32_t n_centroids, int64_t blocks_per_group, int32_t tiles_per_block, float one,
               OutT *__restrict__ out, const float *__restrict__ smooth, int32_t smooth_ns)
@@ -200,7 +213,8 @@ __global__ void __launch_bounds__(128, MINB)
     constexpr bool kF32 = std::is_same<T, float>::value;  // fp32 rows and codebook
     constexpr int kNA = SMOOTH || kF32 ? 2 : 1;  // A pieces: rows not exact in tf32
     constexpr int kNB = kF32 ? 2 : 1;            // B pieces: -2c not exact in tf32
-    using L = TcLayout<SUB, NCOL, GC, kNA, kNB>;
+    using L = TcLayout<SUB, NCOL, GC, kNA, kNB, TPS>;
+    constexpr int THREADS = 128 * TPS;
     constexpr int kK = L::kK;
     constexpr int kKB = kK / 4;  // 16-byte core-matrix columns per row
     constexpr int kGC = L::kGC;
@@ -222,6 +236,8 @@ __global__ void __launch_bounds__(128, MINB)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    const int th = tid >> 7;   // tile of the step this thread works on
+    const int rt = tid & 127;  // its row in that tile, its tensor-memory lane
     const int n_pad = L::padded(n_centroids);
     const int64_t g = blockIdx.x / blocks_per_group;
     const int64_t blk = blockIdx.x - g * blocks_per_group;
@@ -234,15 +250,15 @@ __global__ void __launch_bounds__(128, MINB)
     // buffer extents, for the checked build's bounds checks (vq_check.cuh)
     const int64_t n_groups_all = gridDim.x / blocks_per_group;
     const int64_t nx = n_groups_all * n_per_group * SUB, nout = n_groups_all * n_per_group;
-    constexpr uint64_t kSaBytes = kNA * L::kABytes, kSbBytes = (uint64_t)kNB * 256 * L::kRowBytes;
+    constexpr uint64_t kSaBytes = TPS * kNA * L::kABytes, kSbBytes = (uint64_t)kNB * 256 * L::kRowBytes;
     const uint64_t sx_bytes = (uint64_t)L::groups(n_centroids) * L::kGroupFloats * 4;
-    constexpr uint64_t kMiscBytes = 64 + 128 * 4;
+    constexpr uint64_t kMiscBytes = 64 + 128 * TPS * 4;
     constexpr uint32_t kRowAlign = SUB * sizeof(T) < 16 ? SUB * sizeof(T) : 16;  // load_row
     if constexpr (kChecked) {
         // the layout inside the launch's shared memory, the block inside the
         // grid, its smooth factors inside theirs: else the block does nothing
         if (!dyn_smem_ok(sm, L::used(n_centroids), 16) || !span_ok(bar, 8, misc, kMiscBytes, 8) ||
-            !span_ok(queue, 512, misc, kMiscBytes, 4) || !index_ok(g, n_groups_all) ||
+            !span_ok(queue, 512 * TPS, misc, kMiscBytes, 4) || !index_ok(g, n_groups_all) ||
             (SMOOTH && !VQ_SPAN(sg, (int64_t)smooth_ns * SUB, smooth, n_groups_all * smooth_ns * SUB)))
             return;  // block-uniform
     }
@@ -256,20 +272,20 @@ __global__ void __launch_bounds__(128, MINB)
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tslot)),
-                     "r"(NCOL));
+                     "r"(NCOL * TPS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     {
-        // A row `tid`: columns SUB.. of the row are the constant [1, 1, 1, 0 ...]
-        // in the first piece and zero in the others
+        // A row rt of tile th: columns SUB.. of the row are the constant
+        // [1, 1, 1, 0 ...] in the first piece and zero in the others
 #pragma unroll
         for (int pc = 0; pc < kNA; ++pc) {
-            float *arow = sa + pc * (L::kABytes / 4);
+            float *arow = sa + (th * kNA + pc) * (L::kABytes / 4);
 #pragma unroll
             for (int kb = SUB / 4; kb < kKB; ++kb) {
                 const float4 v = kb == SUB / 4 && pc == 0 ? make_float4(1.f, 1.f, 1.f, 0.f)
                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                float4 *dst = reinterpret_cast<float4 *>(arow + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4);
+                float4 *dst = reinterpret_cast<float4 *>(arow + ((rt >> 3) * (kKB * 128) + kb * 128 + (rt & 7) * 16) / 4);
                 if (span_ok(dst, 16, sa, kSaBytes, 16)) *dst = v;
             }
         }
@@ -277,7 +293,7 @@ __global__ void __launch_bounds__(128, MINB)
     __syncthreads();
 
     // ---- stage the codebook: B operand, exact layout, maxima
-    for (int c = tid; c < 256; c += 128) {
+    for (int c = tid; c < 256; c += THREADS) {
         const bool real = c < n_centroids;
         const bool cb_ok = !real || VQ_SPAN(cb + (size_t)c * SUB, SUB, codebooks, n_groups_all * n_centroids * SUB);
         float v[SUB];
@@ -354,7 +370,8 @@ __global__ void __launch_bounds__(128, MINB)
                        (kF32 ? 7.6293945e-6f : kNA == 2 ? 1.9073486e-6f : 0.0f);
     const float kD = 4.0f * gamma_u(SUB + 2);
     const float kTiny = 7.8886091e-31f;  // 2^-100
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    // this thread's accumulator: lane rt, the NCOL columns of tile th
+    const uint32_t lane_base = ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(th * NCOL);
     const uint32_t sa_addr = smem_addr(sa), sb_addr = smem_addr(sb);
     constexpr uint32_t kSbo = kKB * 128;
 
@@ -369,16 +386,19 @@ __global__ void __launch_bounds__(128, MINB)
             for (int i = 0; i < SUB; ++i) v[i] = 0.f;
         }
     };
-    load_x(row_base + tid, xr);
+    load_x(th < tiles_per_block ? row_base + (int64_t)th * 128 + rt : n_per_group, xr);
 
     uint32_t phase = 0;
     bool alive = true;  // block-wide: every wait so far completed within POLLS polls
     // this thread's waits: kWaitLate, kWaitFailed; thread 0 also keeps, in
     // bits 2-3, one more than the parity of the last phase it started (0: none)
     uint32_t wst = 0;
-    for (int tile = 0; tile < tiles_per_block; ++tile) {
-        const int64_t row = row_base + (int64_t)tile * 128 + tid;
-        if (row_base + (int64_t)tile * 128 >= n_per_group) break;  // block-uniform
+    const int steps = (tiles_per_block + TPS - 1) / TPS;
+    for (int step = 0; step < steps; ++step) {
+        const int tile = step * TPS + th;  // this thread's tile; past tiles_per_block: none
+        const bool own = tile < tiles_per_block;
+        const int64_t row = own ? row_base + (int64_t)tile * 128 + rt : n_per_group;
+        if (row_base + (int64_t)step * TPS * 128 >= n_per_group) break;  // block-uniform
 
         // A rows of this tile (the MMA of the previous tile has completed)
         if constexpr (kNA == 2) {
@@ -392,15 +412,16 @@ __global__ void __launch_bounds__(128, MINB)
             for (int pc = 0; pc < 2; ++pc)
 #pragma unroll
                 for (int kb = 0; kb < SUB / 4; ++kb) {
-                    float4 *dst = reinterpret_cast<float4 *>(sa + pc * (L::kABytes / 4) +
-                                                             ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4);
+                    float4 *dst = reinterpret_cast<float4 *>(sa + (th * 2 + pc) * (L::kABytes / 4) +
+                                                             ((rt >> 3) * (kKB * 128) + kb * 128 + (rt & 7) * 16) / 4);
                     if (span_ok(dst, 16, sa, kSaBytes, 16))
                         *dst = make_float4(pc3[pc][4 * kb], pc3[pc][4 * kb + 1], pc3[pc][4 * kb + 2], pc3[pc][4 * kb + 3]);
                 }
         } else {
 #pragma unroll
             for (int kb = 0; kb < SUB / 4; ++kb) {
-                float4 *dst = reinterpret_cast<float4 *>(sa + ((tid >> 3) * (kKB * 128) + kb * 128 + (tid & 7) * 16) / 4);
+                float4 *dst = reinterpret_cast<float4 *>(sa + th * (L::kABytes / 4) +
+                                                         ((rt >> 3) * (kKB * 128) + kb * 128 + (rt & 7) * 16) / 4);
                 if (span_ok(dst, 16, sa, kSaBytes, 16)) *dst = make_float4(xr[4 * kb], xr[4 * kb + 1], xr[4 * kb + 2], xr[4 * kb + 3]);
             }
         }
@@ -427,26 +448,29 @@ __global__ void __launch_bounds__(128, MINB)
             }
             if (tid == 0 && !(wst & kWaitLate)) {  // never a second phase outstanding
                 const uint32_t idesc = umma_idesc_tf32((uint32_t)ncols);
-                // (A piece, B piece) products: (hi, hi), (mid, hi), (hi, mid)
 #pragma unroll
-                for (int pp = 0; pp < kNA + kNB - 1; ++pp) {
-                    const uint32_t pa = pp == 1 && kNA == 2 ? 1u : 0u;
-                    const uint32_t pb = pp == kNA ? 1u : 0u;
+                for (int h = 0; h < TPS; ++h) {  // the step's tiles, each into its NCOL columns
+                    // (A piece, B piece) products: (hi, hi), (mid, hi), (hi, mid)
 #pragma unroll
-                    for (int kstep = 0; kstep < kK / 8; ++kstep) {
-                        const uint64_t ad =
-                            umma_smem_desc(sa_addr + pa * (uint32_t)L::kABytes + kstep * 256, 128, kSbo);
-                        const uint64_t bd = umma_smem_desc(
-                            sb_addr + pb * (uint32_t)(256 * L::kRowBytes) + (c0 >> 3) * kSbo + kstep * 256, 128, kSbo);
-                        // the bytes the two operands span (16 or ncols / 8
-                        // groups of 8 rows, kSbo apart, 256 bytes each) and
-                        // the accumulator columns
-                        const bool op_ok =
-                            span_ok(sa + (pa * L::kABytes + kstep * 256) / 4, 15 * kSbo + 256, sa, kSaBytes, 16) &&
-                            span_ok(sb + (pb * 256 * L::kRowBytes + (c0 >> 3) * kSbo + kstep * 256) / 4,
-                                    (ncols / 8 - 1) * kSbo + 256, sb, kSbBytes, 16) &&
-                            index_ok(ncols - 1, NCOL);
-                        if (op_ok) umma_tf32(tmem, ad, bd, idesc, pp > 0 || kstep > 0);
+                    for (int pp = 0; pp < kNA + kNB - 1; ++pp) {
+                        const uint32_t pa = (uint32_t)(h * kNA) + (pp == 1 && kNA == 2 ? 1u : 0u);
+                        const uint32_t pb = pp == kNA ? 1u : 0u;
+#pragma unroll
+                        for (int kstep = 0; kstep < kK / 8; ++kstep) {
+                            const uint64_t ad =
+                                umma_smem_desc(sa_addr + pa * (uint32_t)L::kABytes + kstep * 256, 128, kSbo);
+                            const uint64_t bd = umma_smem_desc(
+                                sb_addr + pb * (uint32_t)(256 * L::kRowBytes) + (c0 >> 3) * kSbo + kstep * 256, 128, kSbo);
+                            // the bytes the two operands span (16 or ncols / 8
+                            // groups of 8 rows, kSbo apart, 256 bytes each) and
+                            // the accumulator columns
+                            const bool op_ok =
+                                span_ok(sa + (pa * L::kABytes + kstep * 256) / 4, 15 * kSbo + 256, sa, kSaBytes, 16) &&
+                                span_ok(sb + (pb * 256 * L::kRowBytes + (c0 >> 3) * kSbo + kstep * 256) / 4,
+                                        (ncols / 8 - 1) * kSbo + 256, sb, kSbBytes, 16) &&
+                                index_ok(h * NCOL + ncols - 1, NCOL * TPS);
+                            if (op_ok) umma_tf32(tmem + (uint32_t)(h * NCOL), ad, bd, idesc, pp > 0 || kstep > 0);
+                        }
                     }
                 }
                 umma_commit(bar);
@@ -484,7 +508,7 @@ __global__ void __launch_bounds__(128, MINB)
 
         // next tile's row, in flight during the bookkeeping below
         float xn[SUB];
-        load_x(row + 128, xn);
+        load_x(tile + TPS < tiles_per_block ? row + TPS * 128 : n_per_group, xn);
 
         // ---- bound, candidate groups, exact re-evaluation
         const float m1 = tree_min<kNG>(gmin);
@@ -520,7 +544,7 @@ __global__ void __launch_bounds__(128, MINB)
             alive = false;
             if (tid == 0) {
                 if (wst >> 2) (void)mbar_wait<kWaitPolls>(bar, (wst >> 2) - 1u);
-                *qcount = (uint32_t)tile;
+                *qcount = (uint32_t)step;
                 raise_status(kStatusWaitGaveUp);
             }
             break;
@@ -541,7 +565,7 @@ __global__ void __launch_bounds__(128, MINB)
             id = kQueued;
             if (row < n_per_group) {
                 const uint32_t k = atomicAdd(qcount, 1u);
-                if (VQ_SPAN(queue + k, 1, queue, 128)) queue[k] = (uint32_t)tid;
+                if (VQ_SPAN(queue + k, 1, queue, THREADS)) queue[k] = (uint32_t)tid;
             }
         } else {
             // exact distances, two centroids per packed evaluation, ascending
@@ -583,9 +607,10 @@ __global__ void __launch_bounds__(128, MINB)
 
         // ---- queued rows of this tile: one warp per row, exact scan
         const uint32_t nq = *qcount;
-        for (uint32_t q = (uint32_t)warp; q < nq; q += 4) {
-            if (!VQ_SPAN(queue + q, 1, queue, 128)) break;  // warp-uniform
-            const int64_t qrow = row_base + (int64_t)tile * 128 + queue[q];
+        for (uint32_t q = (uint32_t)warp; q < nq; q += THREADS / 32) {
+            if (!VQ_SPAN(queue + q, 1, queue, THREADS)) break;  // warp-uniform
+            const uint32_t qt = queue[q];  // the queued row's thread: tile qt >> 7 of the step, row qt & 127
+            const int64_t qrow = row_base + (int64_t)(step * TPS + (int)(qt >> 7)) * 128 + (qt & 127);
             if (!VQ_SPAN(xg + (size_t)qrow * SUB, SUB, x, nx)) continue;  // warp-uniform
             float xq[SUB];
 #pragma unroll
@@ -623,14 +648,15 @@ __global__ void __launch_bounds__(128, MINB)
     tc_fence_before();
     __syncthreads();
     if (!alive) {
-        // a wait gave up: mark the rows of the failed tile and of every later one
-        for (int t = (int)*qcount; t < tiles_per_block; ++t) {
-            const int64_t r = row_base + (int64_t)t * 128 + tid;
-            if (r < n_per_group && VQ_SPAN(og + r, 1, out, nout)) store_index(og + r, kQueued);
+        // a wait gave up: mark the rows of the failed step and of every later one
+        for (int st = (int)*qcount; st < steps; ++st) {
+            const int t = st * TPS + th;
+            const int64_t r = row_base + (int64_t)t * 128 + rt;
+            if (t < tiles_per_block && r < n_per_group && VQ_SPAN(og + r, 1, out, nout)) store_index(og + r, kQueued);
         }
     }
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOL));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOL * TPS));
 }
 
 }  // namespace vqk

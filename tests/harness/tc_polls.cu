@@ -16,14 +16,14 @@ cudaError_t launch(const void *x, const void *cb, int64_t n_groups, int64_t n_pe
                    int32_t n_c, int32_t tiles_per_block, void *out, cudaStream_t st)
 {
     using C = vqk::TcConfig<SUB>;
-    using L = vqk::TcLayout<SUB, C::kCols, C::kGroup, 1, 1>;
+    using L = vqk::TcLayout<SUB, C::kCols, C::kGroup, 1, 1, C::kTps>;
     const size_t smem = L::bytes(n_c);
-    auto k = vqk::encode_tc<__half, SUB, C::kCols, C::kGroup, C::kMinBlocks, OutT, false, POLLS>;
+    auto k = vqk::encode_tc<__half, SUB, C::kCols, C::kGroup, C::kMinBlocks, OutT, false, POLLS, C::kTps>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (n_per_group + 127) / 128;
     const int64_t per_group = (tiles + tiles_per_block - 1) / tiles_per_block;
-    k<<<(unsigned)(n_groups * per_group), 128, smem, st>>>(
+    k<<<(unsigned)(n_groups * per_group), 128 * C::kTps, smem, st>>>(
         static_cast<const __half *>(x), static_cast<const __half *>(cb), n_per_group, n_c,
         per_group, tiles_per_block, 1.0f, static_cast<OutT *>(out), nullptr, 1);
     return cudaPeekAtLastError();

@@ -21,14 +21,14 @@ cudaError_t launch(const void *x, const void *cb, int64_t n_groups, int64_t n_pe
 {
     using C = vqk::TcConfig<SUB>;
     constexpr bool kF32 = std::is_same<T, float>::value;
-    using L = vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH || kF32 ? 2 : 1, kF32 ? 2 : 1>;
+    using L = vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH || kF32 ? 2 : 1, kF32 ? 2 : 1, C::kTps>;
     const size_t smem = L::bytes(n_c);
-    auto k = vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks, uint32_t, SMOOTH>;
+    auto k = vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks, uint32_t, SMOOTH, vqk::kWaitPolls, C::kTps>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (n_per_group + 127) / 128;
     const int64_t per_group = (tiles + tiles_per_block - 1) / tiles_per_block;
-    k<<<(unsigned)(n_groups * per_group), 128, smem, st>>>(
+    k<<<(unsigned)(n_groups * per_group), 128 * C::kTps, smem, st>>>(
         static_cast<const T *>(x), static_cast<const T *>(cb), n_per_group, n_c, per_group,
         tiles_per_block, 1.0f, out, smooth, SMOOTH ? head_dim / SUB : 1);
     return cudaPeekAtLastError();
