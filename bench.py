@@ -48,8 +48,8 @@ PAGES_FALCON_SUBVEC_PER_S = 1_048_576 / 7.98e-3
 MEASURED_TRAFFIC = {
     "kernel=encode_tc dtype=f16 sub_dim=4 tmem_cols=64 tiles_per_block=14 tiles_per_step=2 "
     "centroid_group=16 grid=586 smem=47718": 8_425_984,
-    "kernel=encode_tc dtype=f16 sub_dim=8 tmem_cols=64 tiles_per_block=5 tiles_per_step=2 "
-    "centroid_group=8 grid=416 smem=47718": 4_365_312,
+    "kernel=encode_tc dtype=f16 sub_dim=8 tmem_cols=64 tiles_per_block=3 tiles_per_step=1 "
+    "centroid_group=8 grid=704 smem=34880": 4_364_800,
 }
 # The same for the other ops' dominant kernels, keyed by (op, workload, input dtype):
 # attn_partial, hadamard_rows, scalar_scan.

@@ -195,7 +195,7 @@ struct TcConfig<4> {
 };
 template <>
 struct TcConfig<8> {
-    static constexpr int kCols = 64, kGroup = 8, kMinBlocks = 3, kTps = 2;
+    static constexpr int kCols = 64, kGroup = 8, kMinBlocks = 6, kTps = 1;
 };
 
 // ------------------------------------------------------------------ kernel
