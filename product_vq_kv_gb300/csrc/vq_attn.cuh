@@ -193,19 +193,15 @@ __device__ __forceinline__ void load_row(const float *p, int h, float2 (&r)[4])
     r[2] = make_float2(b.x, b.y), r[3] = make_float2(b.z, b.w);
 }
 
-// VW consecutive elements of a value row in shared memory, widened, as
-// column pairs: VW = 4 (any T) or 8 (16-bit T, one 16-byte load).
+// Four consecutive elements of a value row in shared memory (the input
+// type), widened, as column pairs (4-column slices; 8-column slices read the
+// fp32 copies through the overload above).
 template <int VW, typename T>
 __device__ __forceinline__ void load_row(const T *p, float2 (&r)[VW / 2])
 {
-    if constexpr (VW == 4) {
-        const float4 a = load4_f32(p);
-        r[0] = make_float2(a.x, a.y), r[1] = make_float2(a.z, a.w);
-    } else {
-        static_assert(VW == 8 && sizeof(T) == 2, "8-column slices are for 16-bit values");
-        const uint4 u = *reinterpret_cast<const uint4 *>(p);
-        r[0] = pair_f32(u.x, p), r[1] = pair_f32(u.y, p), r[2] = pair_f32(u.z, p), r[3] = pair_f32(u.w, p);
-    }
+    static_assert(VW == 4, "4-column slices");
+    const float4 a = load4_f32(p);
+    r[0] = make_float2(a.x, a.y), r[1] = make_float2(a.z, a.w);
 }
 
 // Code row of one token as 32-bit words (NS bytes, NS % 4 == 0, row address
