@@ -161,8 +161,25 @@ vq_status attn_launch(const AttnPlan &p, const void *q, const uint8_t *kcodes, c
     if (s != VQ_OK) return s;
     const int64_t rows = p.sh.batch * p.sh.heads_q;
     const int threads = (p.sh.head_dim + 31) / 32 * 32;
-    vqk::attn_combine<T><<<(unsigned)rows, threads, 0, st>>>(part, rows, p.sh.head_dim,
-                                                             p.sh.splits, static_cast<T *>(out));
+    // a programmatic dependent of the partials' launch: its blocks are
+    // scheduled as the partial blocks retire and wait on the device for
+    // the whole partial grid (griddepcontrol.wait), instead of a full launch
+    // gap after it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, vqk::attn_combine<T>, (const float *)part, rows, p.sh.head_dim,
+                           p.sh.splits, static_cast<T *>(out)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return VQ_ERR_CUDA;
+    }
     return vqh_launched(st, vqh_status_attn);
 }
 

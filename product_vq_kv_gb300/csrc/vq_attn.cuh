@@ -790,6 +790,10 @@ __global__ void __launch_bounds__(kAttnThreads)
     }
     __syncthreads();  // the tables are reused below
 
+    // the dependent merge kernel may be scheduled from here on; it waits for
+    // this whole grid before it reads any partial
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // ---- block sums and the merge of the token streams
     float *rsum = red + (size_t)2 * GPB * NW;
 #pragma unroll
@@ -837,7 +841,9 @@ __global__ void __launch_bounds__(kAttnThreads)
 }
 
 // Merge the partials: out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k.
-// Launch: grid.x = n_rows (batch * heads_q), block = head_dim rounded up to 32.
+// Launch: grid.x = n_rows (batch * heads_q), block = head_dim rounded up to
+// 32, after attn_partial on the same stream, as its programmatic dependent
+// (or plainly: the wait below then returns at once).
 template <typename T>
 __global__ void attn_combine(const float *__restrict__ part, int64_t n_rows, int32_t head_dim,
                              int32_t splits, T *__restrict__ out)
@@ -845,6 +851,9 @@ __global__ void attn_combine(const float *__restrict__ part, int64_t n_rows, int
     constexpr float kNegInf = -__builtin_huge_valf();
     const int64_t r = blockIdx.x;
     const int j = threadIdx.x;
+    // launched as a programmatic dependent of attn_partial: wait until that
+    // grid has completed and its partials are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (r >= n_rows || j >= head_dim) return;
     const float *pr = part + (size_t)r * splits * (head_dim + 2);
     if (!VQ_SPAN(pr, (int64_t)splits * (head_dim + 2), part, n_rows * splits * (int64_t)(head_dim + 2)) ||
