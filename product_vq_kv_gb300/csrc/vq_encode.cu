@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "vq_encode.h"
 #include "vq_host.h"
@@ -161,16 +162,22 @@ size_t fast_smem(int32_t n_centroids)
 template <int SUB, bool SMOOTH = false>
 size_t tc_smem(int32_t n_centroids, vq_dtype dtype)
 {
-    using C = TcConfig<SUB>;
-    if (dtype == VQ_F32)
+    if (dtype == VQ_F32) {
+        using C = TcConfig<SUB, true>;
         return vqk::TcLayout<SUB, C::kCols, C::kGroup, 2, 2, C::kTps>::bytes(n_centroids);
+    }
+    using C = TcConfig<SUB, SMOOTH>;
     return vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH ? 2 : 1, 1, C::kTps>::bytes(n_centroids);
 }
+
+// Rows go to the tensor cores as two tf32 pieces when they are smoothed or fp32.
+template <typename T, bool SMOOTH>
+constexpr bool tc_split() { return SMOOTH || std::is_same<T, float>::value; }
 
 template <typename T, int SUB, typename OutT = uint32_t, bool SMOOTH = false>
 auto tc_kernel()
 {
-    using C = TcConfig<SUB>;
+    using C = TcConfig<SUB, tc_split<T, SMOOTH>()>;
     return vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks, OutT, SMOOTH, vqk::kWaitPolls, C::kTps>;
 }
 
@@ -178,13 +185,18 @@ auto tc_kernel()
 // bounds admits kMinBlocks per SM, the tensor memory 512 / kCols, and the
 // shared memory of an SM (228 KiB, 1 KiB reserved per block) what `smem`
 // allows.
-// Tiles per step of the tensor-core kernel.
-int tc_tps(int sub_dim) { return sub_dim == 4 ? TcConfig<4>::kTps : TcConfig<8>::kTps; }
+// Tiles per step of the tensor-core kernel; `split` as in tc_split.
+int tc_tps(int sub_dim, bool split)
+{
+    if (sub_dim == 4) return split ? TcConfig<4, true>::kTps : TcConfig<4, false>::kTps;
+    return split ? TcConfig<8, true>::kTps : TcConfig<8, false>::kTps;
+}
 
-int tc_slots(int sub_dim, size_t smem)
+int tc_slots(int sub_dim, bool split, size_t smem)
 {
     const int sms = device_sms();
-    int per_sm = sub_dim == 4 ? TcConfig<4>::kMinBlocks : TcConfig<8>::kMinBlocks;
+    int per_sm = sub_dim == 4 ? (split ? TcConfig<4, true>::kMinBlocks : TcConfig<4, false>::kMinBlocks)
+                              : (split ? TcConfig<8, true>::kMinBlocks : TcConfig<8, false>::kMinBlocks);
     const int by_smem = (int)((size_t)228 * 1024 / (smem + 1024));
     if (by_smem < per_sm) per_sm = by_smem;
     if (per_sm < 1) per_sm = 1;
@@ -220,15 +232,16 @@ Plan make_plan(const Args &a)
         if (p.smem <= kMaxFastSmem) p.kind = kBrute;
     }
     if (p.kind == kTc) {
-        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, p.smem), tc_tps(a.sub_dim), &p.tiles_per_group,
-                 &p.tc_tiles);
+        const bool split = a.dtype == VQ_F32;
+        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, split, p.smem), tc_tps(a.sub_dim, split),
+                 &p.tiles_per_group, &p.tc_tiles);
         p.blocks = a.n_groups * p.tiles_per_group;
-        p.threads = 128 * tc_tps(a.sub_dim);
+        p.threads = 128 * tc_tps(a.sub_dim, split);
     } else if (p.kind != kGeneral) {
         const int64_t tile = p.kind == kFilter ? (int64_t)kFThreads * kFRows : (int64_t)kThreads * kRows;
         p.tiles_per_group = (a.n_per_group + tile - 1) / tile;
         p.blocks = a.n_groups * p.tiles_per_group;
-        p.threads = p.kind == kTc ? 128 : p.kind == kFilter ? kFThreads : kThreads;
+        p.threads = p.kind == kFilter ? kFThreads : kThreads;
     } else {
         p.smem = 0;
         p.tiles_per_group = 0;
@@ -245,7 +258,7 @@ vq_status launch_tc(const Args &a, const Plan &p)
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) !=
         cudaSuccess)
         return VQ_ERR_CUDA;
-    kernel<<<(unsigned)p.blocks, 128 * TcConfig<SUB>::kTps, p.smem, a.stream>>>(
+    kernel<<<(unsigned)p.blocks, 128 * TcConfig<SUB, tc_split<T, SMOOTH>()>::kTps, p.smem, a.stream>>>(
         static_cast<const T *>(a.x), static_cast<const T *>(a.cb), a.n_per_group, a.n_centroids,
         p.tiles_per_group, p.tc_tiles, 1.0f, static_cast<OutT *>(a.out), a.smooth,
         SMOOTH ? (int32_t)(a.head_dim / a.sub_dim) : 1);
@@ -366,10 +379,10 @@ vq_status run_smooth(const Args &a)
     if (a.n_centroids >= kFilterMinCentroids && a.n_centroids <= 256) {
         p.kind = kTc;
         p.smem = a.sub_dim == 4 ? tc_smem<4, true>(a.n_centroids, a.dtype) : tc_smem<8, true>(a.n_centroids, a.dtype);
-        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, p.smem), tc_tps(a.sub_dim), &p.tiles_per_group,
-                 &p.tc_tiles);
+        tc_shape(a.n_groups, a.n_per_group, tc_slots(a.sub_dim, true, p.smem), tc_tps(a.sub_dim, true),
+                 &p.tiles_per_group, &p.tc_tiles);
         p.blocks = a.n_groups * p.tiles_per_group;
-        p.threads = 128 * tc_tps(a.sub_dim);
+        p.threads = 128 * tc_tps(a.sub_dim, true);
     } else {
         p.kind = kFilter;
         p.smem = a.sub_dim == 4 ? filter_smem<4>(a.n_centroids) : filter_smem<8>(a.n_centroids);
@@ -713,7 +726,7 @@ vq_status vq_describe_launch(int64_t n_groups, int64_t n_per_group, int32_t n_ce
                  "kernel=encode_tc dtype=%s sub_dim=%d tmem_cols=%d tiles_per_block=%d "
                  "tiles_per_step=%d centroid_group=%d grid=%lld smem=%zu",
                  dtype_name(dtype), sub_dim, sub_dim == 4 ? TcConfig<4>::kCols : TcConfig<8>::kCols,
-                 (int)p.tc_tiles, tc_tps(sub_dim), sub_dim == 4 ? TcConfig<4>::kGroup : TcConfig<8>::kGroup,
+                 (int)p.tc_tiles, tc_tps(sub_dim, dtype == VQ_F32), sub_dim == 4 ? TcConfig<4>::kGroup : TcConfig<8>::kGroup,
                  (long long)p.blocks, p.smem);
     else if (p.kind == kFilter)
         snprintf(buf, (size_t)buflen,

@@ -182,21 +182,29 @@ struct TcLayout {
     }
 };
 
-// Per sub_dim: tensor-memory columns per tile, centroids per screening group,
-// minimum CTAs per SM (register budget), tiles per step (a CTA has 128 threads
-// per tile of a step and screens the step's tiles with one commit, one wait
-// and one barrier per pass).  Measured best on GB300 for 256-centroid
-// codebooks.
-template <int SUB>
+// Per sub_dim, and per whether each row is carried as two tf32 pieces
+// (SPLIT: smoothed rows or fp32 keys): tensor-memory columns per tile,
+// centroids per screening group, minimum CTAs per SM (register budget), tiles
+// per step (a CTA has 128 threads per tile of a step and screens the step's
+// tiles with one commit, one wait and one barrier per pass).  Measured best on
+// GB300 for 256-centroid codebooks; two tiles per step pay only for 16-bit
+// rows at sub_dim 4, where the per-pass synchronisation is the larger share.
+template <int SUB, bool SPLIT = false>
 struct TcConfig;
 template <>
-struct TcConfig<4> {
+struct TcConfig<4, false> {
     static constexpr int kCols = 64, kGroup = 16, kMinBlocks = 4, kTps = 2;
 };
 template <>
-struct TcConfig<8> {
+struct TcConfig<4, true> {
+    static constexpr int kCols = 64, kGroup = 16, kMinBlocks = 8, kTps = 1;
+};
+template <>
+struct TcConfig<8, false> {
     static constexpr int kCols = 64, kGroup = 8, kMinBlocks = 6, kTps = 1;
 };
+template <>
+struct TcConfig<8, true> : TcConfig<8, false> {};
 
 // ------------------------------------------------------------------ kernel
 

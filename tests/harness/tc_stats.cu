@@ -19,8 +19,8 @@ cudaError_t launch(const void *x, const void *cb, int64_t n_groups, int64_t n_pe
                    int32_t n_c, int32_t tiles_per_block, uint32_t *out, const float *smooth,
                    int32_t head_dim, cudaStream_t st)
 {
-    using C = vqk::TcConfig<SUB>;
     constexpr bool kF32 = std::is_same<T, float>::value;
+    using C = vqk::TcConfig<SUB, SMOOTH || kF32>;
     using L = vqk::TcLayout<SUB, C::kCols, C::kGroup, SMOOTH || kF32 ? 2 : 1, kF32 ? 2 : 1, C::kTps>;
     const size_t smem = L::bytes(n_c);
     auto k = vqk::encode_tc<T, SUB, C::kCols, C::kGroup, C::kMinBlocks, uint32_t, SMOOTH, vqk::kWaitPolls, C::kTps>;
