@@ -52,9 +52,10 @@ MEASURED_TRAFFIC = {
     "centroid_group=8 grid=704 smem=34880": 4_364_800,
 }
 # The same for the other ops' dominant kernels, keyed by (op, workload, input dtype):
-# attn_partial, hadamard_rows, scalar_scan.
+# attn_partial, hadamard_rows, scalar_bucket (fp16 keys), scalar_scan (fp32 keys).
 MEASURED_OP_TRAFFIC = {
     ("attention", "llama_attention", "f16"): 67_280_384 + 391_936,
+    ("scalar", "turboquant_keys", "f16"): 67_177_728 + 4_563_968,
     ("hadamard", "turboquant_keys", "f16"): 67_156_992 + 4_517_376,
     ("scalar", "turboquant_keys", "f32"): 134_288_384 + 12_928_256,
 }
@@ -671,13 +672,16 @@ def bench_sibling(args, fused: bool) -> None:
                    "tokens": sw.tokens, "head_dim": sw.head_dim, "bits": sw.bits,
                    "input_dtype": args.dtype},
         "timing": {"l2": L2_POLICY},
-        "gpu_launches": args.steps * (1 if fused else 2),
+        # bf16 keys: the table build and the lookup pass; fp16 keys (bucket
+        # table built in the kernel), fp32 keys and the fused rotation: one launch
+        "gpu_launches": args.steps * (2 if not fused and args.dtype == "bf16" else 1),
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": MEASURED_OP_TRAFFIC.get(("hadamard" if fused else "scalar", sw.name, args.dtype)),
                      "bytes_per_launch": algo_bytes,
-                     "timed": "whole step" + ("" if fused else " (table build + lookup pass)"),
+                     "timed": "whole step" + (" (table build + lookup pass)" if not fused and args.dtype == "bf16"
+                                              else ""),
                      "accounting": "algorithmic bytes: each key element read once and its "
                                    "uint8 index written once"},
         "e2e": None,

@@ -264,12 +264,16 @@ vq_status vq_attention_decode_static(const void *q, const uint8_t *k_codes,
  * centroids[j])^2), lowest j on ties, NaN never winning, 0 when nothing wins.
  *   x          [n]  device, dtype
  *   out        [n]  device, uint8, written
- *   workspace  device scratch of the caller, 16-byte aligned.  With fp16 /
- *              bf16 input and at least vq_scalar_quantize_workspace_bytes
- *              (65536) bytes, the rule is evaluated once for each of the
- *              65,536 input bit patterns and the pass becomes a table lookup
- *              (same indices); otherwise (fp32 input, or NULL / smaller
- *              workspace) every element scans the codebook.
+ *   workspace  device scratch of the caller, 16-byte aligned.  fp16 input
+ *              with 2, 4, 8 or 16 centroids does not use it: each block
+ *              builds a 2 KiB table of the 1,024 buckets of fp16 patterns
+ *              (top 10 bits) from the codebook's cut points, and looks every
+ *              key up there.  Other fp16 / bf16 input with at least
+ *              vq_scalar_quantize_workspace_bytes (65536) bytes evaluates the
+ *              rule once for each of the 65,536 input bit patterns, and the
+ *              pass becomes a table lookup.  Otherwise (fp32 input, or NULL /
+ *              smaller workspace) every element scans the codebook.  The
+ *              indices are the same on every path.
  */
 size_t vq_scalar_quantize_workspace_bytes(vq_dtype dtype);
 vq_status vq_scalar_quantize(const void *x, vq_dtype dtype, int64_t n, const float *centroids,

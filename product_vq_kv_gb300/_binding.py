@@ -275,9 +275,11 @@ def vq_scalar_quantize(x: torch.Tensor, centroids: torch.Tensor, out: torch.Tens
                        workspace: torch.Tensor | None = None, use_table: bool = True,
                        stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """Scalar (sub_dim = 1) quantize of every element of ``x`` against the
-    float32 ``centroids``: uint8 indices of ``x``'s shape.  For fp16 / bf16
-    input a 64 KiB ``workspace`` enables the table pass (allocated here when
-    omitted and ``use_table``)."""
+    float32 ``centroids``: uint8 indices of ``x``'s shape.  fp16 input with
+    2, 4, 8 or 16 centroids takes the bucket table the kernel builds itself
+    (the workspace goes unused); other fp16 / bf16 input takes the table pass
+    when a 64 KiB ``workspace`` is given (allocated here when omitted and
+    ``use_table``)."""
     _device_tensor(x, "x")
     _f32_vector(centroids, "centroids")
     if out is None:

@@ -154,6 +154,25 @@ vq_status hadamard(const void *x, vq_dtype dtype, const float *diag, int64_t n_r
 
 }  // namespace
 
+// fp16 keys against exactly NC (2, 4, 8 or 16) centroids: one block of
+// kLookupThreads per SM builds the bucket table once (no workspace).
+template <int NC>
+vq_status launch_bucket(const void *x, int64_t n, const float *c, uint8_t *out, cudaStream_t st)
+{
+    const bool vec = (uintptr_t)x % 16 == 0 && (uintptr_t)out % 8 == 0;
+    int64_t blocks = (n + 65535) / 65536;  // at least 64 Ki elements per block
+    const int sms = vqh_device_sms() > 0 ? vqh_device_sms() : 152;
+    if (blocks > sms) blocks = sms;
+    if (blocks < 1) blocks = 1;
+    auto kp = vqs::scalar_bucket<NC>;
+    if (cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, vqs::kBucketSmemBytes) !=
+        cudaSuccess)
+        return VQ_ERR_CUDA;
+    kp<<<(unsigned)blocks, kLookupThreads, vqs::kBucketSmemBytes, st>>>(static_cast<const uint16_t *>(x), n, c,
+                                                                        vec, out);
+    return launched(st);
+}
+
 extern "C" {
 
 size_t vq_scalar_quantize_workspace_bytes(vq_dtype dtype)
@@ -171,6 +190,14 @@ vq_status vq_scalar_quantize(const void *x, vq_dtype dtype, int64_t n, const flo
     if (!x || !centroids || !out) return VQ_ERR_INVALID_ARG;
     if ((uintptr_t)x % elem_size(dtype) || (uintptr_t)centroids % 4) return VQ_ERR_INVALID_ARG;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == VQ_F16) {
+        switch (n_centroids) {
+        case 2: return launch_bucket<2>(x, n, centroids, out, st);
+        case 4: return launch_bucket<4>(x, n, centroids, out, st);
+        case 8: return launch_bucket<8>(x, n, centroids, out, st);
+        case 16: return launch_bucket<16>(x, n, centroids, out, st);
+        }
+    }
     const bool table = dtype != VQ_F32 && workspace != nullptr && workspace_bytes >= kTableBytes;
     if (table) {
         if ((uintptr_t)workspace % 16) return VQ_ERR_INVALID_ARG;

@@ -367,12 +367,17 @@ __device__ __forceinline__ bool cut_decides(float v, const CutCb<NC> &cb)
 // conflicts).  Callers take the rule's scan separately for the rare values
 // the cut points do not decide.
 template <int NC>
-__device__ __forceinline__ uint32_t cut_code(float v, const CutCb<NC> &cb)
+__device__ __forceinline__ int cut_rank(float v, const CutCb<NC> &cb)
 {
     int k = 0;
 #pragma unroll
     for (int step = NC / 2; step > 0; step >>= 1) k += v >= cb.t[k + step - 1] ? step : 0;
-    return (uint32_t)(cb.perm >> (4 * k)) & 15u;
+    return k;
+}
+template <int NC>
+__device__ __forceinline__ uint32_t cut_code(float v, const CutCb<NC> &cb)
+{
+    return (uint32_t)(cb.perm >> (4 * cut_rank<NC>(v, cb))) & 15u;
 }
 
 // Randomised Hadamard rotation of rows of D = LPR * E elements, optionally
@@ -673,6 +678,159 @@ __global__ void __launch_bounds__(256)
         __stcs(reinterpret_cast<uint2 *>(out) + u, quant8(v));
     }
     for (int64_t e = units * 8 + tid; e < n; e += nthreads) out[e] = (uint8_t)quant(widen_elem(x[e]));
+}
+
+// ---- fp16 keys against 2, 4, 8 or 16 centroids: a bucket table from the cut points
+//
+// An fp16 pattern h falls in bucket h >> 6 (sign, exponent and the top four
+// significand bits: 1,024 buckets); over a bucket the value moves
+// monotonically with h & 63 (up in positive buckets, down in negative ones).
+// Where the cut points decide both end values of a bucket they decide all of
+// it, and the rank (cut points at or below the value) is monotone over it.
+// So a bucket whose end ranks differ by at most one has at most one change
+// of code: its entry holds the code below the change (A), the code from it
+// on (B) and the first pattern T that takes B.  The other buckets (two or
+// more changes; the values the cut points leave to the scan: NaN,
+// infinities, keys outside [lo, hi]; every bucket when the codebook fails
+// the cut points' conditions) are flagged, and their elements take cut_code
+// or the rule's scan one by one.  The result is the cut points' (or the
+// scan's) answer for every pattern, bit for bit.
+//
+// Entry (32 bits): T in bits 16-31, A in bits 0-3, B in bits 8-11, the flag
+// in bits 7 and 15 (T = 0 when flagged or when the bucket has one code).  With
+// hx = h << 16 | 0xffff, h < T exactly when hx < entry, so the code byte is
+// the low byte of entry (A) or of entry >> 8 (B), the flag in its bit 7.
+// The 1,024 entries (4 KiB) are copied once per shared-memory bank: lane l
+// finds bucket b at byte (b * 32 + l) * 4, in its own bank whatever b is, so
+// a warp's 32 lookups take one wavefront (random bytes of a 64 KiB table
+// take about four).
+constexpr uint32_t kBucketFlag = 0x8080u;
+constexpr int kBucketCopyBytes = 131072;  // 1,024 entries x 32 banks x 4 bytes
+constexpr int kBucketSmemBytes = kBucketCopyBytes + 4096;
+
+template <int NC>
+__device__ uint32_t bucket_entry(uint32_t b, const CutCb<NC> &cb)
+{
+    const uint32_t base = b << 6;
+    const float v0 = widen16((uint16_t)base, false);
+    const float v1 = widen16((uint16_t)(base | 63u), false);
+    if (!cut_decides<NC>(v0, cb) || !cut_decides<NC>(v1, cb)) return kBucketFlag;
+    const int k0 = cut_rank<NC>(v0, cb), k1 = cut_rank<NC>(v1, cb);
+    const uint32_t c0 = (uint32_t)(cb.perm >> (4 * k0)) & 15u;
+    const uint32_t c1 = (uint32_t)(cb.perm >> (4 * k1)) & 15u;
+    if (k0 == k1) return c0 | c0 << 8;
+    if (k1 - k0 != 1 && k0 - k1 != 1) return kBucketFlag;
+    // rank(lo) == k0, rank(hi) == k1: the first position of rank k1
+    uint32_t lo = 0, hi = 63;
+    while (hi - lo > 1u) {
+        const uint32_t mid = (lo + hi) / 2u;
+        if (cut_rank<NC>(widen16((uint16_t)(base | mid), false), cb) == k1) hi = mid; else lo = mid;
+    }
+    return (base | hi) << 16 | c0 | c1 << 8;
+}
+
+// The code byte (flag in bit 7) of pattern h from its entry; hx = h << 16 | 0xffff.
+__device__ __forceinline__ uint32_t bucket_byte(uint32_t e, uint32_t hx)
+{
+    return hx < e ? e : e >> 8;
+}
+
+// out[e] = the rule's index of fp16 x[e] for a codebook of exactly NC
+// entries.  Launch: any grid of blocks of up to 1024 threads (one block per
+// SM builds the table once), dynamic shared memory kBucketSmemBytes;
+// grid-stride over 8-element units when `vec` (x 16-byte and out 8-byte
+// aligned), the remaining elements one by one.
+template <int NC>
+__global__ void __launch_bounds__(1024)
+    scalar_bucket(const uint16_t *__restrict__ x, int64_t n, const float *__restrict__ centroids,
+                  bool vec, uint8_t *__restrict__ out)
+{
+    extern __shared__ __align__(16) uint8_t sb_tab[];
+    __shared__ float cut_sm[4 * 16];
+    // the copies and the entries must fit the launch's shared memory, else the
+    // block does nothing (checked build; block-uniform); the lookups' offsets
+    // stay below kBucketCopyBytes by construction
+    if (!vqk::dyn_smem_ok(sb_tab, kBucketSmemBytes, 16)) return;
+    CutCb<NC> cb;
+    build_cut_cb<NC>(centroids, cut_sm, cb);
+    uint32_t *entries = reinterpret_cast<uint32_t *>(sb_tab + kBucketCopyBytes);
+    for (uint32_t b = threadIdx.x; b < 1024u; b += blockDim.x)
+        entries[b] = cb.ok ? bucket_entry<NC>(b, cb) : kBucketFlag;
+    __syncthreads();
+    {
+        uint32_t *copies = reinterpret_cast<uint32_t *>(sb_tab);
+        for (int i = threadIdx.x; i < kBucketCopyBytes / 4; i += blockDim.x) copies[i] = entries[i >> 5];
+    }
+    __syncthreads();
+    const uint8_t *mine = sb_tab + (threadIdx.x & 31u) * 4u;
+    // entry of the pattern in bits 0-15 (lo) or 16-31 (hi) of w
+    auto entry_lo = [&](uint32_t w) -> uint32_t {
+        return *reinterpret_cast<const uint32_t *>(mine + ((w & 0xffc0u) << 1));
+    };
+    auto entry_hi = [&](uint32_t w) -> uint32_t {
+        return *reinterpret_cast<const uint32_t *>(mine + ((w >> 15) & 0x1ff80u));
+    };
+    auto slow = [&](uint32_t h) -> uint32_t {
+        const float v = widen16((uint16_t)h, false);
+        return cut_decides<NC>(v, cb) ? cut_code<NC>(v, cb) : nearest(v, cut_sm + NC, NC);
+    };
+    // four patterns (two words) -> four code bytes
+    auto quant4 = [&](uint32_t w0, uint32_t w1) -> uint32_t {
+        const uint32_t b0 = bucket_byte(entry_lo(w0), __byte_perm(w0, 0xffffffffu, 0x1044));
+        const uint32_t b1 = bucket_byte(entry_hi(w0), w0 | 0xffffu);
+        const uint32_t b2 = bucket_byte(entry_lo(w1), __byte_perm(w1, 0xffffffffu, 0x1044));
+        const uint32_t b3 = bucket_byte(entry_hi(w1), w1 | 0xffffu);
+        uint32_t r = __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+        if (r & 0x80808080u) {  // rare: the flagged elements one by one
+            const uint32_t h[4] = {w0 & 0xffffu, w0 >> 16, w1 & 0xffffu, w1 >> 16};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if ((r >> (8 * i)) & 0x80u) r = (r & ~(0xffu << (8 * i))) | slow(h[i]) << (8 * i);
+        }
+        return r;
+    };
+    auto quant8 = [&](uint4 q) -> uint2 { return make_uint2(quant4(q.x, q.y), quant4(q.z, q.w)); };
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t units = vec ? n / 8 : 0;
+    auto load = [&](int64_t k) -> uint4 {
+        return VQ_VSPAN(x + k * 8, 8, x, n, 16) ? __ldcs(reinterpret_cast<const uint4 *>(x) + k)
+                                                : make_uint4(0, 0, 0, 0);
+    };
+    auto store = [&](int64_t k, uint2 r) {
+        if (VQ_VSPAN(out + k * 8, 8, out, n, 8)) __stcs(reinterpret_cast<uint2 *>(out) + k, r);
+    };
+    // U units per thread and step; the next step's loads are issued before
+    // the current step's lookups
+    constexpr int U = 2;
+    int64_t u = tid;
+    if (u + (U - 1) * nthreads < units) {
+        uint4 cur[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) cur[k] = load(u + k * nthreads);
+        for (;;) {
+            const int64_t nu = u + U * nthreads;
+            const bool more = nu + (U - 1) * nthreads < units;
+            uint4 nxt[U];
+            if (more) {
+#pragma unroll
+                for (int k = 0; k < U; ++k) nxt[k] = load(nu + k * nthreads);
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) store(u + k * nthreads, quant8(cur[k]));
+            u = nu;
+            if (!more) break;
+#pragma unroll
+            for (int k = 0; k < U; ++k) cur[k] = nxt[k];
+        }
+    }
+    for (; u < units; u += nthreads) store(u, quant8(load(u)));
+    for (int64_t e = units * 8 + tid; e < n; e += nthreads)
+        if (VQ_SPAN(x + e, 1, x, n) && VQ_SPAN(out + e, 1, out, n)) {
+            const uint32_t h = x[e];
+            const uint32_t byte = bucket_byte(entry_lo(h), h << 16 | 0xffffu) & 0xffu;
+            out[e] = (uint8_t)((byte & 0x80u) ? slow(h) : byte);
+        }
 }
 
 }  // namespace vqs

@@ -40,7 +40,8 @@ def codebook(rng, n_c):
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("n_c", [2, 16, 256])
 def test_scalar_every_16_bit_pattern(vq, oracle_mod, dtype, n_c):
-    """All 65,536 bit patterns (NaN, inf, subnormals included), table and scan."""
+    """All 65,536 bit patterns (NaN, inf, subnormals included), table and
+    scan (fp16 with 2 or 16 centroids: the bucket table either way)."""
     rng = np.random.default_rng(n_c)
     c = codebook(rng, n_c)
     bits = np.arange(65536, dtype=np.uint16)
@@ -326,3 +327,47 @@ def test_cut_points_match_the_rule_where_they_decide(vq, oracle_mod, n_c):
         got = vq.vq_hadamard_quantize(torch.from_numpy(rows).cuda(), torch.from_numpy(diag).cuda(),
                                       cd).cpu().numpy()
         assert np.array_equal(got.astype(np.uint32), oracle_mod.hadamard_quantize(rows, diag, c)), name
+
+
+def bucket_codebooks(n_c):
+    """Codebooks for fp16 keys against 2 to 16 centroids (the bucket table):
+    the cut-point codebooks, the benchmark's Lloyd-Max levels, centroids
+    closer than a bucket is wide (several code changes in one bucket), a
+    decided range that ends inside the fp16 range, tiny centroids (most
+    patterns outside it), and codebooks that fail the cut points' conditions
+    (a repeated value, an infinity: every bucket flagged)."""
+    rng = np.random.default_rng(500 + n_c)
+    out = dict(cut_point_codebooks(n_c))
+    lm = workloads.lloyd_max_gaussian(int(np.log2(n_c)), 20)
+    out["lloyd_max"] = lm
+    out["closer_than_a_bucket"] = (np.float32(1.0) + np.arange(n_c, dtype=np.float32) * np.float32(0.0015)).astype(np.float32)
+    out["range_inside_fp16"] = (np.arange(n_c, dtype=np.float32) * np.float32(0.01)).astype(np.float32)
+    out["tiny"] = (rng.standard_normal(n_c) * 1e-6).astype(np.float32)
+    dup = lm.copy()
+    dup[-1] = dup[0]
+    out["repeated"] = dup
+    inf = lm.copy()
+    inf[n_c // 2] = np.inf
+    out["infinite"] = inf
+    return out
+
+
+@pytest.mark.parametrize("n_c", [2, 4, 8, 16])
+def test_fp16_bucket_table_every_pattern(vq, oracle_mod, n_c):
+    """fp16 keys against 2 to 16 centroids go through the per-block bucket
+    table (one entry per top-10-bit prefix, flagged buckets element by
+    element): all 65,536 patterns against the rule, for every codebook of
+    bucket_codebooks, 16-byte aligned (8-element units) and one element off
+    (element by element)."""
+    bits = np.arange(65536, dtype=np.uint16)
+    host = bits.view(np.float16)
+    buf = torch.zeros(65536 + 16, dtype=torch.int16, device="cuda")
+    for name, c in bucket_codebooks(n_c).items():
+        want = oracle_mod.scalar_quantize(host, c)
+        cd = torch.from_numpy(c).cuda()
+        for off in (0, 1):
+            xv = buf[off:off + 65536]
+            xv.copy_(torch.from_numpy(bits.view(np.int16)))
+            got = vq.vq_scalar_quantize(xv.view(torch.float16), cd).cpu().numpy()
+            bad = np.flatnonzero(got.astype(np.uint32) != want)
+            assert bad.size == 0, f"{name} off {off}: {bad.size} patterns differ, first {bits[bad[:4]]}"
