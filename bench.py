@@ -52,10 +52,9 @@ MEASURED_TRAFFIC = {
     "centroid_group=8 grid=704 smem=34880": 4_364_800,
 }
 # The same for the other ops' dominant kernels, keyed by (op, workload, input dtype):
-# attn_partial, hadamard_rows, scalar_bucket (fp16 keys), scalar_scan (fp32 keys).
+# attn_partial, hadamard_rows, scalar_scan (fp32 keys).
 MEASURED_OP_TRAFFIC = {
     ("attention", "llama_attention", "f16"): 67_280_384 + 391_936,
-    ("scalar", "turboquant_keys", "f16"): 67_177_728 + 4_563_968,
     ("hadamard", "turboquant_keys", "f16"): 67_156_992 + 4_517_376,
     ("scalar", "turboquant_keys", "f32"): 134_288_384 + 12_928_256,
 }

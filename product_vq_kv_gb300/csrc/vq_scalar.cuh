@@ -751,6 +751,38 @@ __global__ void __launch_bounds__(1024)
     // block does nothing (checked build; block-uniform); the lookups' offsets
     // stay below kBucketCopyBytes by construction
     if (!vqk::dyn_smem_ok(sb_tab, kBucketSmemBytes, 16)) return;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t units = vec ? n / 8 : 0;
+    auto load = [&](int64_t k) -> uint4 {
+        return VQ_VSPAN(x + k * 8, 8, x, n, 16) ? __ldcs(reinterpret_cast<const uint4 *>(x) + k)
+                                                : make_uint4(0, 0, 0, 0);
+    };
+    // U units per thread and step; the next step's loads are issued before
+    // the current step's lookups, and the first step's before the set-up
+    constexpr int U = 2;
+    int64_t u = tid;
+    uint4 cur[U];
+    const bool first = u + (U - 1) * nthreads < units;
+    if (first) {
+#pragma unroll
+        for (int k = 0; k < U; ++k) cur[k] = load(u + k * nthreads);
+    }
+    // the block's units of the next kPrefetchSteps steps (blockDim.x
+    // consecutive units per step and k) are brought into L2 during the set-up
+    constexpr int kPrefetchSteps = 3;
+    if (threadIdx.x == 0) {
+        const int64_t b0 = (int64_t)blockIdx.x * blockDim.x;
+        for (int st = 1; st <= kPrefetchSteps; ++st)
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int64_t a = b0 + (int64_t)(st * U + k) * nthreads;
+                const int64_t c = units - a < (int64_t)blockDim.x ? units - a : (int64_t)blockDim.x;
+                if (c > 0 && VQ_VSPAN(x + a * 8, c * 8, x, n, 16))
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                                 :: "l"(x + a * 8), "r"((uint32_t)(c * 16)) : "memory");
+            }
+    }
     CutCb<NC> cb;
     build_cut_cb<NC>(centroids, cut_sm, cb);
     uint32_t *entries = reinterpret_cast<uint32_t *>(sb_tab + kBucketCopyBytes);
@@ -790,24 +822,10 @@ __global__ void __launch_bounds__(1024)
         return r;
     };
     auto quant8 = [&](uint4 q) -> uint2 { return make_uint2(quant4(q.x, q.y), quant4(q.z, q.w)); };
-    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-    const int64_t units = vec ? n / 8 : 0;
-    auto load = [&](int64_t k) -> uint4 {
-        return VQ_VSPAN(x + k * 8, 8, x, n, 16) ? __ldcs(reinterpret_cast<const uint4 *>(x) + k)
-                                                : make_uint4(0, 0, 0, 0);
-    };
     auto store = [&](int64_t k, uint2 r) {
         if (VQ_VSPAN(out + k * 8, 8, out, n, 8)) __stcs(reinterpret_cast<uint2 *>(out) + k, r);
     };
-    // U units per thread and step; the next step's loads are issued before
-    // the current step's lookups
-    constexpr int U = 2;
-    int64_t u = tid;
-    if (u + (U - 1) * nthreads < units) {
-        uint4 cur[U];
-#pragma unroll
-        for (int k = 0; k < U; ++k) cur[k] = load(u + k * nthreads);
+    if (first) {
         for (;;) {
             const int64_t nu = u + U * nthreads;
             const bool more = nu + (U - 1) * nthreads < units;
