@@ -614,10 +614,11 @@ def bench_smooth(args) -> None:
 
 def bench_sibling(args, fused: bool) -> None:
     """Scalar (sub_dim = 1) quantize of one layer's key cache against a 4-bit
-    Lloyd-Max codebook (``--op scalar``: the 64 KiB table pass), or the
-    randomised Hadamard rotation fused with it (``--op hadamard``); one launch
-    per step (plus the table build for the scalar pass), against the HBM
-    roofline of 2 bytes in and 1 byte out per element."""
+    Lloyd-Max codebook (``--op scalar``: fp16 keys take the bucket-table
+    kernel, bf16 keys the 64 KiB table build and lookup pass, fp32 keys the
+    per-element search), or the randomised Hadamard rotation fused with it
+    (``--op hadamard``); one launch per step (two for bf16 keys), against the
+    HBM roofline of the key bytes in and 1 byte out per element."""
     import torch
 
     from product_vq_kv_gb300.build import build

@@ -11,12 +11,17 @@
 // form, each lane rounded alike), arranged so that no compiler contraction
 // can change a result.
 //
-// GB300 shape.  16-bit inputs have only 65,536 values: scalar_table
-// evaluates the formula once for each bit pattern into a 64 KiB table (the
-// caller's workspace), and scalar_lookup stages that table in shared memory
-// and turns the pass into a coalesced 2-byte-in / 1-byte-out stream with one
-// shared-memory lookup per element (HBM-bound, bit-identical to the scan).
-// Other inputs use scalar_scan: codebooks of 2, 4, 8 or 16 finite entries go
+// GB300 shape.  fp16 keys against 2, 4, 8 or 16 centroids take
+// scalar_bucket: each block builds, from the codebook's cut points, one entry
+// per 10-bit prefix of the fp16 pattern (the codes on either side of the
+// bucket's one change of code, or a flag) and copies the entries once per
+// shared-memory bank, so the pass is a coalesced 2-byte-in / 1-byte-out
+// stream with one conflict-free shared-memory lookup per element.  Other
+// 16-bit inputs have only 65,536 values too: scalar_table evaluates the
+// formula once for each bit pattern into a 64 KiB table (the caller's
+// workspace), and scalar_lookup stages that table in shared memory and looks
+// every element up there.  Both are bit-identical to the scan.  Other inputs
+// use scalar_scan: codebooks of 2, 4, 8 or 16 finite entries go
 // through a packed register scan (distances in f32x2 pairs, their least by a
 // min3 tree, the lowest index holding it from sign bits), others through a
 // sorted view of the codebook with the scan as fallback.  The rotation

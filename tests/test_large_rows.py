@@ -209,9 +209,10 @@ def fp16_normal(n: int, seed: int) -> torch.Tensor:
 
 
 def test_scalar_quantize_past_2_31_elements(vq, oracle_mod, centroids16):
-    """Both scalar paths (the 64 KiB table and the register scan) and the
-    dequantize.  A 16-bit key's index depends on its bit pattern alone, so
-    the oracle's answer for all 65,536 patterns checks every element."""
+    """The fp16 scalar quantize (16 centroids: the bucket-table kernel, with
+    and without a workspace) and the dequantize.  A 16-bit key's index
+    depends on its bit pattern alone, so the oracle's answer for all 65,536
+    patterns checks every element."""
     x = fp16_normal(N_SCALAR, 901)
     c = centroids16
     pats = np.arange(1 << 16, dtype=np.uint16).view(np.float16)
