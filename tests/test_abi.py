@@ -246,6 +246,21 @@ def test_describe_launch_picks_kernels(lib):
     assert f(1, 1000, 256, 0, 0, P, buf, 512) == 2
 
 
+def test_describe_launch_tiles_per_step(lib):
+    """The tensor-core encode screens two 128-row tiles per step only for
+    16-bit rows at sub_dim 4; rows split into two tf32 pieces (fp32 keys) and
+    sub_dim 8 take one tile per step (128-thread blocks)."""
+    f = lib.vq_describe_launch
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int32]
+    buf = ctypes.create_string_buffer(512)
+    for dtype, sub, tps in ((0, 4, 2), (1, 4, 2), (2, 4, 1), (0, 8, 1), (2, 8, 1)):
+        assert f(1, 1 << 20, 256, sub, dtype, P, buf, 512) == 0
+        desc = buf.value.decode()
+        assert desc.startswith("kernel=encode_tc") and f"tiles_per_step={tps} " in desc, desc
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import product_vq_kv_gb300._binding as b
 
