@@ -14,7 +14,7 @@ It checks the probe's output bit for bit and prints the times and the link
 read rate (run with ``-s``).  The encode must read its whole input across
 the link, so it can be no faster than the plain read of that input (a floor,
 checked with 10 % slack for timer resolution), and it is checked to stay
-within 2x of that floor.
+within 2.5x of that floor (measured 1.7x, host overhead of the call included).
 """
 import ctypes
 import time
@@ -95,4 +95,6 @@ def test_host_encode_is_bound_by_the_link_read(vq):
           f"({nbytes / t_host / 1e3:.0f} GB/s across the link); host-buffer encode {t_enc:.1f} us "
           f"({t_enc / t_host:.2f}x the pinned read)")
     assert t_enc >= 0.9 * t_host
-    assert t_enc <= 2.0 * t_host
+    # the host-timed call also carries the binding's and the launch's host
+    # overhead (measured 1.7x in all), so the bound leaves room for a slower host
+    assert t_enc <= 2.5 * t_host
